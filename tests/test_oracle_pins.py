@@ -1,0 +1,381 @@
+"""Pins for the CPU oracle: facts that hold independently of its code.
+
+Each test checks the oracle against something other than itself: values
+the page prints or that follow by hand from the E4M3 / UE8M0 definitions
+(tests/golden/), a library implementation of E4M3 (torch.float8_e4m3fn,
+round-to-nearest-even on the finite range), closed forms, invariants, and
+numpy's matmul on dequantised operands.  A plausible slip in the oracle (a
+wrong rounding direction, a dropped sign, a transposed scale index, a
+missing term) fails at least one of them.
+"""
+import math
+import struct
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from golden_io import e4m3_codes, quant_groups
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def f32_bits(v):
+    return struct.unpack("<I", struct.pack("<f", float(v)))[0]
+
+
+def bits_f32(b):
+    return struct.unpack("<f", struct.pack("<I", int(b)))[0]
+
+
+# ---- E4M3 codec -----------------------------------------------------------
+
+def test_e4m3_golden_codes():
+    for code, value in e4m3_codes():
+        got = oracle.e4m3_decode(code)
+        if math.isnan(value):
+            assert math.isnan(got), hex(code)
+        else:
+            assert got == value and math.copysign(1, got) == math.copysign(1, value), hex(code)
+            assert oracle.e4m3_encode(value) == code, hex(code)
+
+
+def test_e4m3_decode_matches_torch_all_codes():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([oracle.e4m3_decode(c) for c in range(256)])
+    nan = np.isnan(ref)
+    assert np.array_equal(nan, np.isnan(got))
+    assert nan.sum() == 2  # 0x7F and 0xFF
+    assert np.array_equal(ref[~nan], got[~nan])
+    assert np.array_equal(np.signbit(ref[~nan]), np.signbit(got[~nan]))
+
+
+def test_e4m3_roundtrip_and_monotone():
+    finite = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    for c in finite:
+        assert oracle.e4m3_encode(oracle.e4m3_decode(c)) == c
+    pos = [oracle.e4m3_decode(c) for c in range(0x7F)]
+    assert all(a < b for a, b in zip(pos, pos[1:]))
+    assert max(pos) == 448.0
+
+
+def _structured_fp32_values():
+    """fp32 patterns around every rounding boundary of E4M3: every exponent
+    from 2^-20 to 2^9, all top-11 mantissa bit patterns, and low bits at the
+    tie point, just below and just above it, for both signs."""
+    vals = []
+    hi = np.arange(2048, dtype=np.uint32) << 12
+    for lo in (0, 1, 0x7FF, 0x800, 0x801, 0xFFF):
+        for e in range(127 - 20, 127 + 9):
+            vals.append((np.uint32(e) << 23) | hi | np.uint32(lo))
+    v = np.concatenate(vals)
+    v = np.concatenate([v, v | np.uint32(0x80000000)])
+    return v.view(np.float32)
+
+
+def test_e4m3_encode_matches_torch_rne():
+    x = _structured_fp32_values()
+    x = x[np.abs(x) < 464.0]  # torch turns |x| >= 464 into NaN instead of saturating
+    ref = torch.from_numpy(x.copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    enc = np.vectorize(oracle.e4m3_encode, otypes=[np.uint8])
+    sample = np.random.default_rng(0).choice(x.size, size=min(x.size, 120000), replace=False)
+    got = enc(x[sample])
+    assert np.array_equal(got, ref[sample])
+
+
+def test_e4m3_saturation_and_signed_zero():
+    for v in (448.0, 449.0, 463.9, 464.0, 480.0, 1e30, 3.0e38):
+        assert oracle.e4m3_encode(v) == 0x7E
+        assert oracle.e4m3_encode(-v) == 0xFE
+    assert oracle.e4m3_encode(0.0) == 0x00
+    assert oracle.e4m3_encode(-0.0) == 0x80
+    assert oracle.e4m3_encode(-1e-30) == 0x80
+    assert oracle.e4m3_encode(2.0 ** -10) == 0x00            # tie with 0 -> even
+    assert oracle.e4m3_encode(2.0 ** -10 + 2.0 ** -30) == 0x01
+
+
+def test_e4m3_midpoints_go_to_even_code():
+    for c in range(0x7E):
+        lo, hi = oracle.e4m3_decode(c), oracle.e4m3_decode(c + 1)
+        mid = (lo + hi) / 2  # exact in fp32: E4M3 values have 4 significant bits
+        assert float(np.float32(mid)) == mid
+        want = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_encode(mid) == want
+        assert oracle.e4m3_encode(-mid) == want | 0x80
+
+
+# ---- scales -----------------------------------------------------------------
+
+def _all_positive_finite_bf16():
+    bits = np.arange(1, 0x7F80, dtype=np.uint32)  # +subnormals .. max finite
+    return (bits << 16).view(np.float32)
+
+
+def test_scale_fp32_puts_amax_on_448():
+    """The group maximum always lands on E4M3 448 in fp32 mode: s is
+    amax/448 rounded once, so amax/s is within an ulp of 448 (or above it
+    and saturates), for every positive bf16 amax."""
+    for amax in _all_positive_finite_bf16()[::7]:
+        s = oracle.scale_from_amax(float(amax), oracle.MODE_FP32)
+        assert s > 0 and math.isfinite(s)
+        y = np.float32(amax) / np.float32(s)
+        if s >= 2.0 ** -126:  # normal scale: one rounding, relative error <= 2^-24
+            assert abs(float(y) - 448.0) <= 448.0 * 2.0 ** -22
+        else:                 # subnormal scale (amax < ~2^-117): coarser, still nearest 448
+            assert abs(float(y) - 448.0) < 16.0
+        assert oracle.e4m3_encode(float(y)) == 0x7E
+
+
+def test_scale_ue8m0_is_power_of_two_ceiling():
+    for amax in _all_positive_finite_bf16()[::5]:
+        t = float(np.float32(amax) / np.float32(448.0))
+        s = oracle.scale_from_amax(float(amax), oracle.MODE_UE8M0)
+        m, e = math.frexp(s)
+        assert m == 0.5, s                       # power of two
+        code = oracle.ue8m0_code(s)
+        assert 0 <= code <= 254 and s == 2.0 ** (code - 127)
+        if s > 2.0 ** -127:
+            assert s >= t and s / 2 < t          # the smallest power >= t
+        else:
+            assert s >= t or s == 2.0 ** -127    # clamped at the bottom code
+
+
+def test_scale_zero_group_and_closed_forms():
+    for mode in (oracle.MODE_FP32, oracle.MODE_UE8M0):
+        assert oracle.scale_from_amax(0.0, mode) == 1.0
+    assert oracle.scale_from_amax(448.0, oracle.MODE_FP32) == 1.0
+    assert oracle.scale_from_amax(224.0, oracle.MODE_FP32) == 0.5
+    assert oracle.scale_from_amax(7.0, oracle.MODE_FP32) == 2.0 ** -6
+    assert oracle.scale_from_amax(448.0, oracle.MODE_UE8M0) == 1.0
+    assert oracle.scale_from_amax(450.0, oracle.MODE_UE8M0) == 2.0
+    assert oracle.scale_from_amax(447.0, oracle.MODE_UE8M0) == 1.0
+    assert oracle.pow2_ceil(1.0) == 1.0 and oracle.pow2_ceil(1.0000001) == 2.0
+    assert oracle.pow2_ceil(0.75) == 1.0 and oracle.pow2_ceil(0.5) == 0.5
+
+
+def test_ue8m0_pack_matches_page_formula():
+    """Blackwell: Native Block Scaling: scale_i = 2^(((packed >> 8i) & 0xFF) - 127)."""
+    codes = [127, 0, 254, 130]
+    packed = oracle.ue8m0_pack4(codes)
+    assert packed == 127 | (0 << 8) | (254 << 16) | (130 << 24)
+    assert [oracle.ue8m0_unpack(packed, i) for i in range(4)] == [1.0, 2.0 ** -127, 2.0 ** 127, 8.0]
+    assert oracle.ue8m0_code(1.0) == 127 and oracle.ue8m0_code(0.75) == -1
+
+
+# ---- quantizers -----------------------------------------------------------
+
+@pytest.mark.parametrize("case", quant_groups(), ids=lambda c: f"{c[0]}-{c[1]}")
+def test_quant_act_golden_groups(case):
+    name, mode, bits, scale_bits, codes = case
+    mode_id = oracle.MODE_UE8M0 if mode == "ue8m0" else oracle.MODE_FP32
+    x = np.zeros((1, 128), dtype=np.uint16)
+    x[0, :len(bits)] = bits
+    q, s = oracle.quant_act_1x128(x, mode_id)
+    assert f32_bits(s[0, 0]) == scale_bits
+    want = np.zeros(128, dtype=np.uint8)
+    want[:len(codes)] = codes
+    assert np.array_equal(q[0], want)
+
+
+@pytest.mark.parametrize("case", quant_groups(), ids=lambda c: f"{c[0]}-{c[1]}")
+def test_quant_w_golden_groups_as_blocks(case):
+    """The same group laid out down a column of a 128x128 block (K direction)
+    and scattered over rows gives the same scale and codes."""
+    name, mode, bits, scale_bits, codes = case
+    mode_id = oracle.MODE_UE8M0 if mode == "ue8m0" else oracle.MODE_FP32
+    w = np.zeros((128, 128), dtype=np.uint16)
+    pos = [(7 * i + 3) % 128 for i in range(len(bits))]
+    for i, b in enumerate(bits):
+        w[pos[i], (5 * i + 11) % 128] = b
+    q, s = oracle.quant_w_128x128(w, mode_id)
+    assert f32_bits(s[0, 0]) == scale_bits
+    for i, c in enumerate(codes):
+        assert q[pos[i], (5 * i + 11) % 128] == c
+    mask = np.ones((128, 128), bool)
+    for i in range(len(bits)):
+        mask[pos[i], (5 * i + 11) % 128] = False
+    assert np.all(q[mask] == 0)
+
+
+def _ulp_e4m3(y):
+    y = np.abs(y)
+    e = np.floor(np.log2(np.maximum(y, 2.0 ** -6)))
+    return np.where(y < 2.0 ** -6, 2.0 ** -9, 2.0 ** (e - 3))
+
+
+@pytest.mark.parametrize("mode", [oracle.MODE_FP32, oracle.MODE_UE8M0])
+def test_quant_act_invariants(mode):
+    import fgq_inputs
+    x = fgq_inputs.student_t((48, 640), 3, 1.0, seed=5)
+    xo = fgq_inputs.outlier((16, 640), 1e-2, 100.0, seed=6)
+    x = torch.cat([x, xo])
+    x[3, 128:256] = 0
+    xb = x.view(torch.int16).numpy().view(np.uint16)
+    xf = x.float().numpy().astype(np.float64)
+    q, s = oracle.quant_act_1x128(xb, mode)
+    M, K = x.shape
+    assert s.shape == (M, K // 128) and q.shape == (M, K)
+    dec = oracle.e4m3_decode_array(q)
+    assert np.all(np.isfinite(dec)) and np.all(np.abs(dec) <= 448)
+    groups = xf.reshape(M, K // 128, 128)
+    dq = dec.reshape(M, K // 128, 128)
+    amax = np.abs(groups).max(axis=2)
+    gmax = np.abs(dq).max(axis=2)
+    nz = amax > 0
+    if mode == oracle.MODE_FP32:
+        assert np.all(gmax[nz] == 448)
+        assert np.allclose(s[nz].astype(np.float64) * 448, amax[nz], rtol=2.0 ** -22, atol=0)
+    else:
+        assert np.all((gmax[nz] >= 224) & (gmax[nz] <= 448))
+        m, _ = np.frexp(s)
+        assert np.all(m == 0.5)
+    assert np.all(s[~nz] == 1.0) and np.all(dq[~nz] == 0)
+    # dequant error bound: half an E4M3 ulp of x/s, plus the fp32 rounding of x/s
+    sc = np.repeat(s.astype(np.float64), 128, axis=1).reshape(M, K // 128, 128)
+    y = groups / sc
+    err = np.abs(y - dq)
+    assert np.all(err <= 0.5 * _ulp_e4m3(y) + np.abs(y) * 2.0 ** -23)
+    # sign: codes carry the sign of x, including for values that round to zero
+    assert np.array_equal((q >= 0x80), np.signbit(xf.reshape(M, K)))
+
+
+def test_quant_lossless_on_representable_groups():
+    """A group made of E4M3 values times 2^j with a member at 448 * 2^j has
+    scale 2^j in both modes and quantizes without loss."""
+    rng = np.random.default_rng(1)
+    pos = np.array([oracle.e4m3_decode(c) for c in range(0x7F)])
+    for j in (-8, 0, 5):
+        vals = rng.choice(pos, size=(4, 256)) * rng.choice([-1.0, 1.0], size=(4, 256))
+        vals[:, 0] = 448.0
+        vals[:, 128] = -448.0
+        x = torch.tensor(vals * 2.0 ** j, dtype=torch.float32)
+        xb = x.to(torch.bfloat16)
+        assert torch.equal(xb.float(), x)
+        for mode in (oracle.MODE_FP32, oracle.MODE_UE8M0):
+            q, s = oracle.quant_act_1x128(xb, mode)
+            assert np.all(s == 2.0 ** j)
+            assert np.array_equal(oracle.e4m3_decode_array(q) * 2.0 ** j, vals * 2.0 ** j)
+
+
+def test_quant_w_block_indexing():
+    """Each 128x128 block gets its own scale at sW[k/128, n/128]: blocks with
+    distinct maxima (non-square block grid) land at the right index."""
+    K, N = 256, 384
+    w = np.zeros((K, N), dtype=np.float32)
+    for i in range(K // 128):
+        for j in range(N // 128):
+            w[i * 128 + 17, j * 128 + 101] = 448.0 * 2.0 ** (i * 3 + j)
+            w[i * 128 + 5, j * 128 + 9] = -1.0
+    wb = torch.from_numpy(w).to(torch.bfloat16)
+    q, s = oracle.quant_w_128x128(wb, oracle.MODE_FP32)
+    assert s.shape == (2, 3)
+    for i in range(2):
+        for j in range(3):
+            assert s[i, j] == 2.0 ** (i * 3 + j)
+            assert q[i * 128 + 17, j * 128 + 101] == 0x7E
+
+
+def test_quant_rejects_bad_shapes_and_nonfinite():
+    with pytest.raises(ValueError):
+        oracle.quant_act_1x128(np.zeros((2, 100), np.uint16))
+    with pytest.raises(ValueError):
+        oracle.quant_w_128x128(np.zeros((128, 100), np.uint16))
+    x = np.zeros((1, 128), np.uint16)
+    x[0, 3] = 0x7F80  # +inf
+    with pytest.raises(ValueError):
+        oracle.quant_act_1x128(x)
+
+
+# ---- GEMM -------------------------------------------------------------------
+
+def _dequant_with_torch(q, s, block_rows, block_cols):
+    """Independent dequantisation: torch's E4M3 decode times the scale of
+    each element's block, in fp64."""
+    dec = torch.from_numpy(np.ascontiguousarray(q)).view(torch.float8_e4m3fn).to(
+        torch.float64).numpy()
+    srep = np.repeat(np.repeat(s.astype(np.float64), block_rows, 0), block_cols, 1)
+    return dec * srep
+
+
+def _quantized_pair(M, N, K, seed, mode=oracle.MODE_FP32):
+    import fgq_inputs
+    a = fgq_inputs.outlier((M, K), 1e-2, 100.0, seed)
+    b = fgq_inputs.normal((K, N), 0.02, seed + 1)
+    aq, sa = oracle.quant_act_1x128(a, mode)
+    bq, sb = oracle.quant_w_128x128(b, mode)
+    return aq, sa, bq, sb
+
+
+@pytest.mark.parametrize("mode", [oracle.MODE_FP32, oracle.MODE_UE8M0])
+def test_gemm_matches_numpy_matmul_of_dequantised(mode):
+    M, N, K = 40, 384, 256  # non-square block grid: kc = 2, nb = 3
+    aq, sa, bq, sb = _quantized_pair(M, N, K, 11, mode)
+    ah = _dequant_with_torch(aq, sa, 1, 128)
+    bh = _dequant_with_torch(bq, sb, 128, 128)
+    c, t = oracle.gemm_dequant(aq, sa, bq, sb)
+    tref = np.abs(ah) @ np.abs(bh)
+    assert np.all(np.abs(c - ah @ bh) <= 1e-12 * tref)
+    assert np.allclose(t, tref, rtol=1e-12, atol=0)
+
+
+def test_gemm_forms_agree_with_bruteforce():
+    M, N, K = 8, 256, 384
+    aq, sa, bq, sb = _quantized_pair(M, N, K, 21)
+    c, t = oracle.gemm_dequant(aq, sa, bq, sb)
+    cb = oracle.gemm_bruteforce(aq, sa, bq, sb)
+    cc = oracle.gemm_chunked(aq, sa, bq, sb)
+    scale = t + 1e-300
+    assert np.all(np.abs(c - cb) <= 1e-13 * scale)
+    assert np.all(np.abs(c - cc) <= 1e-13 * scale)
+    rows = np.array([0, 7, 3, 5]); cols = np.array([0, 255, 128, 17])
+    ca, ta = oracle.gemm_dequant_at(aq, sa, bq, sb, rows, cols)
+    assert np.array_equal(ca, c[rows, cols]) and np.array_equal(ta, t[rows, cols])
+    assert np.all(t >= np.abs(c))
+
+
+def test_gemm_closed_forms():
+    # constant operands: A = 448 (s = 1, code 0x7E), B = 7 (s = 2^-6, code 0x7E)
+    M, N, K = 2, 128, 256
+    a = torch.full((M, K), 448.0).to(torch.bfloat16)
+    b = torch.full((K, N), 7.0).to(torch.bfloat16)
+    aq, sa = oracle.quant_act_1x128(a)
+    bq, sb = oracle.quant_w_128x128(b)
+    c, t = oracle.gemm_dequant(aq, sa, bq, sb)
+    assert np.all(c == K * 448.0 * 7.0) and np.all(t == c)
+    # B = identity (128x128 blocks of I, all with scale 2^-7): C = A_hat / 2^... exactly
+    K = N = 256
+    a = fgq_inputs_normal((4, K), 3)
+    bi = torch.eye(K, dtype=torch.float32).mul(448.0 * 2.0 ** -7).to(torch.bfloat16)
+    aq, sa = oracle.quant_act_1x128(a)
+    bq, sb = oracle.quant_w_128x128(bi)
+    assert np.all(sb[np.eye(2, dtype=bool)] == 2.0 ** -7) and np.all(sb[~np.eye(2, dtype=bool)] == 1.0)
+    c, _ = oracle.gemm_dequant(aq, sa, bq, sb)
+    ah = _dequant_with_torch(aq, sa, 1, 128)
+    assert np.array_equal(c, ah * 448.0 * 2.0 ** -7)
+    # rank one: A = u 1^T (every row constant), B with columns of one value each
+    u = torch.tensor([1.0, -2.0, 0.5]).view(3, 1).expand(3, 128).contiguous()
+    v = torch.linspace(-1, 1, 128).view(1, 128).expand(128, 128).contiguous()
+    aq, sa = oracle.quant_act_1x128(u.to(torch.bfloat16))
+    bq, sb = oracle.quant_w_128x128(v.to(torch.bfloat16))
+    c, _ = oracle.gemm_dequant(aq, sa, bq, sb)
+    bcol = _dequant_with_torch(bq, sb, 128, 128)[0]
+    arow = _dequant_with_torch(aq, sa, 1, 128)[:, 0]
+    expect = arow[:, None] * 128 * bcol[None, :]
+    assert np.allclose(c, expect, rtol=1e-12, atol=0)
+
+
+def fgq_inputs_normal(shape, seed):
+    import fgq_inputs
+    return fgq_inputs.normal(shape, 1.0, seed)
+
+
+def test_tolerance_check_detects_errors():
+    c_ref = np.array([[1.0, -2.0]]); t = np.array([[10.0, 10.0]])
+    ok, r = oracle.gemm_within_tolerance(c_ref + 0.019, c_ref, t)
+    assert ok and r <= 2e-3
+    ok, _ = oracle.gemm_within_tolerance(c_ref + 0.021, c_ref, t)
+    assert not ok
+    ok, _ = oracle.gemm_within_tolerance(np.array([[np.nan, -2.0]]), c_ref, t)
+    assert not ok
