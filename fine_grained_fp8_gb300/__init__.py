@@ -1,0 +1,129 @@
+"""Fine-grained FP8 quantization and block-scaled FP8 GEMM for GB300 (sm_103a).
+
+Tensor-level wrappers over the C ABI of libfgq.so (include/fgq.h).  PyTorch
+provides device memory and the current CUDA stream; all arithmetic runs in
+the library's kernels:
+
+  quant_act_1x128(x)        bf16 [M, K] -> (E4M3 codes [M, K] uint8, fp32 [M, K/128])
+  quant_w_128x128(w)        bf16 [K, N] -> (E4M3 codes [N, K] uint8 (K-major),
+                                            fp32 [K/128, N/128])
+  gemm_fp8_blockscaled(aq, sa, bq, sb, out_dtype)
+                            C [M, N] = sum over 128-wide K chunks of
+                            (Aq Bq)_chunk * sa * sb
+
+("Fine-Grained FP8/FP4 Quantization": §Scaling Granularities, §DeepGEMM.)
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import (FGQ_OUT_BF16, FGQ_OUT_F32, FGQ_SCALE_FP32, FGQ_SCALE_UE8M0, FgqError,
+                   check, load)
+
+__all__ = ["quant_act_1x128", "quant_w_128x128", "gemm_fp8_blockscaled", "device_error",
+           "FgqError", "load", "FGQ_SCALE_FP32", "FGQ_SCALE_UE8M0", "FGQ_OUT_F32",
+           "FGQ_OUT_BF16", "scale_mode"]
+
+
+def scale_mode(mode) -> int:
+    if mode in ("fp32", FGQ_SCALE_FP32, None):
+        return FGQ_SCALE_FP32
+    if mode in ("ue8m0", FGQ_SCALE_UE8M0):
+        return FGQ_SCALE_UE8M0
+    raise ValueError(f"unknown scale mode {mode!r} (use 'fp32' or 'ue8m0')")
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _need_cuda(name: str, t: torch.Tensor, dtype) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def quant_act_1x128(x: torch.Tensor, mode="fp32", xq: torch.Tensor | None = None,
+                    sx: torch.Tensor | None = None):
+    """1x128 tile-wise quantization of bf16 activations x [M, K] (rows may be
+    strided; the last dimension must be contiguous)."""
+    _need_cuda("x", x, torch.bfloat16)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with a contiguous last dimension")
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if sx is None:
+        sx = torch.empty((M, K // 128), dtype=torch.float32, device=x.device)
+    _need_cuda("xq", xq, torch.uint8)
+    _need_cuda("sx", sx, torch.float32)
+    if xq.shape != (M, K) or xq.stride(1) != 1 or sx.shape != (M, K // 128) or not sx.is_contiguous():
+        raise ValueError("xq must be [M, K] (contiguous rows) and sx a dense [M, K/128]")
+    st = _lib.fgq_quant_act_1x128(x.data_ptr(), M, K, x.stride(0), xq.data_ptr(), xq.stride(0),
+                                  sx.data_ptr(), scale_mode(mode), _stream(x))
+    check("fgq_quant_act_1x128", st)
+    return xq, sx
+
+
+def quant_w_128x128(w: torch.Tensor, mode="fp32", wq: torch.Tensor | None = None,
+                    sw: torch.Tensor | None = None):
+    """128x128 block-wise quantization of a bf16 weight w [K, N].  Returns the
+    codes TRANSPOSED, wq [N, K] (K-major), and sw [K/128, N/128]."""
+    _need_cuda("w", w, torch.bfloat16)
+    if w.dim() != 2 or w.stride(1) != 1:
+        raise ValueError("w must be 2-D with a contiguous last dimension")
+    K, N = w.shape
+    if wq is None:
+        wq = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    if sw is None:
+        sw = torch.empty((K // 128, N // 128), dtype=torch.float32, device=w.device)
+    _need_cuda("wq", wq, torch.uint8)
+    _need_cuda("sw", sw, torch.float32)
+    if wq.shape != (N, K) or not wq.is_contiguous() or sw.shape != (K // 128, N // 128) \
+            or not sw.is_contiguous():
+        raise ValueError("wq must be a dense [N, K] and sw a dense [K/128, N/128]")
+    st = _lib.fgq_quant_w_128x128(w.data_ptr(), K, N, w.stride(0), wq.data_ptr(), sw.data_ptr(),
+                                  scale_mode(mode), _stream(w))
+    check("fgq_quant_w_128x128", st)
+    return wq, sw
+
+
+def gemm_fp8_blockscaled(aq: torch.Tensor, sa: torch.Tensor, bq: torch.Tensor,
+                         sb: torch.Tensor, out_dtype=torch.float32, mode="fp32",
+                         out: torch.Tensor | None = None) -> torch.Tensor:
+    """C [M, N] = block-scaled FP8 product of aq [M, K] (1x128 scales sa) and the
+    K-major weight codes bq [N, K] (128x128 scales sb [K/128, N/128])."""
+    _need_cuda("aq", aq, torch.uint8)
+    _need_cuda("bq", bq, torch.uint8)
+    _need_cuda("sa", sa, torch.float32)
+    _need_cuda("sb", sb, torch.float32)
+    for name, t in (("aq", aq), ("bq", bq), ("sa", sa), ("sb", sb)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    M, K = aq.shape
+    N, K2 = bq.shape
+    if K2 != K or sa.shape != (M, K // 128) or sb.shape != (K // 128, N // 128):
+        raise ValueError("shape mismatch: aq [M,K], sa [M,K/128], bq [N,K], sb [K/128,N/128]")
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out_dtype must be torch.float32 or torch.bfloat16")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=aq.device)
+    _need_cuda("out", out, out_dtype)
+    if out.shape != (M, N) or out.stride(1) != 1:
+        raise ValueError("out must be [M, N] with contiguous rows")
+    st = _lib.fgq_gemm_fp8_blockscaled_ex(
+        aq.data_ptr(), sa.data_ptr(), bq.data_ptr(), sb.data_ptr(), out.data_ptr(), out.stride(0),
+        M, N, K, FGQ_OUT_BF16 if out_dtype == torch.bfloat16 else FGQ_OUT_F32, scale_mode(mode),
+        _stream(aq))
+    check("fgq_gemm_fp8_blockscaled_ex", st)
+    return out
+
+
+def device_error(clear: bool = True) -> int:
+    """The library's device error word (0 = no kernel gave up on a wait)."""
+    st, word = _lib.fgq_device_error(clear)
+    if st not in (_lib.FGQ_OK, _lib.FGQ_ERR_DEVICE_TIMEOUT):
+        raise FgqError("fgq_device_error", st)
+    return word

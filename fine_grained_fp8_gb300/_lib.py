@@ -1,0 +1,112 @@
+"""ctypes binding of libfgq.so (C ABI in include/fgq.h).
+
+Argument marshalling only: every step of the quantizers and the GEMM runs in
+the library's CUDA kernels.  There is no fallback of any kind: if the shared
+library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+FGQ_OK = 0
+FGQ_ERR_INVALID_ARG = 1
+FGQ_ERR_UNSUPPORTED = 2
+FGQ_ERR_CUDA = 3
+FGQ_ERR_DEVICE_TIMEOUT = 4
+
+FGQ_SCALE_FP32 = 0
+FGQ_SCALE_UE8M0 = 1
+FGQ_OUT_F32 = 0
+FGQ_OUT_BF16 = 1
+
+# Every symbol include/fgq.h declares, with (restype, argtypes).
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+SIGNATURES = {
+    "fgq_quant_act_1x128": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _int, _vp]),
+    "fgq_quant_w_128x128": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _int, _vp]),
+    "fgq_gemm_fp8_blockscaled": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
+    "fgq_gemm_fp8_blockscaled_ex": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                           _int, _int, _vp]),
+    "fgq_status_string": (ctypes.c_char_p, [_int]),
+    "fgq_device_error": (_int, [ctypes.POINTER(ctypes.c_uint32), _int]),
+    "fgq_version": (_int, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FgqError(RuntimeError):
+    def __init__(self, func: str, status: int):
+        self.status = status
+        super().__init__(f"{func} failed: status {status} ({status_string(status)})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libfgq.so (built by fine_grained_fp8_gb300.build.build())."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or _build.LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"libfgq.so not found at {p}: build it first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().fgq_status_string(int(status)).decode()
+    except Exception:  # library not loadable: still give the code
+        return "unknown"
+
+
+def check(func: str, status: int) -> None:
+    if status != FGQ_OK:
+        raise FgqError(func, status)
+
+
+# Raw C-ABI calls under their C names (pointers as ints, stream as int handle).
+
+def fgq_quant_act_1x128(x, M, K, ldx, xq, ldq, sx, mode, stream) -> int:
+    return load().fgq_quant_act_1x128(x, M, K, ldx, xq, ldq, sx, mode, stream)
+
+
+def fgq_quant_w_128x128(w, K, N, ldw, wq, sw, mode, stream) -> int:
+    return load().fgq_quant_w_128x128(w, K, N, ldw, wq, sw, mode, stream)
+
+
+def fgq_gemm_fp8_blockscaled(A, sA, B, sB, C, M, N, K, stream) -> int:
+    return load().fgq_gemm_fp8_blockscaled(A, sA, B, sB, C, M, N, K, stream)
+
+
+def fgq_gemm_fp8_blockscaled_ex(A, sA, B, sB, C, ldc, M, N, K, out, mode, stream) -> int:
+    return load().fgq_gemm_fp8_blockscaled_ex(A, sA, B, sB, C, ldc, M, N, K, out, mode, stream)
+
+
+def fgq_device_error(clear: bool = True):
+    word = ctypes.c_uint32(0)
+    st = load().fgq_device_error(ctypes.byref(word), 1 if clear else 0)
+    return st, int(word.value)
+
+
+def fgq_version() -> int:
+    return load().fgq_version()

@@ -1,0 +1,150 @@
+// C ABI of libfgq.so (declared in include/fgq.h): argument checks, device
+// checks, then one kernel launch per call on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fgq.h"
+#include "fgq_internal.h"
+
+namespace fgq {
+
+cudaError_t device_info(DeviceInfo* out) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  static bool valid[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!valid[dev]) {
+    DeviceInfo d{};
+    d.device = dev;
+    int smem = 0;
+    if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+      return e;
+    d.smem_optin = static_cast<size_t>(smem);
+    cache[dev] = d;
+    valid[dev] = true;
+  }
+  *out = cache[dev];
+  return cudaSuccess;
+}
+
+}  // namespace fgq
+
+namespace {
+
+inline bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// The kernels are built for sm_103a only.
+fgq_status get_device(fgq::DeviceInfo* dev) {
+  cudaError_t e = fgq::device_info(dev);
+  if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver) return FGQ_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return FGQ_ERR_CUDA;
+  if (dev->cc_major != 10 || dev->cc_minor != 3) return FGQ_ERR_UNSUPPORTED;
+  return FGQ_OK;
+}
+
+inline fgq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FGQ_OK : FGQ_ERR_CUDA; }
+
+constexpr int64_t kMaxGroups = (int64_t{1} << 31) - 1;
+
+}  // namespace
+
+extern "C" {
+
+fgq_status fgq_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
+                               int64_t ldq, float* sx, int mode, void* stream) {
+  if (M < 0 || K <= 0 || K % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (mode != FGQ_SCALE_FP32 && mode != FGQ_SCALE_UE8M0) return FGQ_ERR_INVALID_ARG;
+  if (M == 0) return FGQ_OK;
+  if (!x || !xq || !sx) return FGQ_ERR_INVALID_ARG;
+  if (ldx < K || ldq < K || ldx % 8 != 0 || ldq % 16 != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(xq, 16) || !aligned(sx, 4)) return FGQ_ERR_INVALID_ARG;
+  if (M > kMaxGroups / (K / 128)) return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_quant_act_1x128(x, M, K, ldx, xq, ldq, sx, mode,
+                                               static_cast<cudaStream_t>(stream), dev));
+}
+
+fgq_status fgq_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t ldw, uint8_t* wq,
+                               float* sw, int mode, void* stream) {
+  if (K <= 0 || N <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (mode != FGQ_SCALE_FP32 && mode != FGQ_SCALE_UE8M0) return FGQ_ERR_INVALID_ARG;
+  if (!w || !wq || !sw) return FGQ_ERR_INVALID_ARG;
+  if (ldw < N || ldw % 8 != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(wq, 16) || !aligned(sw, 4)) return FGQ_ERR_INVALID_ARG;
+  if ((K / 128) > kMaxGroups / (N / 128)) return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_quant_w_128x128(w, K, N, ldw, wq, sw, mode,
+                                               static_cast<cudaStream_t>(stream), dev));
+}
+
+fgq_status fgq_gemm_fp8_blockscaled_ex(const uint8_t* A, const float* sA, const uint8_t* B,
+                                       const float* sB, void* C, int64_t ldc, int64_t M,
+                                       int64_t N, int64_t K, int out, int mode, void* stream) {
+  if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (out != FGQ_OUT_F32 && out != FGQ_OUT_BF16) return FGQ_ERR_INVALID_ARG;
+  if (mode != FGQ_SCALE_FP32 && mode != FGQ_SCALE_UE8M0) return FGQ_ERR_INVALID_ARG;
+  // int32 tile coordinates inside the kernel
+  if (M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31) || K >= (int64_t{1} << 31))
+    return FGQ_ERR_INVALID_ARG;
+  if (M == 0) return FGQ_OK;
+  if (!A || !sA || !B || !sB || !C) return FGQ_ERR_INVALID_ARG;
+  const int64_t vec = (out == FGQ_OUT_F32) ? 4 : 8;  // elements per 16-byte store
+  if (ldc < N || ldc % vec != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(sA, 4) || !aligned(sB, 4))
+    return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_gemm_fp8_blockscaled(A, sA, B, sB, C, ldc, M, N, K,
+                                                    out == FGQ_OUT_BF16 ? 1 : 0, mode,
+                                                    static_cast<cudaStream_t>(stream), dev));
+}
+
+fgq_status fgq_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const uint8_t* B,
+                                    const float* sB, float* C, int64_t M, int64_t N, int64_t K,
+                                    void* stream) {
+  return fgq_gemm_fp8_blockscaled_ex(A, sA, B, sB, C, N, M, N, K, FGQ_OUT_F32, FGQ_SCALE_FP32,
+                                     stream);
+}
+
+const char* fgq_status_string(fgq_status status) {
+  switch (status) {
+    case FGQ_OK: return "ok";
+    case FGQ_ERR_INVALID_ARG: return "invalid argument (null pointer, size, stride or alignment)";
+    case FGQ_ERR_UNSUPPORTED: return "unsupported device (needs an sm_103 GPU)";
+    case FGQ_ERR_CUDA: return "CUDA runtime error";
+    case FGQ_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting (device error word set)";
+  }
+  return "unknown status";
+}
+
+fgq_status fgq_device_error(uint32_t* word, int clear) {
+  if (!word) return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return FGQ_ERR_CUDA;
+  e = fgq::read_device_error(word, clear != 0);
+  if (e != cudaSuccess) return FGQ_ERR_CUDA;
+  return *word ? FGQ_ERR_DEVICE_TIMEOUT : FGQ_OK;
+}
+
+int fgq_version(void) { return 100; }
+
+}  // extern "C"

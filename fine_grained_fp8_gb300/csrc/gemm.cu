@@ -1,0 +1,339 @@
+// Block-scaled FP8 GEMM for sm_103a ("Fine-Grained FP8/FP4 Quantization",
+// §DeepGEMM: Tile-wise and Block-wise Scaling):
+//
+//   C[m,n] = sum_c sA[m,c] * sB[c, n/128] * P_c[m,n],
+//   P_c    = sum_{k in chunk c} Aq[m,k] * Bq[k,n]   (one 128-wide K chunk)
+//
+// Design (GB300-native; the page's Hopper promotion loop is prior art):
+//   - Persistent CTAs, one per SM, walking output tiles of 128 x BN with a
+//     static stride-gridDim schedule ("Persistent kernel (grid = SM count,
+//     internal tile loop)", linear scheduler, M fastest).
+//   - Warp 0: TMA producer.  Each stage holds one 128-wide K chunk of A
+//     (128 x 128 bytes) and B (BN x 128 bytes), 128-byte swizzled.
+//   - Warp 1: one thread issues 4 tcgen05.mma (K = 32 each) per chunk into
+//     one of two TMEM partial buffers (128 lanes x BN fp32 columns each),
+//     then commits to the stage's "empty" and the buffer's "full" barriers.
+//   - Warps 2-9: epilogue.  Per chunk they read the partial from TMEM,
+//     multiply by sA[m,c] * sB[c, n/128] and add it into fp32 accumulators
+//     held in registers (the promotion step), release the TMEM buffer, and
+//     after the last chunk convert and store the tile.  Two TMEM buffers let
+//     the tensor core run chunk c+1 while chunk c is promoted.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "fgq_device.cuh"
+#include "fgq_internal.h"
+
+namespace fgq {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;  // one scale chunk per pipeline stage
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+
+template <int BN, int STAGES>
+struct Cfg {
+  static constexpr int kABytes = BM * BK;
+  static constexpr int kBBytes = BN * BK;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;  // two partial buffers
+  static constexpr int kBarBytes = (2 * STAGES + 4) * 8 + 16;
+  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes;
+  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of 2");
+};
+
+// Bounded wait used while unwinding; ignores the abort flag.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > FGQ_WAIT_NS) {
+      record_error(FGQ_DEVERR_DRAIN);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int BN, int STAGES, bool OUT_BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp8_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                                const __grid_constant__ CUtensorMap tmap_b,
+                                const float* __restrict__ sA, const float* __restrict__ sB,
+                                void* __restrict__ C, int64_t ldc, int M, int N, int K) {
+  using CF = Cfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sm_a = smem;
+  uint8_t* sm_b = smem + STAGES * CF::kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm_b + STAGES * CF::kBBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tiles = (M + BM - 1) / BM;
+  const int n_tiles = (N + BN - 1) / BN;
+  const int num_tiles = m_tiles * n_tiles;
+  const int kchunks = K / BK;
+  const int nb = N / 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kEpiWarps);
+    }
+    *abort_flag = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, CF::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (elect_one_sync()) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int tm = tile % m_tiles, tn = tile / m_tiles;
+        for (int kc = 0; kc < kchunks; ++kc, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, FGQ_DEVERR_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], CF::kStageBytes);
+          tma_load_2d(sm_a + s * CF::kABytes, &tmap_a, &full[s], kc * BK, tm * BM);
+          tma_load_2d(sm_b + s * CF::kBBytes, &tmap_b, &full[s], kc * BK, tn * BN);
+        }
+      }
+      // No copy may still target this CTA's shared memory when it exits.
+      const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
+      for (uint32_t j = first; j < it; ++j) mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (elect_one_sync()) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        for (int kc = 0; kc < kchunks; ++kc, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          const uint32_t buf = it & 1u, tph = (it >> 1) & 1u;
+          if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, FGQ_DEVERR_MMA_TMEM) ||
+              !mbar_wait(&full[s], ph, abort_flag, FGQ_DEVERR_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem_base + buf * BN;
+          const uint32_t a0 = smem_u32(sm_a + s * CF::kABytes);
+          const uint32_t b0 = smem_u32(sm_b + s * CF::kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / 32; ++kk)
+            umma_f8f6f4(d, smem_desc_k_sw128(a0 + kk * 32), smem_desc_k_sw128(b0 + kk * 32), idesc,
+                        kk > 0 ? 1u : 0u);
+          umma_commit(&empty[s]);
+          umma_commit(&tfull[buf]);
+        }
+      }
+      // MMAs still in flight must finish before TMEM is released.
+      if (it > 0) mbar_wait_drain(&tfull[(it - 1) & 1u], ((it - 1) >> 1) & 1u);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: promotion + store ----------------
+    constexpr int HALF = BN / 2;  // columns per epilogue warp
+    const int ew = warp - 2;
+    const int quad = warp & 3;      // TMEM lanes this warp may access
+    const int half = ew >> 2;       // which half of the tile's columns
+    const int r_in_tile = quad * 32 + lane;
+    const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      const int tm = tile % m_tiles, tn = tile / m_tiles;
+      const int row = tm * BM + r_in_tile;
+      const bool row_ok = row < M;
+      const int col0 = tn * BN + half * HALF;
+      const bool cols_ok = col0 < N;
+      const int nblk = cols_ok ? col0 / 128 : nb - 1;
+      const float* sa_row = sA + static_cast<int64_t>(row_ok ? row : 0) * kchunks;
+
+      float acc[HALF];
+#pragma unroll
+      for (int j = 0; j < HALF; ++j) acc[j] = 0.0f;
+
+      for (int kc = 0; kc < kchunks; ++kc, ++it) {
+        const uint32_t buf = it & 1u, tph = (it >> 1) & 1u;
+        const float sa = row_ok ? __ldg(sa_row + kc) : 0.0f;
+        const float sb = __ldg(sB + static_cast<int64_t>(kc) * nb + nblk);
+        const float comb = sa * sb;
+        if (!mbar_wait(&tfull[buf], tph, abort_flag, FGQ_DEVERR_EPI_TMEM)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + t_lane + buf * BN + half * HALF;
+#pragma unroll
+        for (int j0 = 0; j0 < HALF; j0 += 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(taddr + j0, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[j0 + j] = fmaf(__uint_as_float(r[j]), comb, acc[j0 + j]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+      }
+      if (!ok) break;
+      if (row_ok && cols_ok) {
+        if (OUT_BF16) {
+          uint16_t* crow = static_cast<uint16_t*>(C) + static_cast<int64_t>(row) * ldc + col0;
+#pragma unroll
+          for (int j = 0; j < HALF; j += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(acc[j + 0], acc[j + 1]);
+            v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+            v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
+            v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+            *reinterpret_cast<uint4*>(crow + j) = v;
+          }
+        } else {
+          float* crow = static_cast<float*>(C) + static_cast<int64_t>(row) * ldc + col0;
+#pragma unroll
+          for (int j = 0; j < HALF; j += 4)
+            *reinterpret_cast<float4*>(crow + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, CF::kTmemCols);
+  }
+}
+
+// ---- host side -------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// K-major E4M3 operand [rows, K] (row stride K bytes), box 128 (K) x box_rows,
+// 128-byte swizzle, out-of-range rows read as zero.
+bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
+  auto encode = get_encode_fn();
+  if (!encode) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                      box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, bool OUT_BF16>
+cudaError_t launch_cfg(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                       void* C, int64_t ldc, int M, int N, int K, cudaStream_t stream,
+                       const DeviceInfo& dev) {
+  using CF = Cfg<BN, STAGES>;
+  auto kern = gemm_fp8_blockscaled_kernel<BN, STAGES, OUT_BF16>;
+  static bool attr_set[64] = {};
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev.device < 64 && !attr_set[dev.device]) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(CF::kSmemBytes));
+      if (e != cudaSuccess) return e;
+      attr_set[dev.device] = true;
+    }
+  }
+  CUtensorMap ta, tb;
+  if (!make_operand_map(&ta, A, M, K, BM) || !make_operand_map(&tb, B, N, K, BN))
+    return cudaErrorInvalidValue;
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
+  kern<<<grid, kThreads, CF::kSmemBytes, stream>>>(ta, tb, sA, sB, C, ldc, M, N, K);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const uint8_t* B,
+                                        const float* sB, void* C, int64_t ldc, int64_t M,
+                                        int64_t N, int64_t K, int out_bf16, int mode,
+                                        cudaStream_t stream, const DeviceInfo& dev) {
+  (void)mode;  // power-of-two scales take the same promotion path (exact products)
+  if (M == 0 || N == 0) return cudaSuccess;
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  const int64_t tiles256 = ((M + BM - 1) / BM) * ((N + 255) / 256);
+  const bool wide = (N % 256 == 0) && tiles256 >= dev.sm_count;
+  if (out_bf16) {
+    return wide ? launch_cfg<256, 4, true>(A, sA, B, sB, C, ldc, m, n, k, stream, dev)
+                : launch_cfg<128, 6, true>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
+  }
+  return wide ? launch_cfg<256, 4, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev)
+              : launch_cfg<128, 6, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
+}
+
+cudaError_t read_device_error(uint32_t* word, bool clear) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (clear && v != 0) {
+    unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) return e;
+  }
+  *word = v;
+  return cudaSuccess;
+}
+
+}  // namespace fgq

@@ -1,0 +1,148 @@
+/*
+ * fgq — fine-grained FP8 quantization and block-scaled FP8 GEMM on GB300
+ * (sm_103a).  C ABI of libfgq.so.
+ *
+ * The method ("Fine-Grained FP8/FP4 Quantization", KernelWiki technique page):
+ *   - §Scaling Granularities: activations carry one scale per 1x128 tile
+ *     (one row, 128 consecutive K elements); weights carry one scale per
+ *     128x128 block.
+ *   - §DeepGEMM: Tile-wise and Block-wise Scaling: A and B are E4M3; the
+ *     scale tensors are scale_A [M, K/128] and scale_B [K/128, N/128]; for
+ *     each 128-wide K chunk the product of the FP8 tiles is multiplied by
+ *     scale_A * scale_B and added into an fp32 accumulator:
+ *       C[m,n] = sum_c  sA[m,c] * sB[c, n/128] * sum_{k in chunk c} Aq[m,k] Bq[k,n]
+ *   - §UE8M0 vs E4M3 Scale Formats, §Blackwell: Native Block Scaling: a
+ *     UE8M0 scale is a power of two 2^(e-127).
+ *
+ * Readings of the page fixed by this library:
+ *   scale   fp32 mode:  s = amax / 448 rounded once to fp32 (448 = largest
+ *           finite E4M3 value); UE8M0 mode: the smallest power of two
+ *           >= that value, exponent clamped to [-127, 127].  A group whose
+ *           amax is 0 gets s = 1.
+ *   encode  q = E4M3(x / s): one IEEE fp32 division, then round to nearest
+ *           with ties to even, magnitudes above 448 saturate to 448, sign
+ *           kept (a negative value that rounds to zero gives 0x80).
+ *   inputs  finite bf16 values; non-finite inputs give unspecified codes.
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are DEVICE pointers into memory the caller owns
+ *     (cudaMalloc / torch allocations).  The library never allocates,
+ *     frees or retains them, and never allocates device memory itself.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream and never
+ *     synchronise the host.
+ *   - Sizes are element counts; leading dimensions are in elements of the
+ *     array they describe.
+ *   - Arguments are checked before anything is launched; a rejected call
+ *     returns FGQ_ERR_INVALID_ARG (or FGQ_ERR_UNSUPPORTED) and touches no
+ *     memory.  A failed launch returns FGQ_ERR_CUDA.
+ *   - M == 0 (or N == 0) is a valid empty problem: nothing is launched.
+ */
+#ifndef FGQ_H_
+#define FGQ_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FGQ_OK = 0,
+  FGQ_ERR_INVALID_ARG = 1,   /* null pointer, bad size, stride or alignment */
+  FGQ_ERR_UNSUPPORTED = 2,   /* no device of a supported architecture */
+  FGQ_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+  FGQ_ERR_DEVICE_TIMEOUT = 4 /* a kernel gave up on a wait (see fgq_device_error) */
+} fgq_status;
+
+typedef enum { FGQ_SCALE_FP32 = 0, FGQ_SCALE_UE8M0 = 1 } fgq_scale_mode;
+typedef enum { FGQ_OUT_F32 = 0, FGQ_OUT_BF16 = 1 } fgq_out_dtype;
+
+/*
+ * 1x128 tile-wise activation quantization (§Scaling Granularities,
+ * per-tile 1x128; scale_A [M, K/128] from §DeepGEMM).
+ *
+ *   x    bf16 [M, K], row r at x + r * ldx (ldx >= K, ldx % 8 == 0),
+ *        16-byte aligned.
+ *   xq   E4M3 codes [M, K], row r at xq + r * ldq (ldq >= K,
+ *        ldq % 16 == 0), 16-byte aligned.
+ *   sx   fp32 [M, K/128] row-major (dense), 4-byte aligned.
+ *   K % 128 == 0, K > 0, M >= 0.  mode: FGQ_SCALE_FP32 or FGQ_SCALE_UE8M0.
+ * Per (row, group): amax over the 128 values, s from amax, q = E4M3(x/s).
+ */
+fgq_status fgq_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
+                               int64_t ldq, float* sx, int mode, void* stream);
+
+/*
+ * 128x128 block-wise weight quantization (§Scaling Granularities,
+ * per-block 128x128; scale_B [K/128, N/128] from §DeepGEMM).
+ *
+ *   w    bf16 [K, N] (the logical weight, K = reduction dimension), row k
+ *        at w + k * ldw (ldw >= N, ldw % 8 == 0), 16-byte aligned.
+ *   wq   E4M3 codes stored TRANSPOSED, [N, K] row-major (dense): code of
+ *        logical element (k, n) at wq[n * K + k].  This K-major layout is
+ *        the operand layout of fgq_gemm_fp8_blockscaled.  16-byte aligned.
+ *   sw   fp32 [K/128, N/128] row-major (dense).
+ *   K % 128 == 0, N % 128 == 0, both > 0.
+ * Per 128x128 block: amax over 16384 values, s from amax, q = E4M3(w/s).
+ */
+fgq_status fgq_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t ldw, uint8_t* wq,
+                               float* sw, int mode, void* stream);
+
+/*
+ * Block-scaled FP8 GEMM (§DeepGEMM: Tile-wise and Block-wise Scaling),
+ * fp32 output, fp32 scales:
+ *   C[m,n] = sum_c sA[m,c] * sB[c,n/128] * sum_{k in chunk c} A[m,k] * B[k,n]
+ *
+ *   A    E4M3 [M, K] row-major (dense, as fgq_quant_act_1x128 writes with
+ *        ldq = K), 16-byte aligned.
+ *   sA   fp32 [M, K/128] row-major.
+ *   B    E4M3 weight codes in the transposed [N, K] layout written by
+ *        fgq_quant_w_128x128, 16-byte aligned.
+ *   sB   fp32 [K/128, N/128] row-major.
+ *   C    fp32 [M, N] row-major (dense), 16-byte aligned.
+ *   K % 128 == 0, N % 128 == 0, K > 0, N > 0, M >= 0; M need not be a
+ *   multiple of anything.
+ * Each 128-wide K chunk is one tensor-core partial product in TMEM, which is
+ * scaled by sA * sB and added into an fp32 accumulator (the page's
+ * promotion step, done by the epilogue warps).
+ */
+fgq_status fgq_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const uint8_t* B,
+                                    const float* sB, float* C, int64_t M, int64_t N,
+                                    int64_t K, void* stream);
+
+/*
+ * Same GEMM with an output type, an output leading dimension and a scale
+ * mode.
+ *   C      fp32 or bf16 [M, N], row m at C + m * ldc (ldc >= N; ldc % 4 == 0
+ *          for fp32, ldc % 8 == 0 for bf16), 16-byte aligned.  bf16 output
+ *          is the fp32 accumulator rounded to nearest even.
+ *   out    FGQ_OUT_F32 or FGQ_OUT_BF16.
+ *   mode   FGQ_SCALE_FP32: any positive finite scales.
+ *          FGQ_SCALE_UE8M0: the caller promises every scale is a power of
+ *          two (as the quantizers write in UE8M0 mode); results are the
+ *          same formula.
+ */
+fgq_status fgq_gemm_fp8_blockscaled_ex(const uint8_t* A, const float* sA, const uint8_t* B,
+                                       const float* sB, void* C, int64_t ldc, int64_t M,
+                                       int64_t N, int64_t K, int out, int mode, void* stream);
+
+/* Static description of a status code. */
+const char* fgq_status_string(fgq_status status);
+
+/*
+ * The device error word of the current device: 0 while no kernel has given
+ * up on a wait; otherwise bits naming the wait that timed out.  If `clear`
+ * is nonzero the word is reset to 0.  Synchronises the current device.
+ * Returns FGQ_ERR_DEVICE_TIMEOUT when the word was nonzero.
+ */
+fgq_status fgq_device_error(uint32_t* word, int clear);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int fgq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FGQ_H_ */

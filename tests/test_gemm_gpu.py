@@ -1,0 +1,196 @@
+"""Parity of the sm_103a block-scaled FP8 GEMM with the oracle.
+
+The bar ("Fine-Grained FP8/FP4 Quantization", §DeepGEMM; tolerance as the
+spec states it): every output satisfies
+    |C - C_ref| <= 2e-3 * sum_k |a_hat[m,k]| |b_hat[k,n]|
+where C_ref is the fp64 product of the dequantised operands.  Small cases
+are compared element by element against the full oracle; full-size cases
+on sampled outputs the oracle computes one by one, plus a full-matrix check
+of the same bound against an fp32 torch product of dequantised operands.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fgq_inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+
+
+def _oracle_operands(a_cpu, b_cpu, mode):
+    aq, sa = oracle.quant_act_1x128(a_cpu, mode)
+    bq, sb = oracle.quant_w_128x128(b_cpu, mode)
+    return aq, sa, bq, sb
+
+
+def _to_dev(aq, sa, bq, sb, dev):
+    """Oracle operands in the library's layout (weight codes [N, K])."""
+    return (torch.from_numpy(aq).to(dev), torch.from_numpy(sa).to(dev),
+            torch.from_numpy(np.ascontiguousarray(bq.T)).to(dev), torch.from_numpy(sb).to(dev))
+
+
+def _run(fgq, ops, out_dtype, mode_name, out=None):
+    c = fgq.gemm_fp8_blockscaled(*ops, out_dtype=out_dtype, mode=mode_name, out=out)
+    torch.cuda.synchronize()
+    return c
+
+
+def _check_full(c_gpu, aq, sa, bq, sb):
+    cref, tref = oracle.gemm_dequant(aq, sa, bq, sb)
+    c = c_gpu.float().cpu().numpy().astype(np.float64)
+    ok, ratio = oracle.gemm_within_tolerance(c, cref, tref, TOL)
+    assert ok, f"max |err|/T = {ratio:.3e} exceeds {TOL}"
+    return ratio
+
+
+def _check_sampled(c_gpu, aq, sa, bq, sb, n_samples=3000, seed=0):
+    M, N = c_gpu.shape
+    rng = np.random.default_rng(seed)
+    rows = rng.integers(0, M, n_samples)
+    cols = rng.integers(0, N, n_samples)
+    # always include the corners and the last (possibly ragged) rows
+    rows = np.concatenate([rows, [0, 0, M - 1, M - 1]])
+    cols = np.concatenate([cols, [0, N - 1, 0, N - 1]])
+    cref, tref = oracle.gemm_dequant_at(aq, sa, bq, sb, rows, cols)
+    c = c_gpu.float().cpu().numpy()[rows, cols].astype(np.float64)
+    ok, ratio = oracle.gemm_within_tolerance(c, cref, tref, TOL)
+    assert ok, f"sampled max |err|/T = {ratio:.3e} exceeds {TOL}"
+    return ratio
+
+
+def _check_full_vs_torch(c_gpu, ops):
+    """Every element against an fp32 (no TF32) torch product of the
+    dequantised operands, with the same bound."""
+    aq, sa, bq, sb = ops
+    M, K = aq.shape
+    N = bq.shape[0]
+    old = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        ah = aq.view(torch.float8_e4m3fn).float() * sa.repeat_interleave(128, dim=1)
+        bh = bq.view(torch.float8_e4m3fn).float() * sb.t().repeat_interleave(128, 0).repeat_interleave(128, 1)
+        cref = ah @ bh.t()
+        tref = ah.abs() @ bh.abs().t()
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = old
+    err = (c_gpu.float() - cref).abs()
+    # the fp32 reference itself carries K * 2^-24 relative error of T
+    bound = TOL * tref + K * 2.0 ** -24 * tref
+    assert torch.isfinite(c_gpu.float()).all()
+    worst = (err / tref.clamp_min(1e-30)).max().item()
+    assert bool((err <= bound).all()), f"max |err|/T = {worst:.3e}"
+    return worst
+
+
+MODES = [("fp32", oracle.MODE_FP32), ("ue8m0", oracle.MODE_UE8M0)]
+
+
+def test_tiny_config(fgq, cuda_dev):
+    """A [128, 256], B [256, 128], N(0, 1), fp32 scales, fp32 C."""
+    a, b = fgq_inputs.tiny(seed=0)
+    host = _oracle_operands(a, b, oracle.MODE_FP32)
+    c = _run(fgq, _to_dev(*host, cuda_dev), torch.float32, "fp32")
+    _check_full(c, *host)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: m[0])
+def test_outlier_config(fgq, cuda_dev, mode):
+    """M = N = K = 1024, N(0, 1) with 0.1% of entries x100, fp32 C."""
+    a, b = fgq_inputs.outlier_gemm(1024, seed=0)
+    host = _oracle_operands(a, b, mode[1])
+    c = _run(fgq, _to_dev(*host, cuda_dev), torch.float32, mode[0])
+    _check_full(c, *host)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (17, 384, 256), (200, 128, 384),
+                                   (300, 640, 128), (129, 256, 1024)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_ragged_small(fgq, cuda_dev, M, N, K, out_dtype):
+    a = fgq_inputs.outlier((M, K), 1e-2, 100.0, seed=M)
+    b = fgq_inputs.normal((K, N), 0.02, seed=N)
+    host = _oracle_operands(a, b, oracle.MODE_FP32)
+    c = _run(fgq, _to_dev(*host, cuda_dev), out_dtype, "fp32")
+    _check_full(c, *host)
+
+
+@pytest.mark.parametrize("M", [2432, 2400])
+def test_wide_tile_path(fgq, cuda_dev, M):
+    """Enough tiles (>= one per SM) for the 128 x 256 tile configuration,
+    with a ragged last M tile; bf16 output into a padded C."""
+    N, K = 2048, 256
+    a = fgq_inputs.normal((M, K), 1.0, seed=1)
+    b = fgq_inputs.normal((K, N), 0.02, seed=2)
+    host = _oracle_operands(a, b, oracle.MODE_FP32)
+    out = torch.full((M, N + 64), float("nan"), dtype=torch.bfloat16, device=cuda_dev)[:, :N]
+    c = _run(fgq, _to_dev(*host, cuda_dev), torch.bfloat16, "fp32", out=out)
+    _check_full(c, *host)
+    pad = out.as_strided((M, 64), (N + 64, 1), storage_offset=N)
+    assert torch.isnan(pad.float()).all(), "GEMM wrote outside C's rows"
+
+
+def test_plain_c_abi_signature(fgq, cuda_dev):
+    """fgq_gemm_fp8_blockscaled(A, sA, B, sB, C, M, N, K, stream): fp32 out."""
+    from fine_grained_fp8_gb300 import _lib
+    a, b = fgq_inputs.tiny(seed=3)
+    host = _oracle_operands(a, b, oracle.MODE_FP32)
+    aq, sa, bq, sb = _to_dev(*host, cuda_dev)
+    c = torch.empty((128, 128), dtype=torch.float32, device=cuda_dev)
+    st = _lib.fgq_gemm_fp8_blockscaled(aq.data_ptr(), sa.data_ptr(), bq.data_ptr(), sb.data_ptr(),
+                                       c.data_ptr(), 128, 128, 256,
+                                       torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    _check_full(c, *host)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: m[0])
+def test_end_to_end_quantize_then_gemm(fgq, cuda_dev, mode):
+    """GPU quantizers feeding the GPU GEMM (the whole hot path)."""
+    a, b = fgq_inputs.outlier_gemm(512, seed=4)
+    aq, sa = fgq.quant_act_1x128(a.to(cuda_dev), mode[0])
+    bq, sb = fgq.quant_w_128x128(b.to(cuda_dev), mode[0])
+    c = _run(fgq, (aq, sa, bq, sb), torch.float32, mode[0])
+    host = _oracle_operands(a, b, mode[1])
+    _check_full(c, *host)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: m[0])
+def test_large_prefill_full_size(fgq, cuda_dev, mode):
+    """A [4096, 7168] N(0,1), B [7168, 7168] N(0,0.02^2), bf16 C, through the
+    GPU quantizers, in the configuration the benchmark times."""
+    a, b = fgq_inputs.large_prefill(seed=0)
+    aq, sa = fgq.quant_act_1x128(a.to(cuda_dev), mode[0])
+    bq, sb = fgq.quant_w_128x128(b.to(cuda_dev), mode[0])
+    c = _run(fgq, (aq, sa, bq, sb), torch.bfloat16, mode[0])
+    host = (aq.cpu().numpy(), sa.cpu().numpy(), np.ascontiguousarray(bq.cpu().numpy().T),
+            sb.cpu().numpy())
+    oq, osa = oracle.quant_act_1x128(a, mode[1])
+    assert np.array_equal(host[0], oq) and np.array_equal(host[1], osa)
+    _check_sampled(c, *host, n_samples=4000)
+    _check_full_vs_torch(c, (aq, sa, bq, sb))
+
+
+@pytest.mark.parametrize("M", [16, 64, 256])
+def test_skinny_full_size(fgq, cuda_dev, M):
+    """M x N=24576 x K=1536, bf16 C (the low-M path)."""
+    a, b = fgq_inputs.skinny(M, seed=0)
+    host = _oracle_operands(a, b, oracle.MODE_FP32)
+    ops = _to_dev(*host, cuda_dev)
+    c = _run(fgq, ops, torch.bfloat16, "fp32")
+    _check_sampled(c, *host, n_samples=4000, seed=M)
+    _check_full_vs_torch(c, ops)
+
+
+def test_repeat_calls_are_deterministic(fgq, cuda_dev):
+    a, b = fgq_inputs.outlier_gemm(1024, seed=5)
+    ops = _to_dev(*_oracle_operands(a, b, oracle.MODE_FP32), cuda_dev)
+    c1 = _run(fgq, ops, torch.float32, "fp32").clone()
+    c2 = _run(fgq, ops, torch.float32, "fp32")
+    assert torch.equal(c1, c2)
+
+
+def test_no_device_error_after_gemms(fgq, cuda_dev):
+    assert fgq.device_error() == 0
