@@ -1,0 +1,435 @@
+"""Benchmark of the fine-grained FP8 hot path on GB300.
+
+One step = the whole hot path on one batch of the large-prefill workload:
+  quantize A [4096, 7168] bf16 (1x128 tiles) -> quantize B [7168, 7168] bf16
+  (128x128 blocks) -> block-scaled FP8 GEMM -> C [4096, 7168] bf16.
+value = 2*M*N*K / (step time), in TFLOP/s, summed over ranks (weak scaling:
+every rank runs its own batch; the path has no exchange step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fgq|reference]
+
+--impl reference times the CPU oracle (the plain C restatement of the
+method) on a bounded sample of the same workload on this machine's host
+cores, extrapolated to the full step.
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "block-scaled FP8 GEMM TFLOP/s + quantize GB/s, % of GB300 roofline, 1 GPU"
+M_, N_, K_ = 4096, 7168, 7168
+WORKLOAD = "large_prefill: A bf16 [4096,7168] N(0,1), B bf16 [7168,7168] N(0,0.02^2); " \
+           "quantize A 1x128 + B 128x128 (E4M3, fp32 scales), block-scaled FP8 GEMM, bf16 C"
+
+# Algorithmic bytes / flops per launch (one unit = one launch on this workload).
+BYTES_QUANT_ACT = M_ * K_ * 2 + M_ * K_ + M_ * (K_ // 128) * 4           # read bf16, write e4m3 + scales
+BYTES_QUANT_W = K_ * N_ * 2 + K_ * N_ + (K_ // 128) * (N_ // 128) * 4
+FLOPS_GEMM = 2 * M_ * N_ * K_
+BYTES_GEMM = M_ * K_ + N_ * K_ + M_ * (K_ // 128) * 4 + (K_ // 128) * (N_ // 128) * 4 + M_ * N_ * 2
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _kernel_sha(name: str) -> str:
+    h = hashlib.sha256()
+    for f in (name, "fgq_device.cuh"):
+        with open(os.path.join(ROOT, "fine_grained_fp8_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel_key: str, source: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since those counters were taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        ent = t[kernel_key]
+        if ent.get("source_sha") != _kernel_sha(source):
+            return None
+        return ent["bytes_per_launch"]
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+# ---- clocks -----------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="fgq_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+        return False
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---- distributed plumbing ---------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(dist, value: float, device) -> float:
+    """Max of a per-rank float over all ranks (identity on one rank)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ---- CPU oracle arm -------------------------------------------------------------
+
+class OracleSample:
+    """The oracle on a bounded sample of one step of the workload.
+
+    Setup (untimed) draws the inputs and quantizes the full weight once so the
+    GEMM sample has valid operands.  A timed sample quantizes `rows_a`
+    activation rows and `blocks_w` 128x128 weight blocks, and computes
+    `outputs` GEMM outputs over the full K; each part is scaled linearly to
+    the full step."""
+
+    def __init__(self, seed: int = 0):
+        import numpy as np
+
+        import fgq_inputs
+        import oracle
+        self.np, self.oracle = np, oracle
+        self.a, self.b = fgq_inputs.large_prefill(seed=seed)
+        self.bq, self.sb = oracle.quant_w_128x128(self.b)
+
+    def step(self, rows_a: int, blocks_w: int, outputs: int, seed: int):
+        np, oracle = self.np, self.oracle
+        rng = np.random.default_rng(seed)
+        r0 = int(rng.integers(0, M_ - rows_a + 1))
+        t0 = time.perf_counter()
+        aq, sa = oracle.quant_act_1x128(self.a[r0:r0 + rows_a])
+        t1 = time.perf_counter()
+        for _ in range(blocks_w):
+            k0 = int(rng.integers(0, K_ // 128)) * 128
+            n0 = int(rng.integers(0, N_ // 128)) * 128
+            oracle.quant_w_128x128(self.b[k0:k0 + 128, n0:n0 + 128].contiguous())
+        t2 = time.perf_counter()
+        rows = rng.integers(0, rows_a, outputs)
+        cols = rng.integers(0, N_, outputs)
+        oracle.gemm_dequant_at(aq, sa, self.bq, self.sb, rows, cols)
+        t3 = time.perf_counter()
+        full = ((t1 - t0) * (M_ / rows_a) + (t2 - t1) * ((K_ // 128) * (N_ // 128) / blocks_w)
+                + (t3 - t2) * (M_ * N_ / outputs))
+        return full, t3 - t0
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    sampler = OracleSample(seed=0)
+    rows_a, blocks_w, outputs = 8, 2, 32
+    for i in range(args.warmup):
+        sampler.step(rows_a, blocks_w, outputs, seed=i)
+    fulls, own = [], 0.0
+    for i in range(args.steps):
+        f, s = sampler.step(rows_a, blocks_w, outputs, seed=1000 + i)
+        fulls.append(f)
+        own += s
+    step_s = sum(fulls) / len(fulls)
+    value = FLOPS_GEMM / step_s / 1e12
+    sample = (f"per step: quantize {rows_a}/{M_} activation rows and {blocks_w}/"
+              f"{(K_ // 128) * (N_ // 128)} weight blocks, {outputs} of {M_}x{N_} GEMM outputs "
+              f"(full K); each part scaled linearly to the full step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M_, "N": N_, "K": K_, "out": "bf16",
+                   "scale_mode": "fp32", "parallelism": f"replicas{world}",
+                   "sampled_seconds": own},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- GPU arm ---------------------------------------------------------------------
+
+def run_fgq(args):
+    import torch
+
+    import fgq_inputs
+    import fine_grained_fp8_gb300 as fgq
+    from fine_grained_fp8_gb300 import build as fbuild
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, os.environ.get("FGQ_BENCH_BACKEND", "nccl"))
+    if rank == 0 or not os.path.exists(fbuild.LIB_PATH):
+        fbuild.build()
+    barrier(dist)
+    fgq.load()
+
+    # Two input sets per rank, rotated, so every step reads inputs larger than
+    # L2 (A 58.7 MB + B 102.8 MB bf16 per set) that the previous step did not.
+    sets = []
+    host_sets = []
+    for i in range(2):
+        a, b = fgq_inputs.large_prefill(seed=100 * rank + 2 * i)
+        host_sets.append((a.pin_memory(), b.pin_memory()))
+        sets.append((a.to(dev), b.to(dev)))
+    aq = torch.empty((M_, K_), dtype=torch.uint8, device=dev)
+    sa = torch.empty((M_, K_ // 128), dtype=torch.float32, device=dev)
+    bq = torch.empty((N_, K_), dtype=torch.uint8, device=dev)
+    sb = torch.empty((K_ // 128, N_ // 128), dtype=torch.float32, device=dev)
+    c = torch.empty((M_, N_), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        a, b = sets[i % 2]
+        if ev is not None:
+            ev[0].record(stream)
+        fgq.quant_act_1x128(a, "fp32", xq=aq, sx=sa)
+        if ev is not None:
+            ev[1].record(stream)
+        fgq.quant_w_128x128(b, "fp32", wq=bq, sw=sb)
+        if ev is not None:
+            ev[2].record(stream)
+        fgq.gemm_fp8_blockscaled(aq, sa, bq, sb, torch.bfloat16, "fp32", out=c)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(dist)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            step(i, events[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+    clk = clocks.summary()
+    ms_total = start.elapsed_time(stop)
+    ms_total = reduce_max(dist, ms_total, dev)
+    ms_step = ms_total / args.steps
+    per = [[e[j].elapsed_time(e[j + 1]) for e in events] for j in range(3)]
+    us_act, us_w, us_gemm = (1e3 * sum(p) / len(p) for p in per)
+    if fgq.device_error() != 0:
+        raise SystemExit("a kernel reported a device wait timeout")
+
+    # e2e: the same step through the public API with host buffers; every step
+    # copies its inputs host -> device and reads C back into pinned memory.
+    e2e_steps = max(3, min(args.steps, 50))
+    c_host = torch.empty((M_, N_), dtype=torch.bfloat16).pin_memory()
+    a_dev = torch.empty((M_, K_), dtype=torch.bfloat16, device=dev)
+    b_dev = torch.empty((K_, N_), dtype=torch.bfloat16, device=dev)
+
+    def e2e_step(i):
+        ah, bh = host_sets[i % 2]
+        a_dev.copy_(ah, non_blocking=True)
+        b_dev.copy_(bh, non_blocking=True)
+        fgq.quant_act_1x128(a_dev, "fp32", xq=aq, sx=sa)
+        fgq.quant_w_128x128(b_dev, "fp32", wq=bq, sw=sb)
+        fgq.gemm_fp8_blockscaled(aq, sa, bq, sb, torch.bfloat16, "fp32", out=c)
+        c_host.copy_(c, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev) / e2e_steps
+
+    # CPU baseline: the oracle on a bounded sample, rank 0 only, N = 1 only.
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sampler = OracleSample(seed=0)
+        rows_a, blocks_w, outputs = 1024, 512, 12000
+        full_s, took = sampler.step(rows_a, blocks_w, outputs, seed=0)
+        cpu = {"value": FLOPS_GEMM / full_s / 1e12, "unit": "TFLOP/s", "cores": 1,
+               "kind": "oracle",
+               "sample": f"quantize {rows_a}/{M_} activation rows and {blocks_w}/"
+                         f"{(K_ // 128) * (N_ // 128)} weight blocks, {outputs} of {M_}x{N_} "
+                         f"GEMM outputs (full K), each scaled linearly to the full step; "
+                         f"{took:.1f} s of single-thread CPU work",
+               "full_step_s": full_s}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, src = _peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]  # nominal fp8 = 2x bf16 dense
+    hbm = peaks["hbm_gbs"]
+    gemm_tflops = FLOPS_GEMM / (us_gemm * 1e-6) / 1e12
+    act_gbs = BYTES_QUANT_ACT / (us_act * 1e-6) / 1e9
+    w_gbs = BYTES_QUANT_W / (us_w * 1e-6) / 1e9
+    value = world * FLOPS_GEMM / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M_, "N": N_, "K": K_, "out": "bf16",
+                   "scale_mode": "fp32", "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (two input sets rotated, 161 MB bf16 each)",
+                   "value_def": "2*M*N*K per step / step time (quantize A + quantize B + GEMM)"},
+        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
+                     "traffic": _traffic("gemm_fp8_blockscaled", "gemm.cu"),
+                     "kernel": "gemm_fp8_blockscaled_kernel",
+                     "peak_source": f"{src}: 2 x bf16_tflops_sustained (fp8 = 2x bf16 nominal)"},
+        "kernels": {
+            "quant_act_1x128": {"us": us_act, "GB/s": act_gbs, "frac_hbm": act_gbs / hbm,
+                                "bytes": BYTES_QUANT_ACT},
+            "quant_w_128x128": {"us": us_w, "GB/s": w_gbs, "frac_hbm": w_gbs / hbm,
+                                "bytes": BYTES_QUANT_W},
+            "gemm_fp8_blockscaled": {"us": us_gemm, "TFLOP/s": gemm_tflops,
+                                     "frac_fp8": gemm_tflops / fp8_peak, "flops": FLOPS_GEMM},
+            "hbm_peak_gbs": hbm, "peak_source": src,
+        },
+        "e2e": {"value": world * FLOPS_GEMM / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": (M_ * K_ + K_ * N_) * 2, "d2h_bytes_per_step": M_ * N_ * 2,
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["fgq", "reference"], default="fgq")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_fgq(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

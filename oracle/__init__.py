@@ -253,13 +253,20 @@ def gemm_bruteforce(aq, sa, bq, sb):
     return c
 
 
-def gemm_within_tolerance(c_gpu, c_ref, t_ref, rel: float = 2e-3):
-    """Elementwise |C - C_ref| <= rel * T; returns (ok, max |err| / T)."""
+def gemm_within_tolerance(c_gpu, c_ref, t_ref, rel: float = 2e-3, out_bf16: bool = False):
+    """Elementwise |C - C_ref| <= rel * T; returns (ok, max |err| / bound * rel).
+
+    The bound applies to the fp32 accumulator.  A bf16 output is that
+    accumulator rounded to nearest even, which adds at most half a bf16 ulp,
+    i.e. 2^-8 of its magnitude (|acc| <= |C_ref| + rel * T), so for bf16
+    outputs the bound is rel * T + 2^-8 * (|C_ref| + rel * T)."""
     c_gpu = np.asarray(c_gpu, dtype=np.float64)
     err = np.abs(c_gpu - c_ref)
     bound = rel * t_ref
+    if out_bf16:
+        bound = bound + 2.0 ** -8 * (np.abs(c_ref) + rel * t_ref)
     ok = bool(np.all(err <= bound)) and bool(np.all(np.isfinite(c_gpu)))
     with np.errstate(divide="ignore", invalid="ignore"):
-        ratio = np.where(t_ref > 0, err / np.where(t_ref > 0, t_ref, 1.0),
-                         np.where(err > 0, np.inf, 0.0))
+        ratio = np.where(bound > 0, err / np.where(bound > 0, bound, 1.0),
+                         np.where(err > 0, np.inf, 0.0)) * rel
     return ok, float(ratio.max()) if ratio.size else 0.0

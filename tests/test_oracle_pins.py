@@ -379,3 +379,11 @@ def test_tolerance_check_detects_errors():
     assert not ok
     ok, _ = oracle.gemm_within_tolerance(np.array([[np.nan, -2.0]]), c_ref, t)
     assert not ok
+    # bf16 output: the output rounding (2^-8 of the value) is added to the bound
+    c_ref = np.array([[100.0]]); t = np.array([[100.0]])
+    ok, _ = oracle.gemm_within_tolerance(c_ref + 0.2 + 0.39, c_ref, t, out_bf16=True)
+    assert ok
+    ok, _ = oracle.gemm_within_tolerance(c_ref + 0.2 + 0.41, c_ref, t, out_bf16=True)
+    assert not ok
+    ok, _ = oracle.gemm_within_tolerance(c_ref + 0.39, c_ref, t, out_bf16=False)
+    assert not ok
