@@ -13,11 +13,13 @@
 //   - Warp 1: one thread issues 4 tcgen05.mma (K = 32 each) per chunk into
 //     one of two TMEM partial buffers (128 lanes x BN fp32 columns each),
 //     then commits to the stage's "empty" and the buffer's "full" barriers.
-//   - Warps 2-9: epilogue.  Per chunk they read the partial from TMEM,
-//     multiply by sA[m,c] * sB[c, n/128] and add it into fp32 accumulators
-//     held in registers (the promotion step), release the TMEM buffer, and
-//     after the last chunk convert and store the tile.  Two TMEM buffers let
-//     the tensor core run chunk c+1 while chunk c is promoted.
+//   - Warps 4-11: epilogue.  Per chunk they read the partial from TMEM in
+//     32-column loads (the next load in flight while the current one is
+//     used), multiply by sA[m,c] * sB[c, n/128] and add it into fp32
+//     accumulators held in registers with packed f32x2 FMAs (the promotion
+//     step), hand the TMEM buffer back as soon as it is read, and after the
+//     last chunk convert and store the tile.  Two TMEM buffers let the
+//     tensor core run chunk c+1 while chunk c is promoted.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -33,8 +35,19 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 128;  // one scale chunk per pipeline stage
+// Warpgroup 0: warp 0 = TMA producer, warp 1 = MMA issuer (and TMEM owner),
+// warps 2-3 idle.  Warpgroups 1-2: eight epilogue warps, two per TMEM lane
+// quadrant.  Registers are moved from warpgroup 0 to the epilogue with
+// setmaxnreg: the launch gives every thread kLaunchRegs, warpgroup 0 drops
+// to kCtlRegs and the epilogue rises to kEpiRegs.
+constexpr int kCtlWarps = 4;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kThreads = 32 * (kCtlWarps + kEpiWarps);
+constexpr int kLaunchRegs = 168;  // 65536 / 384, rounded down to a multiple of 8
+constexpr uint32_t kCtlRegs = 56;
+constexpr uint32_t kEpiRegs = 224;
+static_assert(128 * kCtlRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 
 template <int BN, int STAGES>
 struct Cfg {
@@ -65,6 +78,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// acc[j] += comb * partial[j] for the 32 columns held in r (16 packed pairs).
+// (Called from fully unrolled loops, so j0 is a constant and acc stays in
+// registers.)
+template <int NACC>
+__device__ __forceinline__ void promote32(uint64_t (&acc)[NACC], const uint32_t (&r)[32],
+                                          uint64_t comb2, int j0) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) acc[j0 + j] = ffma2_acc(pack2(r[2 * j], r[2 * j + 1]), comb2, acc[j0 + j]);
+}
+
 template <int BN, int STAGES, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -72,6 +95,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const float* __restrict__ sA, const float* __restrict__ sB,
                                 void* __restrict__ C, int64_t ldc, int M, int N, int K) {
   using CF = Cfg<BN, STAGES>;
+  constexpr int HALF = BN / 2;     // columns per epilogue warp
+  constexpr int NLD = HALF / 32;   // 32-column TMEM loads per chunk
+  static_assert(NLD >= 2, "the load pipeline below assumes at least two loads per chunk");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -114,68 +140,71 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (elect_one_sync()) {
-      uint32_t it = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int tm = tile % m_tiles, tn = tile / m_tiles;
-        for (int kc = 0; kc < kchunks; ++kc, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, FGQ_DEVERR_PRODUCER_EMPTY)) {
-            ok = false;
-            break;
+  if (warp < kCtlWarps) {
+    setmaxnreg_dec<kCtlRegs>();
+    if (warp == 0) {
+      // ---------------- TMA producer ----------------
+      if (elect_one_sync()) {
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+          const int tm = tile % m_tiles, tn = tile / m_tiles;
+          for (int kc = 0; kc < kchunks; ++kc, ++it) {
+            const int s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1u;
+            if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, FGQ_DEVERR_PRODUCER_EMPTY)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[s], CF::kStageBytes);
+            tma_load_2d(sm_a + s * CF::kABytes, &tmap_a, &full[s], kc * BK, tm * BM);
+            tma_load_2d(sm_b + s * CF::kBBytes, &tmap_b, &full[s], kc * BK, tn * BN);
           }
-          mbar_arrive_expect_tx(&full[s], CF::kStageBytes);
-          tma_load_2d(sm_a + s * CF::kABytes, &tmap_a, &full[s], kc * BK, tm * BM);
-          tma_load_2d(sm_b + s * CF::kBBytes, &tmap_b, &full[s], kc * BK, tn * BN);
         }
+        // No copy may still target this CTA's shared memory when it exits.
+        const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
+        for (uint32_t j = first; j < it; ++j) mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1u);
       }
-      // No copy may still target this CTA's shared memory when it exits.
-      const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
-      for (uint32_t j = first; j < it; ++j) mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1u);
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (elect_one_sync()) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
-      uint32_t it = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        for (int kc = 0; kc < kchunks; ++kc, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1u;
-          const uint32_t buf = it & 1u, tph = (it >> 1) & 1u;
-          if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, FGQ_DEVERR_MMA_TMEM) ||
-              !mbar_wait(&full[s], ph, abort_flag, FGQ_DEVERR_MMA_FULL)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d = tmem_base + buf * BN;
-          const uint32_t a0 = smem_u32(sm_a + s * CF::kABytes);
-          const uint32_t b0 = smem_u32(sm_b + s * CF::kBBytes);
+      __syncwarp();
+    } else if (warp == 1) {
+      // ---------------- MMA issuer ----------------
+      if (elect_one_sync()) {
+        constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+          for (int kc = 0; kc < kchunks; ++kc, ++it) {
+            const int s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1u;
+            const uint32_t buf = it & 1u, tph = (it >> 1) & 1u;
+            if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, FGQ_DEVERR_MMA_TMEM) ||
+                !mbar_wait(&full[s], ph, abort_flag, FGQ_DEVERR_MMA_FULL)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem_base + buf * BN;
+            const uint32_t a0 = smem_u32(sm_a + s * CF::kABytes);
+            const uint32_t b0 = smem_u32(sm_b + s * CF::kBBytes);
 #pragma unroll
-          for (int kk = 0; kk < BK / 32; ++kk)
-            umma_f8f6f4(d, smem_desc_k_sw128(a0 + kk * 32), smem_desc_k_sw128(b0 + kk * 32), idesc,
-                        kk > 0 ? 1u : 0u);
-          umma_commit(&empty[s]);
-          umma_commit(&tfull[buf]);
+            for (int kk = 0; kk < BK / 32; ++kk)
+              umma_f8f6f4(d, smem_desc_k_sw128(a0 + kk * 32), smem_desc_k_sw128(b0 + kk * 32),
+                          idesc, kk > 0 ? 1u : 0u);
+            umma_commit(&empty[s]);
+            umma_commit(&tfull[buf]);
+          }
         }
+        // MMAs still in flight must finish before TMEM is released.
+        if (it > 0) mbar_wait_drain(&tfull[(it - 1) & 1u], ((it - 1) >> 1) & 1u);
       }
-      // MMAs still in flight must finish before TMEM is released.
-      if (it > 0) mbar_wait_drain(&tfull[(it - 1) & 1u], ((it - 1) >> 1) & 1u);
+      __syncwarp();
     }
-    __syncwarp();
   } else {
     // ---------------- epilogue: promotion + store ----------------
-    constexpr int HALF = BN / 2;  // columns per epilogue warp
-    const int ew = warp - 2;
-    const int quad = warp & 3;      // TMEM lanes this warp may access
-    const int half = ew >> 2;       // which half of the tile's columns
+    setmaxnreg_inc<kEpiRegs>();
+    const int ew = warp - kCtlWarps;
+    const int quad = warp & 3;   // TMEM lanes this warp may access
+    const int half = ew >> 2;    // which half of the tile's columns
     const int r_in_tile = quad * 32 + lane;
     const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
     uint32_t it = 0;
@@ -188,52 +217,82 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool cols_ok = col0 < N;
       const int nblk = cols_ok ? col0 / 128 : nb - 1;
       const float* sa_row = sA + static_cast<int64_t>(row_ok ? row : 0) * kchunks;
+      const float* sb_col = sB + nblk;
 
-      float acc[HALF];
+      uint64_t acc[HALF / 2];
 #pragma unroll
-      for (int j = 0; j < HALF; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < HALF / 2; ++j) acc[j] = 0ull;
 
+      float sa_next = row_ok ? __ldg(sa_row) : 0.0f;
+      float sb_next = __ldg(sb_col);
       for (int kc = 0; kc < kchunks; ++kc, ++it) {
         const uint32_t buf = it & 1u, tph = (it >> 1) & 1u;
-        const float sa = row_ok ? __ldg(sa_row + kc) : 0.0f;
-        const float sb = __ldg(sB + static_cast<int64_t>(kc) * nb + nblk);
-        const float comb = sa * sb;
+        const float comb = sa_next * sb_next;
+        if (kc + 1 < kchunks) {  // prefetch the next chunk's scales
+          sa_next = row_ok ? __ldg(sa_row + kc + 1) : 0.0f;
+          sb_next = __ldg(sb_col + static_cast<int64_t>(kc + 1) * nb);
+        }
+        const uint64_t comb2 = pack2(__float_as_uint(comb), __float_as_uint(comb));
         if (!mbar_wait(&tfull[buf], tph, abort_flag, FGQ_DEVERR_EPI_TMEM)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + t_lane + buf * BN + half * HALF;
+        uint32_t ra[32], rb[32];
+        tmem_ld_32x32b_x32(taddr, ra);
+        tmem_wait_ld_regs(ra);
 #pragma unroll
-        for (int j0 = 0; j0 < HALF; j0 += 16) {
-          uint32_t r[16];
-          tmem_ld_32x32b_x16(taddr + j0, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) acc[j0 + j] = fmaf(__uint_as_float(r[j]), comb, acc[j0 + j]);
+        for (int q = 0; q < NLD; ++q) {
+          if (q + 1 < NLD) {
+            if (q % 2 == 0)
+              tmem_ld_32x32b_x32(taddr + 32 * (q + 1), rb);
+            else
+              tmem_ld_32x32b_x32(taddr + 32 * (q + 1), ra);
+          } else {
+            // every column of this buffer is in registers: hand it back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[buf]);
+          }
+          if (q % 2 == 0)
+            promote32(acc, ra, comb2, 16 * q);
+          else
+            promote32(acc, rb, comb2, 16 * q);
+          if (q + 1 < NLD) {
+            if (q % 2 == 0)
+              tmem_wait_ld_regs(rb);
+            else
+              tmem_wait_ld_regs(ra);
+          }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[buf]);
       }
       if (!ok) break;
       if (row_ok && cols_ok) {
         if (OUT_BF16) {
           uint16_t* crow = static_cast<uint16_t*>(C) + static_cast<int64_t>(row) * ldc + col0;
 #pragma unroll
-          for (int j = 0; j < HALF; j += 8) {
+          for (int j = 0; j < HALF / 2; j += 4) {
             uint4 v;
-            v.x = pack_bf16x2(acc[j + 0], acc[j + 1]);
-            v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
-            v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
-            v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
-            *reinterpret_cast<uint4*>(crow + j) = v;
+            v.x = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(acc[j])),
+                              __uint_as_float(static_cast<uint32_t>(acc[j] >> 32)));
+            v.y = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(acc[j + 1])),
+                              __uint_as_float(static_cast<uint32_t>(acc[j + 1] >> 32)));
+            v.z = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(acc[j + 2])),
+                              __uint_as_float(static_cast<uint32_t>(acc[j + 2] >> 32)));
+            v.w = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(acc[j + 3])),
+                              __uint_as_float(static_cast<uint32_t>(acc[j + 3] >> 32)));
+            *reinterpret_cast<uint4*>(crow + 2 * j) = v;
           }
         } else {
           float* crow = static_cast<float*>(C) + static_cast<int64_t>(row) * ldc + col0;
 #pragma unroll
-          for (int j = 0; j < HALF; j += 4)
-            *reinterpret_cast<float4*>(crow + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+          for (int j = 0; j < HALF / 2; j += 2) {
+            uint4 v = make_uint4(static_cast<uint32_t>(acc[j]), static_cast<uint32_t>(acc[j] >> 32),
+                                 static_cast<uint32_t>(acc[j + 1]),
+                                 static_cast<uint32_t>(acc[j + 1] >> 32));
+            *reinterpret_cast<uint4*>(crow + 2 * j) = v;
+          }
         }
       }
     }
@@ -295,6 +354,16 @@ cudaError_t launch_cfg(const uint8_t* A, const float* sA, const uint8_t* B, cons
       attr_set[dev.device] = true;
     }
   }
+  // The setmaxnreg split assumes every thread is launched with kLaunchRegs
+  // registers; with fewer the epilogue's increase could never be granted.
+  static int launch_regs = -1;
+  if (launch_regs < 0) {
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    launch_regs = attr.numRegs;
+  }
+  if (launch_regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   CUtensorMap ta, tb;
   if (!make_operand_map(&ta, A, M, K, BM) || !make_operand_map(&tb, B, N, K, BN))
     return cudaErrorInvalidValue;

@@ -5,9 +5,25 @@
 // Both are HBM-bound streaming kernels.  Per group: amax of |x| (exact: the
 // magnitude order of non-NaN bf16 values is the order of their bit patterns
 // with the sign cleared, so it is taken with 16-bit SIMD integer max),
-// s = amax / 448 in fp32 (or its power-of-two ceiling), then each element is
-// divided by s in IEEE fp32 and rounded to E4M3 by the hardware convert
-// (round to nearest even, saturating to +-448).
+// s = amax / 448 in fp32 (or its power-of-two ceiling), then each element
+// becomes E4M3(fl32(x / s)) through the hardware convert (round to nearest
+// even, saturating to +-448).
+//
+// The quotient fl32(x / s) is formed without a per-element division:
+//   r  = RN(1 / s)                      (once per group)
+//   q0 = RN(x * r)
+//   q1 = RN(q0 + r * RN(x - q0 * s))    (both steps fused multiply-adds)
+// which is Markstein's correction of a reciprocal-based quotient (P.
+// Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990).  For the operands these
+// kernels can see -- x a bf16 value with |x| <= amax, s = RN(amax / 448)
+// with amax a bf16 value and s >= 2^-100 -- E4M3(q1) equals E4M3(x / s)
+// for every pair, signs aside (the residual step turns -0 into +0, so the
+// sign bit of every code is taken from x).  This was checked exhaustively
+// over all 1.07e9 such (amax, x) bf16 pairs against IEEE division, and the
+// GPU tests compare every bf16 pattern against the oracle.  Groups with
+// s < 2^-100 (amax below about 2^-91) take IEEE division instead.  In UE8M0
+// mode s = 2^e and x * 2^-e is exact, so a single multiply is used.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -47,47 +63,109 @@ __device__ __forceinline__ uint32_t absmax_pairs(uint4 v) {
   return __vmaxu2(a, b);
 }
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Dequantisation multiplier of a group from the bit pattern of its amax
-// (a non-negative bf16 magnitude widened to fp32).
-template <int MODE>
-__device__ __forceinline__ float scale_from_amax(float amax) {
-  if (amax == 0.0f) return 1.0f;
-  float t = __fdiv_rn(amax, 448.0f);
-  if (MODE == kScaleFp32) return t;
-  // Smallest power of two >= t, exponent clamped at -127 (t < 2^120 always).
-  uint32_t b = __float_as_uint(t);
-  uint32_t e = b >> 23, man = b & 0x7FFFFFu;
-  if (e == 0) return __uint_as_float(b <= 0x00400000u ? 0x00400000u : 0x00800000u);
-  return __uint_as_float((man != 0 ? e + 1 : e) << 23);
+__device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-// q = E4M3(x / s) for the 8 bf16 of v, packed little-endian into 8 bytes.
-// fp32 mode divides (IEEE, round to nearest even).  In UE8M0 mode s = 2^e
-// and inv = 2^-e exactly, so x * inv rounds exactly like x / s.
+// Packed fp32 pair arithmetic (one instruction for two lanes of data).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 d;
+  asm("{.reg .b64 A, B, D;\n\t"
+      "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\t"
+      "mul.rn.f32x2 D, A, B;\n\tmov.b64 {%0, %1}, D;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{.reg .b64 A, B, C, D;\n\t"
+      "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\tmov.b64 C, {%6, %7};\n\t"
+      "fma.rn.f32x2 D, A, B, C;\n\tmov.b64 {%0, %1}, D;}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// Per-group constants of the encode step.
+struct GroupScale {
+  float s;       // dequantisation multiplier written to the scale tensor
+  float2 r2;     // {RN(1/s), RN(1/s)} (fp32 mode) or {2^-e, 2^-e} (UE8M0)
+  float2 ns2;    // {-s, -s}
+  bool exact;    // fp32 mode with s < 2^-100: use IEEE division
+};
+
 template <int MODE>
-__device__ __forceinline__ uint2 encode8(uint4 v, float s, float inv) {
-  float f[8] = {bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y),
-                bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w)};
+__device__ __forceinline__ GroupScale group_scale(uint32_t mag_bits) {
+  GroupScale g;
+  const float amax = __uint_as_float(mag_bits << 16);
+  float s;
+  if (amax == 0.0f) {
+    s = 1.0f;
+  } else {
+    const float t = __fdiv_rn(amax, 448.0f);
+    if (MODE == kScaleFp32) {
+      s = t;
+    } else {
+      // smallest power of two >= t, exponent clamped at -127 (t < 2^120)
+      const uint32_t b = __float_as_uint(t);
+      const uint32_t e = b >> 23, man = b & 0x7FFFFFu;
+      if (e == 0)
+        s = __uint_as_float(b <= 0x00400000u ? 0x00400000u : 0x00800000u);
+      else
+        s = __uint_as_float((man != 0 ? e + 1 : e) << 23);
+    }
+  }
+  const float r = __frcp_rn(s);  // exact for powers of two
+  g.s = s;
+  g.r2 = make_float2(r, r);
+  g.ns2 = make_float2(-s, -s);
+  g.exact = (MODE == kScaleFp32) && !(s >= 0x1p-100f);
+  return g;
+}
+
+// Codes of the 8 bf16 of v, little-endian in 8 bytes: E4M3(fl32(x / s)).
+template <int MODE>
+__device__ __forceinline__ uint2 encode8(uint4 v, const GroupScale& g) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t c[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) f[i] = (MODE == kScaleFp32) ? __fdiv_rn(f[i], s) : __fmul_rn(f[i], inv);
+  for (int p = 0; p < 4; ++p) {
+    const float2 x = bf16x2_to_f32x2(w[p]);
+    float2 q;
+    if (MODE == kScaleUe8m0) {
+      q = mul2(x, g.r2);
+    } else if (!g.exact) {
+      const float2 q0 = mul2(x, g.r2);
+      const float2 d = fma2(q0, g.ns2, x);  // x - q0 * s, exact
+      q = fma2(d, g.r2, q0);
+    } else {
+      q = make_float2(__fdiv_rn(x.x, g.s), __fdiv_rn(x.y, g.s));
+    }
+    c[p] = cvt_e4m3x2(q.x, q.y);
+  }
+  // Sign bit of each code from the sign of its bf16 input (bytes 1 and 3 of
+  // each input word carry the signs of its two elements).
+  const uint32_t s01 = __byte_perm(v.x, v.y, 0x7531) & 0x80808080u;
+  const uint32_t s23 = __byte_perm(v.z, v.w, 0x7531) & 0x80808080u;
   uint2 r;
-  r.x = cvt_e4m3x2(f[0], f[1]) | (cvt_e4m3x2(f[2], f[3]) << 16);
-  r.y = cvt_e4m3x2(f[4], f[5]) | (cvt_e4m3x2(f[6], f[7]) << 16);
+  r.x = __byte_perm(c[0], c[1], 0x5410) | s01;
+  r.y = __byte_perm(c[2], c[3], 0x5410) | s23;
   return r;
 }
 
 // ---- 1x128 activation quantizer ----------------------------------------------
 //
-// A half-warp owns one 128-element group: lane l of the half loads bytes
-// [16 l, 16 l + 16) of the group's 256.  The two halves of a warp take
-// adjacent groups, so each warp load covers 512 contiguous bytes of a dense
-// row.  Each warp first issues UNROLL pairs of group loads, then reduces and
-// encodes them, keeping 16 * UNROLL bytes per lane in flight.
+// Eight lanes own one 128-element (256-byte) group: lane l of the eight loads
+// bytes [16 l, 16 l + 16) and [128 + 16 l, 128 + 16 l + 16), so each warp
+// load instruction covers two full 128-byte lines of each of its four
+// groups.  A warp first issues the loads of kActRounds rounds (4 groups
+// each), then reduces and encodes them: 16 * 2 * kActRounds bytes per lane
+// in flight.
 constexpr int kActThreads = 256;
-constexpr int kActUnroll = 4;
+constexpr int kActRounds = 2;
+constexpr int kActGroupsPerWarp = 4 * kActRounds;
 
 template <int MODE, bool DENSE>
 __global__ void __launch_bounds__(kActThreads)
@@ -95,49 +173,49 @@ __global__ void __launch_bounds__(kActThreads)
                            int64_t ldx, uint8_t* __restrict__ xq, int64_t ldq,
                            float* __restrict__ sx) {
   const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t half = lane >> 4, l16 = lane & 15u;
+  const uint32_t sub = lane >> 3, l8 = lane & 7u;
   const uint32_t warp = (blockIdx.x * kActThreads + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * kActThreads) >> 5;
 
-  for (uint32_t base = warp * (2 * kActUnroll); base < groups;
-       base += nwarps * (2 * kActUnroll)) {
-    uint4 v[kActUnroll];
-    uint32_t g[kActUnroll];
+  for (uint32_t base = warp * kActGroupsPerWarp; base < groups;
+       base += nwarps * kActGroupsPerWarp) {
+    uint4 v[kActRounds][2];
+    uint32_t g[kActRounds];
 #pragma unroll
-    for (int u = 0; u < kActUnroll; ++u) {
-      g[u] = base + 2 * u + half;
-      v[u] = make_uint4(0, 0, 0, 0);
+    for (int u = 0; u < kActRounds; ++u) {
+      g[u] = base + 4 * u + sub;
+      v[u][0] = v[u][1] = make_uint4(0, 0, 0, 0);
       if (g[u] < groups) {
         const uint16_t* src;
         if (DENSE) {
-          src = x + static_cast<uint64_t>(g[u]) * 128 + l16 * 8;
+          src = x + static_cast<uint64_t>(g[u]) * 128;
         } else {
-          uint32_t m = g[u] / kc, c = g[u] - m * kc;
-          src = x + static_cast<int64_t>(m) * ldx + c * 128 + l16 * 8;
+          const uint32_t m = g[u] / kc, c = g[u] - m * kc;
+          src = x + static_cast<int64_t>(m) * ldx + c * 128;
         }
-        v[u] = ld_stream_16(src);
+        v[u][0] = ld_stream_16(src + 8 * l8);
+        v[u][1] = ld_stream_16(src + 64 + 8 * l8);
       }
     }
 #pragma unroll
-    for (int u = 0; u < kActUnroll; ++u) {
-      uint32_t mx = absmax_pairs(v[u]);
+    for (int u = 0; u < kActRounds; ++u) {
+      uint32_t mx = __vmaxu2(absmax_pairs(v[u][0]), absmax_pairs(v[u][1]));
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1) mx = __vmaxu2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
-      uint32_t mag = max(mx & 0xFFFFu, mx >> 16);
-      float amax = __uint_as_float(mag << 16);
-      float s = scale_from_amax<MODE>(amax);
-      float inv = (MODE == kScaleFp32) ? 0.0f : __fdiv_rn(1.0f, s);  // exact for 2^e
+      for (int off = 4; off > 0; off >>= 1) mx = __vmaxu2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+      const GroupScale gs = group_scale<MODE>(max(mx & 0xFFFFu, mx >> 16));
       if (g[u] < groups) {
-        uint2 q = encode8<MODE>(v[u], s, inv);
+        const uint2 q0 = encode8<MODE>(v[u][0], gs);
+        const uint2 q1 = encode8<MODE>(v[u][1], gs);
         uint8_t* dst;
         if (DENSE) {
-          dst = xq + static_cast<uint64_t>(g[u]) * 128 + l16 * 8;
+          dst = xq + static_cast<uint64_t>(g[u]) * 128;
         } else {
-          uint32_t m = g[u] / kc, c = g[u] - m * kc;
-          dst = xq + static_cast<int64_t>(m) * ldq + c * 128 + l16 * 8;
+          const uint32_t m = g[u] / kc, c = g[u] - m * kc;
+          dst = xq + static_cast<int64_t>(m) * ldq + c * 128;
         }
-        st_stream_8(dst, q);
-        if (l16 == 0) sx[g[u]] = s;
+        st_stream_8(dst + 8 * l8, q0);
+        st_stream_8(dst + 64 + 8 * l8, q1);
+        if (l8 == 0) sx[g[u]] = gs.s;
       }
     }
   }
@@ -182,15 +260,13 @@ __global__ void __launch_bounds__(kWThreads)
   uint32_t mag = 0;
 #pragma unroll
   for (int i = 0; i < kWThreads / 32; ++i) mag = max(mag, warp_max[i]);
-  const float amax = __uint_as_float(mag << 16);
-  const float s = scale_from_amax<MODE>(amax);
-  const float inv = (MODE == kScaleFp32) ? 0.0f : __fdiv_rn(1.0f, s);
+  const GroupScale gs = group_scale<MODE>(mag);
 
   // Encode: for column j of the chunk, the 8 rows give 8 consecutive k codes.
   uint32_t codes[8][2];  // [row i][lo: cols 0-3, hi: cols 4-7]
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    uint2 q = encode8<MODE>(v[i], s, inv);
+    const uint2 q = encode8<MODE>(v[i], gs);
     codes[i][0] = q.x;
     codes[i][1] = q.y;
   }
@@ -204,7 +280,7 @@ __global__ void __launch_bounds__(kWThreads)
     const int n = 8 * c + j;
     tile[n * 16 + (rg ^ c)] = make_uint2(lo, hi);
   }
-  if (t == 0) sw[static_cast<int64_t>(kb) * nb_count + nb] = s;
+  if (t == 0) sw[static_cast<int64_t>(kb) * nb_count + nb] = gs.s;
   __syncthreads();
 
   const uint4* tile16 = reinterpret_cast<const uint4*>(tile);
@@ -212,10 +288,10 @@ __global__ void __launch_bounds__(kWThreads)
   for (int p = 0; p < 4; ++p) {
     const int idx = p * kWThreads + t;
     const int n = idx >> 3, q = idx & 7;
-    const int sw_ = (n >> 3) & 15;
+    const int swz = (n >> 3) & 15;
     uint4 val = tile16[n * 8 + q];
-    if (sw_ & 1) val = make_uint4(val.z, val.w, val.x, val.y);
-    uint8_t* dst = wq + (n0 + n) * K + k0 + 16 * (q ^ (sw_ >> 1));
+    if (swz & 1) val = make_uint4(val.z, val.w, val.x, val.y);
+    uint8_t* dst = wq + (n0 + n) * K + k0 + 16 * (q ^ (swz >> 1));
     st_stream_16(dst, val);
   }
 }
@@ -229,7 +305,7 @@ cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t 
   const uint32_t groups = static_cast<uint32_t>(M * (K / 128));
   if (groups == 0) return cudaSuccess;
   const bool dense = (ldx == K) && (ldq == K);
-  const uint32_t groups_per_block = (kActThreads / 32) * 2 * kActUnroll;
+  const uint32_t groups_per_block = (kActThreads / 32) * kActGroupsPerWarp;
   const uint32_t needed = (groups + groups_per_block - 1) / groups_per_block;
 
   using Kern = void (*)(const uint16_t*, uint32_t, uint32_t, int64_t, uint8_t*, int64_t, float*);

@@ -119,6 +119,35 @@ def test_act_every_bf16_pattern(fgq, cuda_dev, mode):
     _assert_act_parity(fgq, xs, mode, cuda_dev)
 
 
+def _every_x_below_amax(exponents):
+    """Groups [amax, x1 .. x127]: for each bf16 amax with one of the given
+    exponent fields and each of the 128 significands, every bf16 x with
+    |x| <= amax, both signs, spread over as many groups as needed."""
+    rows = []
+    for e in exponents:
+        for ma in range(128):
+            amax = (e << 7) | ma
+            mags = np.arange(0, amax + 1, dtype=np.uint32)
+            xs = np.concatenate([mags, mags | 0x8000]).astype(np.uint16)
+            pad = (-len(xs)) % 127
+            xs = np.concatenate([xs, np.zeros(pad, np.uint16)]).reshape(-1, 127)
+            head = np.full((xs.shape[0], 1), amax, np.uint16)
+            rows.append(np.concatenate([head, xs], axis=1))
+    bits = np.concatenate(rows)
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: m[0])
+@pytest.mark.parametrize("exponent", [250, 127, 36, 35, 34, 1])
+def test_act_every_x_for_every_amax_significand(fgq, cuda_dev, mode, exponent):
+    """Within a group only amax's significand (128 values) and exponent fix
+    the scale, so this covers every reachable (scale, x) pair of that amax
+    binade: huge, ordinary, both sides of the 2^-100 scale boundary where
+    the kernel switches to IEEE division, and the smallest normal binade."""
+    x = _every_x_below_amax([exponent])
+    _assert_act_parity(fgq, x, mode, cuda_dev)
+
+
 @pytest.mark.parametrize("mode", MODES, ids=lambda m: m[0])
 @pytest.mark.parametrize("M,K", [(1, 128), (3, 256), (129, 640), (1000, 1024), (77, 7168),
                                  (4096, 384)])
