@@ -5,7 +5,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/fgq.h"
+#include "fgq.h"
 #include "fgq_internal.h"
 
 namespace fgq {
