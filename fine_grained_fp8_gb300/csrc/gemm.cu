@@ -6,8 +6,11 @@
 //
 // Design (GB300-native; the page's Hopper promotion loop is prior art):
 //   - Persistent CTAs, one per SM, walking output tiles of 128 x BN with a
-//     static stride-gridDim schedule ("Persistent kernel (grid = SM count,
-//     internal tile loop)", linear scheduler, M fastest).
+//     static stride schedule ("Persistent kernel (grid = SM count, internal
+//     tile loop)", linear scheduler, M fastest).  For 128 x 256 tiles the
+//     CTAs run in clusters of two along M that share each B tile: each CTA
+//     loads its own A tile and half of B, multicast into both CTAs, which
+//     cuts L2-to-SMEM operand traffic per SM by a third.
 //   - Warp 0: TMA producer.  Each stage holds one 128-wide K chunk of A
 //     (128 x 128 bytes) and B (BN x 128 bytes), 128-byte swizzled.
 //   - Warp 1: one thread issues 4 tcgen05.mma (K = 32 each) per chunk into
@@ -88,7 +91,29 @@ __device__ __forceinline__ void promote32(uint64_t (&acc)[NACC], const uint32_t 
   for (int j = 0; j < 16; ++j) acc[j0 + j] = ffma2_acc(pack2(r[2 * j], r[2 * j + 1]), comb2, acc[j0 + j]);
 }
 
-template <int BN, int STAGES, bool OUT_BF16>
+// Static persistent schedule over work units.  A unit is CM output tiles
+// stacked along M that share one B tile (CM = 2: the two CTAs of a cluster,
+// rank r taking tile row CM * g + r).  Units are walked M-fastest with stride
+// = number of clusters, so all roles of all CTAs agree on the order.
+template <int CM>
+struct TileSched {
+  int m_groups, n_tiles, total, first, stride, rank;
+  __device__ __forceinline__ TileSched(int M, int N, int bn) {
+    const int m_tiles = (M + BM - 1) / BM;
+    m_groups = (m_tiles + CM - 1) / CM;
+    n_tiles = (N + bn - 1) / bn;
+    total = m_groups * n_tiles;
+    rank = CM == 1 ? 0 : static_cast<int>(cluster_ctarank());
+    first = static_cast<int>(blockIdx.x) / CM;
+    stride = static_cast<int>(gridDim.x) / CM;
+  }
+  __device__ __forceinline__ void tile(int u, int& tm, int& tn) const {
+    tm = (u % m_groups) * CM + rank;
+    tn = u / m_groups;
+  }
+};
+
+template <int BN, int STAGES, int CM, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                 const __grid_constant__ CUtensorMap tmap_b,
@@ -110,17 +135,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  static_assert(CM == 1 || CM == 2, "clusters of one or two CTAs along M");
+  constexpr uint16_t kPeers = (1u << CM) - 1;  // multicast mask: every CTA of the cluster
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tiles = (M + BM - 1) / BM;
-  const int n_tiles = (N + BN - 1) / BN;
-  const int num_tiles = m_tiles * n_tiles;
+  const TileSched<CM> sched(M, N, BN);
   const int kchunks = K / BK;
   const int nb = N / 128;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CM);  // one MMA commit from each CTA sharing the stage's B
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -136,7 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if (CM > 1)
+    cluster_sync();  // the peer's barriers exist before any multicast targets them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -147,8 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (elect_one_sync()) {
         uint32_t it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-          const int tm = tile % m_tiles, tn = tile / m_tiles;
+        for (int u = sched.first; u < sched.total && ok; u += sched.stride) {
+          int tm, tn;
+          sched.tile(u, tm, tn);
           for (int kc = 0; kc < kchunks; ++kc, ++it) {
             const int s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1u;
@@ -158,12 +187,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mbar_arrive_expect_tx(&full[s], CF::kStageBytes);
             tma_load_2d(sm_a + s * CF::kABytes, &tmap_a, &full[s], kc * BK, tm * BM);
-            tma_load_2d(sm_b + s * CF::kBBytes, &tmap_b, &full[s], kc * BK, tn * BN);
+            if (CM == 1) {
+              tma_load_2d(sm_b + s * CF::kBBytes, &tmap_b, &full[s], kc * BK, tn * BN);
+            } else {
+              // this CTA's half of the shared B tile, written into both CTAs
+              constexpr int kHalfRows = BN / CM;
+              tma_load_2d_multicast(sm_b + s * CF::kBBytes + sched.rank * kHalfRows * BK, &tmap_b,
+                                    &full[s], kc * BK, tn * BN + sched.rank * kHalfRows, kPeers);
+            }
           }
         }
-        // No copy may still target this CTA's shared memory when it exits.
+        // No copy may still target this CTA's shared memory, and no MMA
+        // commit may still be on its way to its barriers, when it exits.
         const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
-        for (uint32_t j = first; j < it; ++j) mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1u);
+        for (uint32_t j = first; j < it; ++j) {
+          mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1u);
+          mbar_wait_drain(&empty[j % STAGES], (j / STAGES) & 1u);
+        }
       }
       __syncwarp();
     } else if (warp == 1) {
@@ -172,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
         uint32_t it = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        for (int u = sched.first; u < sched.total && ok; u += sched.stride) {
           for (int kc = 0; kc < kchunks; ++kc, ++it) {
             const int s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1u;
@@ -190,7 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < BK / 32; ++kk)
               umma_f8f6f4(d, smem_desc_k_sw128(a0 + kk * 32), smem_desc_k_sw128(b0 + kk * 32),
                           idesc, kk > 0 ? 1u : 0u);
-            umma_commit(&empty[s]);
+            if (CM == 1)
+              umma_commit(&empty[s]);
+            else
+              umma_commit_multicast(&empty[s], kPeers);  // both CTAs wrote this stage's B
             umma_commit(&tfull[buf]);
           }
         }
@@ -209,8 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
     uint32_t it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-      const int tm = tile % m_tiles, tn = tile / m_tiles;
+    for (int u = sched.first; u < sched.total && ok; u += sched.stride) {
+      int tm, tn;
+      sched.tile(u, tm, tn);
       const int row = tm * BM + r_in_tile;
       const bool row_ok = row < M;
       const int col0 = tn * BN + half * HALF;
@@ -233,7 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           sb_next = __ldg(sb_col + static_cast<int64_t>(kc + 1) * nb);
         }
         const uint64_t comb2 = pack2(__float_as_uint(comb), __float_as_uint(comb));
-        if (!mbar_wait(&tfull[buf], tph, abort_flag, FGQ_DEVERR_EPI_TMEM)) {
+        // warp-uniform outcome: the TMEM loads below are warp-collective
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull[buf], tph, abort_flag, FGQ_DEVERR_EPI_TMEM))) {
           ok = false;
           break;
         }
@@ -298,8 +343,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  if (CM > 1)
+    cluster_sync();  // neither CTA leaves while its peer may still reach its memory
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, CF::kTmemCols);
@@ -337,40 +386,59 @@ bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, bool OUT_BF16>
+template <int BN, int STAGES, int CM, bool OUT_BF16>
 cudaError_t launch_cfg(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                        void* C, int64_t ldc, int M, int N, int K, cudaStream_t stream,
                        const DeviceInfo& dev) {
   using CF = Cfg<BN, STAGES>;
-  auto kern = gemm_fp8_blockscaled_kernel<BN, STAGES, OUT_BF16>;
-  static bool attr_set[64] = {};
+  auto kern = gemm_fp8_blockscaled_kernel<BN, STAGES, CM, OUT_BF16>;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CM;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = CF::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+
+  // Per device: shared-memory opt-in, the launch register count the
+  // setmaxnreg split assumes, and how many clusters fit at once.
   static std::mutex mu;
+  static int max_clusters[64] = {};
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (dev.device < 64 && !attr_set[dev.device]) {
+    if (dev.device >= 64) return cudaErrorInvalidDevice;
+    if (max_clusters[dev.device] == 0) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(CF::kSmemBytes));
       if (e != cudaSuccess) return e;
-      attr_set[dev.device] = true;
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      // With fewer registers per thread than kLaunchRegs the epilogue's
+      // setmaxnreg increase could never be granted: refuse to launch.
+      if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+      int n = dev.sm_count / CM;
+      if (CM > 1) {
+        cfg.gridDim = dim3(CM * n);
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+      }
+      max_clusters[dev.device] = n;
     }
   }
-  // The setmaxnreg split assumes every thread is launched with kLaunchRegs
-  // registers; with fewer the epilogue's increase could never be granted.
-  static int launch_regs = -1;
-  if (launch_regs < 0) {
-    cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, kern);
-    if (e != cudaSuccess) return e;
-    launch_regs = attr.numRegs;
-  }
-  if (launch_regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, A, M, K, BM) || !make_operand_map(&tb, B, N, K, BN))
+  if (!make_operand_map(&ta, A, M, K, BM) || !make_operand_map(&tb, B, N, K, BN / CM))
     return cudaErrorInvalidValue;
-  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
-  kern<<<grid, kThreads, CF::kSmemBytes, stream>>>(ta, tb, sA, sB, C, ldc, M, N, K);
-  return cudaGetLastError();
+  const int m_groups = ((M + BM - 1) / BM + CM - 1) / CM;
+  const int units = m_groups * ((N + BN - 1) / BN);
+  const int clusters = units < max_clusters[dev.device] ? units : max_clusters[dev.device];
+  cfg.gridDim = dim3(CM * clusters);
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, sA, sB, C, ldc, M, N, K);
 }
 
 }  // namespace
@@ -382,14 +450,17 @@ cudaError_t launch_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const
   (void)mode;  // power-of-two scales take the same promotion path (exact products)
   if (M == 0 || N == 0) return cudaSuccess;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  const int64_t tiles256 = ((M + BM - 1) / BM) * ((N + 255) / 256);
-  const bool wide = (N % 256 == 0) && tiles256 >= dev.sm_count;
+  // 128 x 256 tiles, pairs of CTAs along M sharing each B tile, when there
+  // are enough of them to fill the GPU; 128 x 128 single-CTA tiles otherwise.
+  const int64_t m_tiles = (M + BM - 1) / BM;
+  const int64_t pairs256 = ((m_tiles + 1) / 2) * ((N + 255) / 256);
+  const bool wide = (N % 256 == 0) && m_tiles >= 2 && 2 * pairs256 >= dev.sm_count;
   if (out_bf16) {
-    return wide ? launch_cfg<256, 4, true>(A, sA, B, sB, C, ldc, m, n, k, stream, dev)
-                : launch_cfg<128, 6, true>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
+    return wide ? launch_cfg<256, 4, 2, true>(A, sA, B, sB, C, ldc, m, n, k, stream, dev)
+                : launch_cfg<128, 6, 1, true>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
   }
-  return wide ? launch_cfg<256, 4, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev)
-              : launch_cfg<128, 6, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
+  return wide ? launch_cfg<256, 4, 2, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev)
+              : launch_cfg<128, 6, 1, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
 }
 
 cudaError_t read_device_error(uint32_t* word, bool clear) {
