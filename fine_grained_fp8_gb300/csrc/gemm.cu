@@ -7,10 +7,13 @@
 // Design (GB300-native; the page's Hopper promotion loop is prior art):
 //   - Persistent CTAs, one per SM, walking output tiles of 128 x BN with a
 //     static stride schedule ("Persistent kernel (grid = SM count, internal
-//     tile loop)", linear scheduler, M fastest).  For 128 x 256 tiles the
-//     CTAs run in clusters of two along M that share each B tile: each CTA
-//     loads its own A tile and half of B, multicast into both CTAs, which
-//     cuts L2-to-SMEM operand traffic per SM by a third.
+//     tile loop)", linear scheduler, M fastest).  Large problems run on CTA
+//     pairs (clusters of two) with tcgen05.mma.cta_group::2: one 256 x 256
+//     MMA tile per pair, each CTA holding 128 rows of A and 128 rows of B per
+//     stage and receiving its 128 output rows in its own TMEM.  The tensor
+//     core reads the peer's operands directly, so each SM fills 32 KB of
+//     shared memory per K chunk instead of 48 KB, which is what bounds the
+//     single-CTA 128 x 256 tile.
 //   - Warp 0: TMA producer.  Each stage holds one 128-wide K chunk of A
 //     (128 x 128 bytes) and B (BN x 128 bytes), 128-byte swizzled.
 //   - Warp 1: one thread issues 4 tcgen05.mma (K = 32 each) per chunk into
@@ -52,15 +55,21 @@ constexpr uint32_t kEpiRegs = 224;
 static_assert(128 * kCtlRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 
-template <int BN, int STAGES>
+// BN: output columns of a tile (and the MMA's N).  CG: CTAs per MMA (1, or 2
+// for the paired tcgen05.mma.cta_group::2, whose 256 x BN tile is split so
+// that each CTA holds 128 rows of A and BN/2 rows of B per stage and
+// receives its own 128 rows of the result in its TMEM).
+template <int BN, int STAGES, int CG>
 struct Cfg {
   static constexpr int kABytes = BM * BK;
-  static constexpr int kBBytes = BN * BK;
-  static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kTmemCols = 2 * BN;  // two partial buffers
+  static constexpr int kBBytes = (BN / CG) * BK;
+  static constexpr int kStageBytes = kABytes + kBBytes;      // per CTA
+  static constexpr uint32_t kTxBytes = CG * kStageBytes;     // per stage of the MMA
+  static constexpr int kTmemCols = 2 * BN;                   // two partial buffers
   static constexpr int kBarBytes = (2 * STAGES + 4) * 8 + 16;
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes;
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of 2");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 // Bounded wait used while unwinding; ignores the abort flag.
@@ -91,38 +100,40 @@ __device__ __forceinline__ void promote32(uint64_t (&acc)[NACC], const uint32_t 
   for (int j = 0; j < 16; ++j) acc[j0 + j] = ffma2_acc(pack2(r[2 * j], r[2 * j + 1]), comb2, acc[j0 + j]);
 }
 
-// Static persistent schedule over work units.  A unit is CM output tiles
-// stacked along M that share one B tile (CM = 2: the two CTAs of a cluster,
-// rank r taking tile row CM * g + r).  Units are walked M-fastest with stride
-// = number of clusters, so all roles of all CTAs agree on the order.
-template <int CM>
+// Static persistent schedule over work units.  A unit is the CG stacked
+// 128-row tiles one MMA covers (CG = 2: the two CTAs of a cluster, rank r
+// taking tile row CG * g + r).  Units are walked M-fastest with stride = the
+// number of MMA groups, so all roles of all CTAs agree on the order.
+template <int CG>
 struct TileSched {
   int m_groups, n_tiles, total, first, stride, rank;
   __device__ __forceinline__ TileSched(int M, int N, int bn) {
     const int m_tiles = (M + BM - 1) / BM;
-    m_groups = (m_tiles + CM - 1) / CM;
+    m_groups = (m_tiles + CG - 1) / CG;
     n_tiles = (N + bn - 1) / bn;
     total = m_groups * n_tiles;
-    rank = CM == 1 ? 0 : static_cast<int>(cluster_ctarank());
-    first = static_cast<int>(blockIdx.x) / CM;
-    stride = static_cast<int>(gridDim.x) / CM;
+    rank = CG == 1 ? 0 : static_cast<int>(cluster_ctarank());
+    first = static_cast<int>(blockIdx.x) / CG;
+    stride = static_cast<int>(gridDim.x) / CG;
   }
   __device__ __forceinline__ void tile(int u, int& tm, int& tn) const {
-    tm = (u % m_groups) * CM + rank;
+    tm = (u % m_groups) * CG + rank;
     tn = u / m_groups;
   }
 };
 
-template <int BN, int STAGES, int CM, bool OUT_BF16>
+template <int BN, int STAGES, int CG, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                 const __grid_constant__ CUtensorMap tmap_b,
                                 const float* __restrict__ sA, const float* __restrict__ sB,
                                 void* __restrict__ C, int64_t ldc, int M, int N, int K) {
-  using CF = Cfg<BN, STAGES>;
+  using CF = Cfg<BN, STAGES, CG>;
+  static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair per MMA");
   constexpr int HALF = BN / 2;     // columns per epilogue warp
   constexpr int NLD = HALF / 32;   // 32-column TMEM loads per chunk
   static_assert(NLD >= 2, "the load pipeline below assumes at least two loads per chunk");
+  constexpr uint16_t kPair = 0x3;  // both CTAs of the pair
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -135,21 +146,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  static_assert(CM == 1 || CM == 2, "clusters of one or two CTAs along M");
-  constexpr uint16_t kPeers = (1u << CM) - 1;  // multicast mask: every CTA of the cluster
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const TileSched<CM> sched(M, N, BN);
+  const TileSched<CG> sched(M, N, BN);
+  const bool leader = sched.rank == 0;  // issues the MMAs (always true for CG = 1)
   const int kchunks = K / BK;
   const int nb = N / 128;
 
   if (threadIdx.x == 0) {
+    // Only the leader's full and tempty barriers are used when CG = 2; every
+    // CTA receives the leader's commits on its own empty and tfull barriers.
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CM);  // one MMA commit from each CTA sharing the stage's B
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], kEpiWarps);
+      mbar_init(&tempty[b], kEpiWarps * CG);
     }
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -157,12 +169,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmap_b);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, CF::kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<CG>(tmem_slot, CF::kTmemCols);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
-  if (CM > 1)
-    cluster_sync();  // the peer's barriers exist before any multicast targets them
+  if (CG > 1)
+    cluster_sync();  // both CTAs' barriers and TMEM exist before either uses the other's
   else
     __syncthreads();
   tc_fence_after();
@@ -171,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kCtlWarps) {
     setmaxnreg_dec<kCtlRegs>();
     if (warp == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer (every CTA loads its own share) ----------------
       if (elect_one_sync()) {
         uint32_t it = 0;
         bool ok = true;
@@ -185,31 +197,34 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full[s], CF::kStageBytes);
-            tma_load_2d(sm_a + s * CF::kABytes, &tmap_a, &full[s], kc * BK, tm * BM);
-            if (CM == 1) {
-              tma_load_2d(sm_b + s * CF::kBBytes, &tmap_b, &full[s], kc * BK, tn * BN);
+            const int b_row = tn * BN + sched.rank * (BN / CG);
+            if (CG == 1) {
+              mbar_arrive_expect_tx(&full[s], CF::kTxBytes);
+              tma_load_2d(sm_a + s * CF::kABytes, &tmap_a, &full[s], kc * BK, tm * BM);
+              tma_load_2d(sm_b + s * CF::kBBytes, &tmap_b, &full[s], kc * BK, b_row);
             } else {
-              // this CTA's half of the shared B tile, written into both CTAs
-              constexpr int kHalfRows = BN / CM;
-              tma_load_2d_multicast(sm_b + s * CF::kBBytes + sched.rank * kHalfRows * BK, &tmap_b,
-                                    &full[s], kc * BK, tn * BN + sched.rank * kHalfRows, kPeers);
+              // both CTAs' copies complete on the leader's barrier
+              if (leader) mbar_arrive_expect_tx(&full[s], CF::kTxBytes);
+              const uint32_t bar = mapa_shared(&full[s], 0);
+              tma_load_2d_pair(sm_a + s * CF::kABytes, &tmap_a, bar, kc * BK, tm * BM);
+              tma_load_2d_pair(sm_b + s * CF::kBBytes, &tmap_b, bar, kc * BK, b_row);
             }
           }
         }
-        // No copy may still target this CTA's shared memory, and no MMA
-        // commit may still be on its way to its barriers, when it exits.
+        // Before leaving: every copy into the pair's shared memory has landed
+        // (the leader's full barriers see both CTAs' copies) and every MMA
+        // commit addressed to this CTA's empty barriers has arrived.
         const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
         for (uint32_t j = first; j < it; ++j) {
-          mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1u);
+          if (leader) mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1u);
           mbar_wait_drain(&empty[j % STAGES], (j / STAGES) & 1u);
         }
       }
       __syncwarp();
-    } else if (warp == 1) {
-      // ---------------- MMA issuer ----------------
+    } else if (warp == 1 && leader) {
+      // ---------------- MMA issuer (the leader CTA of a pair) ----------------
       if (elect_one_sync()) {
-        constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+        constexpr uint32_t idesc = idesc_e4m3_f32(BM * CG, BN);
         uint32_t it = 0;
         bool ok = true;
         for (int u = sched.first; u < sched.total && ok; u += sched.stride) {
@@ -228,13 +243,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t b0 = smem_u32(sm_b + s * CF::kBBytes);
 #pragma unroll
             for (int kk = 0; kk < BK / 32; ++kk)
-              umma_f8f6f4(d, smem_desc_k_sw128(a0 + kk * 32), smem_desc_k_sw128(b0 + kk * 32),
-                          idesc, kk > 0 ? 1u : 0u);
-            if (CM == 1)
+              umma_f8f6f4<CG>(d, smem_desc_k_sw128(a0 + kk * 32), smem_desc_k_sw128(b0 + kk * 32),
+                              idesc, kk > 0 ? 1u : 0u);
+            if (CG == 1) {
               umma_commit(&empty[s]);
-            else
-              umma_commit_multicast(&empty[s], kPeers);  // both CTAs wrote this stage's B
-            umma_commit(&tfull[buf]);
+              umma_commit(&tfull[buf]);
+            } else {
+              umma_commit_pair(&empty[s], kPair);
+              umma_commit_pair(&tfull[buf], kPair);
+            }
           }
         }
         // MMAs still in flight must finish before TMEM is released.
@@ -295,10 +312,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               tmem_ld_32x32b_x32(taddr + 32 * (q + 1), ra);
           } else {
-            // every column of this buffer is in registers: hand it back
+            // every column of this buffer is in registers: hand it back to
+            // the MMA issuer (the leader CTA's barrier when CG = 2)
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[buf]);
+            if (lane == 0) {
+              if (CG == 1)
+                mbar_arrive(&tempty[buf]);
+              else
+                mbar_arrive_cluster(mapa_shared(&tempty[buf], 0));
+            }
           }
           if (q % 2 == 0)
             promote32(acc, ra, comb2, 16 * q);
@@ -345,13 +368,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   __syncwarp();
   tc_fence_before();
-  if (CM > 1)
+  if (CG > 1)
     cluster_sync();  // neither CTA leaves while its peer may still reach its memory
   else
     __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, CF::kTmemCols);
+    tmem_dealloc<CG>(tmem_base, CF::kTmemCols);
   }
 }
 
@@ -386,16 +409,16 @@ bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, int CM, bool OUT_BF16>
+template <int BN, int STAGES, int CG, bool OUT_BF16>
 cudaError_t launch_cfg(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                        void* C, int64_t ldc, int M, int N, int K, cudaStream_t stream,
                        const DeviceInfo& dev) {
-  using CF = Cfg<BN, STAGES>;
-  auto kern = gemm_fp8_blockscaled_kernel<BN, STAGES, CM, OUT_BF16>;
+  using CF = Cfg<BN, STAGES, CG>;
+  auto kern = gemm_fp8_blockscaled_kernel<BN, STAGES, CG, OUT_BF16>;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CM;
+  attr[0].val.clusterDim.x = CG;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(kThreads);
@@ -421,9 +444,9 @@ cudaError_t launch_cfg(const uint8_t* A, const float* sA, const uint8_t* B, cons
       // With fewer registers per thread than kLaunchRegs the epilogue's
       // setmaxnreg increase could never be granted: refuse to launch.
       if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-      int n = dev.sm_count / CM;
-      if (CM > 1) {
-        cfg.gridDim = dim3(CM * n);
+      int n = dev.sm_count / CG;
+      if (CG > 1) {
+        cfg.gridDim = dim3(CG * n);
         e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
         if (e != cudaSuccess) return e;
         if (n < 1) return cudaErrorInvalidConfiguration;
@@ -432,12 +455,12 @@ cudaError_t launch_cfg(const uint8_t* A, const float* sA, const uint8_t* B, cons
     }
   }
   CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, A, M, K, BM) || !make_operand_map(&tb, B, N, K, BN / CM))
+  if (!make_operand_map(&ta, A, M, K, BM) || !make_operand_map(&tb, B, N, K, BN / CG))
     return cudaErrorInvalidValue;
-  const int m_groups = ((M + BM - 1) / BM + CM - 1) / CM;
+  const int m_groups = ((M + BM - 1) / BM + CG - 1) / CG;
   const int units = m_groups * ((N + BN - 1) / BN);
   const int clusters = units < max_clusters[dev.device] ? units : max_clusters[dev.device];
-  cfg.gridDim = dim3(CM * clusters);
+  cfg.gridDim = dim3(CG * clusters);
   return cudaLaunchKernelEx(&cfg, kern, ta, tb, sA, sB, C, ldc, M, N, K);
 }
 
@@ -450,16 +473,16 @@ cudaError_t launch_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const
   (void)mode;  // power-of-two scales take the same promotion path (exact products)
   if (M == 0 || N == 0) return cudaSuccess;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  // 128 x 256 tiles, pairs of CTAs along M sharing each B tile, when there
-  // are enough of them to fill the GPU; 128 x 128 single-CTA tiles otherwise.
+  // 256 x 256 tiles on CTA pairs (tcgen05 cta_group::2) when there are
+  // enough of them to fill the GPU; 128 x 128 single-CTA tiles otherwise.
   const int64_t m_tiles = (M + BM - 1) / BM;
   const int64_t pairs256 = ((m_tiles + 1) / 2) * ((N + 255) / 256);
   const bool wide = (N % 256 == 0) && m_tiles >= 2 && 2 * pairs256 >= dev.sm_count;
   if (out_bf16) {
-    return wide ? launch_cfg<256, 4, 2, true>(A, sA, B, sB, C, ldc, m, n, k, stream, dev)
+    return wide ? launch_cfg<256, 6, 2, true>(A, sA, B, sB, C, ldc, m, n, k, stream, dev)
                 : launch_cfg<128, 6, 1, true>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
   }
-  return wide ? launch_cfg<256, 4, 2, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev)
+  return wide ? launch_cfg<256, 6, 2, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev)
               : launch_cfg<128, 6, 1, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
 }
 
