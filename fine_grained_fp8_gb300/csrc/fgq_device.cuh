@@ -142,10 +142,19 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
   return r;
 }
 
-// Arrive on a barrier given by its shared::cluster address (any CTA of the
-// cluster), release semantics at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+// Relaxed arrives: the arrive orders nothing else.  Used to hand a TMEM
+// buffer back after tcgen05.wait::ld, when every read of it has already
+// completed; a release here would also wait for this thread's earlier
+// global stores, which costs microseconds per hand-off across a cluster.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// Same, on a barrier given by its shared::cluster address (any CTA of the
+// cluster).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                : "memory");
 }
 
@@ -300,16 +309,11 @@ __device__ __forceinline__ void setmaxnreg_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// acc (packed fp32 pair) += p (packed pair) * scale (packed pair), one
-// rounding per lane.  volatile keeps it ordered against TMEM loads/waits.
-__device__ __forceinline__ uint64_t ffma2_acc(uint64_t p, uint64_t scale, uint64_t acc) {
-  uint64_t d;
-  asm volatile("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(p), "l"(scale), "l"(acc));
-  return d;
-}
-
-__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
-  return (static_cast<uint64_t>(hi) << 32) | lo;
+// acc += p * scale with one rounding.  volatile keeps it in program order
+// relative to the TMEM loads and waits around it, so the FMAs on one loaded
+// batch overlap the load of the next.
+__device__ __forceinline__ void fma_acc(float& acc, uint32_t p_bits, float scale) {
+  asm volatile("fma.rn.f32 %0, %1, %2, %0;" : "+f"(acc) : "f"(__uint_as_float(p_bits)), "f"(scale));
 }
 
 // Shared-memory matrix descriptor for a K-major operand stored in the

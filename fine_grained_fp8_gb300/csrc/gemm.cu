@@ -21,8 +21,8 @@
 //     then commits to the stage's "empty" and the buffer's "full" barriers.
 //   - Warps 4-11: epilogue.  Per chunk they read the partial from TMEM in
 //     32-column loads (the next load in flight while the current one is
-//     used), multiply by sA[m,c] * sB[c, n/128] and add it into fp32
-//     accumulators held in registers with packed f32x2 FMAs (the promotion
+//     used), multiply by sA[m,c] * sB[c, n/128] (loaded four chunks ahead)
+//     and add it into fp32 accumulators held in registers (the promotion
 //     step), hand the TMEM buffer back as soon as it is read, and after the
 //     last chunk convert and store the tile.  Two TMEM buffers let the
 //     tensor core run chunk c+1 while chunk c is promoted.
@@ -90,15 +90,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
-// acc[j] += comb * partial[j] for the 32 columns held in r (16 packed pairs).
-// (Called from fully unrolled loops, so j0 is a constant and acc stays in
-// registers.)
+// acc[j0 + j] += comb * partial[j] for the 32 columns held in r.  (Called
+// from fully unrolled loops, so j0 is a constant and acc stays in registers.)
 template <int NACC>
-__device__ __forceinline__ void promote32(uint64_t (&acc)[NACC], const uint32_t (&r)[32],
-                                          uint64_t comb2, int j0) {
+__device__ __forceinline__ void promote32(float (&acc)[NACC], const uint32_t (&r)[32], float comb,
+                                          int j0) {
 #pragma unroll
-  for (int j = 0; j < 16; ++j) acc[j0 + j] = ffma2_acc(pack2(r[2 * j], r[2 * j + 1]), comb2, acc[j0 + j]);
+  for (int j = 0; j < 32; ++j) fma_acc(acc[j0 + j], r[j], comb);
 }
+
+// Scales of the next chunks, loaded kScaleAhead chunks before use: a
+// shift register of (sA[row, c], sB[c, block]) pairs.
+constexpr int kScaleAhead = 4;
 
 // Static persistent schedule over work units.  A unit is the CG stacked
 // 128-row tiles one MMA covers (CG = 2: the two CTAs of a cluster, rank r
@@ -280,20 +283,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* sa_row = sA + static_cast<int64_t>(row_ok ? row : 0) * kchunks;
       const float* sb_col = sB + nblk;
 
-      uint64_t acc[HALF / 2];
+      float acc[HALF];
 #pragma unroll
-      for (int j = 0; j < HALF / 2; ++j) acc[j] = 0ull;
+      for (int j = 0; j < HALF; ++j) acc[j] = 0.0f;
 
-      float sa_next = row_ok ? __ldg(sa_row) : 0.0f;
-      float sb_next = __ldg(sb_col);
+      float sa_q[kScaleAhead], sb_q[kScaleAhead];
+#pragma unroll
+      for (int i = 0; i < kScaleAhead; ++i) {
+        sa_q[i] = (row_ok && i < kchunks) ? __ldg(sa_row + i) : 0.0f;
+        sb_q[i] = i < kchunks ? __ldg(sb_col + static_cast<int64_t>(i) * nb) : 0.0f;
+      }
       for (int kc = 0; kc < kchunks; ++kc, ++it) {
         const uint32_t buf = it & 1u, tph = (it >> 1) & 1u;
-        const float comb = sa_next * sb_next;
-        if (kc + 1 < kchunks) {  // prefetch the next chunk's scales
-          sa_next = row_ok ? __ldg(sa_row + kc + 1) : 0.0f;
-          sb_next = __ldg(sb_col + static_cast<int64_t>(kc + 1) * nb);
+        const float comb = sa_q[0] * sb_q[0];
+#pragma unroll
+        for (int i = 0; i + 1 < kScaleAhead; ++i) {
+          sa_q[i] = sa_q[i + 1];
+          sb_q[i] = sb_q[i + 1];
         }
-        const uint64_t comb2 = pack2(__float_as_uint(comb), __float_as_uint(comb));
+        const int kn = kc + kScaleAhead;
+        sa_q[kScaleAhead - 1] = (row_ok && kn < kchunks) ? __ldg(sa_row + kn) : 0.0f;
+        sb_q[kScaleAhead - 1] = kn < kchunks ? __ldg(sb_col + static_cast<int64_t>(kn) * nb) : 0.0f;
         // warp-uniform outcome: the TMEM loads below are warp-collective
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull[buf], tph, abort_flag, FGQ_DEVERR_EPI_TMEM))) {
           ok = false;
@@ -317,16 +327,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-              if (CG == 1)
-                mbar_arrive(&tempty[buf]);
+              if (leader)
+                mbar_arrive_relaxed(&tempty[buf]);
               else
-                mbar_arrive_cluster(mapa_shared(&tempty[buf], 0));
+                mbar_arrive_cluster_relaxed(mapa_shared(&tempty[buf], 0));
             }
           }
           if (q % 2 == 0)
-            promote32(acc, ra, comb2, 16 * q);
+            promote32(acc, ra, comb, 32 * q);
           else
-            promote32(acc, rb, comb2, 16 * q);
+            promote32(acc, rb, comb, 32 * q);
           if (q + 1 < NLD) {
             if (q % 2 == 0)
               tmem_wait_ld_regs(rb);
@@ -340,27 +350,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (OUT_BF16) {
           uint16_t* crow = static_cast<uint16_t*>(C) + static_cast<int64_t>(row) * ldc + col0;
 #pragma unroll
-          for (int j = 0; j < HALF / 2; j += 4) {
+          for (int j = 0; j < HALF; j += 8) {
             uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(acc[j])),
-                              __uint_as_float(static_cast<uint32_t>(acc[j] >> 32)));
-            v.y = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(acc[j + 1])),
-                              __uint_as_float(static_cast<uint32_t>(acc[j + 1] >> 32)));
-            v.z = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(acc[j + 2])),
-                              __uint_as_float(static_cast<uint32_t>(acc[j + 2] >> 32)));
-            v.w = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(acc[j + 3])),
-                              __uint_as_float(static_cast<uint32_t>(acc[j + 3] >> 32)));
-            *reinterpret_cast<uint4*>(crow + 2 * j) = v;
+            v.x = pack_bf16x2(acc[j + 0], acc[j + 1]);
+            v.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+            v.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
+            v.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+            *reinterpret_cast<uint4*>(crow + j) = v;
           }
         } else {
           float* crow = static_cast<float*>(C) + static_cast<int64_t>(row) * ldc + col0;
 #pragma unroll
-          for (int j = 0; j < HALF / 2; j += 2) {
-            uint4 v = make_uint4(static_cast<uint32_t>(acc[j]), static_cast<uint32_t>(acc[j] >> 32),
-                                 static_cast<uint32_t>(acc[j + 1]),
-                                 static_cast<uint32_t>(acc[j + 1] >> 32));
-            *reinterpret_cast<uint4*>(crow + 2 * j) = v;
-          }
+          for (int j = 0; j < HALF; j += 4)
+            *reinterpret_cast<float4*>(crow + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
         }
       }
     }
