@@ -326,14 +326,24 @@ __device__ __forceinline__ void fma_acc(float& acc, uint32_t p_bits, float scale
 //   bits 46-47  descriptor version, 1 on this architecture
 //   bits 49-51  base offset (0: atoms are 1024-byte aligned)
 //   bits 61-63  swizzle mode, 2 = 128-byte swizzle
-__device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t smem_addr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1u) << 16;
-  d |= static_cast<uint64_t>(1024u >> 4) << 32;
-  d |= static_cast<uint64_t>(1u) << 46;
-  d |= static_cast<uint64_t>(2u) << 61;
+// The descriptor as its two 32-bit words.  The low word holds the start
+// address field and the leading-dimension offset; every operand tile of a
+// kernel shares the high word.  Because shared memory is below 256 KB, the
+// start field of an address a + d is the start field of a plus d >> 4, so a
+// descriptor for an offset tile is one 32-bit add on the low word.
+__device__ __forceinline__ uint32_t smem_desc_k_sw128_lo(uint32_t smem_addr) {
+  return ((smem_addr & 0x3FFFFu) >> 4) | (1u << 16);
+}
+constexpr uint32_t kSmemDescK128Hi = (1024u >> 4) | (1u << 14) | (2u << 29);
+
+__device__ __forceinline__ uint64_t make_desc(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
   return d;
+}
+
+__device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t smem_addr) {
+  return make_desc(smem_desc_k_sw128_lo(smem_addr), kSmemDescK128Hi);
 }
 
 // Instruction descriptor, kind::f8f6f4, dense: D fp32, A and B E4M3, both

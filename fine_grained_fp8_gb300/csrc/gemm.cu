@@ -55,18 +55,23 @@ constexpr uint32_t kEpiRegs = 224;
 static_assert(128 * kCtlRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 
-// BN: output columns of a tile (and the MMA's N).  CG: CTAs per MMA (1, or 2
-// for the paired tcgen05.mma.cta_group::2, whose 256 x BN tile is split so
-// that each CTA holds 128 rows of A and BN/2 rows of B per stage and
-// receives its own 128 rows of the result in its TMEM).
+// BN: output columns of a tile.  Each K chunk is computed as two MMAs of
+// N = BN/2 (the column halves), each with its own TMEM-full / TMEM-empty
+// barrier pair, so the epilogue warps of one half drain while the tensor
+// core works on the other.  CG: CTAs per MMA (1, or 2 for the paired
+// tcgen05.mma.cta_group::2: its 256-row tile is split so that each CTA holds
+// 128 rows of A and, for each column half, BN/4 rows of B, and receives its
+// own 128 rows of the result in its TMEM).
 template <int BN, int STAGES, int CG>
 struct Cfg {
   static constexpr int kABytes = BM * BK;
-  static constexpr int kBBytes = (BN / CG) * BK;
+  static constexpr int kBHalfRows = BN / 2 / CG;              // B rows per column half per CTA
+  static constexpr int kBHalfBytes = kBHalfRows * BK;
+  static constexpr int kBBytes = 2 * kBHalfBytes;
   static constexpr int kStageBytes = kABytes + kBBytes;      // per CTA
   static constexpr uint32_t kTxBytes = CG * kStageBytes;     // per stage of the MMA
   static constexpr int kTmemCols = 2 * BN;                   // two partial buffers
-  static constexpr int kBarBytes = (2 * STAGES + 4) * 8 + 16;
+  static constexpr int kBarBytes = (2 * STAGES + 8) * 8 + 16;
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes;
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of 2");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
@@ -144,9 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm_b = smem + STAGES * CF::kABytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm_b + STAGES * CF::kBBytes);
   uint64_t* empty = full + STAGES;
-  uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tfull = empty + STAGES;  // [buffer * 2 + column half]
+  uint64_t* tempty = tfull + 4;      // [buffer * 2 + column half]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,9 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 4; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], kEpiWarps * CG);
+      mbar_init(&tempty[b], (kEpiWarps / 2) * CG);  // the four warps of one half, per CTA
     }
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -188,29 +193,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       // ---------------- TMA producer (every CTA loads its own share) ----------------
       if (elect_one_sync()) {
+        const uint32_t full_cluster0 = CG > 1 ? mapa_shared(&full[0], 0) : 0u;
         uint32_t it = 0;
+        int s = 0;
+        uint32_t ph = 0;
         bool ok = true;
         for (int u = sched.first; u < sched.total && ok; u += sched.stride) {
           int tm, tn;
           sched.tile(u, tm, tn);
+          // B rows of column half h held by this CTA: BN/2 rows from
+          // tn * BN + h * BN/2, split between the CTAs of a pair.
+          const int b_row = tn * BN + sched.rank * CF::kBHalfRows;
+          const int a_row = tm * BM;
           for (int kc = 0; kc < kchunks; ++kc, ++it) {
-            const int s = it % STAGES;
-            const uint32_t ph = (it / STAGES) & 1u;
             if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, FGQ_DEVERR_PRODUCER_EMPTY)) {
               ok = false;
               break;
             }
-            const int b_row = tn * BN + sched.rank * (BN / CG);
+            uint8_t* a_dst = sm_a + s * CF::kABytes;
+            uint8_t* b_dst = sm_b + s * CF::kBBytes;
             if (CG == 1) {
               mbar_arrive_expect_tx(&full[s], CF::kTxBytes);
-              tma_load_2d(sm_a + s * CF::kABytes, &tmap_a, &full[s], kc * BK, tm * BM);
-              tma_load_2d(sm_b + s * CF::kBBytes, &tmap_b, &full[s], kc * BK, b_row);
+              tma_load_2d(a_dst, &tmap_a, &full[s], kc * BK, a_row);
+              tma_load_2d(b_dst, &tmap_b, &full[s], kc * BK, b_row);
+              tma_load_2d(b_dst + CF::kBHalfBytes, &tmap_b, &full[s], kc * BK, b_row + BN / 2);
             } else {
               // both CTAs' copies complete on the leader's barrier
               if (leader) mbar_arrive_expect_tx(&full[s], CF::kTxBytes);
-              const uint32_t bar = mapa_shared(&full[s], 0);
-              tma_load_2d_pair(sm_a + s * CF::kABytes, &tmap_a, bar, kc * BK, tm * BM);
-              tma_load_2d_pair(sm_b + s * CF::kBBytes, &tmap_b, bar, kc * BK, b_row);
+              const uint32_t bar = full_cluster0 + 8u * s;
+              tma_load_2d_pair(a_dst, &tmap_a, bar, kc * BK, a_row);
+              tma_load_2d_pair(b_dst, &tmap_b, bar, kc * BK, b_row);
+              tma_load_2d_pair(b_dst + CF::kBHalfBytes, &tmap_b, bar, kc * BK, b_row + BN / 2);
+            }
+            if (++s == STAGES) {
+              s = 0;
+              ph ^= 1u;
             }
           }
         }
@@ -227,38 +244,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1 && leader) {
       // ---------------- MMA issuer (the leader CTA of a pair) ----------------
       if (elect_one_sync()) {
-        constexpr uint32_t idesc = idesc_e4m3_f32(BM * CG, BN);
+        constexpr uint32_t idesc = idesc_e4m3_f32(BM * CG, BN / 2);
+        // Lean issue loop: this thread shares its scheduler with two epilogue
+        // warps, so per-chunk work is a few 32-bit adds per MMA.
+        const uint32_t a_lo0 = smem_desc_k_sw128_lo(smem_u32(sm_a));
+        const uint32_t b_lo0 = smem_desc_k_sw128_lo(smem_u32(sm_b));
         uint32_t it = 0;
+        int s = 0;
+        uint32_t ph = 0;
         bool ok = true;
         for (int u = sched.first; u < sched.total && ok; u += sched.stride) {
           for (int kc = 0; kc < kchunks; ++kc, ++it) {
-            const int s = it % STAGES;
-            const uint32_t ph = (it / STAGES) & 1u;
             const uint32_t buf = it & 1u, tph = (it >> 1) & 1u;
-            if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, FGQ_DEVERR_MMA_TMEM) ||
-                !mbar_wait(&full[s], ph, abort_flag, FGQ_DEVERR_MMA_FULL)) {
+            if (!mbar_wait(&full[s], ph, abort_flag, FGQ_DEVERR_MMA_FULL)) {
               ok = false;
               break;
             }
-            tc_fence_after();
-            const uint32_t d = tmem_base + buf * BN;
-            const uint32_t a0 = smem_u32(sm_a + s * CF::kABytes);
-            const uint32_t b0 = smem_u32(sm_b + s * CF::kBBytes);
+            const uint32_t a_lo = a_lo0 + s * (CF::kABytes >> 4);
+            const uint32_t b_lo = b_lo0 + s * (CF::kBBytes >> 4);
 #pragma unroll
-            for (int kk = 0; kk < BK / 32; ++kk)
-              umma_f8f6f4<CG>(d, smem_desc_k_sw128(a0 + kk * 32), smem_desc_k_sw128(b0 + kk * 32),
-                              idesc, kk > 0 ? 1u : 0u);
-            if (CG == 1) {
+            for (int h = 0; h < 2; ++h) {
+              uint64_t* te = &tempty[buf * 2 + h];
+              if (!mbar_wait(te, tph ^ 1u, abort_flag, FGQ_DEVERR_MMA_TMEM)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t d = tmem_base + buf * BN + h * (BN / 2);
+#pragma unroll
+              for (int kk = 0; kk < BK / 32; ++kk)
+                umma_f8f6f4<CG>(d, make_desc(a_lo + kk * 2, kSmemDescK128Hi),
+                                make_desc(b_lo + h * (CF::kBHalfBytes >> 4) + kk * 2, kSmemDescK128Hi),
+                                idesc, kk > 0 ? 1u : 0u);
+              if (CG == 1)
+                umma_commit(&tfull[buf * 2 + h]);
+              else
+                umma_commit_pair(&tfull[buf * 2 + h], kPair);
+            }
+            if (!ok) break;
+            if (CG == 1)
               umma_commit(&empty[s]);
-              umma_commit(&tfull[buf]);
-            } else {
+            else
               umma_commit_pair(&empty[s], kPair);
-              umma_commit_pair(&tfull[buf], kPair);
+            if (++s == STAGES) {
+              s = 0;
+              ph ^= 1u;
             }
           }
         }
-        // MMAs still in flight must finish before TMEM is released.
-        if (it > 0) mbar_wait_drain(&tfull[(it - 1) & 1u], ((it - 1) >> 1) & 1u);
+        // MMAs still in flight must finish before TMEM is released (the last
+        // commit covers every MMA issued before it).
+        if (it > 0) mbar_wait_drain(&tfull[((it - 1) & 1u) * 2 + 1], ((it - 1) >> 1) & 1u);
       }
       __syncwarp();
     }
@@ -305,7 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         sa_q[kScaleAhead - 1] = (row_ok && kn < kchunks) ? __ldg(sa_row + kn) : 0.0f;
         sb_q[kScaleAhead - 1] = kn < kchunks ? __ldg(sb_col + static_cast<int64_t>(kn) * nb) : 0.0f;
         // warp-uniform outcome: the TMEM loads below are warp-collective
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull[buf], tph, abort_flag, FGQ_DEVERR_EPI_TMEM))) {
+        if (!__all_sync(0xFFFFFFFFu,
+                        mbar_wait(&tfull[buf * 2 + half], tph, abort_flag, FGQ_DEVERR_EPI_TMEM))) {
           ok = false;
           break;
         }
@@ -328,9 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) {
               if (leader)
-                mbar_arrive_relaxed(&tempty[buf]);
+                mbar_arrive_relaxed(&tempty[buf * 2 + half]);
               else
-                mbar_arrive_cluster_relaxed(mapa_shared(&tempty[buf], 0));
+                mbar_arrive_cluster_relaxed(mapa_shared(&tempty[buf * 2 + half], 0));
             }
           }
           if (q % 2 == 0)
@@ -457,7 +494,7 @@ cudaError_t launch_cfg(const uint8_t* A, const float* sA, const uint8_t* B, cons
     }
   }
   CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, A, M, K, BM) || !make_operand_map(&tb, B, N, K, BN / CG))
+  if (!make_operand_map(&ta, A, M, K, BM) || !make_operand_map(&tb, B, N, K, CF::kBHalfRows))
     return cudaErrorInvalidValue;
   const int m_groups = ((M + BM - 1) / BM + CG - 1) / CG;
   const int units = m_groups * ((N + BN - 1) / BN);
