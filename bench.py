@@ -354,6 +354,42 @@ def run_fgq(args):
     barrier(dist)
     e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev) / e2e_steps
 
+    # The quantizers on the quantize-bandwidth workload (activations
+    # [16384, 7168] Student-t nu=3, weight [7168, 7168] N(0, 0.02^2)), each
+    # timed alone over rotated input pairs larger than L2.
+    quant_bw = None
+    if not args.no_quant_bw:
+        del sets, host_sets, a_dev, b_dev, c_host
+        torch.cuda.empty_cache()
+        qa = [fgq_inputs.quant_bw(seed=100 * rank + 2 * i)[0].to(dev) for i in range(2)]
+        qw = [fgq_inputs.quant_bw(seed=100 * rank + 2 * i, m=128)[1].to(dev) for i in range(2)]
+        QM, QK = qa[0].shape
+        qaq = torch.empty((QM, QK), dtype=torch.uint8, device=dev)
+        qsa = torch.empty((QM, QK // 128), dtype=torch.float32, device=dev)
+        quant_bw = {"workload": "quantize-bw: act bf16 [16384,7168] Student-t nu=3 (1x128); "
+                                "weight bf16 [7168,7168] N(0,0.02^2) (128x128); fp32 scales"}
+        qsteps = max(10, min(args.steps, 200))
+        for name, fn, nbytes in (
+                ("quant_act_1x128", lambda i: fgq.quant_act_1x128(qa[i % 2], "fp32", xq=qaq, sx=qsa),
+                 QM * QK * 3 + QM * (QK // 128) * 4),
+                ("quant_w_128x128", lambda i: fgq.quant_w_128x128(qw[i % 2], "fp32", wq=bq, sw=sb),
+                 BYTES_QUANT_W)):
+            for i in range(5):
+                fn(i)
+            torch.cuda.synchronize()
+            q0 = torch.cuda.Event(enable_timing=True)
+            q1 = torch.cuda.Event(enable_timing=True)
+            q0.record(stream)
+            for i in range(qsteps):
+                fn(i)
+            q1.record(stream)
+            torch.cuda.synchronize()
+            us = reduce_max(dist, q0.elapsed_time(q1), dev) * 1e3 / qsteps
+            gbs = nbytes / (us * 1e-6) / 1e9
+            quant_bw[name] = {"us": us, "GB/s": gbs, "bytes": nbytes, "launches": qsteps}
+        if fgq.device_error() != 0:
+            raise SystemExit("a kernel reported a device wait timeout")
+
     # CPU baseline: the oracle on a bounded sample, rank 0 only, N = 1 only.
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -374,6 +410,9 @@ def run_fgq(args):
         return 0
 
     peaks, src = _peaks()
+    if quant_bw:
+        for k in ("quant_act_1x128", "quant_w_128x128"):
+            quant_bw[k]["frac_hbm"] = quant_bw[k]["GB/s"] / peaks["hbm_gbs"]
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]  # nominal fp8 = 2x bf16 dense
     hbm = peaks["hbm_gbs"]
     gemm_tflops = FLOPS_GEMM / (us_gemm * 1e-6) / 1e12
@@ -407,6 +446,7 @@ def run_fgq(args):
                 "h2d_bytes_per_step": (M_ * K_ + K_ * N_) * 2, "d2h_bytes_per_step": M_ * N_ * 2,
                 "ms_per_step": e2e_ms, "steps": e2e_steps},
         "gpu_launches": 3 * args.steps,
+        "quant_bw": quant_bw,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
@@ -423,6 +463,8 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["fgq", "reference"], default="fgq")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-quant-bw", action="store_true",
+                   help="skip the separate quantize-bandwidth measurement")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")

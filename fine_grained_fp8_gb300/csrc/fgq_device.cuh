@@ -115,89 +115,22 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, ui
       : "memory");
 }
 
-// 2-CTA form: the copy lands in this CTA's shared memory and completes on
-// the barrier at shared::cluster address `bar_cluster`, which may belong to
-// the peer CTA of the pair.
-__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tmap,
-                                                 uint32_t bar_cluster, int32_t c0, int32_t c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar_cluster), "r"(c0), "r"(c1)
-      : "memory");
-}
-
-// ---- clusters ------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// shared::cluster address of the same shared-memory offset in CTA `rank`.
-__device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-
-// Relaxed arrives: the arrive orders nothing else.  Used to hand a TMEM
-// buffer back after tcgen05.wait::ld, when every read of it has already
-// completed; a release here would also wait for this thread's earlier
-// global stores, which costs microseconds per hand-off across a cluster.
-__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-// Same, on a barrier given by its shared::cluster address (any CTA of the
-// cluster).
-__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
-               : "memory");
-}
-
-// Every thread of every CTA in the cluster arrives, then waits for all.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-
 // ---- tcgen05 -------------------------------------------------------------------
 
-// TMEM allocation.  CG = 1: one warp of the CTA.  CG = 2: one warp in each
-// CTA of the pair executes it (the allocation spans both CTAs' TMEM).
-template <int CG>
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
-  if (CG == 1)
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
-  else
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
 }
 
-template <int CG>
 __device__ __forceinline__ void tmem_relinquish() {
-  if (CG == 1)
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  else
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
-template <int CG>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  if (CG == 1)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-  else
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -208,27 +141,15 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4.  CG = 2: issued by the
-// even CTA of the pair; A rows and B rows are split between the two CTAs'
-// shared memory at the same offsets, and each CTA's TMEM receives its own
-// rows of D.
-template <int CG>
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f8f6f4, one CTA.
 __device__ __forceinline__ void umma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
-  if (CG == 1)
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-  else
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
 // Arrive (once) on `bar` when every tcgen05 op issued so far by this thread
@@ -237,17 +158,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-
-// 2-CTA commit: arrive once on the barrier at `bar`'s offset in every CTA
-// of cta_mask when every tcgen05 op issued so far by this thread has
-// completed.
-__device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(cta_mask)
       : "memory");
 }
 
@@ -309,11 +219,16 @@ __device__ __forceinline__ void setmaxnreg_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// acc += p * scale with one rounding.  volatile keeps it in program order
-// relative to the TMEM loads and waits around it, so the FMAs on one loaded
-// batch overlap the load of the next.
-__device__ __forceinline__ void fma_acc(float& acc, uint32_t p_bits, float scale) {
-  asm volatile("fma.rn.f32 %0, %1, %2, %0;" : "+f"(acc) : "f"(__uint_as_float(p_bits)), "f"(scale));
+// acc (packed fp32 pair) += p (packed pair) * scale (packed pair), one
+// rounding per lane.  volatile keeps it ordered against TMEM loads/waits.
+__device__ __forceinline__ uint64_t ffma2_acc(uint64_t p, uint64_t scale, uint64_t acc) {
+  uint64_t d;
+  asm volatile("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(p), "l"(scale), "l"(acc));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+  return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
 // Shared-memory matrix descriptor for a K-major operand stored in the
@@ -326,24 +241,14 @@ __device__ __forceinline__ void fma_acc(float& acc, uint32_t p_bits, float scale
 //   bits 46-47  descriptor version, 1 on this architecture
 //   bits 49-51  base offset (0: atoms are 1024-byte aligned)
 //   bits 61-63  swizzle mode, 2 = 128-byte swizzle
-// The descriptor as its two 32-bit words.  The low word holds the start
-// address field and the leading-dimension offset; every operand tile of a
-// kernel shares the high word.  Because shared memory is below 256 KB, the
-// start field of an address a + d is the start field of a plus d >> 4, so a
-// descriptor for an offset tile is one 32-bit add on the low word.
-__device__ __forceinline__ uint32_t smem_desc_k_sw128_lo(uint32_t smem_addr) {
-  return ((smem_addr & 0x3FFFFu) >> 4) | (1u << 16);
-}
-constexpr uint32_t kSmemDescK128Hi = (1024u >> 4) | (1u << 14) | (2u << 29);
-
-__device__ __forceinline__ uint64_t make_desc(uint32_t lo, uint32_t hi) {
-  uint64_t d;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
-  return d;
-}
-
 __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t smem_addr) {
-  return make_desc(smem_desc_k_sw128_lo(smem_addr), kSmemDescK128Hi);
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1u) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
 }
 
 // Instruction descriptor, kind::f8f6f4, dense: D fp32, A and B E4M3, both
