@@ -21,7 +21,8 @@ from . import _lib
 from ._lib import (FGQ_OUT_BF16, FGQ_OUT_F32, FGQ_SCALE_FP32, FGQ_SCALE_UE8M0, FgqError,
                    check, load)
 
-__all__ = ["quant_act_1x128", "quant_w_128x128", "gemm_fp8_blockscaled", "device_error",
+__all__ = ["quant_act_1x128", "quant_w_128x128", "gemm_fp8_blockscaled",
+           "gemm_fp8_blockscaled_splitk", "splitk_workspace", "device_error",
            "FgqError", "load", "FGQ_SCALE_FP32", "FGQ_SCALE_UE8M0", "FGQ_OUT_F32",
            "FGQ_OUT_BF16", "scale_mode"]
 
@@ -118,6 +119,36 @@ def gemm_fp8_blockscaled(aq: torch.Tensor, sa: torch.Tensor, bq: torch.Tensor,
         M, N, K, FGQ_OUT_BF16 if out_dtype == torch.bfloat16 else FGQ_OUT_F32, scale_mode(mode),
         _stream(aq))
     check("fgq_gemm_fp8_blockscaled_ex", st)
+    return out
+
+
+def splitk_workspace(M: int, N: int, K: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace for gemm_fp8_blockscaled_splitk on `device`."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        st, n = _lib.fgq_gemm_splitk_workspace_size(M, N, K)
+    check("fgq_gemm_splitk_workspace_size", st)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device=dev)
+
+
+def gemm_fp8_blockscaled_splitk(aq: torch.Tensor, sa: torch.Tensor, bq: torch.Tensor,
+                                sb: torch.Tensor, workspace: torch.Tensor, out_dtype=torch.float32,
+                                mode="fp32", out: torch.Tensor | None = None) -> torch.Tensor:
+    """gemm_fp8_blockscaled with split-K over a caller-owned workspace (see
+    splitk_workspace); deterministic, for M <= 256."""
+    M, K = aq.shape
+    N = bq.shape[0]
+    _need_cuda("workspace", workspace, torch.uint8)
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=aq.device)
+    for name, t in (("aq", aq), ("bq", bq), ("sa", sa), ("sb", sb)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    st = _lib.fgq_gemm_fp8_blockscaled_splitk(
+        aq.data_ptr(), sa.data_ptr(), bq.data_ptr(), sb.data_ptr(), out.data_ptr(), out.stride(0),
+        M, N, K, FGQ_OUT_BF16 if out.dtype == torch.bfloat16 else FGQ_OUT_F32, scale_mode(mode),
+        workspace.data_ptr(), workspace.numel(), _stream(aq))
+    check("fgq_gemm_fp8_blockscaled_splitk", st)
     return out
 
 

@@ -33,6 +33,9 @@ SIGNATURES = {
     "fgq_gemm_fp8_blockscaled": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "fgq_gemm_fp8_blockscaled_ex": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                            _int, _int, _vp]),
+    "fgq_gemm_fp8_blockscaled_splitk": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                               _int, _int, _vp, ctypes.c_size_t, _vp]),
+    "fgq_gemm_splitk_workspace_size": (_int, [_i64, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
     "fgq_status_string": (ctypes.c_char_p, [_int]),
     "fgq_device_error": (_int, [ctypes.POINTER(ctypes.c_uint32), _int]),
     "fgq_version": (_int, []),
@@ -100,6 +103,18 @@ def fgq_gemm_fp8_blockscaled(A, sA, B, sB, C, M, N, K, stream) -> int:
 
 def fgq_gemm_fp8_blockscaled_ex(A, sA, B, sB, C, ldc, M, N, K, out, mode, stream) -> int:
     return load().fgq_gemm_fp8_blockscaled_ex(A, sA, B, sB, C, ldc, M, N, K, out, mode, stream)
+
+
+def fgq_gemm_fp8_blockscaled_splitk(A, sA, B, sB, C, ldc, M, N, K, out, mode, workspace,
+                                    workspace_bytes, stream) -> int:
+    return load().fgq_gemm_fp8_blockscaled_splitk(A, sA, B, sB, C, ldc, M, N, K, out, mode,
+                                                  workspace, workspace_bytes, stream)
+
+
+def fgq_gemm_splitk_workspace_size(M, N, K):
+    n = ctypes.c_size_t(0)
+    st = load().fgq_gemm_splitk_workspace_size(M, N, K, ctypes.byref(n))
+    return st, int(n.value)
 
 
 def fgq_device_error(clear: bool = True):

@@ -92,13 +92,16 @@ fgq_status fgq_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
                                                static_cast<cudaStream_t>(stream), dev));
 }
 
-fgq_status fgq_gemm_fp8_blockscaled_ex(const uint8_t* A, const float* sA, const uint8_t* B,
-                                       const float* sB, void* C, int64_t ldc, int64_t M,
-                                       int64_t N, int64_t K, int out, int mode, void* stream) {
+namespace {
+
+// Checks shared by the GEMM entry points (M == 0 returns OK before pointer checks).
+fgq_status check_gemm_args(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                           const void* C, int64_t ldc, int64_t M, int64_t N, int64_t K, int out,
+                           int mode) {
   if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
   if (out != FGQ_OUT_F32 && out != FGQ_OUT_BF16) return FGQ_ERR_INVALID_ARG;
   if (mode != FGQ_SCALE_FP32 && mode != FGQ_SCALE_UE8M0) return FGQ_ERR_INVALID_ARG;
-  // int32 tile coordinates inside the kernel
+  // int32 tile coordinates inside the kernels
   if (M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31) || K >= (int64_t{1} << 31))
     return FGQ_ERR_INVALID_ARG;
   if (M == 0) return FGQ_OK;
@@ -107,12 +110,57 @@ fgq_status fgq_gemm_fp8_blockscaled_ex(const uint8_t* A, const float* sA, const 
   if (ldc < N || ldc % vec != 0) return FGQ_ERR_INVALID_ARG;
   if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(sA, 4) || !aligned(sB, 4))
     return FGQ_ERR_INVALID_ARG;
+  return FGQ_OK;
+}
+
+// fgq_gemm_fp8_blockscaled_ex sends M up to kLowMDirect to the
+// swapped-operand kernel (measured faster there; at larger M the main
+// kernel's epilogue is cheaper); the split-K entry point uses it up to kLowM.
+constexpr int64_t kLowMDirect = 32;
+constexpr int64_t kLowM = 256;
+
+}  // namespace
+
+fgq_status fgq_gemm_fp8_blockscaled_ex(const uint8_t* A, const float* sA, const uint8_t* B,
+                                       const float* sB, void* C, int64_t ldc, int64_t M,
+                                       int64_t N, int64_t K, int out, int mode, void* stream) {
+  fgq_status st = check_gemm_args(A, sA, B, sB, C, ldc, M, N, K, out, mode);
+  if (st != FGQ_OK || M == 0) return st;
+  fgq::DeviceInfo dev;
+  st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  const int bf16 = out == FGQ_OUT_BF16 ? 1 : 0;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M <= kLowMDirect)
+    return from_cuda(fgq::launch_gemm_lowm(A, sA, B, sB, C, ldc, M, N, K, bf16, 1, nullptr, s, dev));
+  return from_cuda(fgq::launch_gemm_fp8_blockscaled(A, sA, B, sB, C, ldc, M, N, K, bf16, mode, s, dev));
+}
+
+fgq_status fgq_gemm_splitk_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {
+  if (!bytes || M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
   fgq::DeviceInfo dev;
   fgq_status st = get_device(&dev);
   if (st != FGQ_OK) return st;
-  return from_cuda(fgq::launch_gemm_fp8_blockscaled(A, sA, B, sB, C, ldc, M, N, K,
-                                                    out == FGQ_OUT_BF16 ? 1 : 0, mode,
-                                                    static_cast<cudaStream_t>(stream), dev));
+  *bytes = (M == 0 || M > kLowM) ? 0 : fgq::lowm_workspace_bytes(M, N, K, dev.sm_count);
+  return FGQ_OK;
+}
+
+fgq_status fgq_gemm_fp8_blockscaled_splitk(const uint8_t* A, const float* sA, const uint8_t* B,
+                                           const float* sB, void* C, int64_t ldc, int64_t M,
+                                           int64_t N, int64_t K, int out, int mode,
+                                           void* workspace, size_t workspace_bytes, void* stream) {
+  fgq_status st = check_gemm_args(A, sA, B, sB, C, ldc, M, N, K, out, mode);
+  if (st != FGQ_OK || M == 0) return st;
+  if (M > kLowM) return fgq_gemm_fp8_blockscaled_ex(A, sA, B, sB, C, ldc, M, N, K, out, mode, stream);
+  fgq::DeviceInfo dev;
+  st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  if (!workspace || !aligned(workspace, 16) ||
+      workspace_bytes < fgq::lowm_workspace_bytes(M, N, K, dev.sm_count))
+    return FGQ_ERR_INVALID_ARG;
+  const int splits = fgq::lowm_splits(M, N, K, dev.sm_count);
+  return from_cuda(fgq::launch_gemm_lowm(A, sA, B, sB, C, ldc, M, N, K, out == FGQ_OUT_BF16 ? 1 : 0,
+                                         splits, workspace, static_cast<cudaStream_t>(stream), dev));
 }
 
 fgq_status fgq_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const uint8_t* B,

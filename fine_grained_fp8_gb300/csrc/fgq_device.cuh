@@ -45,6 +45,26 @@ __device__ __forceinline__ bool elect_one_sync() {
   return pred != 0;
 }
 
+// Named barrier `id` over `nthreads` threads (whole warps).
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ANDs a predicate over its threads: every thread
+// gets the same result.
+__device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // ---- mbarrier ---------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
@@ -63,6 +83,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
+               : "memory");
+}
+
+// Relaxed arrive: orders nothing else.  Used to hand a TMEM buffer back
+// after tcgen05.wait::ld, when every read of it has already completed.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
 
@@ -241,6 +268,16 @@ __device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
 //   bits 46-47  descriptor version, 1 on this architecture
 //   bits 49-51  base offset (0: atoms are 1024-byte aligned)
 //   bits 61-63  swizzle mode, 2 = 128-byte swizzle
+// Descriptor from its two 32-bit words.  Shared memory is below 256 KB, so
+// the descriptor of an operand tile at byte offset d from another is that
+// descriptor with d >> 4 added to its low word (the start field never
+// carries into the next field).
+__device__ __forceinline__ uint64_t make_desc(uint32_t lo, uint32_t hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+  return d;
+}
+
 __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t smem_addr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);

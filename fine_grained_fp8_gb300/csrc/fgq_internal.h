@@ -1,8 +1,11 @@
 // Internal declarations shared by the translation units of libfgq.so.
 #pragma once
 
-#include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
 
 // Bits of the device error word: which wait gave up.
 #define FGQ_DEVERR_PRODUCER_EMPTY 0x1u  // TMA producer waiting for a free stage
@@ -37,5 +40,18 @@ cudaError_t launch_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const
                                         cudaStream_t stream, const DeviceInfo& dev);
 
 cudaError_t read_device_error(uint32_t* word, bool clear);
+
+// TMA descriptor of a K-major E4M3 operand [rows, K] with a 128 (K) x
+// box_rows box, 128-byte swizzle, zero fill outside the tensor.
+bool make_k_major_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows);
+
+// Low-M GEMM (M <= 256): split count and workspace size for a problem, and
+// the launch (splits == 1 needs no workspace).
+int lowm_splits(int64_t M, int64_t N, int64_t K, int sm_count);
+size_t lowm_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count);
+cudaError_t launch_gemm_lowm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                             void* C, int64_t ldc, int64_t M, int64_t N, int64_t K, int out_bf16,
+                             int splits, void* workspace, cudaStream_t stream,
+                             const DeviceInfo& dev);
 
 }  // namespace fgq

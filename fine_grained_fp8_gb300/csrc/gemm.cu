@@ -326,7 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side -------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+}  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -342,18 +344,20 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
 
 // K-major E4M3 operand [rows, K] (row stride K bytes), box 128 (K) x box_rows,
 // 128-byte swizzle, out-of-range rows read as zero.
-bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
-  auto encode = get_encode_fn();
+bool make_k_major_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
+  auto encode = tensor_map_encoder();
   if (!encode) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estride[2] = {1, 1};
   CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
                       box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <int BN, int STAGES, bool OUT_BF16>
 cudaError_t launch_cfg(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
@@ -383,7 +387,7 @@ cudaError_t launch_cfg(const uint8_t* A, const float* sA, const uint8_t* B, cons
   }
   if (launch_regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   CUtensorMap ta, tb;
-  if (!make_operand_map(&ta, A, M, K, BM) || !make_operand_map(&tb, B, N, K, BN))
+  if (!make_k_major_map(&ta, A, M, K, BM) || !make_k_major_map(&tb, B, N, K, BN))
     return cudaErrorInvalidValue;
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;

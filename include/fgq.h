@@ -41,6 +41,7 @@
 #ifndef FGQ_H_
 #define FGQ_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -105,7 +106,8 @@ fgq_status fgq_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
  *   multiple of anything.
  * Each 128-wide K chunk is one tensor-core partial product in TMEM, which is
  * scaled by sA * sB and added into an fp32 accumulator (the page's
- * promotion step, done by the epilogue warps).
+ * promotion step, done by the epilogue warps).  For M <= 32 the operands
+ * are swapped so the tensor core's 128-row side runs over the weight.
  */
 fgq_status fgq_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const uint8_t* B,
                                     const float* sB, float* C, int64_t M, int64_t N,
@@ -126,6 +128,40 @@ fgq_status fgq_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const uin
 fgq_status fgq_gemm_fp8_blockscaled_ex(const uint8_t* A, const float* sA, const uint8_t* B,
                                        const float* sB, void* C, int64_t ldc, int64_t M,
                                        int64_t N, int64_t K, int out, int mode, void* stream);
+
+/*
+ * Block-scaled FP8 GEMM with split-K for few rows of A, using a caller-owned
+ * workspace.  Same arguments and result as fgq_gemm_fp8_blockscaled_ex.
+ *
+ * For M <= 256 the K chunks of each 128-column tile of C are divided among
+ * several CTAs (about four work units per SM); each writes its fp32 partial
+ * tile to the workspace and the last one to finish adds the partials in a
+ * fixed order and writes C, so results are deterministic and identical
+ * across calls.  For M > 256 this is fgq_gemm_fp8_blockscaled_ex and the
+ * workspace is not touched.  (The weight streaming that bounds this regime
+ * is the same; split-K only balances it over every SM.)
+ *
+ *   workspace        device memory of at least the size that
+ *                    fgq_gemm_splitk_workspace_size returns for (M, N, K) on
+ *                    the current device, 16-byte aligned, owned by the
+ *                    caller.  It must be zero-filled before its first use;
+ *                    every call that returns FGQ_OK leaves it ready for the
+ *                    next (its per-tile counters back at zero).  After a
+ *                    call whose kernel gave up on a wait
+ *                    (FGQ_ERR_DEVICE_TIMEOUT from fgq_device_error) zero it
+ *                    again.  Calls that share a workspace must not overlap
+ *                    on the GPU.
+ *   workspace_bytes  its size; a smaller size than required returns
+ *                    FGQ_ERR_INVALID_ARG.
+ */
+fgq_status fgq_gemm_fp8_blockscaled_splitk(const uint8_t* A, const float* sA, const uint8_t* B,
+                                           const float* sB, void* C, int64_t ldc, int64_t M,
+                                           int64_t N, int64_t K, int out, int mode,
+                                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes fgq_gemm_fp8_blockscaled_splitk needs for (M, N, K) on the
+ * current device (depends on its SM count).  Same size checks as the GEMM. */
+fgq_status fgq_gemm_splitk_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
 
 /* Static description of a status code. */
 const char* fgq_status_string(fgq_status status);
