@@ -36,6 +36,8 @@ SIGNATURES = {
     "fgq_gemm_fp8_blockscaled_splitk": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                                _int, _int, _vp, ctypes.c_size_t, _vp]),
     "fgq_gemm_splitk_workspace_size": (_int, [_i64, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
+    "fgq_gemm_fp8_blockscaled_splitk_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
+                                                       _i64, _int, _int, _vp]),
     "fgq_status_string": (ctypes.c_char_p, [_int]),
     "fgq_device_error": (_int, [ctypes.POINTER(ctypes.c_uint32), _int]),
     "fgq_version": (_int, []),
@@ -109,6 +111,12 @@ def fgq_gemm_fp8_blockscaled_splitk(A, sA, B, sB, C, ldc, M, N, K, out, mode, wo
                                     workspace_bytes, stream) -> int:
     return load().fgq_gemm_fp8_blockscaled_splitk(A, sA, B, sB, C, ldc, M, N, K, out, mode,
                                                   workspace, workspace_bytes, stream)
+
+
+def fgq_gemm_fp8_blockscaled_splitk_noalloc(A, sA, B, sB, C, ldc, M, N, K, out, mode,
+                                            stream) -> int:
+    return load().fgq_gemm_fp8_blockscaled_splitk_noalloc(A, sA, B, sB, C, ldc, M, N, K, out,
+                                                          mode, stream)
 
 
 def fgq_gemm_splitk_workspace_size(M, N, K):

@@ -170,6 +170,34 @@ fgq_status fgq_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const uin
                                      stream);
 }
 
+fgq_status fgq_gemm_fp8_blockscaled_splitk_noalloc(const uint8_t* A, const float* sA,
+                                                   const uint8_t* B, const float* sB, void* C,
+                                                   int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                                   int out, int mode, void* stream) {
+  // Same checks and kernels as fgq_gemm_fp8_blockscaled_splitk, with the
+  // library's fixed scratch array in place of a caller workspace.
+  fgq_status st = check_gemm_args(A, sA, B, sB, C, ldc, M, N, K, out, mode);
+  if (st != FGQ_OK || M == 0) return st;
+  if (M > kLowM) return fgq_gemm_fp8_blockscaled_ex(A, sA, B, sB, C, ldc, M, N, K, out, mode, stream);
+  fgq::DeviceInfo dev;
+  st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  const size_t need = fgq::lowm_workspace_bytes(M, N, K, dev.sm_count);
+  if (need > FGQ_NOALLOC_SCRATCH_BYTES) return FGQ_ERR_INVALID_ARG;  // beyond the fixed array
+  void* scratch = nullptr;
+  if (fgq::noalloc_scratch(dev, &scratch) != cudaSuccess) return FGQ_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int splits = fgq::lowm_splits(M, N, K, dev.sm_count);
+  if (splits > 1) {
+    // the per-tile counters must start at zero; an earlier call that gave
+    // up on a wait may have left them otherwise (they lie inside `need`)
+    const size_t counter_bytes = static_cast<size_t>(N / 128) * sizeof(unsigned int);
+    if (cudaMemsetAsync(scratch, 0, counter_bytes, s) != cudaSuccess) return FGQ_ERR_CUDA;
+  }
+  return from_cuda(fgq::launch_gemm_lowm(A, sA, B, sB, C, ldc, M, N, K, out == FGQ_OUT_BF16 ? 1 : 0,
+                                         splits, scratch, s, dev));
+}
+
 const char* fgq_status_string(fgq_status status) {
   switch (status) {
     case FGQ_OK: return "ok";

@@ -45,6 +45,15 @@ cudaError_t read_device_error(uint32_t* word, bool clear);
 // box_rows box, 128-byte swizzle, zero fill outside the tensor.
 bool make_k_major_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows);
 
+// Bytes of the fixed scratch array behind fgq_gemm_fp8_blockscaled_splitk_noalloc.
+#ifndef FGQ_NOALLOC_SCRATCH_BYTES
+#define FGQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+#endif
+
+// Device address of that array on the current device (looked up on the
+// first call for each device).
+cudaError_t noalloc_scratch(const DeviceInfo& dev, void** ptr);
+
 // Low-M GEMM (M <= 256): split count and workspace size for a problem, and
 // the launch (splits == 1 needs no workspace).
 int lowm_splits(int64_t M, int64_t N, int64_t K, int sm_count);

@@ -476,3 +476,39 @@ cudaError_t launch_gemm_lowm(const uint8_t* A, const float* sA, const uint8_t* B
 }
 
 }  // namespace fgq
+
+// ---- split-K over a fixed scratch array (no allocation) -----------------------
+//
+// For callers that cannot allocate device memory at all: code inside
+// another allocator or a memory-pool callback, hosts that hand out a fixed
+// device-memory budget up front, or embedders with no allocator of their
+// own.  The split-K workspace then lives in this file-scope array: every
+// GPU that loads the library holds it until the process exits, and every
+// call shares it.
+namespace fgq {
+namespace {
+
+static __device__ __align__(256) unsigned char g_splitk_scratch[FGQ_NOALLOC_SCRATCH_BYTES];
+
+}  // namespace
+
+cudaError_t noalloc_scratch(const DeviceInfo& dev, void** ptr) {
+  // The array's name in host code is only a host-side stand-in for the
+  // symbol, so its device address is looked up once per device, with that
+  // device current (the caller made it current).
+  static std::mutex mu;
+  static void* addr[64] = {};
+  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev.device] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_splitk_scratch);
+    if (e != cudaSuccess) return e;
+    if (p == nullptr) return cudaErrorInvalidSymbol;
+    addr[dev.device] = p;
+  }
+  *ptr = addr[dev.device];
+  return cudaSuccess;
+}
+
+}  // namespace fgq

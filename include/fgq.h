@@ -163,6 +163,39 @@ fgq_status fgq_gemm_fp8_blockscaled_splitk(const uint8_t* A, const float* sA, co
  * current device (depends on its SM count).  Same size checks as the GEMM. */
 fgq_status fgq_gemm_splitk_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
 
+/* Size of the fixed scratch array behind fgq_gemm_fp8_blockscaled_splitk_noalloc. */
+#define FGQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * fgq_gemm_fp8_blockscaled_splitk without a workspace argument, for callers
+ * that cannot allocate device memory: code running inside an allocator or a
+ * memory-pool callback, hosts that give a library a fixed device-memory
+ * budget up front, embedders with no allocator of their own.  (The page has
+ * no counterpart to this; it is a convenience of this library.)
+ *
+ * The split-K scratch is a fixed array of FGQ_NOALLOC_SCRATCH_BYTES inside
+ * the library, present on every GPU that loads it until the process exits.
+ * This call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.  Arguments and result are those of
+ * fgq_gemm_fp8_blockscaled_splitk.
+ *   - A problem whose split-K workspace (fgq_gemm_splitk_workspace_size)
+ *     exceeds FGQ_NOALLOC_SCRATCH_BYTES returns FGQ_ERR_INVALID_ARG before
+ *     anything is launched.
+ *   - The first call on each device looks up the array's device address;
+ *     make that first call before capturing any stream on that device.
+ *   - Every call that splits K clears the part of the array that must
+ *     start at zero (the per-tile counters) on `stream` before its kernel
+ *     runs; the rest keeps the previous call's partial results, which are
+ *     always overwritten before they are read.
+ *   - All calls on a device share the one array: calls that can overlap on
+ *     the GPU (different streams without ordering between them) race and
+ *     give wrong results.  Order them, e.g. issue them on one stream.
+ */
+fgq_status fgq_gemm_fp8_blockscaled_splitk_noalloc(const uint8_t* A, const float* sA,
+                                                   const uint8_t* B, const float* sB, void* C,
+                                                   int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                                   int out, int mode, void* stream);
+
 /* Static description of a status code. */
 const char* fgq_status_string(fgq_status status);
 
