@@ -60,6 +60,21 @@ def outlier(shape, frac: float = 1e-3, factor: float = 100.0, seed: int = 0) -> 
     return x.to(torch.bfloat16)
 
 
+def exponent_spread(shape, spread: int, block_rows: int, seed: int = 0) -> torch.Tensor:
+    """N(0, 1) values, each block of block_rows x 128 entries multiplied by
+    2^e with e uniform in [-spread, spread] (exact in bf16): block_rows = 1
+    gives activation-like 1x128 groups of very different magnitudes,
+    block_rows = 128 the same for 128x128 weight blocks."""
+    g = _gen(seed)
+    rows, cols = shape
+    x = torch.randn(rows, cols, generator=g, dtype=torch.float32)
+    br = (rows + block_rows - 1) // block_rows
+    bc = (cols + 127) // 128
+    e = torch.randint(-spread, spread + 1, (br, bc), generator=g).to(torch.float32)
+    f = torch.exp2(e).repeat_interleave(block_rows, 0)[:rows].repeat_interleave(128, 1)[:, :cols]
+    return (x * f).to(torch.bfloat16)
+
+
 # Named workloads with their shapes and distributions.  Seeds are fixed so a
 # run on any machine regenerates the same bits.
 def tiny(seed: int = 0):

@@ -133,6 +133,9 @@ fgq_status fgq_gemm_fp8_blockscaled_ex(const uint8_t* A, const float* sA, const 
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M <= kLowMDirect)
     return from_cuda(fgq::launch_gemm_lowm(A, sA, B, sB, C, ldc, M, N, K, bf16, 1, nullptr, s, dev));
+  // power-of-two scales: applied by the tensor core, no promotion step
+  if (mode == FGQ_SCALE_UE8M0)
+    return from_cuda(fgq::launch_gemm_mx(A, sA, B, sB, C, ldc, M, N, K, bf16, s, dev));
   return from_cuda(fgq::launch_gemm_fp8_blockscaled(A, sA, B, sB, C, ldc, M, N, K, bf16, mode, s, dev));
 }
 
@@ -216,8 +219,15 @@ fgq_status fgq_device_error(uint32_t* word, int clear) {
   if (st != FGQ_OK) return st;
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return FGQ_ERR_CUDA;
-  e = fgq::read_device_error(word, clear != 0);
-  if (e != cudaSuccess) return FGQ_ERR_CUDA;
+  uint32_t w = 0;
+  for (auto read : {fgq::read_device_error_gemm, fgq::read_device_error_lowm,
+                    fgq::read_device_error_mx}) {
+    uint32_t u = 0;
+    e = read(&u, clear != 0);
+    if (e != cudaSuccess) return FGQ_ERR_CUDA;
+    w |= u;
+  }
+  *word = w;
   return *word ? FGQ_ERR_DEVICE_TIMEOUT : FGQ_OK;
 }
 

@@ -16,7 +16,7 @@ namespace fgq {
 
 // Device error word.  Zero while nothing has gone wrong; kernels OR in
 // FGQ_DEVERR_* bits.  Each translation unit that includes this header has
-// its own copy; the GEMM unit's copy is the one the C ABI reports.
+// its own copy; the C ABI reports the OR of the kernel units' copies.
 static __device__ unsigned int g_device_error = 0;
 
 constexpr unsigned long long FGQ_WAIT_NS = 2000000000ull;  // 2 s
@@ -179,6 +179,50 @@ __device__ __forceinline__ void umma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T, kind::mxf8f6f4 with UE8M0 scale
+// factors read from TMEM (scale_vec::1X: one factor per row of A and per
+// column of B for the instruction's K = 32).  Measured layout on sm_103a
+// for M = 128: the factor of A's row m is at lane m, column sfa_col + m/32;
+// the factor of B's column n is at lane 32*q + n%32, column sfb_col + n/32,
+// where q is the TMEM lane quarter of the D row being computed, so B's
+// factors are replicated in all four quarters.  idesc bits 29-30 / 4-5
+// select which byte of those 32-bit cells holds A's / B's factor.
+__device__ __forceinline__ void umma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem,
+                                              uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Store one 32-bit value per lane into column taddr.col of the warp's 32
+// TMEM lanes (lane taddr.lane + thread).
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v)
+               : "memory");
+}
+
+// Store four consecutive columns: a, a, a, a then b, b, b, b in the next four.
+__device__ __forceinline__ void tmem_st_32x32b_x8_aabb(uint32_t taddr, uint32_t a, uint32_t b) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %1, %1, %1, %2, %2, %2, %2};" ::"r"(
+                   taddr),
+               "r"(a), "r"(b)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t a) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %1, %1, %1};" ::"r"(taddr), "r"(a)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 op issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -295,6 +339,31 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(uint32_t smem_addr) {
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
   return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Instruction descriptor, kind::mxf8f6f4 (D fp32 implied), A and B E4M3,
+// both K-major, UE8M0 scale factors (bit 23), scale-factor byte 0 for A
+// (bits 29-30) and B (bits 4-5); OR in (id << 29) | (id << 4) to select
+// byte id of the scale-factor cells.
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3_ue8m0(int m, int n) {
+  return (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// Read (and optionally clear) this translation unit's copy of the device
+// error word.  Each unit with kernels that record errors exports a wrapper
+// around this; the C ABI reports the OR of all of them.
+static inline cudaError_t read_unit_device_error(uint32_t* word, bool clear) {
+  unsigned int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (clear && v != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) return e;
+  }
+  *word = v;
+  return cudaSuccess;
 }
 
 // ---- numeric conversions ------------------------------------------------------

@@ -13,6 +13,8 @@
 #define FGQ_DEVERR_MMA_TMEM 0x4u        // MMA issuer waiting for a drained TMEM buffer
 #define FGQ_DEVERR_EPI_TMEM 0x8u        // epilogue waiting for a finished partial
 #define FGQ_DEVERR_DRAIN 0x10u          // unwinding: waiting for copies in flight
+#define FGQ_DEVERR_SF_SLOT 0x20u        // scale-factor writer waiting for a free TMEM slot
+#define FGQ_DEVERR_MMA_SF 0x40u         // MMA issuer waiting for scale factors in TMEM
 
 namespace fgq {
 
@@ -39,7 +41,18 @@ cudaError_t launch_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const
                                         int64_t N, int64_t K, int out_bf16, int mode,
                                         cudaStream_t stream, const DeviceInfo& dev);
 
-cudaError_t read_device_error(uint32_t* word, bool clear);
+// Power-of-two (UE8M0) scales folded into the tensor core: same arguments
+// and result as launch_gemm_fp8_blockscaled for scales that are powers of
+// two.
+cudaError_t launch_gemm_mx(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                           void* C, int64_t ldc, int64_t M, int64_t N, int64_t K, int out_bf16,
+                           cudaStream_t stream, const DeviceInfo& dev);
+
+// Each kernel translation unit keeps its own device error word; these read
+// (and optionally clear) one unit's word.
+cudaError_t read_device_error_gemm(uint32_t* word, bool clear);
+cudaError_t read_device_error_lowm(uint32_t* word, bool clear);
+cudaError_t read_device_error_mx(uint32_t* word, bool clear);
 
 // TMA descriptor of a K-major E4M3 operand [rows, K] with a 128 (K) x
 // box_rows box, 128-byte swizzle, zero fill outside the tensor.

@@ -414,17 +414,8 @@ cudaError_t launch_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const
               : launch_cfg<128, 6, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
 }
 
-cudaError_t read_device_error(uint32_t* word, bool clear) {
-  unsigned int v = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
-  if (e != cudaSuccess) return e;
-  if (clear && v != 0) {
-    unsigned int zero = 0;
-    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
-    if (e != cudaSuccess) return e;
-  }
-  *word = v;
-  return cudaSuccess;
+cudaError_t read_device_error_gemm(uint32_t* word, bool clear) {
+  return read_unit_device_error(word, clear);
 }
 
 }  // namespace fgq

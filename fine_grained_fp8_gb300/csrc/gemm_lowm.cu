@@ -512,3 +512,11 @@ cudaError_t noalloc_scratch(const DeviceInfo& dev, void** ptr) {
 }
 
 }  // namespace fgq
+
+namespace fgq {
+
+cudaError_t read_device_error_lowm(uint32_t* word, bool clear) {
+  return read_unit_device_error(word, clear);
+}
+
+}  // namespace fgq

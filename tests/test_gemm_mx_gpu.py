@@ -1,0 +1,137 @@
+"""Parity of the GEMM's power-of-two scale path with the oracle.
+
+In UE8M0 mode the scales are applied by the tensor core itself (block-scaled
+MMA with the codes in TMEM; "Fine-Grained FP8/FP4 Quantization",
+§Blackwell: Native Block Scaling), not by promoting per-chunk partials.
+The bar is the one every GEMM test uses (§DeepGEMM):
+|C - C_ref| <= 2e-3 * sum_k |a_hat||b_hat| for the fp32 accumulator, plus
+half a bf16 ulp for bf16 outputs.  The cases cover both tile widths (128
+and 256 columns), K chunk counts that leave a partial group of four in the
+scale-factor ring, ragged M, scales spread over many binades, and the
+smallest code (2^-127).
+"""
+import numpy as np
+import pytest
+import torch
+
+import fgq_inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+UE8M0 = oracle.MODE_UE8M0
+
+
+def _quant(a, b, mode=UE8M0):
+    aq, sa = oracle.quant_act_1x128(a, mode)
+    bq, sb = oracle.quant_w_128x128(b, mode)
+    return aq, sa, bq, sb
+
+
+def _dev(aq, sa, bq, sb, dev):
+    return (torch.from_numpy(aq).to(dev), torch.from_numpy(sa).to(dev),
+            torch.from_numpy(np.ascontiguousarray(bq.T)).to(dev), torch.from_numpy(sb).to(dev))
+
+
+def _check(c_gpu, host, rows=None, cols=None):
+    if rows is None:
+        cref, tref = oracle.gemm_dequant(*host)
+        c = c_gpu.float().cpu().numpy().astype(np.float64)
+    else:
+        cref, tref = oracle.gemm_dequant_at(*host, rows, cols)
+        c = c_gpu.float().cpu().numpy()[rows, cols].astype(np.float64)
+    assert np.isfinite(c).all()
+    ok, ratio = oracle.gemm_within_tolerance(c, cref, tref, TOL,
+                                             out_bf16=c_gpu.dtype == torch.bfloat16)
+    assert ok, f"max |err|/T = {ratio:.3e} exceeds {TOL}"
+    return ratio
+
+
+# (M, N, K): 128-column tiles (too few 256-wide tiles, or N % 256 != 0);
+# 1, 5, 9 and 18 chunks (partial last group of the four-chunk slots, and
+# several passes around the four-slot ring)
+SHAPES = [(33, 384, 640), (128, 256, 128), (129, 640, 1152), (300, 128, 2304),
+          (1000, 512, 1024)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_ue8m0_narrow_tiles(fgq, cuda_dev, M, N, K, out_dtype):
+    a = fgq_inputs.exponent_spread((M, K), 20, 1, seed=M)
+    b = fgq_inputs.exponent_spread((K, N), 20, 128, seed=M + 1)
+    host = _quant(a, b)
+    c = fgq.gemm_fp8_blockscaled(*_dev(*host, cuda_dev), out_dtype=out_dtype, mode="ue8m0")
+    torch.cuda.synchronize()
+    _check(c, host)
+
+
+@pytest.mark.parametrize("M,K", [(1280, 640), (1200, 1152)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_ue8m0_wide_tiles(fgq, cuda_dev, M, K, out_dtype):
+    """N = 4096 with at least one 128x256 tile per SM: the 256-column tile
+    (one accumulator, the next tile waits for the epilogue's read)."""
+    N = 4096
+    a = fgq_inputs.exponent_spread((M, K), 12, 1, seed=7)
+    b = fgq_inputs.exponent_spread((K, N), 12, 128, seed=8)
+    host = _quant(a, b)
+    c = fgq.gemm_fp8_blockscaled(*_dev(*host, cuda_dev), out_dtype=out_dtype, mode="ue8m0")
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(M)
+    rows = np.concatenate([rng.integers(0, M, 4000), np.arange(M - 8, M), [0]])
+    cols = np.concatenate([rng.integers(0, N, 4000), np.arange(N - 8, N), [0]])
+    _check(c, host, rows, cols)
+    # every row of the last (ragged) tile row and every column block
+    r2 = np.repeat(np.arange(M - 64, M), N // 128)
+    c2 = np.tile(np.arange(0, N, 128) + 127, 64)
+    _check(c, host, r2, c2)
+
+
+def test_ue8m0_matches_the_promotion_path(fgq, cuda_dev):
+    """Power-of-two scales also go through the fp32-scale (promotion)
+    kernel: both results lie within the bound of the oracle."""
+    M, N, K = 520, 768, 1536
+    a = fgq_inputs.exponent_spread((M, K), 10, 1, seed=11)
+    b = fgq_inputs.exponent_spread((K, N), 10, 128, seed=12)
+    host = _quant(a, b)
+    ops = _dev(*host, cuda_dev)
+    c_mx = fgq.gemm_fp8_blockscaled(*ops, out_dtype=torch.float32, mode="ue8m0")
+    c_pr = fgq.gemm_fp8_blockscaled(*ops, out_dtype=torch.float32, mode="fp32")
+    torch.cuda.synchronize()
+    _check(c_mx, host)
+    _check(c_pr, host)
+
+
+def test_ue8m0_extreme_codes(fgq, cuda_dev):
+    """Rows whose scales clamp at the smallest code (2^-127), all-zero rows
+    (scale 1), and rows 2^30 larger, against weights scaled by 2^40: every
+    product stays a normal fp32 number, so the bound holds for each row."""
+    M, N, K = 256, 384, 512
+    a = fgq_inputs.normal((M, K), 1.0, seed=21).float()
+    rowf = torch.ones(M)
+    rowf[0:32] = 2.0 ** -122     # amax/448 below 2^-127 (amax < 14): code 0
+    rowf[32:40] = 0.0            # zero groups: scale 1 (code 127)
+    rowf[40:72] = 2.0 ** 30
+    a = (a * rowf[:, None]).to(torch.bfloat16)
+    b = (fgq_inputs.normal((K, N), 0.02, seed=22).float() * 2.0 ** 40).to(torch.bfloat16)
+    host = _quant(a, b)
+    assert (host[1][0:32] == 2.0 ** -127).all(), "the tiny rows should take the smallest code"
+    c = fgq.gemm_fp8_blockscaled(*_dev(*host, cuda_dev), out_dtype=torch.float32, mode="ue8m0")
+    torch.cuda.synchronize()
+    _check(c, host)
+    assert (c[32:40] == 0).all()
+
+
+def test_ue8m0_repeat_calls_are_identical(fgq, cuda_dev):
+    M, N, K = 700, 1024, 2048
+    a = fgq_inputs.exponent_spread((M, K), 8, 1, seed=31)
+    b = fgq_inputs.exponent_spread((K, N), 8, 128, seed=32)
+    ops = _dev(*_quant(a, b), cuda_dev)
+    c1 = fgq.gemm_fp8_blockscaled(*ops, out_dtype=torch.bfloat16, mode="ue8m0")
+    c2 = fgq.gemm_fp8_blockscaled(*ops, out_dtype=torch.bfloat16, mode="ue8m0")
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)
+
+
+def test_no_device_error_after_ue8m0(fgq, cuda_dev):
+    assert fgq.device_error() == 0
