@@ -354,6 +354,45 @@ def run_fgq(args):
     barrier(dist)
     e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev) / e2e_steps
 
+    # The same step with power-of-two (UE8M0) scales: the quantizers round
+    # each scale up to 2^k and the GEMM applies the scales inside the tensor
+    # core (block-scaled MMA) instead of promoting every K chunk.
+    ue8m0 = None
+    if not args.no_ue8m0:
+        usteps = max(10, min(args.steps, 500))
+
+        def ustep(i, ev):
+            a, b = sets[i % 2]
+            ev[0].record(stream)
+            fgq.quant_act_1x128(a, "ue8m0", xq=aq, sx=sa)
+            ev[1].record(stream)
+            fgq.quant_w_128x128(b, "ue8m0", wq=bq, sw=sb)
+            ev[2].record(stream)
+            fgq.gemm_fp8_blockscaled(aq, sa, bq, sb, torch.bfloat16, "ue8m0", out=c)
+            ev[3].record(stream)
+
+        uev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(usteps)]
+        for i in range(5):
+            ustep(i, uev[i])
+        torch.cuda.synchronize()
+        u0 = torch.cuda.Event(enable_timing=True)
+        u1 = torch.cuda.Event(enable_timing=True)
+        u0.record(stream)
+        for i in range(usteps):
+            ustep(i, uev[i])
+        u1.record(stream)
+        torch.cuda.synchronize()
+        ums = reduce_max(dist, u0.elapsed_time(u1), dev) / usteps
+        uper = [[e[j].elapsed_time(e[j + 1]) for e in uev] for j in range(3)]
+        u_act, u_w, u_gemm = (1e3 * sum(p) / len(p) for p in uper)
+        ue8m0 = {"scale_mode": "ue8m0", "steps": usteps, "ms_per_step": ums,
+                 "value": world * FLOPS_GEMM / (ums * 1e-3) / 1e12, "unit": "TFLOP/s",
+                 "quant_act_us": u_act, "quant_w_us": u_w, "gemm_us": u_gemm,
+                 "gemm_TFLOP/s": FLOPS_GEMM / (u_gemm * 1e-6) / 1e12,
+                 "kernel": "gemm_mx_kernel (tcgen05.mma kind::mxf8f6f4.block_scale)"}
+        if fgq.device_error() != 0:
+            raise SystemExit("a kernel reported a device wait timeout")
+
     # The quantizers on the quantize-bandwidth workload (activations
     # [16384, 7168] Student-t nu=3, weight [7168, 7168] N(0, 0.02^2)), each
     # timed alone over rotated input pairs larger than L2.
@@ -390,6 +429,61 @@ def run_fgq(args):
         if fgq.device_error() != 0:
             raise SystemExit("a kernel reported a device wait timeout")
 
+    # The skinny sweep (M in {16, 64, 256} x N = 24576 x K = 1536, bf16 out):
+    # the low-M GEMM paths, bound by streaming the 37.7 MB of weight codes.
+    # Four weight copies (151 MB, more than L2) are rotated, and the launches
+    # are replayed from a CUDA graph so host launch time does not count.
+    skinny = None
+    if not args.no_skinny:
+        SN, SK = 24576, 1536
+        skinny = {"workload": "skinny: M x N=24576 x K=1536, A N(0,1), B N(0,0.02^2), bf16 out; "
+                              "4 weight copies rotated (151 MB > L2); CUDA-graph replay"}
+        wcopies = []
+        for i in range(4):
+            bsk = fgq_inputs.skinny(16, seed=10 + i)[1].to(dev)
+            wcopies.append(fgq.quant_w_128x128(bsk))
+            del bsk
+        for Ms in (16, 64, 256):
+            ask = fgq_inputs.skinny(Ms, seed=Ms)[0].to(dev)
+            aqs, sas = fgq.quant_act_1x128(ask)
+            cs = torch.empty((Ms, SN), dtype=torch.bfloat16, device=dev)
+            ws = fgq.splitk_workspace(Ms, SN, SK, dev)
+            entry = {}
+            for name, fn in (
+                    ("gemm_fp8_blockscaled", lambda j: fgq.gemm_fp8_blockscaled(
+                        aqs, sas, *wcopies[j % 4], torch.bfloat16, out=cs)),
+                    ("gemm_fp8_blockscaled_splitk", lambda j: fgq.gemm_fp8_blockscaled_splitk(
+                        aqs, sas, *wcopies[j % 4], ws, torch.bfloat16, out=cs))):
+                for j in range(8):
+                    fn(j)
+                torch.cuda.synchronize()
+                reps = 40
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for j in range(reps):
+                        fn(j)
+                g.replay()
+                torch.cuda.synchronize()
+                g0 = torch.cuda.Event(enable_timing=True)
+                g1 = torch.cuda.Event(enable_timing=True)
+                g0.record(stream)
+                for _ in range(5):
+                    g.replay()
+                g1.record(stream)
+                torch.cuda.synchronize()
+                us = reduce_max(dist, g0.elapsed_time(g1), dev) * 1e3 / (5 * reps)
+                entry[name] = {"us": us}
+            nbytes = SN * SK + Ms * SK + Ms * SN * 2 + Ms * (SK // 128) * 4 + (SK // 128) * (SN // 128) * 4
+            for name in entry:
+                us = entry[name]["us"]
+                entry[name]["GB/s"] = nbytes / (us * 1e-6) / 1e9
+                entry[name]["TFLOP/s"] = 2 * Ms * SN * SK / (us * 1e-6) / 1e12
+            skinny[f"M{Ms}"] = {"bytes": nbytes, "flops": 2 * Ms * SN * SK, **entry}
+            del ask, aqs, sas, cs, ws
+        del wcopies
+        if fgq.device_error() != 0:
+            raise SystemExit("a kernel reported a device wait timeout")
+
     # CPU baseline: the oracle on a bounded sample, rank 0 only, N = 1 only.
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -413,7 +507,15 @@ def run_fgq(args):
     if quant_bw:
         for k in ("quant_act_1x128", "quant_w_128x128"):
             quant_bw[k]["frac_hbm"] = quant_bw[k]["GB/s"] / peaks["hbm_gbs"]
+    if skinny:
+        for k, v in skinny.items():
+            if isinstance(v, dict):
+                for e in v.values():
+                    if isinstance(e, dict):
+                        e["frac_hbm"] = e["GB/s"] / peaks["hbm_gbs"]
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]  # nominal fp8 = 2x bf16 dense
+    if ue8m0:
+        ue8m0["frac_fp8"] = ue8m0["gemm_TFLOP/s"] / fp8_peak
     hbm = peaks["hbm_gbs"]
     gemm_tflops = FLOPS_GEMM / (us_gemm * 1e-6) / 1e12
     act_gbs = BYTES_QUANT_ACT / (us_act * 1e-6) / 1e9
@@ -447,6 +549,8 @@ def run_fgq(args):
                 "ms_per_step": e2e_ms, "steps": e2e_steps},
         "gpu_launches": 3 * args.steps,
         "quant_bw": quant_bw,
+        "ue8m0": ue8m0,
+        "skinny": skinny,
         "clocks": clk,
         "cpu_baseline": cpu,
     }
@@ -465,6 +569,10 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-quant-bw", action="store_true",
                    help="skip the separate quantize-bandwidth measurement")
+    p.add_argument("--no-ue8m0", action="store_true",
+                   help="skip the power-of-two scale (UE8M0) step")
+    p.add_argument("--no-skinny", action="store_true",
+                   help="skip the skinny-GEMM sweep")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")

@@ -66,12 +66,14 @@ def test_ue8m0_narrow_tiles(fgq, cuda_dev, M, N, K, out_dtype):
     _check(c, host)
 
 
-@pytest.mark.parametrize("M,K", [(1280, 640), (1200, 1152)])
+@pytest.mark.parametrize("M,N,K", [(1280, 4096, 640), (1200, 4096, 1152), (1100, 4096, 640),
+                                   (384, 8192, 512)])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
-def test_ue8m0_wide_tiles(fgq, cuda_dev, M, K, out_dtype):
-    """N = 4096 with at least one 128x256 tile per SM: the 256-column tile
-    (one accumulator, the next tile waits for the epilogue's read)."""
-    N = 4096
+def test_ue8m0_large_n(fgq, cuda_dev, M, N, K, out_dtype):
+    """M = 1280 and 1200 with N = 4096 give at least one 128 x 256 tile per
+    SM (one accumulator; the next tile waits for the epilogue's read), the
+    last one ragged for M = 1200; M = 1100 and 384 fall back to 128 x 128
+    tiles with a ragged last tile row."""
     a = fgq_inputs.exponent_spread((M, K), 12, 1, seed=7)
     b = fgq_inputs.exponent_spread((K, N), 12, 128, seed=8)
     host = _quant(a, b)
