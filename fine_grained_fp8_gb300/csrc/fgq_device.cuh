@@ -65,6 +65,38 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t nthreads
   return r != 0;
 }
 
+// ---- programmatic dependent launch -----------------------------------------------
+
+// Wait until the kernels this grid depends on (the previous kernel in the
+// stream, when launched with launch_pdl) have completed and their memory
+// is visible.  No-op when the launch had no programmatic dependency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next kernel in the stream (if launched with launch_pdl) start its
+// set-up now; it still waits in pdl_wait() for this grid to complete.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with programmatic stream serialization: the kernel may begin
+// before the previous kernel in the stream has finished, and must call
+// pdl_wait() before it touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // ---- mbarrier ---------------------------------------------------------------
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

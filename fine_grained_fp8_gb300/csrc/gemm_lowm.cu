@@ -17,6 +17,12 @@
 //   - Persistent CTAs over units; warp 0 = TMA producer, warp 1 = MMA
 //     issuer, warps 4-11 = promotion epilogue (each warp: 32 n-rows x MP/2
 //     columns), the same roles and bounded waits as gemm.cu.
+//   - Batched promotion: the partials of kBatch = 256 / MP consecutive K
+//     chunks go to adjacent TMEM slices of one of two slots, and the
+//     epilogue waits once per batch, promotes its chunks with the next
+//     slice's load in flight, and hands the slot back.  With the tensor
+//     core filling the other slot meanwhile, the per-chunk wait and load
+//     latency of the epilogue is off the weight stream's critical path.
 // The per-(row, chunk) scales sA[m, c] are staged in shared memory in
 // windows of 16 chunks, transposed ([chunk][m]), so the epilogue reads them
 // as broadcast values.
@@ -51,27 +57,41 @@ struct LowCfg {
   static constexpr int kABytes = MP * BK;        // activation tile (MMA operand B)
   static constexpr int kStageBytes = kBBytes + kABytes;
   static constexpr int STAGES = MP <= 64 ? 6 : 4;
-  // TMEM partial buffers: four when they fit, so that the hand-off latency
-  // between the tensor core and the epilogue is hidden for small tiles.
-  static constexpr int NB = MP <= 128 ? 4 : 2;
-  static constexpr int kTmemCols = (NB * MP < 32) ? 32 : NB * MP;
+  // Two TMEM slots of kBatch chunk partials each (MP columns per partial).
+  static constexpr int kBatch = MP >= 256 ? 1 : 256 / MP;
+  static constexpr int kSlotCols = kBatch * MP;
+  static constexpr int kTmemCols = 2 * kSlotCols;
   static constexpr int kScaleBytes = kScaleWindow * MP * 4;
-  static constexpr int kBarBytes = (2 * STAGES + 2 * NB) * 8 + 16;
+  static constexpr int kBarBytes = (2 * STAGES + 5) * 8 + 16;
   static constexpr size_t kSmemBytes =
       1024 + static_cast<size_t>(STAGES) * kStageBytes + kScaleBytes + kBarBytes + 16;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(MP % 16 == 0 && MP >= 16 && MP <= 256, "MMA N");
+  static_assert(kTmemCols == 512, "TMEM allocation");
+  static_assert(kScaleWindow % kBatch == 0, "a batch never straddles a scale window");
 };
 
-// Loads of 8, 16 or 32 consecutive TMEM columns for the 32 lanes of a warp.
+// Loads of W consecutive TMEM columns into r[0..W-1] (r points into a
+// register array at a compile-time offset).
 template <int W>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[32]);
+__device__ __forceinline__ void tmem_ld_cols_to(uint32_t taddr, uint32_t* r);
 template <>
-__device__ __forceinline__ void tmem_ld_cols<32>(uint32_t taddr, uint32_t (&r)[32]) {
-  tmem_ld_32x32b_x32(taddr, r);
+__device__ __forceinline__ void tmem_ld_cols_to<32>(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
 }
 template <>
-__device__ __forceinline__ void tmem_ld_cols<16>(uint32_t taddr, uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_ld_cols_to<16>(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
       "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
@@ -82,13 +102,21 @@ __device__ __forceinline__ void tmem_ld_cols<16>(uint32_t taddr, uint32_t (&r)[3
       : "memory");
 }
 template <>
-__device__ __forceinline__ void tmem_ld_cols<8>(uint32_t taddr, uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_ld_cols_to<8>(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7])
       : "r"(taddr)
       : "memory");
+}
+
+// Wait for outstanding TMEM loads, tying 64 destination registers to the
+// wait (the second wait finds nothing outstanding and only ties the upper
+// half) so that no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld_regs64(uint32_t* r) {
+  tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(r));
+  tmem_wait_ld_regs(*reinterpret_cast<uint32_t(*)[32]>(r + 32));
 }
 
 // Bounded wait used while unwinding; ignores the abort flag.
@@ -142,10 +170,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sm_sa = reinterpret_cast<float*>(sm_a + STAGES * CF::kABytes);  // [chunk][MP]
   uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sm_sa) + CF::kScaleBytes);
   uint64_t* empty = full + STAGES;
-  constexpr int NB = CF::NB;
-  uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + NB;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + NB);
+  constexpr int kBatch = CF::kBatch;
+  uint64_t* tfull = empty + STAGES;   // [2] slot holds a finished batch
+  uint64_t* tempty = tfull + 2;       // [2] slot drained by the epilogue
+  uint64_t* drain = tempty + 2;       // the MMA issuer's last commit
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
@@ -164,10 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < NB; ++b) {
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], kEpiWarps);
     }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tmap_w);
@@ -181,6 +211,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above (barrier set-up, TMEM allocation) may overlap the
+  // previous kernel in the stream; global memory is touched only after it
+  // has completed.
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (warp < kCtlWarps) {
     setmaxnreg_dec<kCtlRegs>();
@@ -219,22 +254,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dW0 = smem_desc_k_sw128(smem_u32(sm_w));
         const uint32_t w_lo0 = static_cast<uint32_t>(dW0), dhi = static_cast<uint32_t>(dW0 >> 32);
         const uint32_t a_lo0 = static_cast<uint32_t>(smem_desc_k_sw128(smem_u32(sm_a)));
-        uint32_t it = 0;
+        uint32_t bt = 0;  // batches issued
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < sched.total && ok; u += gridDim.x) {
           int nt, sp, c0, c1;
           sched.unit(u, nt, sp, c0, c1);
-          for (int kc = c0; kc < c1; ++kc, ++it) {
-            const uint32_t buf = it % NB, tph = (it / NB) & 1u;
-            if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, FGQ_DEVERR_MMA_TMEM) ||
-                !mbar_wait(&full[s], ph, abort_flag, FGQ_DEVERR_MMA_FULL)) {
+          for (int kc = c0; kc < c1; ++kc) {
+            const int j = (kc - c0) % kBatch;
+            const uint32_t slot = bt & 1u;
+            if (j == 0 && !mbar_wait(&tempty[slot], ((bt >> 1) & 1u) ^ 1u, abort_flag,
+                                     FGQ_DEVERR_MMA_TMEM)) {
+              ok = false;
+              break;
+            }
+            if (!mbar_wait(&full[s], ph, abort_flag, FGQ_DEVERR_MMA_FULL)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t d = tmem_base + buf * MP;
+            const uint32_t d = tmem_base + slot * CF::kSlotCols + j * MP;
             const uint32_t w_lo = w_lo0 + s * (CF::kBBytes >> 4);
             const uint32_t a_lo = a_lo0 + s * (CF::kABytes >> 4);
 #pragma unroll
@@ -242,14 +282,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               umma_f8f6f4(d, make_desc(w_lo + kk * 2, dhi), make_desc(a_lo + kk * 2, dhi), idesc,
                              kk > 0 ? 1u : 0u);
             umma_commit(&empty[s]);
-            umma_commit(&tfull[buf]);
+            if (j == kBatch - 1 || kc == c1 - 1) {
+              umma_commit(&tfull[slot]);
+              ++bt;
+            }
             if (++s == STAGES) {
               s = 0;
               ph ^= 1u;
             }
           }
         }
-        if (it > 0) lowm_wait_drain(&tfull[(it - 1) % NB], ((it - 1) / NB) & 1u);
+        // Every MMA this thread issued must finish before TMEM is released:
+        // a last commit, on a barrier of its own, covers all of them (also
+        // after giving up mid-batch).
+        umma_commit(drain);
+        lowm_wait_drain(drain, 0);
       }
       __syncwarp();
     }
@@ -262,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r_in_tile = quad * 32 + lane;         // weight row within the tile
     const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
     const int m0 = half * HALF;                     // first column (row of A) of this warp
-    uint32_t it = 0;
+    uint32_t bt = 0;  // batches consumed
     bool ok = true;
     for (int u = blockIdx.x; u < sched.total && ok; u += gridDim.x) {
       int nt, sp, c0, c1;
@@ -273,47 +320,85 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < HALF; ++j) acc[j] = 0.0f;
       bool ok_unit = true;
-      float sb_next = __ldg(sB + static_cast<int64_t>(c0) * nb + nt);
-      for (int kc = c0; kc < c1; ++kc, ++it) {
+      for (int kb = c0; kb < c1; kb += kBatch, ++bt) {
+        const int nbt = min(kBatch, c1 - kb);
         // Stage sA[m, window] transposed as [chunk][m] (zero for m >= M) at
-        // the start of every window of kScaleWindow chunks.  Every epilogue
-        // warp runs every iteration (a warp that gave up on a wait only
-        // skips the work), so all of them reach these barriers.
-        const int w = (kc - c0) % kScaleWindow;
-        if (w == 0) {
+        // the start of every window of kScaleWindow chunks (a whole number
+        // of batches).  Every epilogue warp runs every batch (a warp that
+        // gave up on a wait only skips the work), so all of them reach
+        // these barriers.
+        const int w0 = (kb - c0) % kScaleWindow;
+        if (w0 == 0) {
           named_barrier_sync(kEpiBarrier, 32 * kEpiWarps);  // earlier readers done
-          const int nck = min(kScaleWindow, c1 - kc);
+          const int nck = min(kScaleWindow, c1 - kb);
           for (int i = et; i < nck * MP; i += 32 * kEpiWarps) {
             const int c = i / MP, m = i - c * MP;
-            sm_sa[i] = m < M ? __ldg(sA + static_cast<int64_t>(m) * kchunks + kc + c) : 0.0f;
+            sm_sa[i] = m < M ? __ldg(sA + static_cast<int64_t>(m) * kchunks + kb + c) : 0.0f;
           }
           named_barrier_sync(kEpiBarrier, 32 * kEpiWarps);
         }
-        const uint32_t buf = it % NB, tph = (it / NB) & 1u;
-        const float sb = sb_next;
-        if (kc + 1 < c1) sb_next = __ldg(sB + static_cast<int64_t>(kc + 1) * nb + nt);
         if (!ok_unit) continue;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull[buf], tph, abort_flag, FGQ_DEVERR_EPI_TMEM))) {
+        const uint32_t slot = bt & 1u;
+        if (!__all_sync(0xFFFFFFFFu,
+                        mbar_wait(&tfull[slot], (bt >> 1) & 1u, abort_flag, FGQ_DEVERR_EPI_TMEM))) {
           ok_unit = false;
           continue;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + t_lane + buf * MP + m0;
-        const float* sa_c = sm_sa + w * MP + m0;
-        uint32_t r[32];
+        // partial of chunk j of the batch: TMEM columns slot*kSlotCols + j*MP
+        const uint32_t taddr = tmem_base + t_lane + slot * CF::kSlotCols + m0;
+        if (NLD == 1) {
+          // waves of P chunks: P loads in flight, one wait, then P promotions
+          constexpr int P = 64 / LW;
+          for (int j0 = 0; j0 < nbt; j0 += P) {
+            float sbv[P];
+            uint32_t r[64];
 #pragma unroll
-        for (int q = 0; q < NLD; ++q) {
-          tmem_ld_cols<LW>(taddr + q * LW, r);
-          tmem_wait_ld_regs(r);
-          if (q + 1 == NLD) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_relaxed(&tempty[buf]);
+            for (int p = 0; p < P; ++p) {
+              const int j = j0 + p < nbt ? j0 + p : nbt - 1;  // repeat the last in-range chunk
+              sbv[p] = __ldg(sB + static_cast<int64_t>(kb + j) * nb + nt);
+              tmem_ld_cols_to<LW>(taddr + j * MP, r + p * LW);
+            }
+            tmem_wait_ld_regs64(r);
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+              if (j0 + p < nbt) {
+                const float* sa_c = sm_sa + (w0 + j0 + p) * MP + m0;
+#pragma unroll
+                for (int jj = 0; jj < LW; ++jj)
+                  acc[jj] = fmaf(__uint_as_float(r[p * LW + jj]), sa_c[jj] * sbv[p], acc[jj]);
+              }
+            }
           }
+        } else {
+          for (int j = 0; j < nbt; ++j) {
+            const float sb = __ldg(sB + static_cast<int64_t>(kb + j) * nb + nt);
+            const float* sa_c = sm_sa + (w0 + j) * MP + m0;
+            if (NLD == 2) {  // both halves in flight, one wait
+              uint32_t r[64];
+              tmem_ld_cols_to<LW>(taddr + j * MP, r);
+              tmem_ld_cols_to<LW>(taddr + j * MP + LW, r + LW);
+              tmem_wait_ld_regs64(r);
 #pragma unroll
-          for (int j = 0; j < LW; ++j)
-            acc[q * LW + j] = fmaf(__uint_as_float(r[j]), sa_c[q * LW + j] * sb, acc[q * LW + j]);
+              for (int jj = 0; jj < 2 * LW; ++jj)
+                acc[jj] = fmaf(__uint_as_float(r[jj]), sa_c[jj] * sb, acc[jj]);
+            } else {  // a 128-column accumulator leaves room for one load at a time
+#pragma unroll
+              for (int q = 0; q < NLD; ++q) {
+                uint32_t r[32];
+                tmem_ld_cols_to<LW>(taddr + j * MP + q * LW, r);
+                tmem_wait_ld_regs(r);
+#pragma unroll
+                for (int jj = 0; jj < LW; ++jj)
+                  acc[q * LW + jj] = fmaf(__uint_as_float(r[jj]), sa_c[q * LW + jj] * sb, acc[q * LW + jj]);
+              }
+            }
+          }
         }
+        // every partial of the batch is in registers: hand the slot back
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_relaxed(&tempty[slot]);
       }
       // Every epilogue warp reaches this barrier once per unit, whether it
       // finished its chunks or gave up on a wait; continue only together.
@@ -407,9 +492,8 @@ cudaError_t launch_lowm(const uint8_t* A, const float* sA, const uint8_t* B, con
   const int cps = (kchunks + splits - 1) / splits;
   const int units = (N / BN) * splits;
   const int grid = units < dev.sm_count ? units : dev.sm_count;
-  kern<<<grid, kThreads, CF::kSmemBytes, stream>>>(tw, ta, sA, sB, C, ldc, M, N, K, splits, cps,
-                                                   partial, counters);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), CF::kSmemBytes, stream, tw, ta, sA, sB, C,
+                    ldc, M, N, K, splits, cps, partial, counters);
 }
 
 template <bool OUT_BF16>

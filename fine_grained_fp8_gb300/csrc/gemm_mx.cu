@@ -166,6 +166,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Everything above (barrier set-up, TMEM allocation) may overlap the
+  // previous kernel in the stream; global memory is touched only after it
+  // has completed.
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -374,8 +379,8 @@ cudaError_t launch_mx_cfg(const uint8_t* A, const float* sA, const uint8_t* B, c
     return cudaErrorInvalidValue;
   const int tiles = ((M + BM - 1) / BM) * (N / BN);
   const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
-  kern<<<grid, kThreads, CF::kSmemBytes, stream>>>(ta, tb, sA, sB, C, ldc, M, N, K);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), CF::kSmemBytes, stream, ta, tb, sA, sB, C,
+                    ldc, M, N, K);
 }
 
 }  // namespace

@@ -40,8 +40,11 @@ def _check(c_gpu, host, rows=None, cols=None):
     assert ok, f"max |err|/T = {ratio:.3e} exceeds {TOL}"
 
 
-SHAPES = [(1, 384, 512), (7, 128, 256), (16, 640, 384), (33, 256, 1024), (64, 384, 512),
-          (100, 256, 384), (128, 512, 256), (200, 384, 640), (256, 256, 512)]
+# M covers every padded width (16, 32, 64, 128, 256); K covers one batch of
+# chunk partials, several, and a short last batch
+SHAPES = [(1, 384, 512), (7, 128, 256), (16, 640, 384), (24, 384, 1536), (32, 256, 2304),
+          (33, 256, 1024), (64, 384, 512), (100, 256, 384), (128, 512, 256), (200, 384, 640),
+          (256, 256, 512)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -104,7 +107,26 @@ def test_splitk_rejects_small_workspace(fgq, cuda_dev):
     _check(c, host)
 
 
-@pytest.mark.parametrize("M", [16, 64, 256])
+def test_lowm_repeated_calls_complete(fgq, cuda_dev):
+    """Many back-to-back calls at the skinny size for every padded width:
+    each finishes without a kernel giving up on a wait, and repeats agree."""
+    N, K = 24576, 1536
+    for M in (16, 32, 64):
+        a, b = fgq_inputs.skinny(M, seed=3)
+        aq, sa = fgq.quant_act_1x128(a.to(cuda_dev))
+        bq, sb = fgq.quant_w_128x128(b.to(cuda_dev))
+        ws = fgq.splitk_workspace(M, N, K)
+        first = fgq.gemm_fp8_blockscaled(aq, sa, bq, sb, out_dtype=torch.bfloat16)
+        for _ in range(30):
+            c = fgq.gemm_fp8_blockscaled(aq, sa, bq, sb, out_dtype=torch.bfloat16)
+            cs = fgq.gemm_fp8_blockscaled_splitk(aq, sa, bq, sb, ws, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        assert fgq.device_error() == 0, f"M={M}: a kernel gave up on a wait"
+        assert torch.equal(c, first)
+        assert torch.isfinite(cs.float()).all()
+
+
+@pytest.mark.parametrize("M", [16, 32, 64, 256])
 def test_skinny_full_size_splitk(fgq, cuda_dev, M):
     """M x N=24576 x K=1536, bf16 C, split-K path; sampled outputs."""
     a, b = fgq_inputs.skinny(M, seed=0)
