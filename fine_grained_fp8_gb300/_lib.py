@@ -38,6 +38,7 @@ SIGNATURES = {
     "fgq_gemm_splitk_workspace_size": (_int, [_i64, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
     "fgq_gemm_fp8_blockscaled_splitk_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
                                                        _i64, _int, _int, _vp]),
+    "fgq_selftest_wait_timeout": (_int, [_vp]),
     "fgq_status_string": (ctypes.c_char_p, [_int]),
     "fgq_device_error": (_int, [ctypes.POINTER(ctypes.c_uint32), _int]),
     "fgq_version": (_int, []),
@@ -129,6 +130,10 @@ def fgq_device_error(clear: bool = True):
     word = ctypes.c_uint32(0)
     st = load().fgq_device_error(ctypes.byref(word), 1 if clear else 0)
     return st, int(word.value)
+
+
+def fgq_selftest_wait_timeout(stream) -> int:
+    return load().fgq_selftest_wait_timeout(stream)
 
 
 def fgq_version() -> int:

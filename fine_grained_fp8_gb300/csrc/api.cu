@@ -231,6 +231,13 @@ fgq_status fgq_device_error(uint32_t* word, int clear) {
   return *word ? FGQ_ERR_DEVICE_TIMEOUT : FGQ_OK;
 }
 
+fgq_status fgq_selftest_wait_timeout(void* stream) {
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_selftest_wait_timeout(static_cast<cudaStream_t>(stream)));
+}
+
 int fgq_version(void) { return 100; }
 
 }  // extern "C"

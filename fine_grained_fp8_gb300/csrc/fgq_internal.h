@@ -15,6 +15,7 @@
 #define FGQ_DEVERR_DRAIN 0x10u          // unwinding: waiting for copies in flight
 #define FGQ_DEVERR_SF_SLOT 0x20u        // scale-factor writer waiting for a free TMEM slot
 #define FGQ_DEVERR_MMA_SF 0x40u         // MMA issuer waiting for scale factors in TMEM
+#define FGQ_DEVERR_SELFTEST 0x80u       // the self-test's wait on a barrier nothing completes
 
 namespace fgq {
 
@@ -47,6 +48,10 @@ cudaError_t launch_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const
 cudaError_t launch_gemm_mx(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                            void* C, int64_t ldc, int64_t M, int64_t N, int64_t K, int out_bf16,
                            cudaStream_t stream, const DeviceInfo& dev);
+
+// Diagnostic: one warp waits, with the kernels' bounded wait, on a barrier
+// that nothing completes; the wait gives up and records FGQ_DEVERR_SELFTEST.
+cudaError_t launch_selftest_wait_timeout(cudaStream_t stream);
 
 // Each kernel translation unit keeps its own device error word; these read
 // (and optionally clear) one unit's word.

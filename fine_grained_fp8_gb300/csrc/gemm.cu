@@ -419,6 +419,30 @@ cudaError_t launch_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const
               : launch_cfg<128, 6, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
 }
 
+namespace {
+
+// One warp: thread 0 sets up a barrier that expects one arrival, and no
+// thread ever arrives, so the bounded wait (the one every kernel here uses)
+// runs out after FGQ_WAIT_NS, records its site and returns.
+__global__ void selftest_wait_timeout_kernel() {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, FGQ_DEVERR_SELFTEST);
+}
+
+}  // namespace
+
+cudaError_t launch_selftest_wait_timeout(cudaStream_t stream) {
+  selftest_wait_timeout_kernel<<<1, 32, 0, stream>>>();
+  return cudaGetLastError();
+}
+
 cudaError_t read_device_error_gemm(uint32_t* word, bool clear) {
   return read_unit_device_error(word, clear);
 }

@@ -207,6 +207,18 @@ const char* fgq_status_string(fgq_status status);
  */
 fgq_status fgq_device_error(uint32_t* word, int clear);
 
+/*
+ * Diagnostic for the failure path of every kernel's waits (the pages have
+ * no counterpart; it checks this library's own error reporting).  Launches
+ * one warp that waits, with the same bounded wait the GEMM kernels use, on
+ * an mbarrier that nothing ever completes.  After about 2 s the wait gives
+ * up, sets bit 0x80 of the device error word and the kernel returns; no
+ * fault, and the context stays usable.  Afterwards fgq_device_error(&w, 1)
+ * returns FGQ_ERR_DEVICE_TIMEOUT with (w & 0x80) != 0 and clears the word.
+ * Asynchronous on `stream`; returns FGQ_ERR_CUDA if the launch fails.
+ */
+fgq_status fgq_selftest_wait_timeout(void* stream);
+
 /* Library ABI version (major * 10000 + minor * 100 + patch). */
 int fgq_version(void);
 
