@@ -233,8 +233,26 @@ __global__ void __launch_bounds__(kActThreads)
 // conflicts.
 constexpr int kWThreads = 256;
 
+// Transpose a 4x4 byte matrix held as four row words r0..r3 (byte b of r_i
+// = element (i, b)) into column words c0..c3 (byte i of c_b = element (i, b)).
+__device__ __forceinline__ void transpose4x4_bytes(uint32_t r0, uint32_t r1, uint32_t r2,
+                                                   uint32_t r3, uint32_t& c0, uint32_t& c1,
+                                                   uint32_t& c2, uint32_t& c3) {
+  const uint32_t t0 = __byte_perm(r0, r1, 0x5140);  // r0.b0 r1.b0 r0.b1 r1.b1
+  const uint32_t t1 = __byte_perm(r0, r1, 0x7362);  // r0.b2 r1.b2 r0.b3 r1.b3
+  const uint32_t t2 = __byte_perm(r2, r3, 0x5140);
+  const uint32_t t3 = __byte_perm(r2, r3, 0x7362);
+  c0 = __byte_perm(t0, t2, 0x5410);
+  c1 = __byte_perm(t0, t2, 0x7632);
+  c2 = __byte_perm(t1, t3, 0x5410);
+  c3 = __byte_perm(t1, t3, 0x7632);
+}
+
+// Five CTAs per SM (at most 51 registers a thread): measured faster than
+// the four that 55 registers allow, despite a few bytes of spill in the
+// fp32-scale instantiation; six spill heavily and are slower.
 template <int MODE>
-__global__ void __launch_bounds__(kWThreads)
+__global__ void __launch_bounds__(kWThreads, 5)
     quant_w_128x128_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t ldw,
                            uint8_t* __restrict__ wq, float* __restrict__ sw) {
   __shared__ __align__(16) uint2 tile[128 * 16];  // [n][k-chunk of 8], swizzled
@@ -270,15 +288,17 @@ __global__ void __launch_bounds__(kWThreads)
     codes[i][0] = q.x;
     codes[i][1] = q.y;
   }
+  // Column j of the 8x8 code block, as rows 0-3 (lo) and 4-7 (hi): four
+  // 4x4 byte transposes, byte i of each result word = row i.
+  uint32_t lo[8], hi[8];
+  transpose4x4_bytes(codes[0][0], codes[1][0], codes[2][0], codes[3][0], lo[0], lo[1], lo[2], lo[3]);
+  transpose4x4_bytes(codes[0][1], codes[1][1], codes[2][1], codes[3][1], lo[4], lo[5], lo[6], lo[7]);
+  transpose4x4_bytes(codes[4][0], codes[5][0], codes[6][0], codes[7][0], hi[0], hi[1], hi[2], hi[3]);
+  transpose4x4_bytes(codes[4][1], codes[5][1], codes[6][1], codes[7][1], hi[4], hi[5], hi[6], hi[7]);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) lo |= ((codes[i][j >> 2] >> (8 * (j & 3))) & 0xFFu) << (8 * i);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) hi |= ((codes[i + 4][j >> 2] >> (8 * (j & 3))) & 0xFFu) << (8 * i);
     const int n = 8 * c + j;
-    tile[n * 16 + (rg ^ c)] = make_uint2(lo, hi);
+    tile[n * 16 + (rg ^ c)] = make_uint2(lo[j], hi[j]);
   }
   if (t == 0) sw[static_cast<int64_t>(kb) * nb_count + nb] = gs.s;
   __syncthreads();
