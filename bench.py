@@ -516,6 +516,9 @@ def run_fgq(args):
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]  # nominal fp8 = 2x bf16 dense
     if ue8m0:
         ue8m0["frac_fp8"] = ue8m0["gemm_TFLOP/s"] / fp8_peak
+        ue8m0["traffic"] = _traffic("gemm_mx", "gemm_mx.cu")
+    if skinny and "M16" in skinny:
+        skinny["M16"]["traffic_lowm"] = _traffic("gemm_lowm_m16", "gemm_lowm.cu")
     hbm = peaks["hbm_gbs"]
     gemm_tflops = FLOPS_GEMM / (us_gemm * 1e-6) / 1e12
     act_gbs = BYTES_QUANT_ACT / (us_act * 1e-6) / 1e9
