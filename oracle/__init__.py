@@ -86,6 +86,8 @@ def _load():
         lib.fgqo_bf16_to_float.restype = ctypes.c_float
         lib.fgqo_quant_act_1x128.argtypes = [_u16p, _i64, _i64, _u8p, _f32p, ctypes.c_int]
         lib.fgqo_quant_act_1x128.restype = ctypes.c_int
+        lib.fgqo_quant_act_128x1.argtypes = [_u16p, _i64, _i64, _u8p, _f32p, ctypes.c_int]
+        lib.fgqo_quant_act_128x1.restype = ctypes.c_int
         lib.fgqo_quant_w_128x128.argtypes = [_u16p, _i64, _i64, _u8p, _f32p, ctypes.c_int]
         lib.fgqo_quant_w_128x128.restype = ctypes.c_int
         lib.fgqo_gemm_dequant.argtypes = [_u8p, _f32p, _u8p, _f32p, _i64, _i64, _i64,
@@ -176,6 +178,22 @@ def quant_act_1x128(x_bf16, mode: int = MODE_FP32):
     if rc != 0:
         raise ValueError(f"oracle quant_act_1x128 failed ({rc}): "
                          "K must be a multiple of 128 and inputs finite")
+    return q, s
+
+
+def quant_act_128x1(x_bf16, mode: int = MODE_FP32):
+    """X bf16 [M, K] -> (XqT uint8 [K, M], sXT float32 [K, M/128]): groups of
+    128 consecutive rows of one column, written transposed (the A operand of
+    a GEMM that reduces over M)."""
+    x = _bits16(x_bf16)
+    M, K = x.shape
+    q = np.empty((K, M), dtype=np.uint8)
+    s = np.empty((K, M // 128), dtype=np.float32)
+    rc = _load().fgqo_quant_act_128x1(_ptr(x, _u16p), M, K, _ptr(q, _u8p), _ptr(s, _f32p),
+                                      int(mode))
+    if rc != 0:
+        raise ValueError(f"oracle quant_act_128x1 failed ({rc}): "
+                         "M and K must be multiples of 128 and inputs finite")
     return q, s
 
 

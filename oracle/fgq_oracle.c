@@ -190,6 +190,31 @@ int fgqo_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, uint8_t *xq,
   return 0;
 }
 
+/* 128x1 activation quantization, the transposed variant a weight-gradient
+ * GEMM (reducing over the rows M of X) needs: the plainest extension of the
+ * 1x128 tiles of §Scaling Granularities to groups of 128 consecutive rows
+ * of one column.  X is bf16 [M, K] row-major, M and K multiples of 128.
+ * Group (k, mb) is rows 128 mb .. 128 mb + 127 of column k.  Outputs, in
+ * the layout the GEMM takes for its A operand (rows = k, reduction = m):
+ * XqT [K, M] E4M3 codes row-major, XqT[k, m] = code of X[m, k], and
+ * sXT [K, M/128] row-major, sXT[k, mb] = scale of group (k, mb). */
+int fgqo_quant_act_128x1(const uint16_t *x, int64_t M, int64_t K, uint8_t *xqt,
+                         float *sxt, int mode) {
+  if (M % 128 != 0 || K % 128 != 0) return -2;
+  int64_t mc = M / 128;
+  for (int64_t k = 0; k < K; ++k)
+    for (int64_t g = 0; g < mc; ++g) {
+      const uint16_t *src = x + (g * 128) * K + k; /* 128 rows, stride K */
+      float amax;
+      if (group_amax(src, K, 128, 1, &amax) != 0) return -1;
+      float s = fgqo_scale_from_amax(amax, mode);
+      sxt[k * mc + g] = s;
+      /* row r of the group (element X[128 g + r, k]) -> XqT[k, 128 g + r] */
+      group_encode(src, K, 128, 1, s, xqt + k * M + g * 128, 1);
+    }
+  return 0;
+}
+
 /* 128x128 block-wise weight quantization (§Scaling Granularities,
  * "per-block 128x128"): W is bf16 [K, N] row-major, K and N multiples of
  * 128.  Outputs Wq [K, N] E4M3 codes row-major (logical layout) and

@@ -277,11 +277,57 @@ def test_quant_w_block_indexing():
             assert q[i * 128 + 17, j * 128 + 101] == 0x7E
 
 
+@pytest.mark.parametrize("mode", [oracle.MODE_FP32, oracle.MODE_UE8M0])
+@pytest.mark.parametrize("kind", ["normal", "spread", "outlier"])
+def test_quant_act_128x1_is_1x128_of_the_transpose(mode, kind):
+    """Groups of 128 rows of one column of X are the 1x128 groups of X^T, so
+    the transposed quantizer equals the (independently pinned) 1x128
+    quantizer applied to X^T, in the same output layout, bit for bit."""
+    import fgq_inputs
+    M, K = 384, 256
+    if kind == "normal":
+        x = fgq_inputs.normal((M, K), 1.0, seed=1)
+    elif kind == "spread":
+        x = fgq_inputs.exponent_spread((M, K), 30, 128, seed=2)
+    else:
+        x = fgq_inputs.outlier((M, K), 1e-2, 100.0, seed=3)
+    q, s = oracle.quant_act_128x1(x, mode)
+    qt, st = oracle.quant_act_1x128(x.t().contiguous(), mode)
+    assert q.shape == (K, M) and s.shape == (K, M // 128)
+    assert np.array_equal(q, qt)
+    assert np.array_equal(s.view(np.uint32), st.view(np.uint32))
+
+
+def test_quant_act_128x1_group_indexing():
+    """Group (k, mb) = rows 128 mb .. +127 of column k, its scale at sXT[k, mb]
+    and the code of X[m, k] at XqT[k, m]: groups with distinct maxima on a
+    non-square grid land where they belong."""
+    M, K = 384, 256
+    x = np.zeros((M, K), dtype=np.float32)
+    for mb in range(M // 128):
+        for k in (0, 5, 130, 255):
+            x[mb * 128 + 77, k] = 448.0 * 2.0 ** (mb * 4 + k % 7)
+            x[mb * 128 + 3, k] = -1.0
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    q, s = oracle.quant_act_128x1(xb, oracle.MODE_FP32)
+    for mb in range(M // 128):
+        for k in range(K):
+            if k in (0, 5, 130, 255):
+                assert s[k, mb] == 2.0 ** (mb * 4 + k % 7)
+                assert q[k, mb * 128 + 77] == 0x7E
+                assert q[k, mb * 128 + 3] != 0  # -1/s is a nonzero code for these scales
+            else:
+                assert s[k, mb] == 1.0      # all-zero group
+                assert not q[k, mb * 128:(mb + 1) * 128].any()
+
+
 def test_quant_rejects_bad_shapes_and_nonfinite():
     with pytest.raises(ValueError):
         oracle.quant_act_1x128(np.zeros((2, 100), np.uint16))
     with pytest.raises(ValueError):
         oracle.quant_w_128x128(np.zeros((128, 100), np.uint16))
+    with pytest.raises(ValueError):
+        oracle.quant_act_128x1(np.zeros((100, 128), np.uint16))
     x = np.zeros((1, 128), np.uint16)
     x[0, 3] = 0x7F80  # +inf
     with pytest.raises(ValueError):
