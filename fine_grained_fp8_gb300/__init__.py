@@ -5,6 +5,8 @@ provides device memory and the current CUDA stream; all arithmetic runs in
 the library's kernels:
 
   quant_act_1x128(x)        bf16 [M, K] -> (E4M3 codes [M, K] uint8, fp32 [M, K/128])
+  quant_act_128x1(x)        bf16 [M, K] -> (E4M3 codes [K, M] uint8, fp32 [K, M/128]),
+                            groups of 128 rows (for a GEMM reducing over M)
   quant_w_128x128(w)        bf16 [K, N] -> (E4M3 codes [N, K] uint8 (K-major),
                                             fp32 [K/128, N/128])
   gemm_fp8_blockscaled(aq, sa, bq, sb, out_dtype)
@@ -21,7 +23,7 @@ from . import _lib
 from ._lib import (FGQ_OUT_BF16, FGQ_OUT_F32, FGQ_SCALE_FP32, FGQ_SCALE_UE8M0, FgqError,
                    check, load)
 
-__all__ = ["quant_act_1x128", "quant_w_128x128", "gemm_fp8_blockscaled",
+__all__ = ["quant_act_1x128", "quant_act_128x1", "quant_w_128x128", "gemm_fp8_blockscaled",
            "gemm_fp8_blockscaled_splitk", "splitk_workspace", "device_error",
            "FgqError", "load", "FGQ_SCALE_FP32", "FGQ_SCALE_UE8M0", "FGQ_OUT_F32",
            "FGQ_OUT_BF16", "scale_mode"]
@@ -66,6 +68,31 @@ def quant_act_1x128(x: torch.Tensor, mode="fp32", xq: torch.Tensor | None = None
                                   sx.data_ptr(), scale_mode(mode), _stream(x))
     check("fgq_quant_act_1x128", st)
     return xq, sx
+
+
+def quant_act_128x1(x: torch.Tensor, mode="fp32", xqt: torch.Tensor | None = None,
+                    sxt: torch.Tensor | None = None):
+    """128x1 (transposed) quantization of bf16 activations x [M, K] (rows may
+    be strided): groups of 128 rows of one column.  Returns xqt [K, M] E4M3
+    codes and sxt [K, M/128] scales, the A operand of a GEMM reducing over M
+    (the same result as quant_act_1x128(x.t()))."""
+    _need_cuda("x", x, torch.bfloat16)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with a contiguous last dimension")
+    M, K = x.shape
+    if xqt is None:
+        xqt = torch.empty((K, M), dtype=torch.uint8, device=x.device)
+    if sxt is None:
+        sxt = torch.empty((K, M // 128), dtype=torch.float32, device=x.device)
+    _need_cuda("xqt", xqt, torch.uint8)
+    _need_cuda("sxt", sxt, torch.float32)
+    if xqt.shape != (K, M) or not xqt.is_contiguous() or sxt.shape != (K, M // 128) \
+            or not sxt.is_contiguous():
+        raise ValueError("xqt must be a dense [K, M] and sxt a dense [K, M/128]")
+    st = _lib.fgq_quant_act_128x1(x.data_ptr(), M, K, x.stride(0), xqt.data_ptr(), sxt.data_ptr(),
+                                  scale_mode(mode), _stream(x))
+    check("fgq_quant_act_128x1", st)
+    return xqt, sxt
 
 
 def quant_w_128x128(w: torch.Tensor, mode="fp32", wq: torch.Tensor | None = None,

@@ -29,6 +29,7 @@ _i64 = ctypes.c_int64
 _int = ctypes.c_int
 SIGNATURES = {
     "fgq_quant_act_1x128": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _int, _vp]),
+    "fgq_quant_act_128x1": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _int, _vp]),
     "fgq_quant_w_128x128": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _int, _vp]),
     "fgq_gemm_fp8_blockscaled": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "fgq_gemm_fp8_blockscaled_ex": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
@@ -94,6 +95,10 @@ def check(func: str, status: int) -> None:
 
 def fgq_quant_act_1x128(x, M, K, ldx, xq, ldq, sx, mode, stream) -> int:
     return load().fgq_quant_act_1x128(x, M, K, ldx, xq, ldq, sx, mode, stream)
+
+
+def fgq_quant_act_128x1(x, M, K, ldx, xqt, sxt, mode, stream) -> int:
+    return load().fgq_quant_act_128x1(x, M, K, ldx, xqt, sxt, mode, stream)
 
 
 def fgq_quant_w_128x128(w, K, N, ldw, wq, sw, mode, stream) -> int:

@@ -77,6 +77,22 @@ fgq_status fgq_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx,
                                                static_cast<cudaStream_t>(stream), dev));
 }
 
+fgq_status fgq_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xqt,
+                               float* sxt, int mode, void* stream) {
+  if (M < 0 || K <= 0 || M % 128 != 0 || K % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (mode != FGQ_SCALE_FP32 && mode != FGQ_SCALE_UE8M0) return FGQ_ERR_INVALID_ARG;
+  if (M == 0) return FGQ_OK;
+  if (!x || !xqt || !sxt) return FGQ_ERR_INVALID_ARG;
+  if (ldx < K || ldx % 8 != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(xqt, 16) || !aligned(sxt, 4)) return FGQ_ERR_INVALID_ARG;
+  if ((M / 128) > kMaxGroups / (K / 128)) return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_quant_act_128x1(x, M, K, ldx, xqt, sxt, mode,
+                                               static_cast<cudaStream_t>(stream), dev));
+}
+
 fgq_status fgq_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t ldw, uint8_t* wq,
                                float* sw, int mode, void* stream) {
   if (K <= 0 || N <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;

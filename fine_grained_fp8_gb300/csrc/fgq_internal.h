@@ -33,6 +33,10 @@ cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t 
                                    uint8_t* xq, int64_t ldq, float* sx, int mode,
                                    cudaStream_t stream, const DeviceInfo& dev);
 
+cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xqt,
+                                   float* sxt, int mode, cudaStream_t stream,
+                                   const DeviceInfo& dev);
+
 cudaError_t launch_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
                                    uint8_t* wq, float* sw, int mode, cudaStream_t stream,
                                    const DeviceInfo& dev);

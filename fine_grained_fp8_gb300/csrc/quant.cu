@@ -316,7 +316,165 @@ __global__ void __launch_bounds__(kWThreads, 5)
   }
 }
 
+// ---- 128x1 (transposed) activation quantizer -----------------------------------
+//
+// Groups of 128 consecutive rows of one column of X [M, K], written in the
+// layout a GEMM reducing over M takes for its A operand: XqT [K, M] codes
+// and sXT [K, M/128] scales (the 1x128 quantization of X^T).  One CTA per
+// 128x128 block; thread t loads the 8 columns 8c .. 8c+7 (c = t % 16) of
+// rows 8 rg .. 8 rg + 7 (rg = t / 16), as the weight quantizer does.  Each
+// column's amax is reduced over the 16 row groups (one shuffle, then a
+// shared table over the 8 warps); each element is encoded with its
+// column's scale; the codes go out transposed through the same swizzled
+// shared tile as the weight quantizer's.
+
+// Codes of 8 bf16 of v whose element j has the scale of column j.
+template <int MODE>
+__device__ __forceinline__ uint2 encode8_cols(uint4 v, const float (&s)[8], const float (&r)[8],
+                                              uint32_t exact_mask) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t c[4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const float2 x = bf16x2_to_f32x2(w[p]);
+    const float2 r2 = make_float2(r[2 * p], r[2 * p + 1]);
+    float2 q;
+    if (MODE == kScaleUe8m0) {
+      q = mul2(x, r2);
+    } else {
+      const float2 q0 = mul2(x, r2);
+      const float2 d = fma2(q0, make_float2(-s[2 * p], -s[2 * p + 1]), x);  // exact residual
+      q = fma2(d, r2, q0);
+      if (exact_mask & (1u << (2 * p))) q.x = __fdiv_rn(x.x, s[2 * p]);
+      if (exact_mask & (2u << (2 * p))) q.y = __fdiv_rn(x.y, s[2 * p + 1]);
+    }
+    c[p] = cvt_e4m3x2(q.x, q.y);
+  }
+  const uint32_t s01 = __byte_perm(v.x, v.y, 0x7531) & 0x80808080u;
+  const uint32_t s23 = __byte_perm(v.z, v.w, 0x7531) & 0x80808080u;
+  uint2 out;
+  out.x = __byte_perm(c[0], c[1], 0x5410) | s01;
+  out.y = __byte_perm(c[2], c[3], 0x5410) | s23;
+  return out;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kWThreads, 4)
+    quant_act_128x1_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
+                           uint8_t* __restrict__ xqt, float* __restrict__ sxt) {
+  __shared__ __align__(16) uint2 tile[128 * 16];     // [k][m-chunk of 8], swizzled
+  __shared__ uint32_t colmax[kWThreads / 32][16][4];  // per warp: 16 chunks x 4 column pairs
+  __shared__ __align__(16) float col_s[128], col_r[128];  // each column's scale, reciprocal
+
+  const int kb_count = static_cast<int>(K / 128);
+  const int mc = static_cast<int>(M / 128);
+  const int kb = blockIdx.x % kb_count, mb = blockIdx.x / kb_count;
+  const int64_t m0 = static_cast<int64_t>(mb) * 128, k0 = static_cast<int64_t>(kb) * 128;
+  const int t = threadIdx.x, c = t & 15, rg = t >> 4, lane = t & 31, warp = t >> 5;
+
+  uint4 v[8];
+  const uint16_t* src = x + (m0 + 8 * rg) * ldx + k0 + 8 * c;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = ld_stream_16(src + i * ldx);
+
+  // column maxima (16-bit magnitude pairs: columns 2p, 2p+1 of the chunk)
+  const uint32_t msk = 0x7FFF7FFFu;
+  uint32_t cm[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    cm[0] = __vmaxu2(cm[0], v[i].x & msk);
+    cm[1] = __vmaxu2(cm[1], v[i].y & msk);
+    cm[2] = __vmaxu2(cm[2], v[i].z & msk);
+    cm[3] = __vmaxu2(cm[3], v[i].w & msk);
+  }
+#pragma unroll
+  for (int p = 0; p < 4; ++p) cm[p] = __vmaxu2(cm[p], __shfl_xor_sync(0xFFFFFFFFu, cm[p], 16));
+  if (lane < 16) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) colmax[warp][lane][p] = cm[p];
+  }
+  __syncthreads();
+  // one thread per column: its amax over the 8 warps, its scale
+  if (t < 128) {
+    const int cc = t >> 3, p = (t & 7) >> 1;
+    uint32_t mx = 0;
+#pragma unroll
+    for (int w = 0; w < kWThreads / 32; ++w) mx = __vmaxu2(mx, colmax[w][cc][p]);
+    const uint32_t mag = (t & 1) ? (mx >> 16) : (mx & 0xFFFFu);
+    const GroupScale gs = group_scale<MODE>(mag);
+    col_s[t] = gs.s;
+    col_r[t] = gs.r2.x;
+    sxt[(k0 + t) * mc + mb] = gs.s;
+  }
+  __syncthreads();
+
+  float sc[8], rc[8];
+  {
+    const float4 s0 = reinterpret_cast<const float4*>(col_s)[2 * c];
+    const float4 s1 = reinterpret_cast<const float4*>(col_s)[2 * c + 1];
+    const float4 r0 = reinterpret_cast<const float4*>(col_r)[2 * c];
+    const float4 r1 = reinterpret_cast<const float4*>(col_r)[2 * c + 1];
+    sc[0] = s0.x; sc[1] = s0.y; sc[2] = s0.z; sc[3] = s0.w;
+    sc[4] = s1.x; sc[5] = s1.y; sc[6] = s1.z; sc[7] = s1.w;
+    rc[0] = r0.x; rc[1] = r0.y; rc[2] = r0.z; rc[3] = r0.w;
+    rc[4] = r1.x; rc[5] = r1.y; rc[6] = r1.z; rc[7] = r1.w;
+  }
+  uint32_t exact_mask = 0;
+  if (MODE == kScaleFp32) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (!(sc[j] >= 0x1p-100f)) exact_mask |= 1u << j;  // the exact-division range
+  }
+
+  uint32_t codes[8][2];  // [row i][lo: cols 0-3, hi: cols 4-7]
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint2 q = encode8_cols<MODE>(v[i], sc, rc, exact_mask);
+    codes[i][0] = q.x;
+    codes[i][1] = q.y;
+  }
+  uint32_t lo[8], hi[8];
+  transpose4x4_bytes(codes[0][0], codes[1][0], codes[2][0], codes[3][0], lo[0], lo[1], lo[2], lo[3]);
+  transpose4x4_bytes(codes[0][1], codes[1][1], codes[2][1], codes[3][1], lo[4], lo[5], lo[6], lo[7]);
+  transpose4x4_bytes(codes[4][0], codes[5][0], codes[6][0], codes[7][0], hi[0], hi[1], hi[2], hi[3]);
+  transpose4x4_bytes(codes[4][1], codes[5][1], codes[6][1], codes[7][1], hi[4], hi[5], hi[6], hi[7]);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int kk = 8 * c + j;
+    tile[kk * 16 + (rg ^ c)] = make_uint2(lo[j], hi[j]);
+  }
+  __syncthreads();
+
+  const uint4* tile16 = reinterpret_cast<const uint4*>(tile);
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const int idx = p * kWThreads + t;
+    const int kk = idx >> 3, q = idx & 7;
+    const int swz = (kk >> 3) & 15;
+    uint4 val = tile16[kk * 8 + q];
+    if (swz & 1) val = make_uint4(val.z, val.w, val.x, val.y);
+    uint8_t* dst = xqt + (k0 + kk) * M + m0 + 16 * (q ^ (swz >> 1));
+    st_stream_16(dst, val);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xqt,
+                                   float* sxt, int mode, cudaStream_t stream,
+                                   const DeviceInfo& dev) {
+  (void)dev;
+  const int64_t blocks = (M / 128) * (K / 128);
+  if (blocks == 0) return cudaSuccess;
+  if (blocks >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
+  if (mode == kScaleFp32)
+    quant_act_128x1_kernel<kScaleFp32><<<static_cast<unsigned>(blocks), kWThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(x), M, K, ldx, xqt, sxt);
+  else
+    quant_act_128x1_kernel<kScaleUe8m0><<<static_cast<unsigned>(blocks), kWThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(x), M, K, ldx, xqt, sxt);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx,
                                    uint8_t* xq, int64_t ldq, float* sx, int mode,

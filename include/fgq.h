@@ -75,6 +75,25 @@ fgq_status fgq_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx,
                                int64_t ldq, float* sx, int mode, void* stream);
 
 /*
+ * 128x1 (transposed) activation quantization, for a weight-gradient GEMM
+ * that reduces over the rows of X: groups of 128 consecutive rows of one
+ * column -- the plainest extension of the 1x128 tiles of §Scaling
+ * Granularities -- written in the layout fgq_gemm_fp8_blockscaled takes for
+ * its A operand.  The result equals fgq_quant_act_1x128 applied to X^T.
+ *
+ *   x     bf16 [M, K], row m at x + m * ldx (ldx >= K, ldx % 8 == 0),
+ *         16-byte aligned.
+ *   xqt   E4M3 codes [K, M] row-major (dense): the code of X[m, k] at
+ *         xqt[k * M + m].  16-byte aligned.
+ *   sxt   fp32 [K, M/128] row-major (dense): the scale of rows
+ *         128 g .. 128 g + 127 of column k at sxt[k * (M/128) + g].
+ *   M % 128 == 0, K % 128 == 0, K > 0, M >= 0.  mode: FGQ_SCALE_FP32 or
+ *   FGQ_SCALE_UE8M0.  Scale and encode as fgq_quant_act_1x128.
+ */
+fgq_status fgq_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xqt,
+                               float* sxt, int mode, void* stream);
+
+/*
  * 128x128 block-wise weight quantization (§Scaling Granularities,
  * per-block 128x128; scale_B [K/128, N/128] from §DeepGEMM).
  *
