@@ -453,11 +453,21 @@ def run_fgq(args):
             cs = torch.empty((Ms, SN), dtype=torch.bfloat16, device=dev)
             ws = fgq.splitk_workspace(Ms, SN, SK, dev)
             entry = {}
-            for name, fn in (
-                    ("gemm_fp8_blockscaled", lambda j: fgq.gemm_fp8_blockscaled(
-                        aqs, sas, *wcopies[j % 4], torch.bfloat16, out=cs)),
-                    ("gemm_fp8_blockscaled_splitk", lambda j: fgq.gemm_fp8_blockscaled_splitk(
-                        aqs, sas, *wcopies[j % 4], ws, torch.bfloat16, out=cs))):
+            timed = [
+                ("gemm_fp8_blockscaled", lambda j: fgq.gemm_fp8_blockscaled(
+                    aqs, sas, *wcopies[j % 4], torch.bfloat16, out=cs)),
+                ("gemm_fp8_blockscaled_splitk", lambda j: fgq.gemm_fp8_blockscaled_splitk(
+                    aqs, sas, *wcopies[j % 4], ws, torch.bfloat16, out=cs))]
+            if Ms <= 32:
+                # bf16 activations in: quantizer then GEMM (two launches) against
+                # the GEMM that quantizes A itself (one launch)
+                timed += [
+                    ("quant_act_then_gemm", lambda j: (
+                        fgq.quant_act_1x128(ask, xq=aqs, sx=sas),
+                        fgq.gemm_fp8_blockscaled(aqs, sas, *wcopies[j % 4], torch.bfloat16, out=cs))),
+                    ("gemm_fp8_blockscaled_fused_act", lambda j: fgq.gemm_fp8_blockscaled_fused_act(
+                        ask, *wcopies[j % 4], torch.bfloat16, out=cs))]
+            for name, fn in timed:
                 for j in range(8):
                     fn(j)
                 torch.cuda.synchronize()

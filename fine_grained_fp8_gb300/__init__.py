@@ -24,7 +24,7 @@ from ._lib import (FGQ_OUT_BF16, FGQ_OUT_F32, FGQ_SCALE_FP32, FGQ_SCALE_UE8M0, F
                    check, load)
 
 __all__ = ["quant_act_1x128", "quant_act_128x1", "quant_w_128x128", "gemm_fp8_blockscaled",
-           "gemm_fp8_blockscaled_splitk", "splitk_workspace", "device_error",
+           "gemm_fp8_blockscaled_splitk", "gemm_fp8_blockscaled_fused_act", "splitk_workspace", "device_error",
            "FgqError", "load", "FGQ_SCALE_FP32", "FGQ_SCALE_UE8M0", "FGQ_OUT_F32",
            "FGQ_OUT_BF16", "scale_mode"]
 
@@ -146,6 +146,37 @@ def gemm_fp8_blockscaled(aq: torch.Tensor, sa: torch.Tensor, bq: torch.Tensor,
         M, N, K, FGQ_OUT_BF16 if out_dtype == torch.bfloat16 else FGQ_OUT_F32, scale_mode(mode),
         _stream(aq))
     check("fgq_gemm_fp8_blockscaled_ex", st)
+    return out
+
+
+def gemm_fp8_blockscaled_fused_act(a: torch.Tensor, bq: torch.Tensor, sb: torch.Tensor,
+                                   out_dtype=torch.float32, mode="fp32",
+                                   out: torch.Tensor | None = None) -> torch.Tensor:
+    """C [M, N] for bf16 activations a [M, K] (rows may be strided), quantized
+    1x128 inside the GEMM (same codes as quant_act_1x128), times the weight
+    codes bq [N, K] with scales sb [K/128, N/128].  M <= 32 and A small
+    enough to stay on chip (see include/fgq.h)."""
+    _need_cuda("a", a, torch.bfloat16)
+    _need_cuda("bq", bq, torch.uint8)
+    _need_cuda("sb", sb, torch.float32)
+    if a.dim() != 2 or a.stride(1) != 1:
+        raise ValueError("a must be 2-D with a contiguous last dimension")
+    if not bq.is_contiguous() or not sb.is_contiguous():
+        raise ValueError("bq and sb must be contiguous")
+    M, K = a.shape
+    N, K2 = bq.shape
+    if K2 != K or sb.shape != (K // 128, N // 128):
+        raise ValueError("shape mismatch: a [M,K], bq [N,K], sb [K/128,N/128]")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=a.device)
+    _need_cuda("out", out, out_dtype)
+    if out.shape != (M, N) or out.stride(1) != 1:
+        raise ValueError("out must be [M, N] with contiguous rows")
+    st = _lib.fgq_gemm_fp8_blockscaled_fused_act(
+        a.data_ptr(), a.stride(0), bq.data_ptr(), sb.data_ptr(), out.data_ptr(), out.stride(0),
+        M, N, K, FGQ_OUT_BF16 if out_dtype == torch.bfloat16 else FGQ_OUT_F32, scale_mode(mode),
+        _stream(a))
+    check("fgq_gemm_fp8_blockscaled_fused_act", st)
     return out
 
 

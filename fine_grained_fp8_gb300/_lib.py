@@ -37,6 +37,8 @@ SIGNATURES = {
     "fgq_gemm_fp8_blockscaled_splitk": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                                _int, _int, _vp, ctypes.c_size_t, _vp]),
     "fgq_gemm_splitk_workspace_size": (_int, [_i64, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
+    "fgq_gemm_fp8_blockscaled_fused_act": (_int, [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                                  _int, _int, _vp]),
     "fgq_gemm_fp8_blockscaled_splitk_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
                                                        _i64, _int, _int, _vp]),
     "fgq_selftest_wait_timeout": (_int, [_vp]),
@@ -123,6 +125,11 @@ def fgq_gemm_fp8_blockscaled_splitk_noalloc(A, sA, B, sB, C, ldc, M, N, K, out, 
                                             stream) -> int:
     return load().fgq_gemm_fp8_blockscaled_splitk_noalloc(A, sA, B, sB, C, ldc, M, N, K, out,
                                                           mode, stream)
+
+
+def fgq_gemm_fp8_blockscaled_fused_act(A, lda, B, sB, C, ldc, M, N, K, out, mode, stream) -> int:
+    return load().fgq_gemm_fp8_blockscaled_fused_act(A, lda, B, sB, C, ldc, M, N, K, out, mode,
+                                                     stream)
 
 
 def fgq_gemm_splitk_workspace_size(M, N, K):

@@ -155,6 +155,29 @@ fgq_status fgq_gemm_fp8_blockscaled_ex(const uint8_t* A, const float* sA, const 
   return from_cuda(fgq::launch_gemm_fp8_blockscaled(A, sA, B, sB, C, ldc, M, N, K, bf16, mode, s, dev));
 }
 
+fgq_status fgq_gemm_fp8_blockscaled_fused_act(const void* A, int64_t lda, const uint8_t* B,
+                                              const float* sB, void* C, int64_t ldc, int64_t M,
+                                              int64_t N, int64_t K, int out, int mode,
+                                              void* stream) {
+  if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (out != FGQ_OUT_F32 && out != FGQ_OUT_BF16) return FGQ_ERR_INVALID_ARG;
+  if (mode != FGQ_SCALE_FP32 && mode != FGQ_SCALE_UE8M0) return FGQ_ERR_INVALID_ARG;
+  if (N >= (int64_t{1} << 31) || K >= (int64_t{1} << 31)) return FGQ_ERR_INVALID_ARG;
+  if (M == 0) return FGQ_OK;
+  if (!fgq::lowm_fused_fits(M, K)) return FGQ_ERR_INVALID_ARG;  // M <= 32 and A fits on chip
+  if (!A || !B || !sB || !C) return FGQ_ERR_INVALID_ARG;
+  const int64_t vec = (out == FGQ_OUT_F32) ? 4 : 8;
+  if (lda < K || lda % 8 != 0 || ldc < N || ldc % vec != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(sB, 4))
+    return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_gemm_lowm_fused(A, lda, B, sB, C, ldc, M, N, K,
+                                               out == FGQ_OUT_BF16 ? 1 : 0, mode,
+                                               static_cast<cudaStream_t>(stream), dev));
+}
+
 fgq_status fgq_gemm_splitk_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {
   if (!bytes || M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
   fgq::DeviceInfo dev;

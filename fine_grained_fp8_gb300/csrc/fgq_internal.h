@@ -67,6 +67,15 @@ cudaError_t read_device_error_mx(uint32_t* word, bool clear);
 // box_rows box, 128-byte swizzle, zero fill outside the tensor.
 bool make_k_major_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows);
 
+// Low-M GEMM that quantizes bf16 A (1x128, scale mode `mode`) in the kernel
+// and keeps all of it in shared memory: M <= 32 and K small enough for
+// that (lowm_fused_fits); no split.
+bool lowm_fused_fits(int64_t M, int64_t K);
+cudaError_t launch_gemm_lowm_fused(const void* a16, int64_t lda, const uint8_t* B, const float* sB,
+                                   void* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                   int out_bf16, int mode, cudaStream_t stream,
+                                   const DeviceInfo& dev);
+
 // Bytes of the fixed scratch array behind fgq_gemm_fp8_blockscaled_splitk_noalloc.
 #ifndef FGQ_NOALLOC_SCRATCH_BYTES
 #define FGQ_NOALLOC_SCRATCH_BYTES (16u << 20)

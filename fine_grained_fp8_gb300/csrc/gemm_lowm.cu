@@ -35,6 +35,7 @@
 
 #include "fgq_device.cuh"
 #include "fgq_internal.h"
+#include "fgq_quant.cuh"
 
 namespace fgq {
 namespace {
@@ -48,6 +49,9 @@ constexpr int kLaunchRegs = 168;
 constexpr uint32_t kCtlRegs = 56;
 constexpr uint32_t kEpiRegs = 224;
 constexpr uint32_t kEpiBarrier = 1;      // named barrier of the 256 epilogue threads
+constexpr uint32_t kQuantBarrier = 2;    // named barrier closing the in-kernel quantization
+constexpr int kQuantWarps = 11;          // warps 1-11 quantize A (warp 0 streams the weight)
+constexpr int kMaxSmemOptin = 232448;    // 227 KB of shared memory per CTA
 constexpr int kScaleWindow = 16;         // K chunks of staged activation scales
 static_assert(128 * kCtlRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs, "register split");
 
@@ -68,6 +72,14 @@ struct LowCfg {
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(MP % 16 == 0 && MP >= 16 && MP <= 256, "MMA N");
   static_assert(kTmemCols == 512, "TMEM allocation");
+  // Activation scales of all chunks when A is quantized in the kernel.
+  static __host__ __device__ constexpr int fused_scale_bytes(int kchunks) {
+    return ((kchunks * MP * 4 + 15) / 16) * 16;
+  }
+  static constexpr size_t fused_smem_bytes(int kchunks) {
+    return 1024 + static_cast<size_t>(STAGES) * kBBytes + static_cast<size_t>(kchunks) * kABytes +
+           fused_scale_bytes(kchunks) + kBarBytes + 16;
+  }
   static_assert(kScaleWindow % kBatch == 0, "a batch never straddles a scale window");
 };
 
@@ -149,14 +161,21 @@ struct LowSched {
   }
 };
 
-template <int MP, bool OUT_BF16>
+// FUSE = 0: A comes quantized (codes by TMA per stage, scales sA).  FUSE =
+// kScaleFp32 + 1 or kScaleUe8m0 + 1: A comes as bf16 (a16, row stride lda)
+// and is quantized here, 1x128 groups with the same arithmetic as
+// fgq_quant_act_1x128, into shared memory that holds all of A's K chunks
+// (codes in the 128-byte-swizzled layout a TMA load would write) and their
+// scales for the whole kernel.
+template <int MP, bool OUT_BF16, int FUSE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_lowm_kernel(const __grid_constant__ CUtensorMap tmap_w,   // Wq [N, K], box 128 x BN rows
                      const __grid_constant__ CUtensorMap tmap_a,   // Aq [M, K], box 128 x MP rows
                      const float* __restrict__ sA, const float* __restrict__ sB, void* __restrict__ C,
                      int64_t ldc, int M, int N, int K, int splits, int chunks_per_split,
                      float* __restrict__ partial,      // [splits][M][N] fp32 (splits > 1)
-                     unsigned int* __restrict__ counters) {  // [N / 128], zero between calls
+                     unsigned int* __restrict__ counters,  // [N / 128], zero between calls
+                     const uint16_t* __restrict__ a16, int64_t lda) {
   using CF = LowCfg<MP>;
   constexpr int STAGES = CF::STAGES;
   constexpr int HALF = MP / 2;                   // columns (m) per epilogue warp
@@ -165,10 +184,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int kchunks_all = K / BK;
   uint8_t* sm_w = smem;                                   // STAGES x weight tiles
-  uint8_t* sm_a = smem + STAGES * CF::kBBytes;            // STAGES x activation tiles
-  float* sm_sa = reinterpret_cast<float*>(sm_a + STAGES * CF::kABytes);  // [chunk][MP]
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sm_sa) + CF::kScaleBytes);
+  uint8_t* sm_a = smem + STAGES * CF::kBBytes;            // activation tiles: STAGES, or all chunks
+  float* sm_sa = reinterpret_cast<float*>(
+      sm_a + (FUSE ? kchunks_all : STAGES) * CF::kABytes);  // [chunk][MP]: a window, or all chunks
+  uint64_t* full = reinterpret_cast<uint64_t*>(
+      reinterpret_cast<uint8_t*>(sm_sa) + (FUSE ? CF::fused_scale_bytes(kchunks_all) : CF::kScaleBytes));
   uint64_t* empty = full + STAGES;
   constexpr int kBatch = CF::kBatch;
   uint64_t* tfull = empty + STAGES;   // [2] slot holds a finished batch
@@ -201,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tmap_w);
-    tma_prefetch_desc(&tmap_a);
+    if (!FUSE) tma_prefetch_desc(&tmap_a);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, CF::kTmemCols);
@@ -216,6 +238,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   // has completed.
   pdl_wait();
   pdl_launch_dependents();
+
+  if constexpr (FUSE != 0) {
+    // Quantize all of A into shared memory (warp 0 starts streaming the
+    // weight meanwhile).  Eight lanes per 1x128 group, as the activation
+    // quantizer: lane l8 holds elements 8 l8 .. 8 l8 + 7 and 64 + 8 l8 ..
+    // 64 + 8 l8 + 7.  Rows m >= M get zero codes and scale 0.
+    if (warp != 0) {
+      constexpr int QMODE = FUSE - 1;
+      constexpr int kRounds = 6;  // groups per lane-octet with loads in flight together
+      constexpr int kStride = kQuantWarps * 4;
+      const int sub = lane >> 3, l8 = lane & 7;
+      const int groups = MP * kchunks_all;
+      // gw is the same for the whole warp (the shuffles below need all lanes)
+      for (int gw = (warp - 1) * 4; gw < groups; gw += kStride * kRounds) {
+        const int gb = gw + sub;
+        uint4 v0[kRounds], v1[kRounds];
+#pragma unroll
+        for (int r = 0; r < kRounds; ++r) {
+          const int g = gb + r * kStride, c = g / MP, m = g - c * MP;
+          v0[r] = v1[r] = make_uint4(0, 0, 0, 0);
+          if (g < groups && m < M) {
+            const uint16_t* src = a16 + static_cast<int64_t>(m) * lda + c * BK;
+            v0[r] = ld_stream_16(src + 8 * l8);
+            v1[r] = ld_stream_16(src + 64 + 8 * l8);
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < kRounds; ++r) {
+          const int g = gb + r * kStride, c = g / MP, m = g - c * MP;
+          uint32_t mx = __vmaxu2(absmax_pairs(v0[r]), absmax_pairs(v1[r]));
+#pragma unroll
+          for (int off = 4; off > 0; off >>= 1) mx = __vmaxu2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+          const GroupScale gs = group_scale<QMODE>(max(mx & 0xFFFFu, mx >> 16));
+          if (g < groups) {
+            const uint2 q0 = encode8<QMODE>(v0[r], gs), q1 = encode8<QMODE>(v1[r], gs);
+            // row m of chunk c: 128 bytes in its 1024-byte atom, 16-byte
+            // units XOR-swizzled by m % 8 (the TMA SWIZZLE_128B layout)
+            uint8_t* row = sm_a + c * CF::kABytes + (m >> 3) * 1024 + (m & 7) * 128;
+            const int u0 = (l8 >> 1) ^ (m & 7), u1 = (4 + (l8 >> 1)) ^ (m & 7);
+            *reinterpret_cast<uint2*>(row + u0 * 16 + (l8 & 1) * 8) = q0;
+            *reinterpret_cast<uint2*>(row + u1 * 16 + (l8 & 1) * 8) = q1;
+            if (l8 == 0) sm_sa[c * MP + m] = m < M ? gs.s : 0.0f;
+          }
+        }
+      }
+      // the tensor core reads these codes through the async proxy
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      named_barrier_sync(kQuantBarrier, 32 * kQuantWarps);
+    }
+  }
 
   if (warp < kCtlWarps) {
     setmaxnreg_dec<kCtlRegs>();
@@ -234,9 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full[s], CF::kStageBytes);
+            mbar_arrive_expect_tx(&full[s], FUSE ? CF::kBBytes : CF::kStageBytes);
             tma_load_2d(sm_w + s * CF::kBBytes, &tmap_w, &full[s], kc * BK, nt * BN);
-            tma_load_2d(sm_a + s * CF::kABytes, &tmap_a, &full[s], kc * BK, 0);
+            if (!FUSE) tma_load_2d(sm_a + s * CF::kABytes, &tmap_a, &full[s], kc * BK, 0);
             if (++s == STAGES) {
               s = 0;
               ph ^= 1u;
@@ -276,7 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t d = tmem_base + slot * CF::kSlotCols + j * MP;
             const uint32_t w_lo = w_lo0 + s * (CF::kBBytes >> 4);
-            const uint32_t a_lo = a_lo0 + s * (CF::kABytes >> 4);
+            // the stage's A tile, or the resident tile of chunk kc
+            const uint32_t a_lo = a_lo0 + (FUSE ? kc : s) * (CF::kABytes >> 4);
 #pragma unroll
             for (int kk = 0; kk < BK / 32; ++kk)
               umma_f8f6f4(d, make_desc(w_lo + kk * 2, dhi), make_desc(a_lo + kk * 2, dhi), idesc,
@@ -327,8 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // of batches).  Every epilogue warp runs every batch (a warp that
         // gave up on a wait only skips the work), so all of them reach
         // these barriers.
-        const int w0 = (kb - c0) % kScaleWindow;
-        if (w0 == 0) {
+        const int w0 = FUSE ? kb : (kb - c0) % kScaleWindow;  // row of sm_sa for chunk kb
+        if (!FUSE && w0 == 0) {
           named_barrier_sync(kEpiBarrier, 32 * kEpiWarps);  // earlier readers done
           const int nck = min(kScaleWindow, c1 - kb);
           for (int i = et; i < nck * MP; i += 32 * kEpiWarps) {
@@ -467,7 +540,7 @@ cudaError_t launch_lowm(const uint8_t* A, const float* sA, const uint8_t* B, con
                         void* C, int64_t ldc, int M, int N, int K, int splits, float* partial,
                         unsigned int* counters, cudaStream_t stream, const DeviceInfo& dev) {
   using CF = LowCfg<MP>;
-  auto kern = gemm_lowm_kernel<MP, OUT_BF16>;
+  auto kern = gemm_lowm_kernel<MP, OUT_BF16, 0>;
   static std::mutex mu;
   static bool ready[64] = {};
   {
@@ -493,7 +566,43 @@ cudaError_t launch_lowm(const uint8_t* A, const float* sA, const uint8_t* B, con
   const int units = (N / BN) * splits;
   const int grid = units < dev.sm_count ? units : dev.sm_count;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), CF::kSmemBytes, stream, tw, ta, sA, sB, C,
-                    ldc, M, N, K, splits, cps, partial, counters);
+                    ldc, M, N, K, splits, cps, partial, counters,
+                    static_cast<const uint16_t*>(nullptr), int64_t{0});
+}
+
+// A as bf16, quantized inside the kernel (FUSE = scale mode + 1); no split.
+template <int MP, bool OUT_BF16, int FUSE>
+cudaError_t launch_lowm_fused(const uint16_t* a16, int64_t lda, const uint8_t* B, const float* sB,
+                              void* C, int64_t ldc, int M, int N, int K, cudaStream_t stream,
+                              const DeviceInfo& dev) {
+  using CF = LowCfg<MP>;
+  auto kern = gemm_lowm_kernel<MP, OUT_BF16, FUSE>;
+  const size_t smem = CF::fused_smem_bytes(K / BK);
+  if (smem > static_cast<size_t>(kMaxSmemOptin)) return cudaErrorInvalidValue;
+  static std::mutex mu;
+  static bool ready[64] = {};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev.device >= 64) return cudaErrorInvalidDevice;
+    if (!ready[dev.device]) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kMaxSmemOptin);
+      if (e != cudaSuccess) return e;
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+      ready[dev.device] = true;
+    }
+  }
+  CUtensorMap tw, ta_unused = {};
+  if (!make_k_major_map(&tw, B, N, K, BN)) return cudaErrorInvalidValue;
+  const int kchunks = K / BK;
+  const int units = N / BN;
+  const int grid = units < dev.sm_count ? units : dev.sm_count;
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, tw, ta_unused,
+                    static_cast<const float*>(nullptr), sB, C, ldc, M, N, K, 1, kchunks,
+                    static_cast<float*>(nullptr), static_cast<unsigned int*>(nullptr), a16, lda);
 }
 
 template <bool OUT_BF16>
@@ -539,6 +648,38 @@ size_t lowm_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count) {
   const size_t counters = static_cast<size_t>(N / BN) * sizeof(unsigned int);
   if (s <= 1) return 256;  // never touched; a non-empty buffer keeps the contract simple
   return ((counters + 255) / 256) * 256 + static_cast<size_t>(s) * M * N * sizeof(float);
+}
+
+size_t lowm_fused_smem_bytes(int64_t M, int64_t K) {
+  const int kc = static_cast<int>(K / BK);
+  return M <= 16 ? LowCfg<16>::fused_smem_bytes(kc) : LowCfg<32>::fused_smem_bytes(kc);
+}
+
+bool lowm_fused_fits(int64_t M, int64_t K) {
+  return M >= 1 && M <= 32 && K / BK <= 4096 && lowm_fused_smem_bytes(M, K) <= kMaxSmemOptin;
+}
+
+cudaError_t launch_gemm_lowm_fused(const void* a16, int64_t lda, const uint8_t* B, const float* sB,
+                                   void* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                   int out_bf16, int mode, cudaStream_t stream,
+                                   const DeviceInfo& dev) {
+  if (M == 0) return cudaSuccess;
+  if (!lowm_fused_fits(M, K)) return cudaErrorInvalidValue;
+  const auto* a = static_cast<const uint16_t*>(a16);
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  const bool ue = mode != 0;
+  if (M <= 16) {
+    if (out_bf16)
+      return ue ? launch_lowm_fused<16, true, 2>(a, lda, B, sB, C, ldc, m, n, k, stream, dev)
+                : launch_lowm_fused<16, true, 1>(a, lda, B, sB, C, ldc, m, n, k, stream, dev);
+    return ue ? launch_lowm_fused<16, false, 2>(a, lda, B, sB, C, ldc, m, n, k, stream, dev)
+              : launch_lowm_fused<16, false, 1>(a, lda, B, sB, C, ldc, m, n, k, stream, dev);
+  }
+  if (out_bf16)
+    return ue ? launch_lowm_fused<32, true, 2>(a, lda, B, sB, C, ldc, m, n, k, stream, dev)
+              : launch_lowm_fused<32, true, 1>(a, lda, B, sB, C, ldc, m, n, k, stream, dev);
+  return ue ? launch_lowm_fused<32, false, 2>(a, lda, B, sB, C, ldc, m, n, k, stream, dev)
+            : launch_lowm_fused<32, false, 1>(a, lda, B, sB, C, ldc, m, n, k, stream, dev);
 }
 
 cudaError_t launch_gemm_lowm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,

@@ -178,6 +178,33 @@ fgq_status fgq_gemm_fp8_blockscaled_splitk(const uint8_t* A, const float* sA, co
                                            int64_t N, int64_t K, int out, int mode,
                                            void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Block-scaled FP8 GEMM whose activations come as bf16 and are quantized
+ * inside the GEMM: the quantize -> GEMM fusion the page lists for DeepGEMM
+ * (the Xq round trip through memory is dropped), for few rows of A (the
+ * decode regime).
+ *
+ * Same result as fgq_quant_act_1x128(A) followed by
+ * fgq_gemm_fp8_blockscaled_ex on its codes and scales: every CTA quantizes
+ * all of A (1x128 groups, scale mode `mode`, the same arithmetic as the
+ * quantizer) into its shared memory and keeps it there, while the weight
+ * streams through.  The codes and scales of A are not written to memory.
+ *
+ *   A      bf16 [M, K], row m at A + m * lda (lda >= K, lda % 8 == 0),
+ *          16-byte aligned.
+ *   B, sB  as fgq_gemm_fp8_blockscaled_ex (weight codes [N, K], scales
+ *          [K/128, N/128]); for FGQ_SCALE_UE8M0, sB must hold powers of two.
+ *   C      fp32 or bf16 [M, N], row m at C + m * ldc (as _ex).
+ *   1 <= M <= 32 (M == 0 is an empty problem), and A must fit in shared
+ *   memory next to the weight pipeline: M <= 16 allows K up to 7936,
+ *   17 <= M <= 32 up to 3968 (K % 128 == 0).  Larger problems return
+ *   FGQ_ERR_INVALID_ARG; use the quantizer and the GEMM separately.
+ */
+fgq_status fgq_gemm_fp8_blockscaled_fused_act(const void* A, int64_t lda, const uint8_t* B,
+                                              const float* sB, void* C, int64_t ldc, int64_t M,
+                                              int64_t N, int64_t K, int out, int mode,
+                                              void* stream);
+
 /* Workspace bytes fgq_gemm_fp8_blockscaled_splitk needs for (M, N, K) on the
  * current device (depends on its SM count).  Same size checks as the GEMM. */
 fgq_status fgq_gemm_splitk_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
