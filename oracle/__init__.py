@@ -88,6 +88,16 @@ def _load():
         lib.fgqo_quant_act_1x128.restype = ctypes.c_int
         lib.fgqo_quant_act_128x1.argtypes = [_u16p, _i64, _i64, _u8p, _f32p, ctypes.c_int]
         lib.fgqo_quant_act_128x1.restype = ctypes.c_int
+        lib.fgqo_e2m1_decode.argtypes = [ctypes.c_uint8]
+        lib.fgqo_e2m1_decode.restype = ctypes.c_double
+        lib.fgqo_e2m1_encode.argtypes = [ctypes.c_double]
+        lib.fgqo_e2m1_encode.restype = ctypes.c_uint8
+        lib.fgqo_quant_mxfp4_1x32.argtypes = [_u16p, _i64, _i64, _u8p, _u8p]
+        lib.fgqo_quant_mxfp4_1x32.restype = ctypes.c_int
+        lib.fgqo_gemm_mxfp4.argtypes = [_u8p, _u8p, _u8p, _u8p, _i64, _i64, _i64,
+                                        ctypes.POINTER(ctypes.c_double),
+                                        ctypes.POINTER(ctypes.c_double)]
+        lib.fgqo_gemm_mxfp4.restype = ctypes.c_int
         lib.fgqo_quant_w_128x128.argtypes = [_u16p, _i64, _i64, _u8p, _f32p, ctypes.c_int]
         lib.fgqo_quant_w_128x128.restype = ctypes.c_int
         lib.fgqo_gemm_dequant.argtypes = [_u8p, _f32p, _u8p, _f32p, _i64, _i64, _i64,
@@ -195,6 +205,43 @@ def quant_act_128x1(x_bf16, mode: int = MODE_FP32):
         raise ValueError(f"oracle quant_act_128x1 failed ({rc}): "
                          "M and K must be multiples of 128 and inputs finite")
     return q, s
+
+
+def e2m1_decode(code: int) -> float:
+    return _load().fgqo_e2m1_decode(int(code))
+
+
+def e2m1_encode(v: float) -> int:
+    return _load().fgqo_e2m1_encode(float(v))
+
+
+def quant_mxfp4_1x32(x_bf16):
+    """X bf16 [R, K] -> (Xq uint8 [R, K/2] E2M1 pairs, low nibble = even
+    element; sX uint8 [R, K/32] UE8M0 codes)."""
+    x = _bits16(x_bf16)
+    R, K = x.shape
+    q = np.empty((R, K // 2), dtype=np.uint8)
+    s = np.empty((R, K // 32), dtype=np.uint8)
+    rc = _load().fgqo_quant_mxfp4_1x32(_ptr(x, _u16p), R, K, _ptr(q, _u8p), _ptr(s, _u8p))
+    if rc != 0:
+        raise ValueError(f"oracle quant_mxfp4_1x32 failed ({rc}): "
+                         "K must be a multiple of 32 and inputs finite")
+    return q, s
+
+
+def gemm_mxfp4(aq, sa, bq, sb):
+    """fp64 reference of the MXFP4 GEMM: A [M, K] and B^T [N, K] as quantized
+    by quant_mxfp4_1x32 -> (C [M, N], T [M, N])."""
+    aq, sa, bq, sb = (np.ascontiguousarray(v, dtype=np.uint8) for v in (aq, sa, bq, sb))
+    M, N, K = aq.shape[0], bq.shape[0], 2 * aq.shape[1]
+    c = np.empty((M, N), dtype=np.float64)
+    t = np.empty((M, N), dtype=np.float64)
+    dp = ctypes.POINTER(ctypes.c_double)
+    rc = _load().fgqo_gemm_mxfp4(_ptr(aq, _u8p), _ptr(sa, _u8p), _ptr(bq, _u8p), _ptr(sb, _u8p),
+                                 M, N, K, c.ctypes.data_as(dp), t.ctypes.data_as(dp))
+    if rc != 0:
+        raise ValueError(f"oracle gemm_mxfp4 failed ({rc})")
+    return c, t
 
 
 def quant_w_128x128(w_bf16, mode: int = MODE_FP32):

@@ -340,3 +340,87 @@ double fgqo_ue8m0_unpack(uint32_t packed, int i) {
   int code = (int)((packed >> (8 * i)) & 0xFFu);
   return ldexp(1.0, code - 127);
 }
+
+/* ---- MXFP4: E2M1 elements, one UE8M0 scale per 32 ------------------------
+ *
+ * "Fine-Grained FP8/FP4 Quantization", §UE8M0 vs E4M3 Scale Formats (UE8M0
+ * scales, block size 32, the MXFP standard), §NVFP4 Two-Level Scaling (the
+ * E2M1 value list 0, 0.5, 1, 1.5, 2, 3, 4, 6) and §When to Use (MXFP4 with
+ * UE8M0 scales for native hardware acceleration).  Readings: the scale of a
+ * group is the smallest power of two >= amax / 6 (6 = largest E2M1 value),
+ * the rounding-up rule the page gives for UE8M0 scales, so no element
+ * saturates; a zero group gets scale 1; codes are E2M1(x / s) rounded to
+ * nearest, ties to even. */
+
+/* E2M1: bit 3 sign, bits 2-1 exponent (bias 1), bit 0 mantissa; codes 0..7
+ * are 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double fgqo_e2m1_decode(uint8_t code) {
+  static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  double v = mag[code & 7];
+  return (code & 8) ? -v : v;
+}
+
+/* Nearest E2M1 code to v, ties to the code with mantissa bit 0, magnitudes
+ * beyond 6 saturate to 6, the sign kept (a negative value rounding to 0
+ * gives 8). */
+uint8_t fgqo_e2m1_encode(double v) {
+  const double a = fabs(v);
+  int best = 0;
+  for (int c = 1; c < 8; ++c) {
+    const double dc = fabs(fgqo_e2m1_decode((uint8_t)c) - a);
+    const double db = fabs(fgqo_e2m1_decode((uint8_t)best) - a);
+    if (dc < db || (dc == db && (c & 1) == 0)) best = c;
+  }
+  if (a > 6.0) best = 7;
+  return (uint8_t)(best | (signbit(v) ? 8 : 0));
+}
+
+/* MXFP4 quantization of the rows of X bf16 [R, K] row-major, K % 32 == 0.
+ * Outputs Xq [R, K/2] bytes (element 2j in the low nibble of byte j,
+ * element 2j+1 in the high nibble) and sX [R, K/32] UE8M0 codes
+ * (scale 2^(code - 127)). */
+int fgqo_quant_mxfp4_1x32(const uint16_t *x, int64_t R, int64_t K, uint8_t *xq, uint8_t *sx) {
+  if (K % 32 != 0) return -2;
+  const int64_t kg = K / 32;
+  for (int64_t r = 0; r < R; ++r)
+    for (int64_t g = 0; g < kg; ++g) {
+      const uint16_t *src = x + r * K + g * 32;
+      float amax;
+      if (group_amax(src, K, 1, 32, &amax) != 0) return -1;
+      const float s = amax == 0.0f ? 1.0f : fgqo_pow2_ceil(amax / 6.0f);
+      sx[r * kg + g] = (uint8_t)fgqo_ue8m0_code(s);
+      for (int64_t j = 0; j < 32; j += 2) {
+        const uint8_t lo = fgqo_e2m1_encode((double)fgqo_bf16_to_float(src[j]) / s);
+        const uint8_t hi = fgqo_e2m1_encode((double)fgqo_bf16_to_float(src[j + 1]) / s);
+        xq[r * (K / 2) + (g * 32 + j) / 2] = (uint8_t)(lo | (hi << 4));
+      }
+    }
+  return 0;
+}
+
+static double mx_hat(const uint8_t *q, const uint8_t *s, int64_t K, int64_t r, int64_t k) {
+  const uint8_t byte = q[r * (K / 2) + k / 2];
+  const uint8_t code = (k & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+  return fgqo_e2m1_decode(code) * ldexp(1.0, (int)s[r * (K / 32) + k / 32] - 127);
+}
+
+/* MXFP4 GEMM reference: both operands as rows along K (A [M, K], B given as
+ * its transpose [N, K], each quantized by fgqo_quant_mxfp4_1x32):
+ * C[m,n] = sum_k A_hat[m,k] B_hat[n,k] in fp64, k ascending, and
+ * T[m,n] = sum_k |A_hat| |B_hat| (each product is exact in fp64). */
+int fgqo_gemm_mxfp4(const uint8_t *aq, const uint8_t *sa, const uint8_t *bq, const uint8_t *sb,
+                    int64_t M, int64_t N, int64_t K, double *c, double *t) {
+  if (K % 32 != 0) return -2;
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0, tt = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const double p = mx_hat(aq, sa, K, m, k) * mx_hat(bq, sb, K, n, k);
+        acc += p;
+        tt += fabs(p);
+      }
+      c[m * N + n] = acc;
+      t[m * N + n] = tt;
+    }
+  return 0;
+}

@@ -433,3 +433,81 @@ def test_tolerance_check_detects_errors():
     assert not ok
     ok, _ = oracle.gemm_within_tolerance(c_ref + 0.39, c_ref, t, out_bf16=False)
     assert not ok
+
+
+# ---- MXFP4: E2M1 elements, UE8M0 scale per 32 ------------------------------
+
+# The E2M1 values the page lists (§NVFP4 Two-Level Scaling).
+E2M1_PAGE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_decode_is_the_page_list():
+    for c in range(8):
+        assert oracle.e2m1_decode(c) == E2M1_PAGE[c]
+        neg = oracle.e2m1_decode(c | 8)
+        assert neg == -E2M1_PAGE[c] and math.copysign(1.0, neg) == -1.0
+
+
+def test_e2m1_encode_nearest_even_saturating():
+    for c in range(16):
+        assert oracle.e2m1_encode(oracle.e2m1_decode(c)) == c
+    # brute-force nearest over a fine grid, ties to the even code
+    vals = np.concatenate([np.linspace(-8, 8, 4097), [1e-30, -1e-30, 1e30, -1e30]])
+    for v in vals:
+        c = oracle.e2m1_encode(v)
+        mag = abs(v)
+        dists = [abs(e - min(mag, 6.0)) for e in E2M1_PAGE]
+        best = min(dists)
+        ties = [i for i, d in enumerate(dists) if d == best]
+        want = ties[0] if len(ties) == 1 else [i for i in ties if i % 2 == 0][0]
+        assert c & 7 == want, (v, c)
+        if v < 0:
+            assert c & 8
+    for lo, hi in zip(range(7), range(1, 8)):  # every midpoint goes to the even code
+        mid = (E2M1_PAGE[lo] + E2M1_PAGE[hi]) / 2
+        assert oracle.e2m1_encode(mid) == (lo if lo % 2 == 0 else hi)
+
+
+def test_mxfp4_scales_codes_and_packing():
+    import fgq_inputs
+    R, K = 64, 512
+    x = fgq_inputs.exponent_spread((R, K), 40, 1, seed=9)
+    x[3, 64:96] = 0.0                      # a zero group
+    q, s = oracle.quant_mxfp4_1x32(x)
+    assert q.shape == (R, K // 2) and s.shape == (R, K // 32)
+    xf = x.float().numpy().astype(np.float64)
+    dec = np.array([oracle.e2m1_decode(c) for c in range(16)])
+    codes = np.stack([q & 15, q >> 4], axis=-1).reshape(R, K)   # element 2j = low nibble
+    for r in range(R):
+        for g in range(K // 32):
+            grp = xf[r, 32 * g:32 * g + 32]
+            amax = np.abs(grp).max()
+            scale = 2.0 ** (int(s[r, g]) - 127)
+            if amax == 0:
+                assert s[r, g] == 127
+            else:
+                assert 3.0 < amax / scale <= 6.0   # power-of-two ceiling of amax / 6
+            y = grp / scale
+            got = dec[codes[r, 32 * g:32 * g + 32]]
+            err = np.abs(got - y)
+            nearest = np.min(np.abs(np.abs(y)[:, None] - np.array(E2M1_PAGE)[None, :]), axis=1)
+            assert np.all(err <= nearest + 1e-300)  # every code is a nearest value
+
+
+def test_mxfp4_gemm_matches_numpy_dequant():
+    import fgq_inputs
+    M, N, K = 24, 40, 256
+    a = fgq_inputs.exponent_spread((M, K), 10, 1, seed=1)
+    b = fgq_inputs.exponent_spread((N, K), 10, 1, seed=2)
+    aq, sa = oracle.quant_mxfp4_1x32(a)
+    bq, sb = oracle.quant_mxfp4_1x32(b)
+    table = np.array(E2M1_PAGE + [-v for v in E2M1_PAGE])
+
+    def deq(q, s):
+        codes = np.stack([q & 15, q >> 4], axis=-1).reshape(q.shape[0], -1)
+        return table[codes] * np.repeat(np.exp2(s.astype(np.float64) - 127.0), 32, axis=1)
+
+    ah, bh = deq(aq, sa), deq(bq, sb)
+    c, t = oracle.gemm_mxfp4(aq, sa, bq, sb)
+    assert np.allclose(c, ah @ bh.T, rtol=0, atol=1e-12 * (np.abs(ah) @ np.abs(bh).T).max())
+    assert np.allclose(t, np.abs(ah) @ np.abs(bh).T, rtol=1e-12)
