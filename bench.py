@@ -405,16 +405,20 @@ def run_fgq(args):
         QM, QK = qa[0].shape
         qaq = torch.empty((QM, QK), dtype=torch.uint8, device=dev)
         qsa = torch.empty((QM, QK // 128), dtype=torch.float32, device=dev)
-        quant_bw = {"workload": "quantize-bw: act bf16 [16384,7168] Student-t nu=3 (1x128, and 128x1 "
-                                "transposed); weight bf16 [7168,7168] N(0,0.02^2) (128x128); fp32 scales"}
+        quant_bw = {"workload": "quantize-bw: act bf16 [16384,7168] Student-t nu=3 (1x128, 128x1 "
+                                "transposed, MXFP4 1x32); weight bf16 [7168,7168] N(0,0.02^2) (128x128); fp32 scales"}
         qsteps = max(10, min(args.steps, 200))
         qaqt = torch.empty((QK, QM), dtype=torch.uint8, device=dev)
+        qmx = torch.empty((QM, QK // 2), dtype=torch.uint8, device=dev)
+        qmxs = torch.empty((QM, QK // 32), dtype=torch.uint8, device=dev)
         qsat = torch.empty((QK, QM // 128), dtype=torch.float32, device=dev)
         for name, fn, nbytes in (
                 ("quant_act_1x128", lambda i: fgq.quant_act_1x128(qa[i % 2], "fp32", xq=qaq, sx=qsa),
                  QM * QK * 3 + QM * (QK // 128) * 4),
                 ("quant_act_128x1", lambda i: fgq.quant_act_128x1(qa[i % 2], "fp32", xqt=qaqt, sxt=qsat),
                  QM * QK * 3 + QK * (QM // 128) * 4),
+                ("quant_mxfp4_1x32", lambda i: fgq.quant_mxfp4_1x32(qa[i % 2], xq=qmx, sx=qmxs),
+                 QM * QK * 2 + QM * QK // 2 + QM * (QK // 32)),
                 ("quant_w_128x128", lambda i: fgq.quant_w_128x128(qw[i % 2], "fp32", wq=bq, sw=sb),
                  BYTES_QUANT_W)):
             for i in range(5):
@@ -519,7 +523,7 @@ def run_fgq(args):
 
     peaks, src = _peaks()
     if quant_bw:
-        for k in ("quant_act_1x128", "quant_act_128x1", "quant_w_128x128"):
+        for k in ("quant_act_1x128", "quant_act_128x1", "quant_mxfp4_1x32", "quant_w_128x128"):
             quant_bw[k]["frac_hbm"] = quant_bw[k]["GB/s"] / peaks["hbm_gbs"]
     if skinny:
         for k, v in skinny.items():

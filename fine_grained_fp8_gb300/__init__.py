@@ -23,7 +23,7 @@ from . import _lib
 from ._lib import (FGQ_OUT_BF16, FGQ_OUT_F32, FGQ_SCALE_FP32, FGQ_SCALE_UE8M0, FgqError,
                    check, load)
 
-__all__ = ["quant_act_1x128", "quant_act_128x1", "quant_w_128x128", "gemm_fp8_blockscaled",
+__all__ = ["quant_act_1x128", "quant_act_128x1", "quant_mxfp4_1x32", "quant_w_128x128", "gemm_fp8_blockscaled",
            "gemm_fp8_blockscaled_splitk", "gemm_fp8_blockscaled_fused_act", "splitk_workspace", "device_error",
            "FgqError", "load", "FGQ_SCALE_FP32", "FGQ_SCALE_UE8M0", "FGQ_OUT_F32",
            "FGQ_OUT_BF16", "scale_mode"]
@@ -93,6 +93,30 @@ def quant_act_128x1(x: torch.Tensor, mode="fp32", xqt: torch.Tensor | None = Non
                                   scale_mode(mode), _stream(x))
     check("fgq_quant_act_128x1", st)
     return xqt, sxt
+
+
+def quant_mxfp4_1x32(x: torch.Tensor, xq: torch.Tensor | None = None,
+                     sx: torch.Tensor | None = None):
+    """MXFP4 quantization of the rows of bf16 x [R, K]: E2M1 codes packed two
+    per byte, xq [R, K/2] uint8 (even element in the low nibble), and one
+    UE8M0 scale code per 32 elements, sx [R, K/32] uint8."""
+    _need_cuda("x", x, torch.bfloat16)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with a contiguous last dimension")
+    R, K = x.shape
+    if xq is None:
+        xq = torch.empty((R, K // 2), dtype=torch.uint8, device=x.device)
+    if sx is None:
+        sx = torch.empty((R, K // 32), dtype=torch.uint8, device=x.device)
+    _need_cuda("xq", xq, torch.uint8)
+    _need_cuda("sx", sx, torch.uint8)
+    if xq.shape != (R, K // 2) or not xq.is_contiguous() or sx.shape != (R, K // 32) \
+            or not sx.is_contiguous():
+        raise ValueError("xq must be a dense [R, K/2] and sx a dense [R, K/32]")
+    st = _lib.fgq_quant_mxfp4_1x32(x.data_ptr(), R, K, x.stride(0), xq.data_ptr(), sx.data_ptr(),
+                                   _stream(x))
+    check("fgq_quant_mxfp4_1x32", st)
+    return xq, sx
 
 
 def quant_w_128x128(w: torch.Tensor, mode="fp32", wq: torch.Tensor | None = None,

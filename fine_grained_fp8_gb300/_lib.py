@@ -30,6 +30,7 @@ _int = ctypes.c_int
 SIGNATURES = {
     "fgq_quant_act_1x128": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _int, _vp]),
     "fgq_quant_act_128x1": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _int, _vp]),
+    "fgq_quant_mxfp4_1x32": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
     "fgq_quant_w_128x128": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _int, _vp]),
     "fgq_gemm_fp8_blockscaled": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "fgq_gemm_fp8_blockscaled_ex": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
@@ -101,6 +102,10 @@ def fgq_quant_act_1x128(x, M, K, ldx, xq, ldq, sx, mode, stream) -> int:
 
 def fgq_quant_act_128x1(x, M, K, ldx, xqt, sxt, mode, stream) -> int:
     return load().fgq_quant_act_128x1(x, M, K, ldx, xqt, sxt, mode, stream)
+
+
+def fgq_quant_mxfp4_1x32(x, R, K, ldx, xq, sx, stream) -> int:
+    return load().fgq_quant_mxfp4_1x32(x, R, K, ldx, xq, sx, stream)
 
 
 def fgq_quant_w_128x128(w, K, N, ldw, wq, sw, mode, stream) -> int:

@@ -93,6 +93,21 @@ fgq_status fgq_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx,
                                                static_cast<cudaStream_t>(stream), dev));
 }
 
+fgq_status fgq_quant_mxfp4_1x32(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* xq,
+                                uint8_t* sx, void* stream) {
+  if (R < 0 || K <= 0 || K % 32 != 0) return FGQ_ERR_INVALID_ARG;
+  if (R == 0) return FGQ_OK;
+  if (!x || !xq || !sx) return FGQ_ERR_INVALID_ARG;
+  if (ldx < K || ldx % 8 != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(xq, 4)) return FGQ_ERR_INVALID_ARG;
+  if (R > kMaxGroups / (K / 32)) return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_quant_mxfp4_1x32(x, R, K, ldx, xq, sx,
+                                                static_cast<cudaStream_t>(stream), dev));
+}
+
 fgq_status fgq_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t ldw, uint8_t* wq,
                                float* sw, int mode, void* stream) {
   if (K <= 0 || N <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;

@@ -37,6 +37,9 @@ cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t 
                                    float* sxt, int mode, cudaStream_t stream,
                                    const DeviceInfo& dev);
 
+cudaError_t launch_quant_mxfp4_1x32(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* xq,
+                                    uint8_t* sx, cudaStream_t stream, const DeviceInfo& dev);
+
 cudaError_t launch_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
                                    uint8_t* wq, float* sw, int mode, cudaStream_t stream,
                                    const DeviceInfo& dev);

@@ -338,7 +338,117 @@ __global__ void __launch_bounds__(kWThreads, 4)
   }
 }
 
+// ---- MXFP4 1x32 quantizer --------------------------------------------------------
+//
+// E2M1 elements with one UE8M0 scale per 32 consecutive elements of a row
+// ("Fine-Grained FP8/FP4 Quantization", §UE8M0 vs E4M3 Scale Formats, block
+// size 32).  Scale 2^e = the smallest power of two >= amax / 6 (6 = largest
+// E2M1 value), exponent clamped to [-127, 127], 1 for a zero group; each
+// element is x * 2^-e (exact) converted to E2M1, round to nearest even.
+// Four lanes own a group (8 elements, 16 bytes each); codes are packed two
+// per byte, the even element in the low nibble.
+constexpr int kMxThreads = 256;
+constexpr int kMxRounds = 2;
+
+// Eight fp32 -> eight E2M1 codes in 32 bits: byte j = element 2j (low
+// nibble) and element 2j+1 (high nibble).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&y)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
+  return r;
+}
+
+// UE8M0 exponent field of the smallest power of two >= amax / 6 (field 0 =
+// 2^-127, the clamp; 127 = 2^0 for a zero group).
+__device__ __forceinline__ uint32_t mx_scale_code(uint32_t mag_bits) {
+  const float amax = __uint_as_float(mag_bits << 16);
+  if (amax == 0.0f) return 127u;
+  const uint32_t b = __float_as_uint(__fdiv_rn(amax, 6.0f));
+  const uint32_t e = b >> 23, man = b & 0x7FFFFFu;
+  if (e == 0) return b <= 0x00400000u ? 0u : 1u;  // subnormal quotient: 2^-127 or 2^-126
+  return man != 0 ? e + 1 : e;
+}
+
+template <bool DENSE>
+__global__ void __launch_bounds__(kMxThreads)
+    quant_mxfp4_1x32_kernel(const uint16_t* __restrict__ x, uint32_t kg, uint32_t groups,
+                            int64_t ldx, uint8_t* __restrict__ xq, uint8_t* __restrict__ sx) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t sub = lane >> 2, l4 = lane & 3u;
+  const uint32_t warp = (blockIdx.x * kMxThreads + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * kMxThreads) >> 5;
+  constexpr uint32_t kPerWarp = 8 * kMxRounds;
+  for (uint32_t base = warp * kPerWarp; base < groups; base += nwarps * kPerWarp) {
+    uint4 v[kMxRounds];
+    uint32_t g[kMxRounds];
+#pragma unroll
+    for (int u = 0; u < kMxRounds; ++u) {
+      g[u] = base + 8 * u + sub;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (g[u] < groups) {
+        const uint16_t* src;
+        if (DENSE) {
+          src = x + static_cast<uint64_t>(g[u]) * 32;
+        } else {
+          const uint32_t r = g[u] / kg, c = g[u] - r * kg;
+          src = x + static_cast<int64_t>(r) * ldx + c * 32;
+        }
+        v[u] = ld_stream_16(src + 8 * l4);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kMxRounds; ++u) {
+      uint32_t mx = absmax_pairs(v[u]);
+      mx = __vmaxu2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+      mx = __vmaxu2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+      const uint32_t code = mx_scale_code(max(mx & 0xFFFFu, mx >> 16));
+      // 2^-e: exponent field 254 - code; code 0 (2^-127) gives 2^127
+      const float inv = __uint_as_float((254u - code) << 23);
+      if (g[u] < groups) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        float y[8];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const float2 f = bf16x2_to_f32x2(w[p]);
+          y[2 * p] = f.x * inv;
+          y[2 * p + 1] = f.y * inv;
+        }
+        const uint32_t packed = cvt_e2m1x8(y);
+        // row-major [R, K/2]: group g covers bytes 16 g .. 16 g + 15
+        *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(g[u]) * 16 + 4 * l4) = packed;
+        if (l4 == 0) sx[g[u]] = static_cast<uint8_t>(code);
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_quant_mxfp4_1x32(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* xq,
+                                    uint8_t* sx, cudaStream_t stream, const DeviceInfo& dev) {
+  const uint32_t kg = static_cast<uint32_t>(K / 32);
+  const uint32_t groups = static_cast<uint32_t>(R * (K / 32));
+  if (groups == 0) return cudaSuccess;
+  const bool dense = ldx == K;
+  auto k = dense ? quant_mxfp4_1x32_kernel<true> : quant_mxfp4_1x32_kernel<false>;
+  int per_sm = 0;
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kMxThreads, 0);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) per_sm = 1;
+  const uint32_t per_block = (kMxThreads / 32) * 8 * kMxRounds;
+  const uint32_t needed = (groups + per_block - 1) / per_block;
+  uint32_t grid = static_cast<uint32_t>(dev.sm_count) * static_cast<uint32_t>(per_sm);
+  if (grid > needed) grid = needed;
+  k<<<grid, kMxThreads, 0, stream>>>(static_cast<const uint16_t*>(x), kg, groups, ldx, xq, sx);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xqt,
                                    float* sxt, int mode, cudaStream_t stream,

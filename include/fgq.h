@@ -94,6 +94,28 @@ fgq_status fgq_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx,
                                float* sxt, int mode, void* stream);
 
 /*
+ * MXFP4 quantization (§UE8M0 vs E4M3 Scale Formats: UE8M0 scales, block
+ * size 32; E2M1 values 0, 0.5, 1, 1.5, 2, 3, 4, 6 from §NVFP4 Two-Level
+ * Scaling): one UE8M0 scale per 32 consecutive elements of each row.  For
+ * a GEMM both operands are quantized this way along K (the weight as its
+ * transpose [N, K]).
+ *
+ *   x    bf16 [R, K], row r at x + r * ldx (ldx >= K, ldx % 8 == 0),
+ *        16-byte aligned.
+ *   xq   E2M1 codes [R, K/2] bytes, row-major (dense), 4-byte aligned:
+ *        element 2j of a row in the low nibble of byte j, element 2j+1 in
+ *        the high nibble; code bit 3 = sign.
+ *   sx   UE8M0 codes [R, K/32] bytes, row-major (dense): the scale of
+ *        elements 32 g .. 32 g + 31 of row r is 2^(sx[r * K/32 + g] - 127).
+ *   K % 32 == 0, K > 0, R >= 0.
+ * Scale: the smallest power of two >= amax / 6 (exponent clamped at -127;
+ * a zero group gets 1); each element becomes E2M1(x / s), round to nearest
+ * with ties to even (x / s is exact; no element exceeds 6).
+ */
+fgq_status fgq_quant_mxfp4_1x32(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* xq,
+                                uint8_t* sx, void* stream);
+
+/*
  * 128x128 block-wise weight quantization (§Scaling Granularities,
  * per-block 128x128; scale_B [K/128, N/128] from §DeepGEMM).
  *

@@ -1,0 +1,70 @@
+"""Parity of the MXFP4 quantizer (E2M1 elements, one UE8M0 scale per 32;
+"Fine-Grained FP8/FP4 Quantization", §UE8M0 vs E4M3 Scale Formats) with the
+oracle: codes and scale codes bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import fgq_inputs
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(fgq, x_cpu, dev, pad=0):
+    R, K = x_cpu.shape
+    if pad:
+        big = torch.zeros((R, K + pad), dtype=torch.bfloat16)
+        big[:, :K] = x_cpu
+        x = big.to(dev)[:, :K]
+    else:
+        x = x_cpu.to(dev)
+    q, s = fgq.quant_mxfp4_1x32(x)
+    torch.cuda.synchronize()
+    qo, so = oracle.quant_mxfp4_1x32(x_cpu)
+    sg, qg = s.cpu().numpy(), q.cpu().numpy()
+    bad_s = np.argwhere(sg != so)
+    assert bad_s.size == 0, f"{len(bad_s)} scale codes differ, first at {tuple(bad_s[0])}"
+    bad = np.argwhere(qg != qo)
+    assert bad.size == 0, (f"{len(bad)} code bytes differ, first at {tuple(bad[0])}: "
+                           f"{qg[tuple(bad[0])]:#04x} vs {qo[tuple(bad[0])]:#04x}")
+
+
+@pytest.mark.parametrize("R,K,pad", [(1, 32, 0), (7, 96, 8), (64, 1024, 0), (33, 7168, 64)])
+def test_mxfp4_matches_oracle(fgq, cuda_dev, R, K, pad):
+    x = fgq_inputs.outlier((R, K), 1e-2, 100.0, seed=R + K)
+    _check(fgq, x, cuda_dev, pad)
+
+
+def test_mxfp4_scales_across_binades_zero_groups(fgq, cuda_dev):
+    """Group maxima over 250 binades (down to the 2^-127 clamp and up to the
+    largest bf16 values), zero groups and groups of negative zeros."""
+    x = fgq_inputs.exponent_spread((256, 1024), 125, 1, seed=3)
+    x[0, :32] = 0.0
+    x[1, 32:64] = -0.0
+    x[2, :] = torch.tensor(3.3e38, dtype=torch.bfloat16)  # near the bf16 maximum
+    _check(fgq, x, cuda_dev)
+
+
+def test_mxfp4_every_bf16_magnitude(fgq, cuda_dev):
+    """Every finite bf16 value as an element of a group, under group maxima in
+    several binades: each group is its maximum plus 31 values below it."""
+    allbits = np.arange(0, 0x7F80, dtype=np.uint16)          # finite non-negative patterns
+    rows = []
+    for amax_bits in (0x3F80, 0x3FC0, 0x0080, 0x0001, 0x7F7F, 0x2000, 0x5555):
+        vals = allbits[allbits <= amax_bits]
+        signs = np.where(np.arange(vals.size) % 2 == 0, 0, 0x8000).astype(np.uint16)
+        vals = vals | signs
+        n = (vals.size + 30) // 31
+        vals = np.concatenate([vals, np.zeros(n * 31 - vals.size, np.uint16)]).reshape(n, 31)
+        grp = np.concatenate([np.full((n, 1), amax_bits, np.uint16), vals], axis=1)  # [n, 32]
+        rows.append(grp)
+    groups = np.concatenate(rows)                            # [G, 32]
+    G = groups.shape[0] - groups.shape[0] % 8
+    x = torch.from_numpy(groups[:G].reshape(-1, 256).view(np.int16)).view(torch.bfloat16)
+    _check(fgq, x, cuda_dev)
+
+
+def test_mxfp4_full_size(fgq, cuda_dev):
+    x = fgq_inputs.student_t((4096, 7168), 3, 1.0, seed=6)
+    _check(fgq, x, cuda_dev)
