@@ -393,6 +393,48 @@ def run_fgq(args):
         if fgq.device_error() != 0:
             raise SystemExit("a kernel reported a device wait timeout")
 
+    # MXFP4 on the same workload: A quantized (E2M1, UE8M0 per 32) every step,
+    # the weight quantized once as its transpose [N, K] (inference), and the
+    # block-scaled FP4 GEMM (tcgen05.mma kind::mxf4).
+    mxfp4 = None
+    if not args.no_mxfp4:
+        msteps = max(10, min(args.steps, 500))
+        wq4 = [fgq.quant_mxfp4_1x32(b.t().contiguous()) for _, b in sets]
+        aq4 = torch.empty((M_, K_ // 2), dtype=torch.uint8, device=dev)
+        sa4 = torch.empty((M_, K_ // 32), dtype=torch.uint8, device=dev)
+
+        def mstep(i, ev):
+            a, _ = sets[i % 2]
+            ev[0].record(stream)
+            fgq.quant_mxfp4_1x32(a, xq=aq4, sx=sa4)
+            ev[1].record(stream)
+            fgq.gemm_mxfp4(aq4, sa4, *wq4[i % 2], torch.bfloat16, out=c)
+            ev[2].record(stream)
+
+        mev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(msteps)]
+        for i in range(5):
+            mstep(i, mev[i])
+        torch.cuda.synchronize()
+        m0 = torch.cuda.Event(enable_timing=True)
+        m1 = torch.cuda.Event(enable_timing=True)
+        m0.record(stream)
+        for i in range(msteps):
+            mstep(i, mev[i])
+        m1.record(stream)
+        torch.cuda.synchronize()
+        mms = reduce_max(dist, m0.elapsed_time(m1), dev) / msteps
+        m_act = 1e3 * sum(e[0].elapsed_time(e[1]) for e in mev) / msteps
+        m_gemm = 1e3 * sum(e[1].elapsed_time(e[2]) for e in mev) / msteps
+        mxfp4 = {"format": "MXFP4 (E2M1, UE8M0 scale per 32, both operands along K)",
+                 "steps": msteps, "ms_per_step": mms,
+                 "value": world * FLOPS_GEMM / (mms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                 "quant_act_us": m_act, "gemm_us": m_gemm,
+                 "gemm_TFLOP/s": FLOPS_GEMM / (m_gemm * 1e-6) / 1e12,
+                 "kernel": "gemm_mxf4_kernel (tcgen05.mma kind::mxf4.block_scale)"}
+        del wq4, aq4, sa4
+        if fgq.device_error() != 0:
+            raise SystemExit("a kernel reported a device wait timeout")
+
     # The quantizers on the quantize-bandwidth workload (activations
     # [16384, 7168] Student-t nu=3, weight [7168, 7168] N(0, 0.02^2)), each
     # timed alone over rotated input pairs larger than L2.
@@ -532,6 +574,11 @@ def run_fgq(args):
                     if isinstance(e, dict):
                         e["frac_hbm"] = e["GB/s"] / peaks["hbm_gbs"]
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]  # nominal fp8 = 2x bf16 dense
+    if mxfp4:
+        fp4_peak = 6.0 * peaks["bf16_tflops_sustained"]  # nominal fp4 = 6x bf16 dense on GB300
+        mxfp4["peak_fp4"] = fp4_peak
+        mxfp4["frac_fp4"] = mxfp4["gemm_TFLOP/s"] / fp4_peak
+        mxfp4["peak_source"] = f"{src}: 6 x bf16_tflops_sustained (nominal 13.5 / 2.25 PFLOP/s)"
     if ue8m0:
         ue8m0["frac_fp8"] = ue8m0["gemm_TFLOP/s"] / fp8_peak
         ue8m0["traffic"] = _traffic("gemm_mx", "gemm_mx.cu")
@@ -571,6 +618,7 @@ def run_fgq(args):
         "gpu_launches": 3 * args.steps,
         "quant_bw": quant_bw,
         "ue8m0": ue8m0,
+        "mxfp4": mxfp4,
         "skinny": skinny,
         "clocks": clk,
         "cpu_baseline": cpu,
@@ -594,6 +642,8 @@ def main(argv=None):
                    help="skip the power-of-two scale (UE8M0) step")
     p.add_argument("--no-skinny", action="store_true",
                    help="skip the skinny-GEMM sweep")
+    p.add_argument("--no-mxfp4", action="store_true",
+                   help="skip the MXFP4 step")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")

@@ -24,7 +24,7 @@ from ._lib import (FGQ_OUT_BF16, FGQ_OUT_F32, FGQ_SCALE_FP32, FGQ_SCALE_UE8M0, F
                    check, load)
 
 __all__ = ["quant_act_1x128", "quant_act_128x1", "quant_mxfp4_1x32", "quant_w_128x128", "gemm_fp8_blockscaled",
-           "gemm_fp8_blockscaled_splitk", "gemm_fp8_blockscaled_fused_act", "splitk_workspace", "device_error",
+           "gemm_fp8_blockscaled_splitk", "gemm_fp8_blockscaled_fused_act", "gemm_mxfp4", "splitk_workspace", "device_error",
            "FgqError", "load", "FGQ_SCALE_FP32", "FGQ_SCALE_UE8M0", "FGQ_OUT_F32",
            "FGQ_OUT_BF16", "scale_mode"]
 
@@ -201,6 +201,32 @@ def gemm_fp8_blockscaled_fused_act(a: torch.Tensor, bq: torch.Tensor, sb: torch.
         M, N, K, FGQ_OUT_BF16 if out_dtype == torch.bfloat16 else FGQ_OUT_F32, scale_mode(mode),
         _stream(a))
     check("fgq_gemm_fp8_blockscaled_fused_act", st)
+    return out
+
+
+def gemm_mxfp4(aq: torch.Tensor, sa: torch.Tensor, bq: torch.Tensor, sb: torch.Tensor,
+               out_dtype=torch.float32, out: torch.Tensor | None = None) -> torch.Tensor:
+    """C [M, N] from MXFP4 operands as quant_mxfp4_1x32 writes them: aq [M, K/2]
+    and sa [M, K/32], bq [N, K/2] and sb [N, K/32] (the weight quantized as
+    its transpose)."""
+    for name, t in (("aq", aq), ("sa", sa), ("bq", bq), ("sb", sb)):
+        _need_cuda(name, t, torch.uint8)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    M, K = aq.shape[0], 2 * aq.shape[1]
+    N = bq.shape[0]
+    if bq.shape != (N, K // 2) or sa.shape != (M, K // 32) or sb.shape != (N, K // 32):
+        raise ValueError("shape mismatch: aq [M,K/2], sa [M,K/32], bq [N,K/2], sb [N,K/32]")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=aq.device)
+    _need_cuda("out", out, out_dtype)
+    if out.shape != (M, N) or out.stride(1) != 1:
+        raise ValueError("out must be [M, N] with contiguous rows")
+    st = _lib.fgq_gemm_mxfp4(aq.data_ptr(), sa.data_ptr(), bq.data_ptr(), sb.data_ptr(),
+                             out.data_ptr(), out.stride(0), M, N, K,
+                             FGQ_OUT_BF16 if out_dtype == torch.bfloat16 else FGQ_OUT_F32,
+                             _stream(aq))
+    check("fgq_gemm_mxfp4", st)
     return out
 
 

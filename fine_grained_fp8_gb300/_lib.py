@@ -38,6 +38,7 @@ SIGNATURES = {
     "fgq_gemm_fp8_blockscaled_splitk": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                                _int, _int, _vp, ctypes.c_size_t, _vp]),
     "fgq_gemm_splitk_workspace_size": (_int, [_i64, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
+    "fgq_gemm_mxfp4": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _vp]),
     "fgq_gemm_fp8_blockscaled_fused_act": (_int, [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                                   _int, _int, _vp]),
     "fgq_gemm_fp8_blockscaled_splitk_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
@@ -135,6 +136,10 @@ def fgq_gemm_fp8_blockscaled_splitk_noalloc(A, sA, B, sB, C, ldc, M, N, K, out, 
 def fgq_gemm_fp8_blockscaled_fused_act(A, lda, B, sB, C, ldc, M, N, K, out, mode, stream) -> int:
     return load().fgq_gemm_fp8_blockscaled_fused_act(A, lda, B, sB, C, ldc, M, N, K, out, mode,
                                                      stream)
+
+
+def fgq_gemm_mxfp4(A, sA, B, sB, C, ldc, M, N, K, out, stream) -> int:
+    return load().fgq_gemm_mxfp4(A, sA, B, sB, C, ldc, M, N, K, out, stream)
 
 
 def fgq_gemm_splitk_workspace_size(M, N, K):

@@ -193,6 +193,26 @@ fgq_status fgq_gemm_fp8_blockscaled_fused_act(const void* A, int64_t lda, const 
                                                static_cast<cudaStream_t>(stream), dev));
 }
 
+fgq_status fgq_gemm_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                          const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
+                          int64_t K, int out, void* stream) {
+  if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (out != FGQ_OUT_F32 && out != FGQ_OUT_BF16) return FGQ_ERR_INVALID_ARG;
+  if (M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31) || K >= (int64_t{1} << 31))
+    return FGQ_ERR_INVALID_ARG;
+  if (M == 0) return FGQ_OK;
+  if (!A || !sA || !B || !sB || !C) return FGQ_ERR_INVALID_ARG;
+  const int64_t vec = (out == FGQ_OUT_F32) ? 4 : 8;
+  if (ldc < N || ldc % vec != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(sA, 4) || !aligned(sB, 4))
+    return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_gemm_mxf4(A, sA, B, sB, C, ldc, M, N, K, out == FGQ_OUT_BF16 ? 1 : 0,
+                                         static_cast<cudaStream_t>(stream), dev));
+}
+
 fgq_status fgq_gemm_splitk_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {
   if (!bytes || M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
   fgq::DeviceInfo dev;
@@ -275,7 +295,7 @@ fgq_status fgq_device_error(uint32_t* word, int clear) {
   if (e != cudaSuccess) return FGQ_ERR_CUDA;
   uint32_t w = 0;
   for (auto read : {fgq::read_device_error_gemm, fgq::read_device_error_lowm,
-                    fgq::read_device_error_mx}) {
+                    fgq::read_device_error_mx, fgq::read_device_error_mxf4}) {
     uint32_t u = 0;
     e = read(&u, clear != 0);
     if (e != cudaSuccess) return FGQ_ERR_CUDA;

@@ -60,11 +60,18 @@ cudaError_t launch_gemm_mx(const uint8_t* A, const float* sA, const uint8_t* B, 
 // that nothing completes; the wait gives up and records FGQ_DEVERR_SELFTEST.
 cudaError_t launch_selftest_wait_timeout(cudaStream_t stream);
 
+// MXFP4 GEMM: A codes [M, K/2], B codes [N, K/2] (E2M1 pairs), UE8M0 codes
+// sA [M, K/32], sB [N, K/32]; K % 128 == 0, N % 128 == 0.
+cudaError_t launch_gemm_mxf4(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                             const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
+                             int64_t K, int out_bf16, cudaStream_t stream, const DeviceInfo& dev);
+
 // Each kernel translation unit keeps its own device error word; these read
 // (and optionally clear) one unit's word.
 cudaError_t read_device_error_gemm(uint32_t* word, bool clear);
 cudaError_t read_device_error_lowm(uint32_t* word, bool clear);
 cudaError_t read_device_error_mx(uint32_t* word, bool clear);
+cudaError_t read_device_error_mxf4(uint32_t* word, bool clear);
 
 // TMA descriptor of a K-major E4M3 operand [rows, K] with a 128 (K) x
 // box_rows box, 128-byte swizzle, zero fill outside the tensor.

@@ -1,0 +1,417 @@
+// MXFP4 GEMM for sm_103a: E2M1 elements with one UE8M0 scale per 32 along K
+// on both operands ("Fine-Grained FP8/FP4 Quantization", §UE8M0 vs E4M3
+// Scale Formats, block size 32; §When to Use: MXFP4 with UE8M0 scales for
+// native hardware acceleration):
+//
+//   C[m,n] = sum_k e2m1(A[m,k]) 2^(sA[m,k/32]-127) e2m1(B[n,k]) 2^(sB[n,k/32]-127)
+//
+// tcgen05.mma kind::mxf4.block_scale.scale_vec::2X takes K = 64 packed E2M1
+// elements (32 bytes a row) and two UE8M0 factors per row of A and per
+// column of B, applied by the tensor core; the fp32 accumulator stays in
+// TMEM for the whole K loop.  Measured factor layout (as for kind::mxf8f6f4
+// with scale_vec::1X): A's row m at lane m, column base + m/32; B's column
+// n at lane 32 q + n%32, column base + n/32; the descriptor's factor id 0
+// reads bytes 0-1 of the cell (the two 32-element blocks of one MMA), id 2
+// bytes 2-3.
+//
+// Same structure as the power-of-two FP8 kernel (gemm_mx.cu): persistent
+// CTAs on 128 x BN tiles, warp 0 TMA producer (one 128-byte stage = 256
+// elements of K), warp 1 MMA issuer (four MMAs per stage), warps 4-7 write
+// the factors into a TMEM ring (one slot = one 32-bit cell per row or column
+// = four 32-element blocks = two MMAs), warps 8-15 epilogue.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "fgq_device.cuh"
+#include "fgq_internal.h"
+
+namespace fgq {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 128;
+constexpr int kThreads = 512;  // warpgroup 0 control, 1 scale factors, 2-3 epilogue
+constexpr int kEpiWarps = 8;
+constexpr int kSlots = 4;  // scale-factor ring; a slot = 128 elements of K = two K = 64 MMAs
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfaCol0 = 256;     // slot r: A factors at kSfaCol0 + 32 r (+ 0..3)
+constexpr uint32_t kSfbCol0 = 384;     // slot r: B factors at kSfbCol0 + 32 r (+ 0..7)
+
+template <int BN, int STAGES>
+struct Mxf4Cfg {
+  static constexpr int kNAcc = BN == 128 ? 2 : 1;  // accumulators in TMEM columns 0..255
+  static constexpr int kABytes = BM * BK;
+  static constexpr int kBBytes = BN * BK;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kNumBars = 2 * STAGES + 2 * kSlots + 2 * kNAcc + 1;
+  static constexpr size_t kSmemBytes =
+      1024 + static_cast<size_t>(STAGES) * kStageBytes + kNumBars * 8 + 16;
+  static_assert(kNAcc * BN <= static_cast<int>(kSfaCol0), "accumulators overlap the scale ring");
+  static_assert(BN / 32 <= 8, "B factors of one slot take BN/32 <= 8 columns");
+};
+
+__device__ __forceinline__ bool mxf4_wait_drain(uint64_t* bar, uint32_t parity) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > FGQ_WAIT_NS) {
+      record_error(FGQ_DEVERR_DRAIN);
+      return false;
+    }
+  }
+  return true;
+}
+
+// kind::mxf4: A and B E2M1 (type 1), UE8M0 factors (bit 23), factor id 0.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int m, int n) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Eight consecutive TMEM columns of the warp's 32 lanes, one value each.
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                   taddr),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 32 accumulator columns of one row: convert and store (16-byte stores).
+template <bool OUT_BF16>
+__device__ __forceinline__ void store32(void* C, int64_t ldc, int row, int col,
+                                        const uint32_t (&r)[32]) {
+  if (OUT_BF16) {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(C) + row * ldc + col);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 v;
+      v.x = bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
+      v.y = bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
+      v.z = bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
+      v.w = bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
+      dst[j] = v;
+    }
+  } else {
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(C) + row * ldc + col);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) dst[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+  }
+}
+
+template <int BN, int STAGES, bool OUT_BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_mxf4_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_b, const uint8_t* __restrict__ sA,
+                   const uint8_t* __restrict__ sB, void* __restrict__ C, int64_t ldc, int M, int N,
+                   int K) {
+  using CF = Mxf4Cfg<BN, STAGES>;
+  constexpr int NACC = CF::kNAcc;
+  constexpr int HALF = BN / 2;    // columns per epilogue warp
+  constexpr int NLD = HALF / 32;  // 32-column loads per warp and tile
+  static_assert(NLD >= 2, "the load pipeline assumes at least two loads");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sm_a = smem;
+  uint8_t* sm_b = smem + STAGES * CF::kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm_b + STAGES * CF::kBBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* sf_full = empty + STAGES;
+  uint64_t* sf_empty = sf_full + kSlots;
+  uint64_t* acc_full = sf_empty + kSlots;
+  uint64_t* acc_empty = acc_full + NACC;
+  uint64_t* drain = acc_empty + NACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tiles = (M + BM - 1) / BM;
+  const int n_tiles = N / BN;
+  const int num_tiles = m_tiles * n_tiles;
+  const int kstages = (K + 255) / 256;  // 128-byte stages of 256 elements (the last may be half)
+  const int khalves = K / 128;          // scale slots: 128 elements = four 32-element blocks
+  const int kg = K / 32;                // UE8M0 codes per row of sA / sB
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int r = 0; r < kSlots; ++r) {
+      mbar_init(&sf_full[r], 4);
+      mbar_init(&sf_empty[r], 1);
+    }
+    for (int b = 0; b < NACC; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // Everything above (barrier set-up, TMEM allocation) may overlap the
+  // previous kernel in the stream; global memory is touched only after it
+  // has completed.
+  pdl_wait();
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (elect_one_sync()) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int tm = tile % m_tiles, tn = tile / m_tiles;
+        for (int kc = 0; kc < kstages; ++kc, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, FGQ_DEVERR_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], CF::kStageBytes);
+          tma_load_2d(sm_a + s * CF::kABytes, &tmap_a, &full[s], kc * BK, tm * BM);
+          tma_load_2d(sm_b + s * CF::kBBytes, &tmap_b, &full[s], kc * BK, tn * BN);
+        }
+      }
+      // No copy may still target this CTA's shared memory when it exits.
+      const uint32_t first = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
+      for (uint32_t j = first; j < it; ++j) mxf4_wait_drain(&full[j % STAGES], (j / STAGES) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (elect_one_sync()) {
+      constexpr uint32_t idesc0 = idesc_mxf4(BM, BN);
+      const uint64_t dA0 = smem_desc_k_sw128(smem_u32(sm_a));
+      const uint32_t a_lo0 = static_cast<uint32_t>(dA0), dhi = static_cast<uint32_t>(dA0 >> 32);
+      const uint32_t b_lo0 = static_cast<uint32_t>(smem_desc_k_sw128(smem_u32(sm_b)));
+      int ls = 0;
+      uint32_t lph = 0, g_it = 0, t_it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++t_it) {
+        const uint32_t buf = t_it % NACC, aph = (t_it / NACC) & 1u;
+        if (!mbar_wait(&acc_empty[buf], aph ^ 1u, abort_flag, FGQ_DEVERR_MMA_TMEM)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * BN;
+        uint32_t tsfa = 0, tsfb = 0, r = 0;
+        for (int kc = 0; kc < kstages; ++kc) {
+          if (!mbar_wait(&full[ls], lph, abort_flag, FGQ_DEVERR_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_lo = a_lo0 + ls * (CF::kABytes >> 4);
+          const uint32_t b_lo = b_lo0 + ls * (CF::kBBytes >> 4);
+          const int n_mma = (K - kc * 256) >= 256 ? 4 : 2;  // a half stage at the end
+          for (int kk = 0; kk < n_mma; ++kk) {
+            const uint32_t id = static_cast<uint32_t>(kk & 1) * 2u;  // factor bytes 0-1 or 2-3
+            if (id == 0) {
+              r = g_it % kSlots;
+              if (!mbar_wait(&sf_full[r], (g_it / kSlots) & 1u, abort_flag, FGQ_DEVERR_MMA_SF)) {
+                ok = false;
+                break;
+              }
+              tsfa = tmem_base + kSfaCol0 + 32u * r;
+              tsfb = tmem_base + kSfbCol0 + 32u * r;
+            }
+            umma_mxf4(d, make_desc(a_lo + kk * 2, dhi), make_desc(b_lo + kk * 2, dhi),
+                      idesc0 | (id << 29) | (id << 4), tsfa, tsfb, (kc > 0 || kk > 0) ? 1u : 0u);
+            if (id != 0) {
+              umma_commit(&sf_empty[r]);
+              ++g_it;
+            }
+          }
+          if (!ok) break;
+          umma_commit(&empty[ls]);
+          if (++ls == STAGES) {
+            ls = 0;
+            lph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[buf]);
+      }
+      // Every MMA this thread issued must finish before TMEM is released.
+      umma_commit(drain);
+      mxf4_wait_drain(drain, 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- scale-factor writers ----------------
+    const int q = warp & 3;
+    const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
+    uint32_t g_it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+      const int tm = tile % m_tiles, tn = tile / m_tiles;
+      const int row = tm * BM + 32 * q + lane;
+      const bool row_ok = row < M;
+      const uint8_t* sa_row = sA + static_cast<int64_t>(row_ok ? row : 0) * kg;
+      for (int h = 0; h < khalves; ++h, ++g_it) {
+        const uint32_t r = g_it % kSlots;
+        // the four codes of blocks 4h .. 4h+3: this thread's row of A, and
+        // B's columns n = tn*BN + 32 j + lane (replicated in every quarter)
+        const uint32_t wa = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(sa_row + 4 * h)) : 0x7F7F7F7Fu;
+        uint32_t wb[8];
+#pragma unroll
+        for (int j = 0; j < BN / 32; ++j) {
+          const int64_t n = static_cast<int64_t>(tn) * BN + 32 * j + lane;
+          wb[j] = __ldg(reinterpret_cast<const uint32_t*>(sB + n * kg + 4 * h));
+        }
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_empty[r], ((g_it / kSlots) & 1u) ^ 1u,
+                                               abort_flag, FGQ_DEVERR_SF_SLOT))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        tmem_st_32x32b_x1(tmem_base + t_lane + kSfaCol0 + 32u * r + static_cast<uint32_t>(q), wa);
+        if (BN == 256) {
+          tmem_st_32x32b_x8(tmem_base + t_lane + kSfbCol0 + 32u * r, wb);
+        } else {
+          const uint32_t w4[8] = {wb[0], wb[1], wb[2], wb[3], wb[0], wb[1], wb[2], wb[3]};
+          tmem_st_32x32b_x8(tmem_base + t_lane + kSfbCol0 + 32u * r, w4);  // columns 4-7 unused
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_full[r]);
+      }
+    }
+  } else if (warp >= 8) {
+    // ---------------- epilogue ----------------
+    const int ew = warp - 8;
+    const int q = warp & 3;
+    const int half = ew >> 2;
+    const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
+    uint32_t t_it = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t_it) {
+      const int tm = tile % m_tiles, tn = tile / m_tiles;
+      const int row = tm * BM + 32 * q + lane;
+      const bool row_ok = row < M;
+      const int col0 = tn * BN + half * HALF;
+      const uint32_t buf = t_it % NACC, aph = (t_it / NACC) & 1u;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[buf], aph, abort_flag, FGQ_DEVERR_EPI_TMEM)))
+        break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + t_lane + buf * BN + half * HALF;
+      uint32_t ra[32], rb[32];
+      tmem_ld_32x32b_x32(taddr, ra);
+      tmem_wait_ld_regs(ra);
+#pragma unroll
+      for (int j = 0; j < NLD; ++j) {
+        if (j + 1 < NLD) {
+          if (j % 2 == 0)
+            tmem_ld_32x32b_x32(taddr + 32 * (j + 1), rb);
+          else
+            tmem_ld_32x32b_x32(taddr + 32 * (j + 1), ra);
+        } else {
+          // the whole accumulator is in registers: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+        if (row_ok) {
+          if (j % 2 == 0)
+            store32<OUT_BF16>(C, ldc, row, col0 + 32 * j, ra);
+          else
+            store32<OUT_BF16>(C, ldc, row, col0 + 32 * j, rb);
+        }
+        if (j + 1 < NLD) {
+          if (j % 2 == 0)
+            tmem_wait_ld_regs(rb);
+          else
+            tmem_wait_ld_regs(ra);
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int BN, int STAGES, bool OUT_BF16>
+cudaError_t launch_mxf4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
+                          void* C, int64_t ldc, int M, int N, int K, cudaStream_t stream,
+                          const DeviceInfo& dev) {
+  using CF = Mxf4Cfg<BN, STAGES>;
+  auto kern = gemm_mxf4_kernel<BN, STAGES, OUT_BF16>;
+  static bool attr_set[64] = {};
+  static std::mutex mu;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev.device < 64 && !attr_set[dev.device]) {
+      const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(CF::kSmemBytes));
+      if (e != cudaSuccess) return e;
+      attr_set[dev.device] = true;
+    }
+  }
+  CUtensorMap ta, tb;
+  // rows of K/2 bytes (two E2M1 per byte)
+  if (!make_k_major_map(&ta, A, M, K / 2, BM) || !make_k_major_map(&tb, B, N, K / 2, BN))
+    return cudaErrorInvalidValue;
+  const int tiles = ((M + BM - 1) / BM) * (N / BN);
+  const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), CF::kSmemBytes, stream, ta, tb, sA, sB, C,
+                    ldc, M, N, K);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_mxf4(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                             const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
+                             int64_t K, int out_bf16, cudaStream_t stream, const DeviceInfo& dev) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  const int64_t tiles256 = ((M + BM - 1) / BM) * (N / 256);
+  const bool wide = (N % 256 == 0) && tiles256 >= dev.sm_count;
+  if (out_bf16) {
+    return wide ? launch_mxf4_cfg<256, 4, true>(A, sA, B, sB, C, ldc, m, n, k, stream, dev)
+                : launch_mxf4_cfg<128, 6, true>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
+  }
+  return wide ? launch_mxf4_cfg<256, 4, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev)
+              : launch_mxf4_cfg<128, 6, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
+}
+
+cudaError_t read_device_error_mxf4(uint32_t* word, bool clear) {
+  return read_unit_device_error(word, clear);
+}
+
+}  // namespace fgq

@@ -227,6 +227,25 @@ fgq_status fgq_gemm_fp8_blockscaled_fused_act(const void* A, int64_t lda, const 
                                               int64_t N, int64_t K, int out, int mode,
                                               void* stream);
 
+/*
+ * MXFP4 GEMM (§UE8M0 vs E4M3 Scale Formats: UE8M0 scales, block 32; §When to
+ * Use: MXFP4 for native hardware acceleration): both operands quantized by
+ * fgq_quant_mxfp4_1x32 along K, the weight as its transpose,
+ *   C[m,n] = sum_k e2m1(A[m,k]) 2^(sA[m,k/32]-127) e2m1(B[n,k]) 2^(sB[n,k/32]-127)
+ * with the factors applied by the tensor core (block-scaled FP4 MMA) and an
+ * fp32 accumulator.
+ *
+ *   A    E2M1 codes [M, K/2] bytes (layout of fgq_quant_mxfp4_1x32),
+ *        16-byte aligned.       sA  UE8M0 codes [M, K/32], 4-byte aligned.
+ *   B    E2M1 codes [N, K/2] bytes, 16-byte aligned.
+ *                               sB  UE8M0 codes [N, K/32], 4-byte aligned.
+ *   C    fp32 or bf16 [M, N], row m at C + m * ldc (as _ex).
+ *   K % 128 == 0, N % 128 == 0, K > 0, N > 0, M >= 0.
+ */
+fgq_status fgq_gemm_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                          const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
+                          int64_t K, int out, void* stream);
+
 /* Workspace bytes fgq_gemm_fp8_blockscaled_splitk needs for (M, N, K) on the
  * current device (depends on its SM count).  Same size checks as the GEMM. */
 fgq_status fgq_gemm_splitk_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);

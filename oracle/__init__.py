@@ -98,6 +98,12 @@ def _load():
                                         ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_double)]
         lib.fgqo_gemm_mxfp4.restype = ctypes.c_int
+        lib.fgqo_gemm_mxfp4_at.argtypes = [_u8p, _u8p, _u8p, _u8p, _i64, _i64, _i64,
+                                           ctypes.POINTER(ctypes.c_int64),
+                                           ctypes.POINTER(ctypes.c_int64), _i64,
+                                           ctypes.POINTER(ctypes.c_double),
+                                           ctypes.POINTER(ctypes.c_double)]
+        lib.fgqo_gemm_mxfp4_at.restype = ctypes.c_int
         lib.fgqo_quant_w_128x128.argtypes = [_u16p, _i64, _i64, _u8p, _f32p, ctypes.c_int]
         lib.fgqo_quant_w_128x128.restype = ctypes.c_int
         lib.fgqo_gemm_dequant.argtypes = [_u8p, _f32p, _u8p, _f32p, _i64, _i64, _i64,
@@ -241,6 +247,23 @@ def gemm_mxfp4(aq, sa, bq, sb):
                                  M, N, K, c.ctypes.data_as(dp), t.ctypes.data_as(dp))
     if rc != 0:
         raise ValueError(f"oracle gemm_mxfp4 failed ({rc})")
+    return c, t
+
+
+def gemm_mxfp4_at(aq, sa, bq, sb, rows, cols):
+    """The MXFP4 reference at outputs (rows[i], cols[i]) -> (C [n], T [n])."""
+    aq, sa, bq, sb = (np.ascontiguousarray(v, dtype=np.uint8) for v in (aq, sa, bq, sb))
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    M, N, K = aq.shape[0], bq.shape[0], 2 * aq.shape[1]
+    c = np.empty(rows.size, dtype=np.float64)
+    t = np.empty(rows.size, dtype=np.float64)
+    dp, ip = ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)
+    rc = _load().fgqo_gemm_mxfp4_at(_ptr(aq, _u8p), _ptr(sa, _u8p), _ptr(bq, _u8p), _ptr(sb, _u8p),
+                                    M, N, K, rows.ctypes.data_as(ip), cols.ctypes.data_as(ip),
+                                    rows.size, c.ctypes.data_as(dp), t.ctypes.data_as(dp))
+    if rc != 0:
+        raise ValueError(f"oracle gemm_mxfp4_at failed ({rc})")
     return c, t
 
 

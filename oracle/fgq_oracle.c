@@ -404,23 +404,61 @@ static double mx_hat(const uint8_t *q, const uint8_t *s, int64_t K, int64_t r, i
   return fgqo_e2m1_decode(code) * ldexp(1.0, (int)s[r * (K / 32) + k / 32] - 127);
 }
 
+/* Dequantised MXFP4 rows in fp64: out[r * K + k] = A_hat[r, k] (exact). */
+static double *mx_dequant(const uint8_t *q, const uint8_t *s, int64_t R, int64_t K) {
+  double *h = (double *)malloc((size_t)(R * K) * sizeof(double));
+  if (!h) return NULL;
+  for (int64_t r = 0; r < R; ++r)
+    for (int64_t k = 0; k < K; ++k) h[r * K + k] = mx_hat(q, s, K, r, k);
+  return h;
+}
+
 /* MXFP4 GEMM reference: both operands as rows along K (A [M, K], B given as
  * its transpose [N, K], each quantized by fgqo_quant_mxfp4_1x32):
  * C[m,n] = sum_k A_hat[m,k] B_hat[n,k] in fp64, k ascending, and
- * T[m,n] = sum_k |A_hat| |B_hat| (each product is exact in fp64). */
+ * T[m,n] = sum_k |A_hat| |B_hat| (each product is exact in fp64).  Both
+ * operands are dequantised once; returns -3 if that memory is not there. */
 int fgqo_gemm_mxfp4(const uint8_t *aq, const uint8_t *sa, const uint8_t *bq, const uint8_t *sb,
                     int64_t M, int64_t N, int64_t K, double *c, double *t) {
   if (K % 32 != 0) return -2;
+  double *ah = mx_dequant(aq, sa, M, K), *bh = mx_dequant(bq, sb, N, K);
+  if (!ah || !bh) {
+    free(ah);
+    free(bh);
+    return -3;
+  }
   for (int64_t m = 0; m < M; ++m)
     for (int64_t n = 0; n < N; ++n) {
       double acc = 0.0, tt = 0.0;
       for (int64_t k = 0; k < K; ++k) {
-        const double p = mx_hat(aq, sa, K, m, k) * mx_hat(bq, sb, K, n, k);
+        const double p = ah[m * K + k] * bh[n * K + k];
         acc += p;
         tt += fabs(p);
       }
       c[m * N + n] = acc;
       t[m * N + n] = tt;
     }
+  free(ah);
+  free(bh);
+  return 0;
+}
+
+/* The same at listed outputs (rows[i], cols[i]), i < count. */
+int fgqo_gemm_mxfp4_at(const uint8_t *aq, const uint8_t *sa, const uint8_t *bq,
+                       const uint8_t *sb, int64_t M, int64_t N, int64_t K, const int64_t *rows,
+                       const int64_t *cols, int64_t count, double *c, double *t) {
+  if (K % 32 != 0) return -2;
+  for (int64_t i = 0; i < count; ++i) {
+    const int64_t m = rows[i], n = cols[i];
+    if (m < 0 || m >= M || n < 0 || n >= N) return -4;
+    double acc = 0.0, tt = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      const double p = mx_hat(aq, sa, K, m, k) * mx_hat(bq, sb, K, n, k);
+      acc += p;
+      tt += fabs(p);
+    }
+    c[i] = acc;
+    t[i] = tt;
+  }
   return 0;
 }
