@@ -35,10 +35,14 @@ constexpr int BM = 128;
 constexpr int BK = 128;
 constexpr int kThreads = 512;  // warpgroup 0 control, 1 scale factors, 2-3 epilogue
 constexpr int kEpiWarps = 8;
-constexpr int kSlots = 4;  // scale-factor ring; a slot = 128 elements of K = two K = 64 MMAs
+// Scale-factor ring: a slot = 128 elements of K = two K = 64 MMAs.  The
+// factor addresses need only 4-column (A) and 8-column (B) alignment
+// (measured), so sixteen slots fit: 32 MMAs of lookahead for the writers.
+constexpr int kSlots = 16;
+constexpr uint32_t kSfaStride = 4, kSfbStride = 8;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfaCol0 = 256;     // slot r: A factors at kSfaCol0 + 32 r (+ 0..3)
-constexpr uint32_t kSfbCol0 = 384;     // slot r: B factors at kSfbCol0 + 32 r (+ 0..7)
+constexpr uint32_t kSfaCol0 = 256;     // slot r: A factors at kSfaCol0 + 4 r (+ 0..3)
+constexpr uint32_t kSfbCol0 = 320;     // slot r: B factors at kSfbCol0 + 8 r (+ 0..7)
 
 template <int BN, int STAGES>
 struct Mxf4Cfg {
@@ -50,6 +54,8 @@ struct Mxf4Cfg {
   static constexpr size_t kSmemBytes =
       1024 + static_cast<size_t>(STAGES) * kStageBytes + kNumBars * 8 + 16;
   static_assert(kNAcc * BN <= static_cast<int>(kSfaCol0), "accumulators overlap the scale ring");
+  static_assert(kSfaCol0 + kSfaStride * kSlots <= kSfbCol0 && kSfbCol0 + kSfbStride * kSlots <= 512,
+                "scale ring within TMEM");
   static_assert(BN / 32 <= 8, "B factors of one slot take BN/32 <= 8 columns");
 };
 
@@ -242,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
               }
-              tsfa = tmem_base + kSfaCol0 + 32u * r;
-              tsfb = tmem_base + kSfbCol0 + 32u * r;
+              tsfa = tmem_base + kSfaCol0 + kSfaStride * r;
+              tsfb = tmem_base + kSfbCol0 + kSfbStride * r;
             }
             umma_mxf4(d, make_desc(a_lo + kk * 2, dhi), make_desc(b_lo + kk * 2, dhi),
                       idesc0 | (id << 29) | (id << 4), tsfa, tsfb, (kc > 0 || kk > 0) ? 1u : 0u);
@@ -278,34 +284,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = tm * BM + 32 * q + lane;
       const bool row_ok = row < M;
       const uint8_t* sa_row = sA + static_cast<int64_t>(row_ok ? row : 0) * kg;
-      for (int h = 0; h < khalves; ++h, ++g_it) {
-        const uint32_t r = g_it % kSlots;
-        // the four codes of blocks 4h .. 4h+3: this thread's row of A, and
-        // B's columns n = tn*BN + 32 j + lane (replicated in every quarter)
-        const uint32_t wa = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(sa_row + 4 * h)) : 0x7F7F7F7Fu;
-        uint32_t wb[8];
+      // Software pipeline over the slots: the codes of slot h + 1 are
+      // loaded (L2) while slot h is written, two slots per iteration with
+      // fixed register sets.
+      uint32_t wa0 = 0, wa1 = 0, wb0[8], wb1[8];
+      auto load = [&](int h, uint32_t& wa, uint32_t (&wb)[8]) {
+        wa = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(sa_row + 4 * h)) : 0x7F7F7F7Fu;
 #pragma unroll
-        for (int j = 0; j < BN / 32; ++j) {
-          const int64_t n = static_cast<int64_t>(tn) * BN + 32 * j + lane;
+        for (int j = 0; j < 8; ++j) {
+          const int jj = j < BN / 32 ? j : j - BN / 32;  // BN = 128: columns 4-7 repeat 0-3
+          const int64_t n = static_cast<int64_t>(tn) * BN + 32 * jj + lane;
           wb[j] = __ldg(reinterpret_cast<const uint32_t*>(sB + n * kg + 4 * h));
         }
+      };
+      auto store = [&](uint32_t wa, const uint32_t (&wb)[8]) -> bool {
+        const uint32_t r = g_it % kSlots;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_empty[r], ((g_it / kSlots) & 1u) ^ 1u,
-                                               abort_flag, FGQ_DEVERR_SF_SLOT))) {
-          ok = false;
-          break;
-        }
+                                               abort_flag, FGQ_DEVERR_SF_SLOT)))
+          return false;
         tc_fence_after();
-        tmem_st_32x32b_x1(tmem_base + t_lane + kSfaCol0 + 32u * r + static_cast<uint32_t>(q), wa);
-        if (BN == 256) {
-          tmem_st_32x32b_x8(tmem_base + t_lane + kSfbCol0 + 32u * r, wb);
-        } else {
-          const uint32_t w4[8] = {wb[0], wb[1], wb[2], wb[3], wb[0], wb[1], wb[2], wb[3]};
-          tmem_st_32x32b_x8(tmem_base + t_lane + kSfbCol0 + 32u * r, w4);  // columns 4-7 unused
-        }
+        tmem_st_32x32b_x1(tmem_base + t_lane + kSfaCol0 + kSfaStride * r + static_cast<uint32_t>(q), wa);
+        tmem_st_32x32b_x8(tmem_base + t_lane + kSfbCol0 + kSfbStride * r, wb);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sf_full[r]);
+        ++g_it;
+        return true;
+      };
+      load(0, wa0, wb0);
+      for (int h = 0; h < khalves && ok; h += 2) {
+        if (h + 1 < khalves) load(h + 1, wa1, wb1);
+        if (!store(wa0, wb0)) {
+          ok = false;
+          break;
+        }
+        if (h + 1 >= khalves) break;
+        if (h + 2 < khalves) load(h + 2, wa0, wb0);
+        if (!store(wa1, wb1)) {
+          ok = false;
+          break;
+        }
       }
     }
   } else if (warp >= 8) {
