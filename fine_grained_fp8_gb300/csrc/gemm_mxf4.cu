@@ -17,8 +17,8 @@
 // Same structure as the power-of-two FP8 kernel (gemm_mx.cu): persistent
 // CTAs on 128 x BN tiles, warp 0 TMA producer (one 128-byte stage = 256
 // elements of K), warp 1 MMA issuer (four MMAs per stage), warps 4-7 write
-// the factors into a TMEM ring (one slot = one 32-bit cell per row or column
-// = four 32-element blocks = two MMAs), warps 8-15 epilogue.
+// the factors into a TMEM ring (one slot per stage = two 32-bit cells per
+// row or column = eight 32-element blocks = four MMAs), warps 8-15 epilogue.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -35,14 +35,17 @@ constexpr int BM = 128;
 constexpr int BK = 128;
 constexpr int kThreads = 512;  // warpgroup 0 control, 1 scale factors, 2-3 epilogue
 constexpr int kEpiWarps = 8;
-// Scale-factor ring: a slot = 128 elements of K = two K = 64 MMAs.  The
-// factor addresses need only 4-column (A) and 8-column (B) alignment
-// (measured), so sixteen slots fit: 32 MMAs of lookahead for the writers.
-constexpr int kSlots = 16;
-constexpr uint32_t kSfaStride = 4, kSfbStride = 8;
+// Scale-factor ring: a slot = one stage = 256 elements of K = four K = 64
+// MMAs = two 32-bit cells per row of A and per column of B.  Cell w of A
+// sits at the slot's A base + 4 w (+ 0..3 for the four row quarters), cell
+// w of B at its B base + 8 w (+ 0..7 for the column groups); the factor
+// addresses need only 4-column (A) and 8-column (B) alignment (measured).
+constexpr int kSlots = 8;
+constexpr uint32_t kSfaSlot = 8, kSfbSlot = 16;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfaCol0 = 256;     // slot r: A factors at kSfaCol0 + 4 r (+ 0..3)
-constexpr uint32_t kSfbCol0 = 320;     // slot r: B factors at kSfbCol0 + 8 r (+ 0..7)
+constexpr uint32_t kSfBarrier = 1;    // named barrier of the four factor-writer warps
+constexpr uint32_t kSfaCol0 = 256;     // slot r: A cells at kSfaCol0 + 8 r + {0, 4} (+ 0..3)
+constexpr uint32_t kSfbCol0 = 320;     // slot r: B cells at kSfbCol0 + 16 r + {0, 8} (+ 0..7)
 
 template <int BN, int STAGES>
 struct Mxf4Cfg {
@@ -51,10 +54,14 @@ struct Mxf4Cfg {
   static constexpr int kBBytes = BN * BK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kNumBars = 2 * STAGES + 2 * kSlots + 2 * kNAcc + 1;
-  static constexpr size_t kSmemBytes =
-      1024 + static_cast<size_t>(STAGES) * kStageBytes + kNumBars * 8 + 16;
+  // factor staging: two buffers of four stages' codes, rows padded to 9 words
+  static constexpr int kSfRowWords = 9;
+  static constexpr int kSfBufWords = (BM + BN) * kSfRowWords;
+  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes +
+                                       2 * kSfBufWords * 4 + kNumBars * 8 + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(kNAcc * BN <= static_cast<int>(kSfaCol0), "accumulators overlap the scale ring");
-  static_assert(kSfaCol0 + kSfaStride * kSlots <= kSfbCol0 && kSfbCol0 + kSfbStride * kSlots <= 512,
+  static_assert(kSfaCol0 + kSfaSlot * kSlots <= kSfbCol0 && kSfbCol0 + kSfbSlot * kSlots <= 512,
                 "scale ring within TMEM");
   static_assert(BN / 32 <= 8, "B factors of one slot take BN/32 <= 8 columns");
 };
@@ -140,7 +147,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sm_a = smem;
   uint8_t* sm_b = smem + STAGES * CF::kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm_b + STAGES * CF::kBBytes);
+  uint32_t* sf_stage = reinterpret_cast<uint32_t*>(sm_b + STAGES * CF::kBBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sf_stage + 2 * CF::kSfBufWords);
   uint64_t* empty = full + STAGES;
   uint64_t* sf_full = empty + STAGES;
   uint64_t* sf_empty = sf_full + kSlots;
@@ -155,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = N / BN;
   const int num_tiles = m_tiles * n_tiles;
   const int kstages = (K + 255) / 256;  // 128-byte stages of 256 elements (the last may be half)
-  const int khalves = K / 128;          // scale slots: 128 elements = four 32-element blocks
+  const bool half_last = (K % 256) != 0;  // the last stage holds 128 elements of K
   const int kg = K / 32;                // UE8M0 codes per row of sA / sB
 
   if (threadIdx.x == 0) {
@@ -219,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- MMA issuer ----------------
     if (elect_one_sync()) {
       constexpr uint32_t idesc0 = idesc_mxf4(BM, BN);
+      constexpr uint32_t kId2 = (2u << 29) | (2u << 4);  // factor bytes 2-3 of A and B
       const uint64_t dA0 = smem_desc_k_sw128(smem_u32(sm_a));
       const uint32_t a_lo0 = static_cast<uint32_t>(dA0), dhi = static_cast<uint32_t>(dA0 >> 32);
       const uint32_t b_lo0 = static_cast<uint32_t>(smem_desc_k_sw128(smem_u32(sm_b)));
@@ -230,35 +239,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&acc_empty[buf], aph ^ 1u, abort_flag, FGQ_DEVERR_MMA_TMEM)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + buf * BN;
-        uint32_t tsfa = 0, tsfb = 0, r = 0;
-        for (int kc = 0; kc < kstages; ++kc) {
-          if (!mbar_wait(&full[ls], lph, abort_flag, FGQ_DEVERR_MMA_FULL)) {
+        for (int kc = 0; kc < kstages; ++kc, ++g_it) {
+          const uint32_t r = g_it % kSlots;
+          if (!mbar_wait(&full[ls], lph, abort_flag, FGQ_DEVERR_MMA_FULL) ||
+              !mbar_wait(&sf_full[r], (g_it / kSlots) & 1u, abort_flag, FGQ_DEVERR_MMA_SF)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_lo = a_lo0 + ls * (CF::kABytes >> 4);
           const uint32_t b_lo = b_lo0 + ls * (CF::kBBytes >> 4);
-          const int n_mma = (K - kc * 256) >= 256 ? 4 : 2;  // a half stage at the end
-          for (int kk = 0; kk < n_mma; ++kk) {
-            const uint32_t id = static_cast<uint32_t>(kk & 1) * 2u;  // factor bytes 0-1 or 2-3
-            if (id == 0) {
-              r = g_it % kSlots;
-              if (!mbar_wait(&sf_full[r], (g_it / kSlots) & 1u, abort_flag, FGQ_DEVERR_MMA_SF)) {
-                ok = false;
-                break;
-              }
-              tsfa = tmem_base + kSfaCol0 + kSfaStride * r;
-              tsfb = tmem_base + kSfbCol0 + kSfbStride * r;
-            }
-            umma_mxf4(d, make_desc(a_lo + kk * 2, dhi), make_desc(b_lo + kk * 2, dhi),
-                      idesc0 | (id << 29) | (id << 4), tsfa, tsfb, (kc > 0 || kk > 0) ? 1u : 0u);
-            if (id != 0) {
-              umma_commit(&sf_empty[r]);
-              ++g_it;
-            }
+          const uint32_t sfa = tmem_base + kSfaCol0 + kSfaSlot * r;
+          const uint32_t sfb = tmem_base + kSfbCol0 + kSfbSlot * r;
+          // four K = 64 MMAs (32 bytes of each row apart): factor bytes 0-1
+          // and 2-3 of cell 0, then of cell 1; a final half stage has two
+          umma_mxf4(d, make_desc(a_lo, dhi), make_desc(b_lo, dhi), idesc0, sfa, sfb,
+                    kc > 0 ? 1u : 0u);
+          umma_mxf4(d, make_desc(a_lo + 2, dhi), make_desc(b_lo + 2, dhi), idesc0 | kId2, sfa, sfb,
+                    1u);
+          if (kc + 1 < kstages || !half_last) {
+            umma_mxf4(d, make_desc(a_lo + 4, dhi), make_desc(b_lo + 4, dhi), idesc0, sfa + 4,
+                      sfb + 8, 1u);
+            umma_mxf4(d, make_desc(a_lo + 6, dhi), make_desc(b_lo + 6, dhi), idesc0 | kId2,
+                      sfa + 4, sfb + 8, 1u);
           }
-          if (!ok) break;
+          umma_commit(&sf_empty[r]);
           umma_commit(&empty[ls]);
           if (++ls == STAGES) {
             ls = 0;
@@ -275,36 +280,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4 && warp < 8) {
     // ---------------- scale-factor writers ----------------
+    // The factors of a tile's rows (columns) are one contiguous block of
+    // BM (BN) rows of K/32 codes.  The four warps copy four stages of it
+    // at a time (32 bytes of each row) with coalesced loads into a
+    // shared-memory buffer, then each warp reads the cells of its 32
+    // rows (and of all BN columns, which every lane quarter of B needs)
+    // from there.  The next chunk's loads are in flight while the current
+    // chunk's slots are written.  A warp that gives up on a wait keeps
+    // walking the same chunks and barriers (skipping the slot work) so
+    // that the others never wait for it at a named barrier.
+    constexpr int kRowW = CF::kSfRowWords;
+    constexpr int kNA = BM * 8 / 128, kNB = BN * 8 / 128;  // words per thread per chunk
     const int q = warp & 3;
+    const int wt = threadIdx.x - 128;
     const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
+    const int nchunks = (kstages + 3) / 4;
+    auto ld32 = [](const uint8_t* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); };
     uint32_t g_it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
       const int tm = tile % m_tiles, tn = tile / m_tiles;
-      const int row = tm * BM + 32 * q + lane;
-      const bool row_ok = row < M;
-      const uint8_t* sa_row = sA + static_cast<int64_t>(row_ok ? row : 0) * kg;
-      // Software pipeline over the slots: the codes of slot h + 1 are
-      // loaded (L2) while slot h is written, two slots per iteration with
-      // fixed register sets.
-      uint32_t wa0 = 0, wa1 = 0, wb0[8], wb1[8];
-      auto load = [&](int h, uint32_t& wa, uint32_t (&wb)[8]) {
-        wa = row_ok ? __ldg(reinterpret_cast<const uint32_t*>(sa_row + 4 * h)) : 0x7F7F7F7Fu;
+      const uint8_t* a_blk = sA + static_cast<int64_t>(tm) * BM * kg;
+      const uint8_t* b_blk = sB + static_cast<int64_t>(tn) * BN * kg;
+      const int a_rows = M - tm * BM < BM ? M - tm * BM : BM;
+      uint32_t ra[kNA], rb[kNB];
+      // thread wt, word i of a chunk: row (wt + 128 i) / 8, cell (wt + 128 i) % 8;
+      // codes past the row's end (a final partial chunk) and rows past M read
+      // as 0x7F (2^0) and are never used by an MMA
+      auto fetch = [&](int c) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int jj = j < BN / 32 ? j : j - BN / 32;  // BN = 128: columns 4-7 repeat 0-3
-          const int64_t n = static_cast<int64_t>(tn) * BN + 32 * jj + lane;
-          wb[j] = __ldg(reinterpret_cast<const uint32_t*>(sB + n * kg + 4 * h));
+        for (int i = 0; i < kNA; ++i) {
+          const int w = wt + 128 * i, row = w >> 3, byte = 32 * c + 4 * (w & 7);
+          ra[i] = row < a_rows && byte < kg ? ld32(a_blk + row * kg + byte) : 0x7F7F7F7Fu;
+        }
+#pragma unroll
+        for (int i = 0; i < kNB; ++i) {
+          const int w = wt + 128 * i, row = w >> 3, byte = 32 * c + 4 * (w & 7);
+          rb[i] = byte < kg ? ld32(b_blk + row * kg + byte) : 0x7F7F7F7Fu;
         }
       };
-      auto store = [&](uint32_t wa, const uint32_t (&wb)[8]) -> bool {
+      auto deposit = [&](int c) {
+        uint32_t* sa = sf_stage + (c & 1) * CF::kSfBufWords;
+        uint32_t* sb = sa + BM * kRowW;
+#pragma unroll
+        for (int i = 0; i < kNA; ++i) {
+          const int w = wt + 128 * i;
+          sa[(w >> 3) * kRowW + (w & 7)] = ra[i];
+        }
+#pragma unroll
+        for (int i = 0; i < kNB; ++i) {
+          const int w = wt + 128 * i;
+          sb[(w >> 3) * kRowW + (w & 7)] = rb[i];
+        }
+      };
+      auto store = [&](const uint32_t (&wa)[2], const uint32_t (&wb)[2][8]) -> bool {
         const uint32_t r = g_it % kSlots;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_empty[r], ((g_it / kSlots) & 1u) ^ 1u,
                                                abort_flag, FGQ_DEVERR_SF_SLOT)))
           return false;
         tc_fence_after();
-        tmem_st_32x32b_x1(tmem_base + t_lane + kSfaCol0 + kSfaStride * r + static_cast<uint32_t>(q), wa);
-        tmem_st_32x32b_x8(tmem_base + t_lane + kSfbCol0 + kSfbStride * r, wb);
+        const uint32_t ca = tmem_base + t_lane + kSfaCol0 + kSfaSlot * r + static_cast<uint32_t>(q);
+        const uint32_t cb = tmem_base + t_lane + kSfbCol0 + kSfbSlot * r;
+        tmem_st_32x32b_x1(ca, wa[0]);
+        tmem_st_32x32b_x1(ca + 4, wa[1]);
+        tmem_st_32x32b_x8(cb, wb[0]);
+        tmem_st_32x32b_x8(cb + 8, wb[1]);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -312,18 +352,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++g_it;
         return true;
       };
-      load(0, wa0, wb0);
-      for (int h = 0; h < khalves && ok; h += 2) {
-        if (h + 1 < khalves) load(h + 1, wa1, wb1);
-        if (!store(wa0, wb0)) {
-          ok = false;
-          break;
+      fetch(0);
+      deposit(0);
+      named_barrier_sync(kSfBarrier, 128);
+      for (int c = 0; c < nchunks; ++c) {
+        if (c + 1 < nchunks) fetch(c + 1);
+        const uint32_t* sa = sf_stage + (c & 1) * CF::kSfBufWords + (32 * q + lane) * kRowW;
+        const uint32_t* sb = sf_stage + (c & 1) * CF::kSfBufWords + BM * kRowW + lane * kRowW;
+#pragma unroll 1
+        for (int st = 0; st < 4 && 4 * c + st < kstages && ok; ++st) {
+          const uint32_t wa[2] = {sa[2 * st], sa[2 * st + 1]};
+          uint32_t wb[2][8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int jj = j < BN / 32 ? j : j - BN / 32;  // BN = 128: columns 4-7 repeat 0-3
+            wb[0][j] = sb[32 * jj * kRowW + 2 * st];
+            wb[1][j] = sb[32 * jj * kRowW + 2 * st + 1];
+          }
+          ok = store(wa, wb);
         }
-        if (h + 1 >= khalves) break;
-        if (h + 2 < khalves) load(h + 2, wa0, wb0);
-        if (!store(wa1, wb1)) {
-          ok = false;
-          break;
+        if (c + 1 < nchunks) {
+          // every warp has read chunk c - 1 (it did so before the last barrier)
+          deposit(c + 1);
+          named_barrier_sync(kSfBarrier, 128);
         }
       }
     }
