@@ -11,15 +11,16 @@
 //   - Warp 0: TMA producer.  Each stage holds one 128-wide K chunk of A
 //     (128 x 128 bytes) and B (BN x 128 bytes), 128-byte swizzled.
 //   - Warp 1: one thread issues 4 tcgen05.mma (K = 32 each) per chunk into
-//     one of two TMEM partial buffers (128 lanes x BN fp32 columns each),
+//     one of 512 / BN TMEM partial buffers (128 lanes x BN fp32 columns
+//     each: two for BN = 256, four for BN = 128),
 //     then commits to the stage's "empty" and the buffer's "full" barriers.
 //   - Warps 4-11: epilogue.  Per chunk they read the partial from TMEM in
 //     32-column loads (the next load in flight while the current one is
 //     used), multiply by sA[m,c] * sB[c, n/128] and add it into fp32
 //     accumulators held in registers with packed f32x2 FMAs (the promotion
 //     step), hand the TMEM buffer back as soon as it is read, and after the
-//     last chunk convert and store the tile.  Two TMEM buffers let the
-//     tensor core run chunk c+1 while chunk c is promoted.
+//     last chunk convert and store the tile.  The buffers let the tensor
+//     core run chunks ahead while chunk c is promoted.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -54,8 +55,9 @@ struct Cfg {
   static constexpr int kABytes = BM * BK;
   static constexpr int kBBytes = BN * BK;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kTmemCols = 2 * BN;  // two partial buffers
-  static constexpr int kBarBytes = (2 * STAGES + 4) * 8 + 16;
+  static constexpr int kNBuf = 512 / BN;    // partial buffers: all 512 TMEM columns
+  static constexpr int kTmemCols = kNBuf * BN;
+  static constexpr int kBarBytes = (2 * STAGES + 2 * kNBuf) * 8 + 16;
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes;
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of 2");
 };
@@ -95,6 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const float* __restrict__ sA, const float* __restrict__ sB,
                                 void* __restrict__ C, int64_t ldc, int M, int N, int K) {
   using CF = Cfg<BN, STAGES>;
+  constexpr uint32_t NBUF = CF::kNBuf;
   constexpr int HALF = BN / 2;     // columns per epilogue warp
   constexpr int NLD = HALF / 32;   // 32-column TMEM loads per chunk
   static_assert(NLD >= 2, "the load pipeline below assumes at least two loads per chunk");
@@ -106,8 +109,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(sm_b + STAGES * CF::kBBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* tempty = tfull + NBUF;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + NBUF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NBUF; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], kEpiWarps);
     }
@@ -190,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
           for (int kc = 0; kc < kchunks; ++kc, ++it) {
-            const uint32_t buf = it & 1u, tph = (it >> 1) & 1u;
+            const uint32_t buf = it % NBUF, tph = (it / NBUF) & 1u;
             if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, FGQ_DEVERR_MMA_TMEM) ||
                 !mbar_wait(&full[ls], lph, abort_flag, FGQ_DEVERR_MMA_FULL)) {
               ok = false;
@@ -216,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // MMAs still in flight must finish before TMEM is released.
-        if (it > 0) mbar_wait_drain(&tfull[(it - 1) & 1u], ((it - 1) >> 1) & 1u);
+        if (it > 0) mbar_wait_drain(&tfull[(it - 1) % NBUF], ((it - 1) / NBUF) & 1u);
       }
       __syncwarp();
     }
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float sa_next = row_ok ? __ldg(sa_row) : 0.0f;
       float sb_next = __ldg(sb_col);
       for (int kc = 0; kc < kchunks; ++kc, ++it) {
-        const uint32_t buf = it & 1u, tph = (it >> 1) & 1u;
+        const uint32_t buf = it % NBUF, tph = (it / NBUF) & 1u;
         const float comb = sa_next * sb_next;
         if (kc + 1 < kchunks) {  // prefetch the next chunk's scales
           sa_next = row_ok ? __ldg(sa_row + kc + 1) : 0.0f;
