@@ -54,8 +54,10 @@ struct Mxf4Cfg {
   static constexpr int kBBytes = BN * BK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kNumBars = 2 * STAGES + 2 * kSlots + 2 * kNAcc + 1;
-  // factor staging: two buffers of four stages' codes, rows padded to 9 words
-  static constexpr int kSfRowWords = 9;
+  // factor staging: two buffers of four stages' codes, rows padded to 10
+  // words (8-byte aligned cell pairs, two-way bank conflicts at most when a
+  // warp reads one cell of 32 rows)
+  static constexpr int kSfRowWords = 10;
   static constexpr int kSfBufWords = (BM + BN) * kSfRowWords;
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes +
                                        2 * kSfBufWords * 4 + kNumBars * 8 + 16;
@@ -94,6 +96,19 @@ __device__ __forceinline__ void umma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
+
+// 4- and 8-byte asynchronous copies global -> shared (cp.async), the group
+// commit and the wait for all of this thread's groups.
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Eight consecutive TMEM columns of the warp's 32 lanes, one value each.
 __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
@@ -282,20 +297,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- scale-factor writers ----------------
     // The factors of a tile's rows (columns) are one contiguous block of
     // BM (BN) rows of K/32 codes.  The four warps copy four stages of it
-    // at a time (32 bytes of each row) with coalesced loads into a
-    // shared-memory buffer, then each warp reads the cells of its 32
-    // rows (and of all BN columns, which every lane quarter of B needs)
-    // from there.  The next chunk's loads are in flight while the current
-    // chunk's slots are written.  A warp that gives up on a wait keeps
-    // walking the same chunks and barriers (skipping the slot work) so
-    // that the others never wait for it at a named barrier.
+    // at a time (32 bytes of each row) into a shared-memory buffer with
+    // coalesced asynchronous copies (whole 32-byte sectors per warp
+    // instruction), then each warp reads the cells of its 32 rows (and of
+    // all BN columns, which every lane quarter of B needs) from there.
+    // Chunk c + 1 is in flight while chunk c's slots are written.  Codes
+    // past a row's end (the final partial chunk) and rows past M are not
+    // copied: their cells feed only the unused second cell of a final half
+    // stage or accumulator rows that are never stored.  A warp that gives
+    // up on a wait keeps walking the same chunks and barriers (skipping the
+    // slot work) so that the others never wait for it at a named barrier.
     constexpr int kRowW = CF::kSfRowWords;
     constexpr int kNA = BM * 8 / 128, kNB = BN * 8 / 128;  // words per thread per chunk
     const int q = warp & 3;
     const int wt = threadIdx.x - 128;
     const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
     const int nchunks = (kstages + 3) / 4;
-    auto ld32 = [](const uint8_t* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); };
     uint32_t g_it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -303,35 +320,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint8_t* a_blk = sA + static_cast<int64_t>(tm) * BM * kg;
       const uint8_t* b_blk = sB + static_cast<int64_t>(tn) * BN * kg;
       const int a_rows = M - tm * BM < BM ? M - tm * BM : BM;
-      uint32_t ra[kNA], rb[kNB];
-      // thread wt, word i of a chunk: row (wt + 128 i) / 8, cell (wt + 128 i) % 8;
-      // codes past the row's end (a final partial chunk) and rows past M read
-      // as 0x7F (2^0) and are never used by an MMA
+      // 8-byte copies (rows of a multiple of 8 codes, 8-byte aligned
+      // arrays): thread wt copies cells 2 (wt % 4) and 2 (wt % 4) + 1 of rows
+      // wt / 4 + 32 i; else 4-byte copies: cell wt % 8 of rows wt / 8 + 16 i.
+      const bool pairs = (kg & 7) == 0 && ((reinterpret_cast<uintptr_t>(sA) |
+                                            reinterpret_cast<uintptr_t>(sB)) & 7) == 0;
+      const int cell = pairs ? 2 * (wt & 3) : wt & 7, row0 = pairs ? wt >> 2 : wt >> 3;
+      const uint8_t* a_src = a_blk + row0 * kg + 4 * cell;
+      const uint8_t* b_src = b_blk + row0 * kg + 4 * cell;
+      const int dst0 = row0 * kRowW + cell;
       auto fetch = [&](int c) {
+        uint32_t* sa = sf_stage + (c & 1) * CF::kSfBufWords + dst0;
+        uint32_t* sb = sf_stage + (c & 1) * CF::kSfBufWords + BM * kRowW + dst0;
+        if (32 * c + 4 * cell < kg) {
+          if (pairs) {
 #pragma unroll
-        for (int i = 0; i < kNA; ++i) {
-          const int w = wt + 128 * i, row = w >> 3, byte = 32 * c + 4 * (w & 7);
-          ra[i] = row < a_rows && byte < kg ? ld32(a_blk + row * kg + byte) : 0x7F7F7F7Fu;
-        }
+            for (int i = 0; i < kNA / 2; ++i)
+              if (row0 + 32 * i < a_rows) cp_async8(sa + 32 * i * kRowW, a_src + 32 * i * kg + 32 * c);
 #pragma unroll
-        for (int i = 0; i < kNB; ++i) {
-          const int w = wt + 128 * i, row = w >> 3, byte = 32 * c + 4 * (w & 7);
-          rb[i] = byte < kg ? ld32(b_blk + row * kg + byte) : 0x7F7F7F7Fu;
-        }
-      };
-      auto deposit = [&](int c) {
-        uint32_t* sa = sf_stage + (c & 1) * CF::kSfBufWords;
-        uint32_t* sb = sa + BM * kRowW;
+            for (int i = 0; i < kNB / 2; ++i) cp_async8(sb + 32 * i * kRowW, b_src + 32 * i * kg + 32 * c);
+          } else {
 #pragma unroll
-        for (int i = 0; i < kNA; ++i) {
-          const int w = wt + 128 * i;
-          sa[(w >> 3) * kRowW + (w & 7)] = ra[i];
-        }
+            for (int i = 0; i < kNA; ++i)
+              if (row0 + 16 * i < a_rows) cp_async4(sa + 16 * i * kRowW, a_src + 16 * i * kg + 32 * c);
 #pragma unroll
-        for (int i = 0; i < kNB; ++i) {
-          const int w = wt + 128 * i;
-          sb[(w >> 3) * kRowW + (w & 7)] = rb[i];
+            for (int i = 0; i < kNB; ++i) cp_async4(sb + 16 * i * kRowW, b_src + 16 * i * kg + 32 * c);
+          }
         }
+        cp_async_commit();
       };
       auto store = [&](const uint32_t (&wa)[2], const uint32_t (&wb)[2][8]) -> bool {
         const uint32_t r = g_it % kSlots;
@@ -352,11 +368,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++g_it;
         return true;
       };
+      // every warp has read the previous tile's last chunk (which may sit
+      // in buffer 0) before any warp refills buffer 0
+      named_barrier_sync(kSfBarrier, 128);
       fetch(0);
-      deposit(0);
+      cp_async_wait_all();
       named_barrier_sync(kSfBarrier, 128);
       for (int c = 0; c < nchunks; ++c) {
-        if (c + 1 < nchunks) fetch(c + 1);
         const uint32_t* sa = sf_stage + (c & 1) * CF::kSfBufWords + (32 * q + lane) * kRowW;
         const uint32_t* sb = sf_stage + (c & 1) * CF::kSfBufWords + BM * kRowW + lane * kRowW;
 #pragma unroll 1
@@ -370,10 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             wb[1][j] = sb[32 * jj * kRowW + 2 * st + 1];
           }
           ok = store(wa, wb);
+          // chunk c + 1 goes into buffer (c + 1) & 1, which held chunk
+          // c - 1: every warp finished reading it before the last barrier
+          if (st == 0 && c + 1 < nchunks) fetch(c + 1);
         }
         if (c + 1 < nchunks) {
-          // every warp has read chunk c - 1 (it did so before the last barrier)
-          deposit(c + 1);
+          cp_async_wait_all();
           named_barrier_sync(kSfBarrier, 128);
         }
       }
