@@ -579,6 +579,7 @@ def run_fgq(args):
         mxfp4["peak_fp4"] = fp4_peak
         mxfp4["frac_fp4"] = mxfp4["gemm_TFLOP/s"] / fp4_peak
         mxfp4["peak_source"] = f"{src}: 6 x bf16_tflops_sustained (nominal 13.5 / 2.25 PFLOP/s)"
+        mxfp4["traffic"] = _traffic("gemm_mxf4", "gemm_mxf4.cu")
     if ue8m0:
         ue8m0["frac_fp8"] = ue8m0["gemm_TFLOP/s"] / fp8_peak
         ue8m0["traffic"] = _traffic("gemm_mx", "gemm_mx.cu")
