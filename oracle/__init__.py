@@ -104,6 +104,16 @@ def _load():
                                            ctypes.POINTER(ctypes.c_double),
                                            ctypes.POINTER(ctypes.c_double)]
         lib.fgqo_gemm_mxfp4_at.restype = ctypes.c_int
+        lib.fgqo_nvfp4_global_scale.argtypes = [_u16p, _i64, _i64]
+        lib.fgqo_nvfp4_global_scale.restype = ctypes.c_float
+        lib.fgqo_quant_nvfp4_1x16.argtypes = [_u16p, _i64, _i64, ctypes.c_float, _u8p, _u8p]
+        lib.fgqo_quant_nvfp4_1x16.restype = ctypes.c_int
+        lib.fgqo_gemm_nvfp4.argtypes = [_u8p, _u8p, ctypes.c_float, _u8p, _u8p, ctypes.c_float,
+                                        _i64, _i64, _i64, _f64p, _f64p]
+        lib.fgqo_gemm_nvfp4.restype = ctypes.c_int
+        lib.fgqo_gemm_nvfp4_at.argtypes = [_u8p, _u8p, ctypes.c_float, _u8p, _u8p, ctypes.c_float,
+                                           _i64, _i64, _i64, _i64p, _i64p, _i64, _f64p, _f64p]
+        lib.fgqo_gemm_nvfp4_at.restype = ctypes.c_int
         lib.fgqo_quant_w_128x128.argtypes = [_u16p, _i64, _i64, _u8p, _f32p, ctypes.c_int]
         lib.fgqo_quant_w_128x128.restype = ctypes.c_int
         lib.fgqo_gemm_dequant.argtypes = [_u8p, _f32p, _u8p, _f32p, _i64, _i64, _i64,
@@ -264,6 +274,64 @@ def gemm_mxfp4_at(aq, sa, bq, sb, rows, cols):
                                     rows.size, c.ctypes.data_as(dp), t.ctypes.data_as(dp))
     if rc != 0:
         raise ValueError(f"oracle gemm_mxfp4_at failed ({rc})")
+    return c, t
+
+
+def nvfp4_global_scale(x_bf16) -> np.float32:
+    """NVFP4 per-tensor scale of X bf16: fl32(amax / 2688), 1 for all zeros."""
+    x = _bits16(x_bf16)
+    R, K = x.shape
+    g = _load().fgqo_nvfp4_global_scale(_ptr(x, _u16p), R, K)
+    if not np.isfinite(g):
+        raise ValueError("oracle nvfp4_global_scale: inputs must be finite")
+    return np.float32(g)
+
+
+def quant_nvfp4_1x16(x_bf16, g=None):
+    """X bf16 [R, K] -> (Xq uint8 [R, K/2] E2M1 pairs, low nibble = even
+    element; sX uint8 [R, K/16] E4M3 block-scale codes; g float32 global
+    scale).  g defaults to nvfp4_global_scale(X)."""
+    x = _bits16(x_bf16)
+    R, K = x.shape
+    if g is None:
+        g = nvfp4_global_scale(x)
+    g = np.float32(g)
+    q = np.empty((R, K // 2), dtype=np.uint8)
+    s = np.empty((R, K // 16), dtype=np.uint8)
+    rc = _load().fgqo_quant_nvfp4_1x16(_ptr(x, _u16p), R, K, float(g), _ptr(q, _u8p), _ptr(s, _u8p))
+    if rc != 0:
+        raise ValueError(f"oracle quant_nvfp4_1x16 failed ({rc}): "
+                         "K must be a multiple of 16, g positive and inputs finite")
+    return q, s, g
+
+
+def gemm_nvfp4(aq, sa, ga, bq, sb, gb):
+    """fp64 reference of the NVFP4 GEMM: A [M, K] and B^T [N, K] as quantized
+    by quant_nvfp4_1x16 (global scales ga, gb) -> (C [M, N], T [M, N])."""
+    aq, sa, bq, sb = (np.ascontiguousarray(v, dtype=np.uint8) for v in (aq, sa, bq, sb))
+    M, N, K = aq.shape[0], bq.shape[0], 2 * aq.shape[1]
+    c = np.empty((M, N), dtype=np.float64)
+    t = np.empty((M, N), dtype=np.float64)
+    rc = _load().fgqo_gemm_nvfp4(_ptr(aq, _u8p), _ptr(sa, _u8p), float(ga), _ptr(bq, _u8p),
+                                 _ptr(sb, _u8p), float(gb), M, N, K, _ptr(c, _f64p), _ptr(t, _f64p))
+    if rc != 0:
+        raise ValueError(f"oracle gemm_nvfp4 failed ({rc})")
+    return c, t
+
+
+def gemm_nvfp4_at(aq, sa, ga, bq, sb, gb, rows, cols):
+    """The NVFP4 reference at outputs (rows[i], cols[i]) -> (C [n], T [n])."""
+    aq, sa, bq, sb = (np.ascontiguousarray(v, dtype=np.uint8) for v in (aq, sa, bq, sb))
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    M, N, K = aq.shape[0], bq.shape[0], 2 * aq.shape[1]
+    c = np.empty(rows.size, dtype=np.float64)
+    t = np.empty(rows.size, dtype=np.float64)
+    rc = _load().fgqo_gemm_nvfp4_at(_ptr(aq, _u8p), _ptr(sa, _u8p), float(ga), _ptr(bq, _u8p),
+                                    _ptr(sb, _u8p), float(gb), M, N, K, _ptr(rows, _i64p),
+                                    _ptr(cols, _i64p), rows.size, _ptr(c, _f64p), _ptr(t, _f64p))
+    if rc != 0:
+        raise ValueError(f"oracle gemm_nvfp4_at failed ({rc})")
     return c, t
 
 

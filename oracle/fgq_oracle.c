@@ -17,6 +17,9 @@
  *     scale is a pure power of two.
  *   - §Blackwell: Native Block Scaling: UE8M0 value = 2^(e - 127), four
  *     codes per 32-bit word, byte i = block i.
+ *   - §UE8M0 vs E4M3 Scale Formats and §NVFP4 Two-Level Scaling: E2M1
+ *     values 0, .5, 1, 1.5, 2, 3, 4, 6; MXFP4 = a UE8M0 scale per 32;
+ *     NVFP4 = an E4M3 scale per 16 times an fp32 per-tensor scale.
  *
  * Readings where the page is silent (each is listed with its reason in the
  * design notes of this repository):
@@ -454,6 +457,125 @@ int fgqo_gemm_mxfp4_at(const uint8_t *aq, const uint8_t *sa, const uint8_t *bq,
     double acc = 0.0, tt = 0.0;
     for (int64_t k = 0; k < K; ++k) {
       const double p = mx_hat(aq, sa, K, m, k) * mx_hat(bq, sb, K, n, k);
+      acc += p;
+      tt += fabs(p);
+    }
+    c[i] = acc;
+    t[i] = tt;
+  }
+  return 0;
+}
+
+/* ---- NVFP4 (§NVFP4 Two-Level Scaling) ------------------------------- */
+
+/* The page defines NVFP4 by its dequantization: a value is
+ *   global_scale * block_scale * e2m1
+ * with one E4M3 block scale per 16 consecutive elements of a row
+ * (scale_A [M, K/16]) and one fp32 global scale per tensor.  It gives no
+ * encoder; the readings here (the FP8 rule amax / 448 applied at both
+ * levels, with 6 = the largest E2M1 value):
+ *   global   g = fl32(amax / 2688) over the whole tensor (2688 = 6 * 448),
+ *            1 for an all-zero tensor;
+ *   block    s_b = E4M3(fl32(amax_b / fl32(6 g))): nearest, ties to even,
+ *            saturating at 448 (fgqo_e4m3_encode);
+ *   element  q = E2M1(fl32(x / D)) with D = fl32(g * s_b): nearest, ties
+ *            to even, saturating at 6 (s_b may have rounded down);
+ *            a block whose D is 0 gets signed zeros. */
+float fgqo_nvfp4_global_scale(const uint16_t *x, int64_t R, int64_t K) {
+  float amax;
+  if (group_amax(x, K, R, K, &amax) != 0) return NAN;
+  if (amax == 0.0f) return 1.0f;
+  return amax / 2688.0f; /* one fp32 division */
+}
+
+/* X bf16 [R, K] row-major, K % 16 == 0, global scale g (> 0) ->
+ * Xq [R, K/2] E2M1 pairs (element 2j in the low nibble of byte j) and
+ * sX [R, K/16] E4M3 codes. */
+int fgqo_quant_nvfp4_1x16(const uint16_t *x, int64_t R, int64_t K, float g, uint8_t *xq,
+                          uint8_t *sx) {
+  if (K % 16 != 0) return -2;
+  if (!(g > 0.0f) || !isfinite(g)) return -5;
+  const int64_t kb = K / 16;
+  const float d6 = 6.0f * g;
+  for (int64_t r = 0; r < R; ++r)
+    for (int64_t b = 0; b < kb; ++b) {
+      const uint16_t *src = x + r * K + b * 16;
+      float amax;
+      if (group_amax(src, K, 1, 16, &amax) != 0) return -1;
+      const float t = amax / d6;
+      const uint8_t sc = fgqo_e4m3_encode(t);
+      sx[r * kb + b] = sc;
+      const float d = g * (float)fgqo_e4m3_decode(sc);
+      for (int64_t j = 0; j < 16; j += 2) {
+        uint8_t code[2];
+        for (int h = 0; h < 2; ++h) {
+          const float v = fgqo_bf16_to_float(src[j + h]);
+          code[h] = d == 0.0f ? (uint8_t)(signbit(v) ? 8 : 0) : fgqo_e2m1_encode((double)(v / d));
+        }
+        xq[r * (K / 2) + (b * 16 + j) / 2] = (uint8_t)(code[0] | (code[1] << 4));
+      }
+    }
+  return 0;
+}
+
+/* The page's dequantization, global * block * e2m1, in fp64 (exact). */
+static double nv_hat(const uint8_t *q, const uint8_t *s, float g, int64_t K, int64_t r,
+                     int64_t k) {
+  const uint8_t byte = q[r * (K / 2) + k / 2];
+  const uint8_t code = (k & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+  return (double)g * fgqo_e4m3_decode(s[r * (K / 16) + k / 16]) * fgqo_e2m1_decode(code);
+}
+
+static double *nv_dequant(const uint8_t *q, const uint8_t *s, float g, int64_t R, int64_t K) {
+  double *h = (double *)malloc((size_t)(R * K) * sizeof(double));
+  if (!h) return NULL;
+  for (int64_t r = 0; r < R; ++r)
+    for (int64_t k = 0; k < K; ++k) h[r * K + k] = nv_hat(q, s, g, K, r, k);
+  return h;
+}
+
+/* NVFP4 GEMM reference: A [M, K] and B as its transpose [N, K], each
+ * quantized by fgqo_quant_nvfp4_1x16 with its own global scale:
+ * C[m,n] = sum_k A_hat[m,k] B_hat[n,k] in fp64, k ascending, and
+ * T[m,n] = sum_k |A_hat| |B_hat|. */
+int fgqo_gemm_nvfp4(const uint8_t *aq, const uint8_t *sa, float ga, const uint8_t *bq,
+                    const uint8_t *sb, float gb, int64_t M, int64_t N, int64_t K, double *c,
+                    double *t) {
+  if (K % 16 != 0) return -2;
+  double *ah = nv_dequant(aq, sa, ga, M, K), *bh = nv_dequant(bq, sb, gb, N, K);
+  if (!ah || !bh) {
+    free(ah);
+    free(bh);
+    return -3;
+  }
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      double acc = 0.0, tt = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const double p = ah[m * K + k] * bh[n * K + k];
+        acc += p;
+        tt += fabs(p);
+      }
+      c[m * N + n] = acc;
+      t[m * N + n] = tt;
+    }
+  free(ah);
+  free(bh);
+  return 0;
+}
+
+/* The same at listed outputs (rows[i], cols[i]), i < count. */
+int fgqo_gemm_nvfp4_at(const uint8_t *aq, const uint8_t *sa, float ga, const uint8_t *bq,
+                       const uint8_t *sb, float gb, int64_t M, int64_t N, int64_t K,
+                       const int64_t *rows, const int64_t *cols, int64_t count, double *c,
+                       double *t) {
+  if (K % 16 != 0) return -2;
+  for (int64_t i = 0; i < count; ++i) {
+    const int64_t m = rows[i], n = cols[i];
+    if (m < 0 || m >= M || n < 0 || n >= N) return -4;
+    double acc = 0.0, tt = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      const double p = nv_hat(aq, sa, ga, K, m, k) * nv_hat(bq, sb, gb, K, n, k);
       acc += p;
       tt += fabs(p);
     }

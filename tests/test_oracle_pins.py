@@ -511,3 +511,116 @@ def test_mxfp4_gemm_matches_numpy_dequant():
     c, t = oracle.gemm_mxfp4(aq, sa, bq, sb)
     assert np.allclose(c, ah @ bh.T, rtol=0, atol=1e-12 * (np.abs(ah) @ np.abs(bh).T).max())
     assert np.allclose(t, np.abs(ah) @ np.abs(bh).T, rtol=1e-12)
+
+
+# ---- NVFP4 (§NVFP4 Two-Level Scaling: global fp32 x E4M3 per 16 x E2M1) ----
+
+def _bf16_row(vals):
+    """A bf16 row from values that bf16 represents exactly."""
+    t = torch.tensor(vals, dtype=torch.float32)
+    b = t.to(torch.bfloat16)
+    assert torch.equal(b.float(), t)
+    return b
+
+
+def _nv_codes(q):
+    return np.stack([q & 15, q >> 4], axis=-1).reshape(q.shape[0], -1)
+
+
+def test_nvfp4_global_scale_closed_forms():
+    # amax = 2688 * 2^k (2688 = 6 * 448 = 1.3125 * 2^11, exact in bf16) gives 2^k
+    for k in (-20, -3, 0, 1, 7):
+        amax = 2688.0 * 2.0 ** k
+        x = _bf16_row([0.5 * amax, -amax, 0.25 * amax, 0.0]).reshape(2, 2)
+        assert oracle.nvfp4_global_scale(x) == np.float32(2.0 ** k)
+    assert oracle.nvfp4_global_scale(torch.zeros((3, 16), dtype=torch.bfloat16)) == 1.0
+    neg0 = torch.full((2, 16), -0.0, dtype=torch.bfloat16)
+    assert oracle.nvfp4_global_scale(neg0) == 1.0
+
+
+def test_nvfp4_blocks_by_hand():
+    """Blocks worked out by hand from the E4M3 and E2M1 definitions (g = 1)."""
+    blk_a = [6, -6, 3, 1.5, 0.75, 0.25, -0.25, 5, 2.5, 1.25, 0.5, 4, 2, 1, 0, -0.0]
+    # amax 6: t = 6/6 = 1 -> E4M3 0x38 (1.0), D = 1; 0.75, 0.25, 5, 2.5 and 1.25
+    # are midpoints and go to the even code (1.0, 0, 4, 2, 1)
+    want_a = [7, 15, 5, 3, 2, 0, 8, 6, 4, 2, 1, 6, 4, 2, 0, 8]
+    # amax 6.375: t = 1.0625, the midpoint of 1.0 and 1.125 -> 1.0 (even);
+    # 6.375 / 1 saturates to 6
+    blk_b = [6.375, 1, -2, 0.5] + [0.0] * 12
+    want_b = [7, 2, 12, 1] + [0] * 12
+    # all zeros: t = 0 -> code 0, D = 0 -> signed zeros
+    blk_c = [0.0, -0.0] * 8
+    want_c = [0, 8] * 8
+    # amax 12: t = 2 -> 0x40, D = 2: 12 -> 6, 3 -> 1.5, 1 -> 0.5, 0.5 -> 0.25 (tie -> 0)
+    blk_d = [12, 3, 1, 0.5, -7, 9] + [0.0] * 10
+    # -7 / 2 = -3.5, midpoint of 3 and 4 -> 4 (even code 6); 9 / 2 = 4.5 -> 4
+    want_d = [7, 3, 1, 0, 14, 6] + [0] * 10
+    x = _bf16_row(blk_a + blk_b + blk_c + blk_d).reshape(1, 64)
+    q, s, g = oracle.quant_nvfp4_1x16(x, g=1.0)
+    assert g == 1.0
+    assert list(s[0]) == [0x38, 0x38, 0x00, 0x40]
+    assert list(_nv_codes(q)[0]) == want_a + want_b + want_c + want_d
+    assert q[0, 0] == (7 | (15 << 4))  # element 0 in the low nibble
+
+
+def test_nvfp4_block_scale_under_a_global_scale():
+    # tensor amax 336 = 2688 / 8 -> g = 0.125, 6 g = 0.75
+    # block 0: amax 336 -> t = 448 -> 0x7E, D = 56: 336 -> 6, 28 -> 0.5
+    # block 1: amax 21 -> t = 28 = 1.75 * 2^4 -> 0x5E, D = 3.5: 21 -> 6, 7 -> 2
+    x = _bf16_row([336, 28] + [0.0] * 14 + [21, -7] + [0.0] * 14).reshape(1, 32)
+    q, s, g = oracle.quant_nvfp4_1x16(x)
+    assert g == np.float32(0.125)
+    assert list(s[0]) == [0x7E, 0x5E]
+    assert oracle.e4m3_decode(0x5E) == 28.0
+    assert list(_nv_codes(q)[0][[0, 1, 16, 17]]) == [7, 1, 7, 12]
+
+
+def test_nvfp4_block_maximum_maps_to_six():
+    """With a normal E4M3 block scale s (within 2^-4 of t), the block's
+    largest element lands in [6/(1+2^-4), 6/(1-2^-4)] in units of g s, which
+    E2M1 rounds (or saturates) to 6."""
+    import fgq_inputs
+    x = fgq_inputs.exponent_spread((64, 512), 6, 1, seed=21)
+    q, s, g = oracle.quant_nvfp4_1x16(x)
+    codes = _nv_codes(q)
+    xf = x.float().numpy()
+    sdec = torch.from_numpy(s.copy()).view(torch.float8_e4m3fn).float().numpy()
+    checked = 0
+    for r in range(64):
+        for b in range(32):
+            blk = xf[r, 16 * b:16 * b + 16]
+            if sdec[r, b] < 2.0 ** -6:   # subnormal block scale: wider rounding
+                continue
+            i = int(np.argmax(np.abs(blk)))
+            assert codes[r, 16 * b + i] & 7 == 7
+            assert (codes[r, 16 * b + i] >> 3) == (1 if blk[i] < 0 else 0)
+            checked += 1
+    assert checked > 1000
+
+
+def test_nvfp4_gemm_matches_numpy_page_dequant():
+    """C against numpy's matmul of operands decoded by the page's formula,
+    global * float(block_scale) * e2m1, with torch's E4M3 decode."""
+    import fgq_inputs
+    M, N, K = 24, 40, 256
+    a = fgq_inputs.exponent_spread((M, K), 8, 1, seed=3)
+    b = fgq_inputs.exponent_spread((N, K), 8, 1, seed=4)
+    aq, sa, ga = oracle.quant_nvfp4_1x16(a)
+    bq, sb, gb = oracle.quant_nvfp4_1x16(b)
+    table = np.array(E2M1_PAGE + [-v for v in E2M1_PAGE])
+
+    def deq(q, s, g):
+        blk = torch.from_numpy(s.copy()).view(torch.float8_e4m3fn).double().numpy()
+        return float(g) * np.repeat(blk, 16, axis=1) * table[_nv_codes(q)]
+
+    ah, bh = deq(aq, sa, ga), deq(bq, sb, gb)
+    c, t = oracle.gemm_nvfp4(aq, sa, ga, bq, sb, gb)
+    assert np.allclose(c, ah @ bh.T, rtol=0, atol=1e-12 * (np.abs(ah) @ np.abs(bh).T).max())
+    assert np.allclose(t, np.abs(ah) @ np.abs(bh).T, rtol=1e-12)
+    rows, cols = np.array([0, 5, 23]), np.array([39, 0, 17])
+    c2, t2 = oracle.gemm_nvfp4_at(aq, sa, ga, bq, sb, gb, rows, cols)
+    assert np.array_equal(c2, c[rows, cols]) and np.array_equal(t2, t[rows, cols])
+    # and the dequantised values stay within one E2M1 step of the inputs
+    af = a.float().numpy().astype(np.float64)
+    d = np.repeat(float(ga) * torch.from_numpy(sa.copy()).view(torch.float8_e4m3fn).double().numpy(), 16, axis=1)
+    assert np.all(np.abs(ah - af) <= 2.0 * d + 1e-300)
