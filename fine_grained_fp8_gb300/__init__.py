@@ -23,8 +23,10 @@ from . import _lib
 from ._lib import (FGQ_OUT_BF16, FGQ_OUT_F32, FGQ_SCALE_FP32, FGQ_SCALE_UE8M0, FgqError,
                    check, load)
 
-__all__ = ["quant_act_1x128", "quant_act_128x1", "quant_mxfp4_1x32", "quant_w_128x128", "gemm_fp8_blockscaled",
-           "gemm_fp8_blockscaled_splitk", "gemm_fp8_blockscaled_fused_act", "gemm_mxfp4", "splitk_workspace", "device_error",
+__all__ = ["quant_act_1x128", "quant_act_128x1", "quant_mxfp4_1x32", "nvfp4_global_scale",
+           "quant_nvfp4_1x16", "quant_w_128x128", "gemm_fp8_blockscaled",
+           "gemm_fp8_blockscaled_splitk", "gemm_fp8_blockscaled_fused_act", "gemm_mxfp4",
+           "gemm_nvfp4", "splitk_workspace", "device_error",
            "FgqError", "load", "FGQ_SCALE_FP32", "FGQ_SCALE_UE8M0", "FGQ_OUT_F32",
            "FGQ_OUT_BF16", "scale_mode"]
 
@@ -117,6 +119,50 @@ def quant_mxfp4_1x32(x: torch.Tensor, xq: torch.Tensor | None = None,
                                    _stream(x))
     check("fgq_quant_mxfp4_1x32", st)
     return xq, sx
+
+
+def nvfp4_global_scale(x: torch.Tensor, g: torch.Tensor | None = None) -> torch.Tensor:
+    """NVFP4 per-tensor scale of bf16 x [R, K] (amax / 2688, 1 for all zeros)
+    as a one-element fp32 device tensor."""
+    _need_cuda("x", x, torch.bfloat16)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with a contiguous last dimension")
+    R, K = x.shape
+    if g is None:
+        g = torch.empty((1,), dtype=torch.float32, device=x.device)
+    _need_cuda("g", g, torch.float32)
+    st = _lib.fgq_nvfp4_global_scale(x.data_ptr(), R, K, x.stride(0), g.data_ptr(), _stream(x))
+    check("fgq_nvfp4_global_scale", st)
+    return g
+
+
+def quant_nvfp4_1x16(x: torch.Tensor, g: torch.Tensor | None = None,
+                     xq: torch.Tensor | None = None, sx: torch.Tensor | None = None):
+    """NVFP4 quantization of the rows of bf16 x [R, K] under the global scale
+    g (a one-element fp32 device tensor; computed with nvfp4_global_scale when
+    None): E2M1 codes xq [R, K/2] uint8 (even element in the low nibble) and
+    one E4M3 block-scale code per 16 elements, sx [R, K/16] uint8.  Returns
+    (xq, sx, g)."""
+    _need_cuda("x", x, torch.bfloat16)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with a contiguous last dimension")
+    R, K = x.shape
+    if g is None:
+        g = nvfp4_global_scale(x)
+    _need_cuda("g", g, torch.float32)
+    if xq is None:
+        xq = torch.empty((R, K // 2), dtype=torch.uint8, device=x.device)
+    if sx is None:
+        sx = torch.empty((R, K // 16), dtype=torch.uint8, device=x.device)
+    _need_cuda("xq", xq, torch.uint8)
+    _need_cuda("sx", sx, torch.uint8)
+    if xq.shape != (R, K // 2) or not xq.is_contiguous() or sx.shape != (R, K // 16) \
+            or not sx.is_contiguous():
+        raise ValueError("xq must be a dense [R, K/2] and sx a dense [R, K/16]")
+    st = _lib.fgq_quant_nvfp4_1x16(x.data_ptr(), R, K, x.stride(0), g.data_ptr(), xq.data_ptr(),
+                                   sx.data_ptr(), _stream(x))
+    check("fgq_quant_nvfp4_1x16", st)
+    return xq, sx, g
 
 
 def quant_w_128x128(w: torch.Tensor, mode="fp32", wq: torch.Tensor | None = None,
@@ -227,6 +273,35 @@ def gemm_mxfp4(aq: torch.Tensor, sa: torch.Tensor, bq: torch.Tensor, sb: torch.T
                              FGQ_OUT_BF16 if out_dtype == torch.bfloat16 else FGQ_OUT_F32,
                              _stream(aq))
     check("fgq_gemm_mxfp4", st)
+    return out
+
+
+def gemm_nvfp4(aq: torch.Tensor, sa: torch.Tensor, ga: torch.Tensor, bq: torch.Tensor,
+               sb: torch.Tensor, gb: torch.Tensor, out_dtype=torch.float32,
+               out: torch.Tensor | None = None) -> torch.Tensor:
+    """C [M, N] from NVFP4 operands as quant_nvfp4_1x16 writes them: aq [M, K/2],
+    sa [M, K/16] and the global scale ga; bq [N, K/2], sb [N, K/16] and gb
+    (the weight quantized as its transpose)."""
+    for name, t in (("aq", aq), ("sa", sa), ("bq", bq), ("sb", sb)):
+        _need_cuda(name, t, torch.uint8)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    _need_cuda("ga", ga, torch.float32)
+    _need_cuda("gb", gb, torch.float32)
+    M, K = aq.shape[0], 2 * aq.shape[1]
+    N = bq.shape[0]
+    if bq.shape != (N, K // 2) or sa.shape != (M, K // 16) or sb.shape != (N, K // 16):
+        raise ValueError("shape mismatch: aq [M,K/2], sa [M,K/16], bq [N,K/2], sb [N,K/16]")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=aq.device)
+    _need_cuda("out", out, out_dtype)
+    if out.shape != (M, N) or out.stride(1) != 1:
+        raise ValueError("out must be [M, N] with contiguous rows")
+    st = _lib.fgq_gemm_nvfp4(aq.data_ptr(), sa.data_ptr(), ga.data_ptr(), bq.data_ptr(),
+                             sb.data_ptr(), gb.data_ptr(), out.data_ptr(), out.stride(0), M, N, K,
+                             FGQ_OUT_BF16 if out_dtype == torch.bfloat16 else FGQ_OUT_F32,
+                             _stream(aq))
+    check("fgq_gemm_nvfp4", st)
     return out
 
 

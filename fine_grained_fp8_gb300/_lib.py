@@ -31,6 +31,8 @@ SIGNATURES = {
     "fgq_quant_act_1x128": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _int, _vp]),
     "fgq_quant_act_128x1": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _int, _vp]),
     "fgq_quant_mxfp4_1x32": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
+    "fgq_nvfp4_global_scale": (_int, [_vp, _i64, _i64, _i64, _vp, _vp]),
+    "fgq_quant_nvfp4_1x16": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
     "fgq_quant_w_128x128": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _int, _vp]),
     "fgq_gemm_fp8_blockscaled": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "fgq_gemm_fp8_blockscaled_ex": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
@@ -39,6 +41,8 @@ SIGNATURES = {
                                                _int, _int, _vp, ctypes.c_size_t, _vp]),
     "fgq_gemm_splitk_workspace_size": (_int, [_i64, _i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
     "fgq_gemm_mxfp4": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _vp]),
+    "fgq_gemm_nvfp4": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int,
+                              _vp]),
     "fgq_gemm_fp8_blockscaled_fused_act": (_int, [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                                   _int, _int, _vp]),
     "fgq_gemm_fp8_blockscaled_splitk_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
@@ -109,6 +113,14 @@ def fgq_quant_mxfp4_1x32(x, R, K, ldx, xq, sx, stream) -> int:
     return load().fgq_quant_mxfp4_1x32(x, R, K, ldx, xq, sx, stream)
 
 
+def fgq_nvfp4_global_scale(x, R, K, ldx, g, stream) -> int:
+    return load().fgq_nvfp4_global_scale(x, R, K, ldx, g, stream)
+
+
+def fgq_quant_nvfp4_1x16(x, R, K, ldx, g, xq, sx, stream) -> int:
+    return load().fgq_quant_nvfp4_1x16(x, R, K, ldx, g, xq, sx, stream)
+
+
 def fgq_quant_w_128x128(w, K, N, ldw, wq, sw, mode, stream) -> int:
     return load().fgq_quant_w_128x128(w, K, N, ldw, wq, sw, mode, stream)
 
@@ -140,6 +152,10 @@ def fgq_gemm_fp8_blockscaled_fused_act(A, lda, B, sB, C, ldc, M, N, K, out, mode
 
 def fgq_gemm_mxfp4(A, sA, B, sB, C, ldc, M, N, K, out, stream) -> int:
     return load().fgq_gemm_mxfp4(A, sA, B, sB, C, ldc, M, N, K, out, stream)
+
+
+def fgq_gemm_nvfp4(A, sA, gA, B, sB, gB, C, ldc, M, N, K, out, stream) -> int:
+    return load().fgq_gemm_nvfp4(A, sA, gA, B, sB, gB, C, ldc, M, N, K, out, stream)
 
 
 def fgq_gemm_splitk_workspace_size(M, N, K):

@@ -108,6 +108,34 @@ fgq_status fgq_quant_mxfp4_1x32(const void* x, int64_t R, int64_t K, int64_t ldx
                                                 static_cast<cudaStream_t>(stream), dev));
 }
 
+fgq_status fgq_nvfp4_global_scale(const void* x, int64_t R, int64_t K, int64_t ldx, float* g,
+                                  void* stream) {
+  if (R < 0 || K <= 0 || K % 16 != 0) return FGQ_ERR_INVALID_ARG;
+  if (!x || !g) return FGQ_ERR_INVALID_ARG;
+  if (ldx < K || ldx % 8 != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(g, 4)) return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_nvfp4_global_scale(x, R, K, ldx, g,
+                                                  static_cast<cudaStream_t>(stream), dev));
+}
+
+fgq_status fgq_quant_nvfp4_1x16(const void* x, int64_t R, int64_t K, int64_t ldx, const float* g,
+                                uint8_t* xq, uint8_t* sx, void* stream) {
+  if (R < 0 || K <= 0 || K % 16 != 0) return FGQ_ERR_INVALID_ARG;
+  if (R == 0) return FGQ_OK;
+  if (!x || !g || !xq || !sx) return FGQ_ERR_INVALID_ARG;
+  if (ldx < K || ldx % 8 != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(g, 4) || !aligned(xq, 4)) return FGQ_ERR_INVALID_ARG;
+  if (R > kMaxGroups / (K / 16)) return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_quant_nvfp4_1x16(x, R, K, ldx, g, xq, sx,
+                                                static_cast<cudaStream_t>(stream), dev));
+}
+
 fgq_status fgq_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t ldw, uint8_t* wq,
                                float* sw, int mode, void* stream) {
   if (K <= 0 || N <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
@@ -210,6 +238,28 @@ fgq_status fgq_gemm_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
   fgq_status st = get_device(&dev);
   if (st != FGQ_OK) return st;
   return from_cuda(fgq::launch_gemm_mxf4(A, sA, B, sB, C, ldc, M, N, K, out == FGQ_OUT_BF16 ? 1 : 0,
+                                         static_cast<cudaStream_t>(stream), dev));
+}
+
+fgq_status fgq_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const float* gA,
+                          const uint8_t* B, const uint8_t* sB, const float* gB, void* C,
+                          int64_t ldc, int64_t M, int64_t N, int64_t K, int out, void* stream) {
+  if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (out != FGQ_OUT_F32 && out != FGQ_OUT_BF16) return FGQ_ERR_INVALID_ARG;
+  if (M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31) || K >= (int64_t{1} << 31))
+    return FGQ_ERR_INVALID_ARG;
+  if (M == 0) return FGQ_OK;
+  if (!A || !sA || !gA || !B || !sB || !gB || !C) return FGQ_ERR_INVALID_ARG;
+  const int64_t vec = (out == FGQ_OUT_F32) ? 4 : 8;
+  if (ldc < N || ldc % vec != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(sA, 4) ||
+      !aligned(sB, 4) || !aligned(gA, 4) || !aligned(gB, 4))
+    return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_gemm_nvf4(A, sA, gA, B, sB, gB, C, ldc, M, N, K,
+                                         out == FGQ_OUT_BF16 ? 1 : 0,
                                          static_cast<cudaStream_t>(stream), dev));
 }
 

@@ -65,6 +65,15 @@ cudaError_t launch_selftest_wait_timeout(cudaStream_t stream);
 cudaError_t launch_gemm_mxf4(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
                              const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
                              int64_t K, int out_bf16, cudaStream_t stream, const DeviceInfo& dev);
+cudaError_t launch_gemm_nvf4(const uint8_t* A, const uint8_t* sA, const float* ga,
+                             const uint8_t* B, const uint8_t* sB, const float* gb, void* C,
+                             int64_t ldc, int64_t M, int64_t N, int64_t K, int out_bf16,
+                             cudaStream_t stream, const DeviceInfo& dev);
+cudaError_t launch_nvfp4_global_scale(const void* x, int64_t R, int64_t K, int64_t ldx, float* g,
+                                      cudaStream_t stream, const DeviceInfo& dev);
+cudaError_t launch_quant_nvfp4_1x16(const void* x, int64_t R, int64_t K, int64_t ldx,
+                                    const float* g, uint8_t* xq, uint8_t* sx, cudaStream_t stream,
+                                    const DeviceInfo& dev);
 
 // Each kernel translation unit keeps its own device error word; these read
 // (and optionally clear) one unit's word.

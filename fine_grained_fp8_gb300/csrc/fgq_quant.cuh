@@ -1,8 +1,9 @@
 // Device helpers of the quantizers, shared by the quantizer kernels and the
 // GEMM that quantizes its activations itself: 16-byte streaming loads and
-// stores, the exact amax of bf16 groups, the group scale (fp32 or UE8M0)
-// and the E4M3 encode with the division-free exact quotient (see
-// quant.cu for the method and its check).
+// stores, the exact amax of bf16 groups, the group scale (fp32 or UE8M0),
+// the E4M3 encode with the division-free exact quotient (see quant.cu for
+// the method and its check) and the E2M1 pair conversion of the FP4
+// quantizers.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -41,6 +42,21 @@ __device__ __forceinline__ uint32_t absmax_pairs(uint4 v) {
   uint32_t a = __vmaxu2(v.x & m, v.y & m);
   uint32_t b = __vmaxu2(v.z & m, v.w & m);
   return __vmaxu2(a, b);
+}
+
+// Eight fp32 -> eight E2M1 codes in 32 bits: byte j = element 2j (low
+// nibble) and element 2j+1 (high nibble).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&y)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
+  return r;
 }
 
 __device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w) {

@@ -1,24 +1,25 @@
-// MXFP4 GEMM for sm_103a: E2M1 elements with one UE8M0 scale per 32 along K
-// on both operands ("Fine-Grained FP8/FP4 Quantization", §UE8M0 vs E4M3
-// Scale Formats, block size 32; §When to Use: MXFP4 with UE8M0 scales for
-// native hardware acceleration):
+// FP4 GEMMs for sm_103a: E2M1 elements with block scales along K on both
+// operands ("Fine-Grained FP8/FP4 Quantization", §UE8M0 vs E4M3 Scale
+// Formats; §NVFP4 Two-Level Scaling; §When to Use: NVFP4 with E4M3 block
+// scales for precision, MXFP4 with UE8M0 scales for native acceleration):
 //
-//   C[m,n] = sum_k e2m1(A[m,k]) 2^(sA[m,k/32]-127) e2m1(B[n,k]) 2^(sB[n,k/32]-127)
+//   MXFP4  C[m,n] = sum_k e2m1(A[m,k]) 2^(sA[m,k/32]-127) e2m1(B[n,k]) 2^(sB[n,k/32]-127)
+//   NVFP4  C[m,n] = gA gB sum_k e2m1(A[m,k]) e4m3(sA[m,k/16]) e2m1(B[n,k]) e4m3(sB[n,k/16])
 //
-// tcgen05.mma kind::mxf4.block_scale.scale_vec::2X takes K = 64 packed E2M1
-// elements (32 bytes a row) and two UE8M0 factors per row of A and per
-// column of B, applied by the tensor core; the fp32 accumulator stays in
-// TMEM for the whole K loop.  Measured factor layout (as for kind::mxf8f6f4
-// with scale_vec::1X): A's row m at lane m, column base + m/32; B's column
-// n at lane 32 q + n%32, column base + n/32; the descriptor's factor id 0
+// tcgen05.mma kind::mxf4 (scale_vec::2X, UE8M0) or kind::mxf4nvf4
+// (scale_vec::4X, UE4M3) takes K = 64 packed E2M1 elements (32 bytes a
+// row) and the block factors of that K range per row of A and per column
+// of B, applied by the tensor core; the fp32 accumulator stays in TMEM for
+// the whole K loop.  Measured factor layout (as for kind::mxf8f6f4 with
+// scale_vec::1X): A's row m at lane m, column base + m/32; B's column n at
+// lane 32 q + n%32, column base + n/32.  2X: the descriptor's factor id 0
 // reads bytes 0-1 of the cell (the two 32-element blocks of one MMA), id 2
-// bytes 2-3.
+// bytes 2-3.  4X: byte b of the cell scales the MMA's b-th 16-element block.
 //
 // Same structure as the power-of-two FP8 kernel (gemm_mx.cu): persistent
 // CTAs on 128 x BN tiles, warp 0 TMA producer (one 128-byte stage = 256
 // elements of K), warp 1 MMA issuer (four MMAs per stage), warps 4-7 write
-// the factors into a TMEM ring (one slot per stage = two 32-bit cells per
-// row or column = eight 32-element blocks = four MMAs), warps 8-15 epilogue.
+// the factors into a TMEM ring (one slot per stage), warps 8-15 epilogue.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -35,35 +36,52 @@ constexpr int BM = 128;
 constexpr int BK = 128;
 constexpr int kThreads = 512;  // warpgroup 0 control, 1 scale factors, 2-3 epilogue
 constexpr int kEpiWarps = 8;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfBarrier = 1;    // named barrier of the four factor-writer warps
+
+// The two FP4 formats.  MXFP4: one UE8M0 factor per 32 elements, MMA
+// kind::mxf4 with scale_vec::2X (a 32-bit factor cell serves two K = 64
+// MMAs, the descriptor's factor id picking bytes 0-1 or 2-3).  NVFP4: one
+// E4M3 factor per 16 elements, kind::mxf4nvf4 with scale_vec::4X (one cell
+// per MMA, byte b scaling its b-th 16-element block; measured), and an fp32
+// per-tensor scale on each operand, applied in the epilogue.
+//
 // Scale-factor ring: a slot = one stage = 256 elements of K = four K = 64
-// MMAs = two 32-bit cells per row of A and per column of B.  Cell w of A
+// MMAs = kCells 32-bit cells per row of A and per column of B.  Cell w of A
 // sits at the slot's A base + 4 w (+ 0..3 for the four row quarters), cell
 // w of B at its B base + 8 w (+ 0..7 for the column groups); the factor
 // addresses need only 4-column (A) and 8-column (B) alignment (measured).
-constexpr int kSlots = 8;
-constexpr uint32_t kSfaSlot = 8, kSfbSlot = 16;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfBarrier = 1;    // named barrier of the four factor-writer warps
-constexpr uint32_t kSfaCol0 = 256;     // slot r: A cells at kSfaCol0 + 8 r + {0, 4} (+ 0..3)
-constexpr uint32_t kSfbCol0 = 320;     // slot r: B cells at kSfbCol0 + 16 r + {0, 8} (+ 0..7)
+// The writers stage the codes in chunks of 32 bytes per row, kChunkStages
+// stages.
+template <bool NV>
+struct Fp4Fmt {
+  static constexpr int kBlock = NV ? 16 : 32;      // elements per factor
+  static constexpr int kCells = NV ? 4 : 2;        // factor cells per row per stage
+  static constexpr int kSlots = NV ? 4 : 8;
+  static constexpr uint32_t kSfaSlot = 4 * kCells, kSfbSlot = 8 * kCells;
+  static constexpr uint32_t kSfaCol0 = 256;        // after the accumulators
+  static constexpr uint32_t kSfbCol0 = kSfaCol0 + kSfaSlot * kSlots;
+  static constexpr int kChunkStages = 8 / kCells;  // 32 bytes of codes per row
+};
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool NV>
 struct Mxf4Cfg {
+  using F = Fp4Fmt<NV>;
   static constexpr int kNAcc = BN == 128 ? 2 : 1;  // accumulators in TMEM columns 0..255
   static constexpr int kABytes = BM * BK;
   static constexpr int kBBytes = BN * BK;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kNumBars = 2 * STAGES + 2 * kSlots + 2 * kNAcc + 1;
-  // factor staging: two buffers of four stages' codes, rows padded to 10
-  // words (8-byte aligned cell pairs, two-way bank conflicts at most when a
-  // warp reads one cell of 32 rows)
+  static constexpr int kNumBars = 2 * STAGES + 2 * F::kSlots + 2 * kNAcc + 1;
+  // factor staging: two buffers of one chunk's codes (32 bytes a row), rows
+  // padded to 10 words (8-byte aligned cell pairs, two-way bank conflicts
+  // at most when a warp reads one cell of 32 rows)
   static constexpr int kSfRowWords = 10;
   static constexpr int kSfBufWords = (BM + BN) * kSfRowWords;
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes +
                                        2 * kSfBufWords * 4 + kNumBars * 8 + 16;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-  static_assert(kNAcc * BN <= static_cast<int>(kSfaCol0), "accumulators overlap the scale ring");
-  static_assert(kSfaCol0 + kSfaSlot * kSlots <= kSfbCol0 && kSfbCol0 + kSfbSlot * kSlots <= 512,
+  static_assert(kNAcc * BN <= static_cast<int>(F::kSfaCol0), "accumulators overlap the scale ring");
+  static_assert(F::kSfbCol0 % 8 == 0 && F::kSfbCol0 + F::kSfbSlot * F::kSlots <= kTmemCols,
                 "scale ring within TMEM");
   static_assert(BN / 32 <= 8, "B factors of one slot take BN/32 <= 8 columns");
 };
@@ -79,9 +97,10 @@ __device__ __forceinline__ bool mxf4_wait_drain(uint64_t* bar, uint32_t parity) 
   return true;
 }
 
-// kind::mxf4: A and B E2M1 (type 1), UE8M0 factors (bit 23), factor id 0.
-__host__ __device__ constexpr uint32_t idesc_mxf4(int m, int n) {
-  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+// A and B E2M1 (type 1); factors UE8M0 (bit 23 set, MXFP4) or UE4M3 (bit 23
+// clear, NVFP4); factor ids 0.
+__host__ __device__ constexpr uint32_t idesc_fp4(int m, int n, bool nv) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (nv ? 0u : 1u << 23) |
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
@@ -92,6 +111,18 @@ __device__ __forceinline__ void umma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
       "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
@@ -146,13 +177,19 @@ __device__ __forceinline__ void store32(void* C, int64_t ldc, int row, int col,
   }
 }
 
-template <int BN, int STAGES, bool OUT_BF16>
+template <int BN, int STAGES, bool OUT_BF16, bool NV>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mxf4_kernel(const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ CUtensorMap tmap_b, const uint8_t* __restrict__ sA,
-                   const uint8_t* __restrict__ sB, void* __restrict__ C, int64_t ldc, int M, int N,
+                   const uint8_t* __restrict__ sB, const float* __restrict__ ga,
+                   const float* __restrict__ gb, void* __restrict__ C, int64_t ldc, int M, int N,
                    int K) {
-  using CF = Mxf4Cfg<BN, STAGES>;
+  using CF = Mxf4Cfg<BN, STAGES, NV>;
+  using F = Fp4Fmt<NV>;
+  constexpr int kSlots = F::kSlots;
+  constexpr uint32_t kSfaSlot = F::kSfaSlot, kSfbSlot = F::kSfbSlot;
+  constexpr uint32_t kSfaCol0 = F::kSfaCol0, kSfbCol0 = F::kSfbCol0;
+  constexpr int kCells = F::kCells, kCh = F::kChunkStages;
   constexpr int NACC = CF::kNAcc;
   constexpr int HALF = BN / 2;    // columns per epilogue warp
   constexpr int NLD = HALF / 32;  // 32-column loads per warp and tile
@@ -179,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_tiles = m_tiles * n_tiles;
   const int kstages = (K + 255) / 256;  // 128-byte stages of 256 elements (the last may be half)
   const bool half_last = (K % 256) != 0;  // the last stage holds 128 elements of K
-  const int kg = K / 32;                // UE8M0 codes per row of sA / sB
+  const int kg = K / F::kBlock;         // factor codes per row of sA / sB
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -241,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (elect_one_sync()) {
-      constexpr uint32_t idesc0 = idesc_mxf4(BM, BN);
+      constexpr uint32_t idesc0 = idesc_fp4(BM, BN, NV);
       constexpr uint32_t kId2 = (2u << 29) | (2u << 4);  // factor bytes 2-3 of A and B
       const uint64_t dA0 = smem_desc_k_sw128(smem_u32(sm_a));
       const uint32_t a_lo0 = static_cast<uint32_t>(dA0), dhi = static_cast<uint32_t>(dA0 >> 32);
@@ -266,17 +303,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_lo = b_lo0 + ls * (CF::kBBytes >> 4);
           const uint32_t sfa = tmem_base + kSfaCol0 + kSfaSlot * r;
           const uint32_t sfb = tmem_base + kSfbCol0 + kSfbSlot * r;
-          // four K = 64 MMAs (32 bytes of each row apart): factor bytes 0-1
-          // and 2-3 of cell 0, then of cell 1; a final half stage has two
-          umma_mxf4(d, make_desc(a_lo, dhi), make_desc(b_lo, dhi), idesc0, sfa, sfb,
-                    kc > 0 ? 1u : 0u);
-          umma_mxf4(d, make_desc(a_lo + 2, dhi), make_desc(b_lo + 2, dhi), idesc0 | kId2, sfa, sfb,
-                    1u);
-          if (kc + 1 < kstages || !half_last) {
-            umma_mxf4(d, make_desc(a_lo + 4, dhi), make_desc(b_lo + 4, dhi), idesc0, sfa + 4,
+          // four K = 64 MMAs (32 bytes of each row apart); a final half
+          // stage has two.  MXFP4: factor bytes 0-1 and 2-3 of cell 0, then
+          // of cell 1.  NVFP4: cell kk for MMA kk.
+          const bool full_stage = kc + 1 < kstages || !half_last;
+          if constexpr (NV) {
+            umma_nvf4(d, make_desc(a_lo, dhi), make_desc(b_lo, dhi), idesc0, sfa, sfb,
+                      kc > 0 ? 1u : 0u);
+            umma_nvf4(d, make_desc(a_lo + 2, dhi), make_desc(b_lo + 2, dhi), idesc0, sfa + 4,
                       sfb + 8, 1u);
-            umma_mxf4(d, make_desc(a_lo + 6, dhi), make_desc(b_lo + 6, dhi), idesc0 | kId2,
-                      sfa + 4, sfb + 8, 1u);
+            if (full_stage) {
+              umma_nvf4(d, make_desc(a_lo + 4, dhi), make_desc(b_lo + 4, dhi), idesc0, sfa + 8,
+                        sfb + 16, 1u);
+              umma_nvf4(d, make_desc(a_lo + 6, dhi), make_desc(b_lo + 6, dhi), idesc0, sfa + 12,
+                        sfb + 24, 1u);
+            }
+          } else {
+            umma_mxf4(d, make_desc(a_lo, dhi), make_desc(b_lo, dhi), idesc0, sfa, sfb,
+                      kc > 0 ? 1u : 0u);
+            umma_mxf4(d, make_desc(a_lo + 2, dhi), make_desc(b_lo + 2, dhi), idesc0 | kId2, sfa,
+                      sfb, 1u);
+            if (full_stage) {
+              umma_mxf4(d, make_desc(a_lo + 4, dhi), make_desc(b_lo + 4, dhi), idesc0, sfa + 4,
+                        sfb + 8, 1u);
+              umma_mxf4(d, make_desc(a_lo + 6, dhi), make_desc(b_lo + 6, dhi), idesc0 | kId2,
+                        sfa + 4, sfb + 8, 1u);
+            }
           }
           umma_commit(&sf_empty[r]);
           umma_commit(&empty[ls]);
@@ -296,15 +348,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4 && warp < 8) {
     // ---------------- scale-factor writers ----------------
     // The factors of a tile's rows (columns) are one contiguous block of
-    // BM (BN) rows of K/32 codes.  The four warps copy four stages of it
-    // at a time (32 bytes of each row) into a shared-memory buffer with
+    // BM (BN) rows of kg codes.  The four warps copy one chunk of it at a
+    // time (32 bytes of each row: four MXFP4 or two NVFP4 stages) into a
+    // shared-memory buffer with
     // coalesced asynchronous copies (whole 32-byte sectors per warp
     // instruction), then each warp reads the cells of its 32 rows (and of
     // all BN columns, which every lane quarter of B needs) from there.
     // Chunk c + 1 is in flight while chunk c's slots are written.  Codes
     // past a row's end (the final partial chunk) and rows past M are not
-    // copied: their cells feed only the unused second cell of a final half
-    // stage or accumulator rows that are never stored.  A warp that gives
+    // copied: their cells feed only the unused second half of a final half
+    // stage's cells or accumulator rows that are never stored.  A warp that gives
     // up on a wait keeps walking the same chunks and barriers (skipping the
     // slot work) so that the others never wait for it at a named barrier.
     constexpr int kRowW = CF::kSfRowWords;
@@ -312,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int wt = threadIdx.x - 128;
     const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
-    const int nchunks = (kstages + 3) / 4;
+    const int nchunks = (kstages + kCh - 1) / kCh;
     uint32_t g_it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -349,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cp_async_commit();
       };
-      auto store = [&](const uint32_t (&wa)[2], const uint32_t (&wb)[2][8]) -> bool {
+      auto store = [&](const uint32_t (&wa)[kCells], const uint32_t (&wb)[kCells][8]) -> bool {
         const uint32_t r = g_it % kSlots;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_empty[r], ((g_it / kSlots) & 1u) ^ 1u,
                                                abort_flag, FGQ_DEVERR_SF_SLOT)))
@@ -357,10 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t ca = tmem_base + t_lane + kSfaCol0 + kSfaSlot * r + static_cast<uint32_t>(q);
         const uint32_t cb = tmem_base + t_lane + kSfbCol0 + kSfbSlot * r;
-        tmem_st_32x32b_x1(ca, wa[0]);
-        tmem_st_32x32b_x1(ca + 4, wa[1]);
-        tmem_st_32x32b_x8(cb, wb[0]);
-        tmem_st_32x32b_x8(cb + 8, wb[1]);
+#pragma unroll
+        for (int j = 0; j < kCells; ++j) {
+          tmem_st_32x32b_x1(ca + 4 * j, wa[j]);
+          tmem_st_32x32b_x8(cb + 8 * j, wb[j]);
+        }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -378,14 +432,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t* sa = sf_stage + (c & 1) * CF::kSfBufWords + (32 * q + lane) * kRowW;
         const uint32_t* sb = sf_stage + (c & 1) * CF::kSfBufWords + BM * kRowW + lane * kRowW;
 #pragma unroll 1
-        for (int st = 0; st < 4 && 4 * c + st < kstages && ok; ++st) {
-          const uint32_t wa[2] = {sa[2 * st], sa[2 * st + 1]};
-          uint32_t wb[2][8];
+        for (int st = 0; st < kCh && kCh * c + st < kstages && ok; ++st) {
+          uint32_t wa[kCells], wb[kCells][8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int jj = j < BN / 32 ? j : j - BN / 32;  // BN = 128: columns 4-7 repeat 0-3
-            wb[0][j] = sb[32 * jj * kRowW + 2 * st];
-            wb[1][j] = sb[32 * jj * kRowW + 2 * st + 1];
+          for (int w = 0; w < kCells; ++w) {
+            wa[w] = sa[kCells * st + w];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int jj = j < BN / 32 ? j : j - BN / 32;  // BN = 128: columns 4-7 repeat 0-3
+              wb[w][j] = sb[32 * jj * kRowW + kCells * st + w];
+            }
           }
           ok = store(wa, wb);
           // chunk c + 1 goes into buffer (c + 1) & 1, which held chunk
@@ -404,6 +460,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int half = ew >> 2;
     const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
+    // NVFP4: C = gA gB * (the tensor core's sum over E2M1 x E4M3 products)
+    float alpha = 1.0f;
+    if constexpr (NV) alpha = __fmul_rn(__ldg(ga), __ldg(gb));
+    auto scale32 = [&](uint32_t (&r)[32]) {
+      if constexpr (NV) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), alpha));
+      }
+    };
     uint32_t t_it = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t_it) {
       const int tm = tile % m_tiles, tn = tile / m_tiles;
@@ -432,10 +497,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
         if (row_ok) {
-          if (j % 2 == 0)
+          if (j % 2 == 0) {
+            scale32(ra);
             store32<OUT_BF16>(C, ldc, row, col0 + 32 * j, ra);
-          else
+          } else {
+            scale32(rb);
             store32<OUT_BF16>(C, ldc, row, col0 + 32 * j, rb);
+          }
         }
         if (j + 1 < NLD) {
           if (j % 2 == 0)
@@ -456,12 +524,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int STAGES, bool OUT_BF16>
+template <int BN, int STAGES, bool OUT_BF16, bool NV>
 cudaError_t launch_mxf4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
-                          void* C, int64_t ldc, int M, int N, int K, cudaStream_t stream,
-                          const DeviceInfo& dev) {
-  using CF = Mxf4Cfg<BN, STAGES>;
-  auto kern = gemm_mxf4_kernel<BN, STAGES, OUT_BF16>;
+                          const float* ga, const float* gb, void* C, int64_t ldc, int M, int N,
+                          int K, cudaStream_t stream, const DeviceInfo& dev) {
+  using CF = Mxf4Cfg<BN, STAGES, NV>;
+  auto kern = gemm_mxf4_kernel<BN, STAGES, OUT_BF16, NV>;
   static bool attr_set[64] = {};
   static std::mutex mu;
   {
@@ -479,8 +547,25 @@ cudaError_t launch_mxf4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* 
     return cudaErrorInvalidValue;
   const int tiles = ((M + BM - 1) / BM) * (N / BN);
   const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), CF::kSmemBytes, stream, ta, tb, sA, sB, C,
-                    ldc, M, N, K);
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), CF::kSmemBytes, stream, ta, tb, sA, sB, ga,
+                    gb, C, ldc, M, N, K);
+}
+
+template <bool NV>
+cudaError_t launch_fp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
+                       const float* ga, const float* gb, void* C, int64_t ldc, int64_t M,
+                       int64_t N, int64_t K, int out_bf16, cudaStream_t stream,
+                       const DeviceInfo& dev) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  const int64_t tiles256 = ((M + BM - 1) / BM) * (N / 256);
+  const bool wide = (N % 256 == 0) && tiles256 >= dev.sm_count;
+  if (out_bf16) {
+    return wide ? launch_mxf4_cfg<256, 4, true, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, stream, dev)
+                : launch_mxf4_cfg<128, 6, true, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, stream, dev);
+  }
+  return wide ? launch_mxf4_cfg<256, 4, false, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, stream, dev)
+              : launch_mxf4_cfg<128, 6, false, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, stream, dev);
 }
 
 }  // namespace
@@ -488,16 +573,14 @@ cudaError_t launch_mxf4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* 
 cudaError_t launch_gemm_mxf4(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
                              const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
                              int64_t K, int out_bf16, cudaStream_t stream, const DeviceInfo& dev) {
-  if (M == 0 || N == 0) return cudaSuccess;
-  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  const int64_t tiles256 = ((M + BM - 1) / BM) * (N / 256);
-  const bool wide = (N % 256 == 0) && tiles256 >= dev.sm_count;
-  if (out_bf16) {
-    return wide ? launch_mxf4_cfg<256, 4, true>(A, sA, B, sB, C, ldc, m, n, k, stream, dev)
-                : launch_mxf4_cfg<128, 6, true>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
-  }
-  return wide ? launch_mxf4_cfg<256, 4, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev)
-              : launch_mxf4_cfg<128, 6, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
+  return launch_fp4<false>(A, sA, B, sB, nullptr, nullptr, C, ldc, M, N, K, out_bf16, stream, dev);
+}
+
+cudaError_t launch_gemm_nvf4(const uint8_t* A, const uint8_t* sA, const float* ga,
+                             const uint8_t* B, const uint8_t* sB, const float* gb, void* C,
+                             int64_t ldc, int64_t M, int64_t N, int64_t K, int out_bf16,
+                             cudaStream_t stream, const DeviceInfo& dev) {
+  return launch_fp4<true>(A, sA, B, sB, ga, gb, C, ldc, M, N, K, out_bf16, stream, dev);
 }
 
 cudaError_t read_device_error_mxf4(uint32_t* word, bool clear) {

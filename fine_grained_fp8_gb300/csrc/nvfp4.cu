@@ -1,0 +1,191 @@
+// NVFP4 quantization for sm_103a ("Fine-Grained FP8/FP4 Quantization",
+// §NVFP4 Two-Level Scaling: a value is global_scale * block_scale * e2m1,
+// with one E4M3 block scale per 16 consecutive elements of a row and one
+// fp32 global scale per tensor; E2M1 values 0, 0.5, 1, 1.5, 2, 3, 4, 6).
+//
+// The page gives the dequantization only.  The encoder applies the FP8
+// rule amax / 448 at both levels, with 6 the largest E2M1 value:
+//   global   g = amax / 2688 over the whole tensor (2688 = 6 * 448), 1 for
+//            an all-zero tensor;
+//   block    s_b = E4M3(amax_b / (6 g)), round to nearest even, saturating;
+//   element  q = E2M1(x / D), D = g * s_b (fp32), round to nearest even,
+//            saturating at 6; a block whose D is 0 gets signed zeros.
+// Every quotient is the IEEE fp32 quotient (__fdiv_rn).
+//
+// Two entry points: the global scale (a max reduction of |x| with one
+// atomic per warp into the output word, then one thread turns it into g in
+// place) and the block quantizer, which reads g from device memory.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fgq_device.cuh"
+#include "fgq_internal.h"
+#include "fgq_quant.cuh"
+
+namespace fgq {
+namespace {
+
+constexpr int kAmaxThreads = 256;
+
+// Max of the bf16 magnitude bits (non-negative bf16 patterns order like
+// their values) over 16-byte chunks of the rows; one atomicMax per warp.
+template <bool DENSE>
+__global__ void __launch_bounds__(kAmaxThreads)
+    nvfp4_amax_kernel(const uint16_t* __restrict__ x, uint64_t chunks_per_row, uint64_t chunks,
+                      int64_t ldx, unsigned int* __restrict__ out) {
+  uint32_t m = 0;
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kAmaxThreads;
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kAmaxThreads + threadIdx.x; i < chunks;
+       i += stride) {
+    const uint16_t* src;
+    if (DENSE) {
+      src = x + i * 8;
+    } else {
+      const uint64_t r = i / chunks_per_row, c = i - r * chunks_per_row;
+      src = x + static_cast<int64_t>(r) * ldx + c * 8;
+    }
+    const uint32_t p = absmax_pairs(ld_stream_16(src));
+    m = max(m, max(p & 0xFFFFu, p >> 16));
+  }
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  if ((threadIdx.x & 31u) == 0 && m != 0) atomicMax(out, m);
+}
+
+// g = amax / 2688 (1 for amax == 0), written over the magnitude bits.
+__global__ void nvfp4_global_scale_kernel(float* g) {
+  const uint32_t bits = *reinterpret_cast<const uint32_t*>(g);
+  const float amax = __uint_as_float(bits << 16);
+  *g = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+}
+
+// E4M3 code of t >= 0: nearest, ties to even, saturating at 448.
+__device__ __forceinline__ uint32_t e4m3_code(float t) {
+  uint16_t h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(h) : "f"(t));
+  return h & 0xFFu;
+}
+
+// Value of a non-negative E4M3 code (0 .. 0x7E): m 2^-9 for exponent field
+// 0, else (1 + m/8) 2^(e - 7).
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const uint32_t e = c >> 3, m = c & 7u;
+  return e == 0 ? static_cast<float>(m) * 0x1p-9f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// One block of 16 per two lanes (8 elements, 16 bytes each), 16 blocks per
+// warp per round, kNvRounds rounds of loads in flight.
+constexpr int kNvThreads = 256;
+constexpr int kNvRounds = 2;
+
+template <bool DENSE>
+__global__ void __launch_bounds__(kNvThreads)
+    quant_nvfp4_1x16_kernel(const uint16_t* __restrict__ x, uint32_t kb, uint32_t blocks,
+                            int64_t ldx, const float* __restrict__ gptr, uint8_t* __restrict__ xq,
+                            uint8_t* __restrict__ sx) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t sub = lane >> 1, l2 = lane & 1u;
+  const uint32_t warp = (blockIdx.x * kNvThreads + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * kNvThreads) >> 5;
+  constexpr uint32_t kPerWarp = 16 * kNvRounds;
+  const float g = __ldg(gptr);
+  const float d6 = __fmul_rn(6.0f, g);
+  for (uint32_t base = warp * kPerWarp; base < blocks; base += nwarps * kPerWarp) {
+    uint4 v[kNvRounds];
+    uint32_t b[kNvRounds];
+#pragma unroll
+    for (int u = 0; u < kNvRounds; ++u) {
+      b[u] = base + 16 * u + sub;
+      v[u] = make_uint4(0, 0, 0, 0);
+      if (b[u] < blocks) {
+        const uint16_t* src;
+        if (DENSE) {
+          src = x + static_cast<uint64_t>(b[u]) * 16;
+        } else {
+          const uint32_t r = b[u] / kb, c = b[u] - r * kb;
+          src = x + static_cast<int64_t>(r) * ldx + c * 16;
+        }
+        v[u] = ld_stream_16(src + 8 * l2);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kNvRounds; ++u) {
+      uint32_t mx = absmax_pairs(v[u]);
+      mx = __vmaxu2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+      const float amax = __uint_as_float(max(mx & 0xFFFFu, mx >> 16) << 16);
+      const uint32_t sc = e4m3_code(__fdiv_rn(amax, d6));
+      const float d = __fmul_rn(g, e4m3_value(sc));
+      if (b[u] < blocks) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t packed = 0;
+        if (d == 0.0f) {
+          // signed zeros: code 8 where the bf16 sign bit is set
+#pragma unroll
+          for (int p = 0; p < 4; ++p)
+            packed |= (((w[p] >> 12) & 0x8u) | ((w[p] >> 24) & 0x80u)) << (8 * p);
+        } else {
+          float y[8];
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const float2 f = bf16x2_to_f32x2(w[p]);
+            y[2 * p] = __fdiv_rn(f.x, d);
+            y[2 * p + 1] = __fdiv_rn(f.y, d);
+          }
+          packed = cvt_e2m1x8(y);
+        }
+        // row-major [R, K/2]: block b covers bytes 8 b .. 8 b + 7
+        *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(b[u]) * 8 + 4 * l2) = packed;
+        if (l2 == 0) sx[b[u]] = static_cast<uint8_t>(sc);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_nvfp4_global_scale(const void* x, int64_t R, int64_t K, int64_t ldx, float* g,
+                                      cudaStream_t stream, const DeviceInfo& dev) {
+  cudaError_t e = cudaMemsetAsync(g, 0, sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  const uint64_t per_row = static_cast<uint64_t>(K / 8);
+  const uint64_t chunks = static_cast<uint64_t>(R) * per_row;
+  if (chunks > 0) {
+    const bool dense = ldx == K;
+    auto k = dense ? nvfp4_amax_kernel<true> : nvfp4_amax_kernel<false>;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kAmaxThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const uint64_t needed = (chunks + kAmaxThreads - 1) / kAmaxThreads;
+    uint64_t grid = static_cast<uint64_t>(dev.sm_count) * static_cast<uint64_t>(per_sm);
+    if (grid > needed) grid = needed;
+    k<<<static_cast<unsigned>(grid), kAmaxThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(x), per_row, chunks, ldx, reinterpret_cast<unsigned int*>(g));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  nvfp4_global_scale_kernel<<<1, 1, 0, stream>>>(g);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_nvfp4_1x16(const void* x, int64_t R, int64_t K, int64_t ldx,
+                                    const float* g, uint8_t* xq, uint8_t* sx, cudaStream_t stream,
+                                    const DeviceInfo& dev) {
+  const uint32_t kb = static_cast<uint32_t>(K / 16);
+  const uint32_t blocks = static_cast<uint32_t>(R * (K / 16));
+  if (blocks == 0) return cudaSuccess;
+  const bool dense = ldx == K;
+  auto k = dense ? quant_nvfp4_1x16_kernel<true> : quant_nvfp4_1x16_kernel<false>;
+  int per_sm = 0;
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kNvThreads, 0);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) per_sm = 1;
+  const uint32_t per_block = (kNvThreads / 32) * 16 * kNvRounds;
+  const uint32_t needed = (blocks + per_block - 1) / per_block;
+  uint32_t grid = static_cast<uint32_t>(dev.sm_count) * static_cast<uint32_t>(per_sm);
+  if (grid > needed) grid = needed;
+  k<<<grid, kNvThreads, 0, stream>>>(static_cast<const uint16_t*>(x), kb, blocks, ldx, g, xq, sx);
+  return cudaGetLastError();
+}
+
+}  // namespace fgq

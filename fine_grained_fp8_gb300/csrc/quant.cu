@@ -350,21 +350,6 @@ __global__ void __launch_bounds__(kWThreads, 4)
 constexpr int kMxThreads = 256;
 constexpr int kMxRounds = 2;
 
-// Eight fp32 -> eight E2M1 codes in 32 bits: byte j = element 2j (low
-// nibble) and element 2j+1 (high nibble).
-__device__ __forceinline__ uint32_t cvt_e2m1x8(const float (&y)[8]) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
-      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
-      : "=r"(r)
-      : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
-  return r;
-}
-
 // UE8M0 exponent field of the smallest power of two >= amax / 6 (field 0 =
 // 2^-127, the clamp; 127 = 2^0 for a zero group).
 __device__ __forceinline__ uint32_t mx_scale_code(uint32_t mag_bits) {

@@ -246,6 +246,64 @@ fgq_status fgq_gemm_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
                           const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
                           int64_t K, int out, void* stream);
 
+/*
+ * NVFP4 per-tensor (global) scale (§NVFP4 Two-Level Scaling: a value is
+ * global_scale * block_scale * e2m1).  The page gives no encoder; this
+ * library's: g = amax / 2688 over the whole tensor (2688 = 6 * 448, the
+ * largest E2M1 value times the largest E4M3 value, as the FP8 rule
+ * amax / 448 at both levels), 1 for an all-zero tensor; IEEE fp32 division.
+ *
+ *   x    bf16 [R, K], row r at x + r * ldx (ldx >= K, ldx % 8 == 0),
+ *        16-byte aligned.  K % 16 == 0, K > 0, R >= 0 (R == 0 gives 1).
+ *   g    one fp32 in device memory, 4-byte aligned: written with the scale
+ *        (used as scratch for the running maximum until then).
+ * Finite inputs are a precondition.  Asynchronous on `stream`.
+ */
+fgq_status fgq_nvfp4_global_scale(const void* x, int64_t R, int64_t K, int64_t ldx, float* g,
+                                  void* stream);
+
+/*
+ * NVFP4 quantization (§NVFP4 Two-Level Scaling): one E4M3 block scale per 16
+ * consecutive elements of each row, under the per-tensor scale g from
+ * fgq_nvfp4_global_scale (or any positive finite fp32 the caller chooses).
+ * For a GEMM both operands are quantized this way along K (the weight as
+ * its transpose [N, K]).
+ *
+ *   x    bf16 [R, K], row r at x + r * ldx (ldx >= K, ldx % 8 == 0),
+ *        16-byte aligned.
+ *   g    device pointer to the fp32 global scale, 4-byte aligned.
+ *   xq   E2M1 codes [R, K/2] bytes, row-major (dense), 4-byte aligned:
+ *        element 2j of a row in the low nibble of byte j; code bit 3 = sign.
+ *   sx   E4M3 block-scale codes [R, K/16] bytes, row-major (dense).
+ *   K % 16 == 0, K > 0, R >= 0.
+ * Per block: s = E4M3(amax_b / (6 g)) (round to nearest even, saturating
+ * at 448); D = g * s in fp32; each element becomes E2M1(x / D), round to
+ * nearest even, saturating at 6; a block with D == 0 gets signed zeros.
+ * Every quotient is the IEEE fp32 quotient, so codes are exact functions of
+ * the inputs.  Dequantization: g * e4m3(s) * e2m1(q).
+ */
+fgq_status fgq_quant_nvfp4_1x16(const void* x, int64_t R, int64_t K, int64_t ldx, const float* g,
+                                uint8_t* xq, uint8_t* sx, void* stream);
+
+/*
+ * NVFP4 GEMM (§NVFP4 Two-Level Scaling; §When to Use: NVFP4 with E4M3 block
+ * scales for FP4 inference): both operands quantized by
+ * fgq_quant_nvfp4_1x16 along K, the weight as its transpose,
+ *   C[m,n] = gA gB sum_k e2m1(A[m,k]) e4m3(sA[m,k/16]) e2m1(B[n,k]) e4m3(sB[n,k/16])
+ * with the block factors applied by the tensor core (block-scaled FP4 MMA
+ * with E4M3 factors) into an fp32 accumulator, times gA gB (fp32) in the
+ * epilogue.
+ *
+ *   A    E2M1 codes [M, K/2] bytes, 16-byte aligned.   sA  E4M3 codes [M, K/16], 4-byte aligned.
+ *   B    E2M1 codes [N, K/2] bytes, 16-byte aligned.   sB  E4M3 codes [N, K/16], 4-byte aligned.
+ *   gA, gB  device pointers to the two fp32 global scales, 4-byte aligned.
+ *   C    fp32 or bf16 [M, N], row m at C + m * ldc (as _ex).
+ *   K % 128 == 0, N % 128 == 0, K > 0, N > 0, M >= 0.
+ */
+fgq_status fgq_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const float* gA,
+                          const uint8_t* B, const uint8_t* sB, const float* gB, void* C,
+                          int64_t ldc, int64_t M, int64_t N, int64_t K, int out, void* stream);
+
 /* Workspace bytes fgq_gemm_fp8_blockscaled_splitk needs for (M, N, K) on the
  * current device (depends on its SM count).  Same size checks as the GEMM. */
 fgq_status fgq_gemm_splitk_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
