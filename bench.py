@@ -435,6 +435,53 @@ def run_fgq(args):
         if fgq.device_error() != 0:
             raise SystemExit("a kernel reported a device wait timeout")
 
+    # NVFP4 on the same workload: A's per-tensor scale and its E2M1 codes with
+    # an E4M3 scale per 16 every step, the weight quantized once as its
+    # transpose, and the block-scaled FP4 GEMM with E4M3 factors
+    # (tcgen05.mma kind::mxf4nvf4) times the two per-tensor scales.
+    nvfp4 = None
+    if not args.no_nvfp4:
+        nsteps = max(10, min(args.steps, 500))
+        wn4 = [fgq.quant_nvfp4_1x16(b.t().contiguous()) for _, b in sets]
+        an4 = torch.empty((M_, K_ // 2), dtype=torch.uint8, device=dev)
+        sn4 = torch.empty((M_, K_ // 16), dtype=torch.uint8, device=dev)
+        gn4 = torch.empty((1,), dtype=torch.float32, device=dev)
+
+        def nstep(i, ev):
+            a, _ = sets[i % 2]
+            ev[0].record(stream)
+            fgq.nvfp4_global_scale(a, g=gn4)
+            fgq.quant_nvfp4_1x16(a, g=gn4, xq=an4, sx=sn4)
+            ev[1].record(stream)
+            bq4, bs4, bg4 = wn4[i % 2]
+            fgq.gemm_nvfp4(an4, sn4, gn4, bq4, bs4, bg4, torch.bfloat16, out=c)
+            ev[2].record(stream)
+
+        nev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nsteps)]
+        for i in range(5):
+            nstep(i, nev[i])
+        torch.cuda.synchronize()
+        n0 = torch.cuda.Event(enable_timing=True)
+        n1 = torch.cuda.Event(enable_timing=True)
+        n0.record(stream)
+        for i in range(nsteps):
+            nstep(i, nev[i])
+        n1.record(stream)
+        torch.cuda.synchronize()
+        nms = reduce_max(dist, n0.elapsed_time(n1), dev) / nsteps
+        n_act = 1e3 * sum(e[0].elapsed_time(e[1]) for e in nev) / nsteps
+        n_gemm = 1e3 * sum(e[1].elapsed_time(e[2]) for e in nev) / nsteps
+        nvfp4 = {"format": "NVFP4 (E2M1, E4M3 scale per 16 and an fp32 per-tensor scale, "
+                           "both operands along K)",
+                 "steps": nsteps, "ms_per_step": nms,
+                 "value": world * FLOPS_GEMM / (nms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                 "quant_act_us": n_act, "gemm_us": n_gemm,
+                 "gemm_TFLOP/s": FLOPS_GEMM / (n_gemm * 1e-6) / 1e12,
+                 "kernel": "gemm_mxf4_kernel<..., NV> (tcgen05.mma kind::mxf4nvf4.block_scale.scale_vec::4X)"}
+        del wn4, an4, sn4, gn4
+        if fgq.device_error() != 0:
+            raise SystemExit("a kernel reported a device wait timeout")
+
     # The quantizers on the quantize-bandwidth workload (activations
     # [16384, 7168] Student-t nu=3, weight [7168, 7168] N(0, 0.02^2)), each
     # timed alone over rotated input pairs larger than L2.
@@ -448,12 +495,17 @@ def run_fgq(args):
         qaq = torch.empty((QM, QK), dtype=torch.uint8, device=dev)
         qsa = torch.empty((QM, QK // 128), dtype=torch.float32, device=dev)
         quant_bw = {"workload": "quantize-bw: act bf16 [16384,7168] Student-t nu=3 (1x128, 128x1 "
-                                "transposed, MXFP4 1x32); weight bf16 [7168,7168] N(0,0.02^2) (128x128); fp32 scales"}
+                                "transposed, MXFP4 1x32, NVFP4 per-tensor scale and 1x16); weight "
+                                "bf16 [7168,7168] N(0,0.02^2) (128x128); fp32 scales"}
         qsteps = max(10, min(args.steps, 200))
         qaqt = torch.empty((QK, QM), dtype=torch.uint8, device=dev)
         qmx = torch.empty((QM, QK // 2), dtype=torch.uint8, device=dev)
         qmxs = torch.empty((QM, QK // 32), dtype=torch.uint8, device=dev)
         qsat = torch.empty((QK, QM // 128), dtype=torch.float32, device=dev)
+        qnv = torch.empty((QM, QK // 2), dtype=torch.uint8, device=dev)
+        qnvs = torch.empty((QM, QK // 16), dtype=torch.uint8, device=dev)
+        qg = [fgq.nvfp4_global_scale(qa[i]) for i in range(2)]
+        qg_out = torch.empty((1,), dtype=torch.float32, device=dev)
         for name, fn, nbytes in (
                 ("quant_act_1x128", lambda i: fgq.quant_act_1x128(qa[i % 2], "fp32", xq=qaq, sx=qsa),
                  QM * QK * 3 + QM * (QK // 128) * 4),
@@ -461,6 +513,11 @@ def run_fgq(args):
                  QM * QK * 3 + QK * (QM // 128) * 4),
                 ("quant_mxfp4_1x32", lambda i: fgq.quant_mxfp4_1x32(qa[i % 2], xq=qmx, sx=qmxs),
                  QM * QK * 2 + QM * QK // 2 + QM * (QK // 32)),
+                ("nvfp4_global_scale", lambda i: fgq.nvfp4_global_scale(qa[i % 2], g=qg_out),
+                 QM * QK * 2 + 4),
+                ("quant_nvfp4_1x16", lambda i: fgq.quant_nvfp4_1x16(qa[i % 2], g=qg[i % 2], xq=qnv,
+                                                                    sx=qnvs),
+                 QM * QK * 2 + QM * QK // 2 + QM * (QK // 16)),
                 ("quant_w_128x128", lambda i: fgq.quant_w_128x128(qw[i % 2], "fp32", wq=bq, sw=sb),
                  BYTES_QUANT_W)):
             for i in range(5):
@@ -565,7 +622,8 @@ def run_fgq(args):
 
     peaks, src = _peaks()
     if quant_bw:
-        for k in ("quant_act_1x128", "quant_act_128x1", "quant_mxfp4_1x32", "quant_w_128x128"):
+        for k in ("quant_act_1x128", "quant_act_128x1", "quant_mxfp4_1x32", "nvfp4_global_scale",
+                  "quant_nvfp4_1x16", "quant_w_128x128"):
             quant_bw[k]["frac_hbm"] = quant_bw[k]["GB/s"] / peaks["hbm_gbs"]
     if skinny:
         for k, v in skinny.items():
@@ -580,6 +638,12 @@ def run_fgq(args):
         mxfp4["frac_fp4"] = mxfp4["gemm_TFLOP/s"] / fp4_peak
         mxfp4["peak_source"] = f"{src}: 6 x bf16_tflops_sustained (nominal 13.5 / 2.25 PFLOP/s)"
         mxfp4["traffic"] = _traffic("gemm_mxf4", "gemm_mxf4.cu")
+    if nvfp4:
+        fp4_peak = 6.0 * peaks["bf16_tflops_sustained"]
+        nvfp4["peak_fp4"] = fp4_peak
+        nvfp4["frac_fp4"] = nvfp4["gemm_TFLOP/s"] / fp4_peak
+        nvfp4["peak_source"] = f"{src}: 6 x bf16_tflops_sustained (nominal 13.5 / 2.25 PFLOP/s)"
+        nvfp4["traffic"] = _traffic("gemm_nvf4", "gemm_mxf4.cu")
     if ue8m0:
         ue8m0["frac_fp8"] = ue8m0["gemm_TFLOP/s"] / fp8_peak
         ue8m0["traffic"] = _traffic("gemm_mx", "gemm_mx.cu")
@@ -620,6 +684,7 @@ def run_fgq(args):
         "quant_bw": quant_bw,
         "ue8m0": ue8m0,
         "mxfp4": mxfp4,
+        "nvfp4": nvfp4,
         "skinny": skinny,
         "clocks": clk,
         "cpu_baseline": cpu,
@@ -645,6 +710,8 @@ def main(argv=None):
                    help="skip the skinny-GEMM sweep")
     p.add_argument("--no-mxfp4", action="store_true",
                    help="skip the MXFP4 step")
+    p.add_argument("--no-nvfp4", action="store_true",
+                   help="skip the NVFP4 step")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")

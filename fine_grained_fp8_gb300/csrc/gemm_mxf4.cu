@@ -141,12 +141,26 @@ __device__ __forceinline__ void cp_async8(void* smem_dst, const void* gsrc) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Eight consecutive TMEM columns of the warp's 32 lanes, one value each.
-__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
-                   taddr),
-               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
+// 16 / 32 consecutive TMEM columns of the warp's 32 lanes, one value each.
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+      "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]),
+      "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]),
+      "r"(v[30]), "r"(v[31])
+      : "memory");
 }
 
 __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
@@ -402,7 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cp_async_commit();
       };
-      auto store = [&](const uint32_t (&wa)[kCells], const uint32_t (&wb)[kCells][8]) -> bool {
+      // wa: the warp's rows' cells; wb[8 w + j]: cell w of column group j,
+      // which sits at TMEM column 8 w + j of the slot's B part (consecutive)
+      auto store = [&](const uint32_t (&wa)[kCells], const uint32_t (&wb)[8 * kCells]) -> bool {
         const uint32_t r = g_it % kSlots;
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_empty[r], ((g_it / kSlots) & 1u) ^ 1u,
                                                abort_flag, FGQ_DEVERR_SF_SLOT)))
@@ -411,10 +427,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ca = tmem_base + t_lane + kSfaCol0 + kSfaSlot * r + static_cast<uint32_t>(q);
         const uint32_t cb = tmem_base + t_lane + kSfbCol0 + kSfbSlot * r;
 #pragma unroll
-        for (int j = 0; j < kCells; ++j) {
-          tmem_st_32x32b_x1(ca + 4 * j, wa[j]);
-          tmem_st_32x32b_x8(cb + 8 * j, wb[j]);
-        }
+        for (int j = 0; j < kCells; ++j) tmem_st_32x32b_x1(ca + 4 * j, wa[j]);
+        if constexpr (kCells == 4)
+          tmem_st_32x32b_x32(cb, wb);
+        else
+          tmem_st_32x32b_x16(cb, wb);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -433,14 +450,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t* sb = sf_stage + (c & 1) * CF::kSfBufWords + BM * kRowW + lane * kRowW;
 #pragma unroll 1
         for (int st = 0; st < kCh && kCh * c + st < kstages && ok; ++st) {
-          uint32_t wa[kCells], wb[kCells][8];
+          // cell pairs as 8-byte loads (rows of 10 words: no bank conflict
+          // within a half warp)
+          uint32_t wa[kCells], wb[8 * kCells];
 #pragma unroll
-          for (int w = 0; w < kCells; ++w) {
-            wa[w] = sa[kCells * st + w];
+          for (int w = 0; w < kCells; w += 2) {
+            const uint2 a2 = *reinterpret_cast<const uint2*>(sa + kCells * st + w);
+            wa[w] = a2.x;
+            wa[w + 1] = a2.y;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const int jj = j < BN / 32 ? j : j - BN / 32;  // BN = 128: columns 4-7 repeat 0-3
-              wb[w][j] = sb[32 * jj * kRowW + kCells * st + w];
+              const uint2 b2 = *reinterpret_cast<const uint2*>(sb + 32 * jj * kRowW + kCells * st + w);
+              wb[8 * w + j] = b2.x;
+              wb[8 * (w + 1) + j] = b2.y;
             }
           }
           ok = store(wa, wb);
