@@ -37,7 +37,6 @@ constexpr int BK = 128;
 constexpr int kThreads = 512;  // warpgroup 0 control, 1 scale factors, 2-3 epilogue
 constexpr int kEpiWarps = 8;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfBarrier = 1;    // named barrier of the four factor-writer warps
 
 // The two FP4 formats.  MXFP4: one UE8M0 factor per 32 elements, MMA
 // kind::mxf4 with scale_vec::2X (a 32-bit factor cell serves two K = 64
@@ -52,12 +51,18 @@ constexpr uint32_t kSfBarrier = 1;    // named barrier of the four factor-writer
 // w of B at its B base + 8 w (+ 0..7 for the column groups); the factor
 // addresses need only 4-column (A) and 8-column (B) alignment (measured).
 // The writers stage the codes in chunks of 32 bytes per row, kChunkStages
-// stages.
+// stages, in shared memory tiles the issuer copies into the slot with
+// tcgen05.cp.32x128b.warpx4 (32 rows of 16 bytes, row i to lane 32 q + i of
+// every lane quarter q, word j to column j; measured).  A tile of cell c
+// holds, in row i, the cells of rows i, 32 + i, 64 + i, 96 + i of A (of
+// columns 128 h + i + 32 j of B): A's row m lands at lane m, column
+// base + m/32, and B's column n at lane 32 q + n%32, column base + n/32 —
+// the layouts the MMA reads.
 template <bool NV>
 struct Fp4Fmt {
   static constexpr int kBlock = NV ? 16 : 32;      // elements per factor
   static constexpr int kCells = NV ? 4 : 2;        // factor cells per row per stage
-  static constexpr int kSlots = NV ? 4 : 8;
+  static constexpr int kSlots = NV ? 5 : 8;  // >= operand stages + kChunkStages - 1
   static constexpr uint32_t kSfaSlot = 4 * kCells, kSfbSlot = 8 * kCells;
   static constexpr uint32_t kSfaCol0 = 256;        // after the accumulators
   static constexpr uint32_t kSfbCol0 = kSfaCol0 + kSfaSlot * kSlots;
@@ -71,14 +76,21 @@ struct Mxf4Cfg {
   static constexpr int kABytes = BM * BK;
   static constexpr int kBBytes = BN * BK;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kNumBars = 2 * STAGES + 2 * F::kSlots + 2 * kNAcc + 1;
-  // factor staging: two buffers of one chunk's codes (32 bytes a row), rows
-  // padded to 10 words (8-byte aligned cell pairs, two-way bank conflicts
-  // at most when a warp reads one cell of 32 rows)
-  static constexpr int kSfRowWords = 10;
-  static constexpr int kSfBufWords = (BM + BN) * kSfRowWords;
+  static constexpr int kNumBars = 2 * STAGES + 4 + 2 * kNAcc + 1;
+  // factor staging: two chunk buffers of 8 A tiles (one per cell of the
+  // chunk) and 8 BN/128 B tiles; tiles 528 bytes apart (16-byte aligned, and
+  // shifted by four banks so a warp's 4-byte writes to eight tiles at one
+  // row and four words never share a bank)
+  static constexpr int kSfTile = 528;
+  static constexpr int kTilesB = 8 * (BN / 128);
+  static constexpr int kSfBufBytes = (8 + kTilesB) * kSfTile;
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes +
-                                       2 * kSfBufWords * 4 + kNumBars * 8 + 16;
+                                       2 * kSfBufBytes + kNumBars * 8 + 16;
+  // At the first stage s of a chunk the issuer, past the full[] wait of
+  // stage s (whose TMA waited for the MMAs of stage s - STAGES), copies the
+  // factors of stages s .. s + kChunkStages - 1; the slot of stage s + j last
+  // served stage s + j - kSlots <= s - STAGES, whose MMAs have completed.
+  static_assert(F::kSlots >= STAGES + F::kChunkStages - 1, "factor ring too short");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(kNAcc * BN <= static_cast<int>(F::kSfaCol0), "accumulators overlap the scale ring");
   static_assert(F::kSfbCol0 % 8 == 0 && F::kSfbCol0 + F::kSfbSlot * F::kSlots <= kTmemCols,
@@ -128,39 +140,28 @@ __device__ __forceinline__ void umma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
-// 4- and 8-byte asynchronous copies global -> shared (cp.async), the group
-// commit and the wait for all of this thread's groups.
+// tcgen05.cp of a 32-row x 16-byte shared-memory tile to TMEM columns
+// taddr .. taddr + 3 of all four lane quarters, and the no-swizzle
+// descriptor of such a tile (four 8-row core matrices 128 bytes apart).
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+__device__ __forceinline__ uint64_t sf_tile_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128 >> 4) << 32) |
+         (uint64_t{1} << 46);
+}
+
+// 4-byte asynchronous copy global -> shared (cp.async), the group commit,
+// the wait for all of this thread's groups, and the fence that orders this
+// thread's shared-memory writes before later async-proxy (tensor core) reads.
 __device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
                : "memory");
 }
-__device__ __forceinline__ void cp_async8(void* smem_dst, const void* gsrc) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
-               : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// 16 / 32 consecutive TMEM columns of the warp's 32 lanes, one value each.
-__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
-      "%29, %30, %31, %32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
-      "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]),
-      "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]),
-      "r"(v[30]), "r"(v[31])
-      : "memory");
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
@@ -213,12 +214,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sm_a = smem;
   uint8_t* sm_b = smem + STAGES * CF::kABytes;
-  uint32_t* sf_stage = reinterpret_cast<uint32_t*>(sm_b + STAGES * CF::kBBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sf_stage + 2 * CF::kSfBufWords);
+  uint8_t* sf_stage = sm_b + STAGES * CF::kBBytes;  // two chunk buffers of factor tiles
+  uint64_t* full = reinterpret_cast<uint64_t*>(sf_stage + 2 * CF::kSfBufBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* sf_full = empty + STAGES;
-  uint64_t* sf_empty = sf_full + kSlots;
-  uint64_t* acc_full = sf_empty + kSlots;
+  uint64_t* sf_empty = sf_full + 2;
+  uint64_t* acc_full = sf_empty + 2;
   uint64_t* acc_empty = acc_full + NACC;
   uint64_t* drain = acc_empty + NACC;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -237,9 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int r = 0; r < kSlots; ++r) {
-      mbar_init(&sf_full[r], 4);
-      mbar_init(&sf_empty[r], 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sf_full[b], 4);   // one arrival per writer warp
+      mbar_init(&sf_empty[b], 1);  // the issuer's commit after the chunk's MMAs
     }
     for (int b = 0; b < NACC; ++b) {
       mbar_init(&acc_full[b], 1);
@@ -297,8 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dA0 = smem_desc_k_sw128(smem_u32(sm_a));
       const uint32_t a_lo0 = static_cast<uint32_t>(dA0), dhi = static_cast<uint32_t>(dA0 >> 32);
       const uint32_t b_lo0 = static_cast<uint32_t>(smem_desc_k_sw128(smem_u32(sm_b)));
+      const uint32_t sf0 = smem_u32(sf_stage);
       int ls = 0;
-      uint32_t lph = 0, g_it = 0, t_it = 0;
+      uint32_t lph = 0, g_it = 0, t_it = 0, gch = 0;  // gch: factor chunks consumed
       bool ok = true;
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++t_it) {
         const uint32_t buf = t_it % NACC, aph = (t_it / NACC) & 1u;
@@ -306,15 +308,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + buf * BN;
         for (int kc = 0; kc < kstages; ++kc, ++g_it) {
-          const uint32_t r = g_it % kSlots;
-          if (!mbar_wait(&full[ls], lph, abort_flag, FGQ_DEVERR_MMA_FULL) ||
-              !mbar_wait(&sf_full[r], (g_it / kSlots) & 1u, abort_flag, FGQ_DEVERR_MMA_SF)) {
+          const int st = kc % kCh;  // stage within the factor chunk
+          if (!mbar_wait(&full[ls], lph, abort_flag, FGQ_DEVERR_MMA_FULL)) {
             ok = false;
             break;
           }
+          // Factors into their slots, in order before the MMAs that read
+          // them: cell w of A to columns 4 w .. 4 w + 3 of a slot's A part,
+          // cell w of B columns 128 h .. 128 h + 127 to columns 8 w + 4 h ..
+          // + 3 of its B part.  NVFP4 (two-stage chunks) copies a whole
+          // chunk at its first stage and hands the buffer back at once;
+          // MXFP4 copies stage by stage and hands it back after its last
+          // stage's copies, before that stage's MMAs.
+          constexpr bool kBulk = NV;
+          const uint32_t cb = gch & 1u;
+          const bool last = st == kCh - 1 || kc + 1 == kstages;
+          if (st == 0 && !mbar_wait(&sf_full[cb], (gch >> 1) & 1u, abort_flag, FGQ_DEVERR_MMA_SF)) {
+            ok = false;
+            break;
+          }
+          if (!kBulk || st == 0) {
+            tc_fence_after();
+            const uint32_t tiles = sf0 + cb * CF::kSfBufBytes;
+            const int j0 = kBulk ? 0 : st;
+            const int j1 = kBulk ? (kstages - kc < kCh ? kstages - kc : kCh) : st + 1;
+            for (int j = j0; j < j1; ++j) {
+              const uint32_t rj = (g_it + (j - st)) % kSlots;
+#pragma unroll
+              for (int w = 0; w < kCells; ++w) {
+                const int cc = j * kCells + w;
+                tmem_cp_32x128b_x4(tmem_base + kSfaCol0 + kSfaSlot * rj + 4 * w,
+                                   sf_tile_desc(tiles + cc * CF::kSfTile));
+#pragma unroll
+                for (int h = 0; h < BN / 128; ++h)
+                  tmem_cp_32x128b_x4(tmem_base + kSfbCol0 + kSfbSlot * rj + 8 * w + 4 * h,
+                                     sf_tile_desc(tiles + (8 + cc * (BN / 128) + h) * CF::kSfTile));
+              }
+            }
+            if (kBulk || last) umma_commit(&sf_empty[cb]);
+          }
+          if (last) ++gch;
           tc_fence_after();
           const uint32_t a_lo = a_lo0 + ls * (CF::kABytes >> 4);
           const uint32_t b_lo = b_lo0 + ls * (CF::kBBytes >> 4);
+          const uint32_t r = g_it % kSlots;
           const uint32_t sfa = tmem_base + kSfaCol0 + kSfaSlot * r;
           const uint32_t sfb = tmem_base + kSfbCol0 + kSfbSlot * r;
           // four K = 64 MMAs (32 bytes of each row apart); a final half
@@ -344,7 +381,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sfa + 4, sfb + 8, 1u);
             }
           }
-          umma_commit(&sf_empty[r]);
           umma_commit(&empty[ls]);
           if (++ls == STAGES) {
             ls = 0;
@@ -362,119 +398,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 4 && warp < 8) {
     // ---------------- scale-factor writers ----------------
     // The factors of a tile's rows (columns) are one contiguous block of
-    // BM (BN) rows of kg codes.  The four warps copy one chunk of it at a
-    // time (32 bytes of each row: four MXFP4 or two NVFP4 stages) into a
-    // shared-memory buffer with
-    // coalesced asynchronous copies (whole 32-byte sectors per warp
-    // instruction), then each warp reads the cells of its 32 rows (and of
-    // all BN columns, which every lane quarter of B needs) from there.
-    // Chunk c + 1 is in flight while chunk c's slots are written.  Codes
-    // past a row's end (the final partial chunk) and rows past M are not
-    // copied: their cells feed only the unused second half of a final half
-    // stage's cells or accumulator rows that are never stored.  A warp that gives
-    // up on a wait keeps walking the same chunks and barriers (skipping the
-    // slot work) so that the others never wait for it at a named barrier.
-    constexpr int kRowW = CF::kSfRowWords;
-    constexpr int kNA = BM * 8 / 128, kNB = BN * 8 / 128;  // words per thread per chunk
-    const int q = warp & 3;
-    const int wt = threadIdx.x - 128;
-    const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
-    const int nchunks = (kstages + kCh - 1) / kCh;
-    uint32_t g_it = 0;
+    // BM (BN) rows of kg codes.  Per chunk (32 bytes of every row) the four
+    // warps copy each 4-byte cell with cp.async straight into its place in
+    // the chunk buffer's tiles: lane l takes cell l % 8 of the chunk and row
+    // quarter l / 8, so a warp instruction reads whole 32-byte sectors of
+    // four rows and writes 32 different banks.  Then wait for the copies,
+    // fence them to the async proxy (the tensor core reads the tiles) and
+    // arrive on the buffer's full barrier.  Codes past a row's end (the final
+    // partial chunk) and rows past M are not copied: they feed only unused
+    // factor bytes of a final half stage or accumulator rows never stored.
+    const int wq = warp & 3;
+    const int c8 = lane & 7, kq = lane >> 3;
+    uint32_t gch = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
       const int tm = tile % m_tiles, tn = tile / m_tiles;
       const uint8_t* a_blk = sA + static_cast<int64_t>(tm) * BM * kg;
       const uint8_t* b_blk = sB + static_cast<int64_t>(tn) * BN * kg;
       const int a_rows = M - tm * BM < BM ? M - tm * BM : BM;
-      // 8-byte copies (rows of a multiple of 8 codes, 8-byte aligned
-      // arrays): thread wt copies cells 2 (wt % 4) and 2 (wt % 4) + 1 of rows
-      // wt / 4 + 32 i; else 4-byte copies: cell wt % 8 of rows wt / 8 + 16 i.
-      const bool pairs = (kg & 7) == 0 && ((reinterpret_cast<uintptr_t>(sA) |
-                                            reinterpret_cast<uintptr_t>(sB)) & 7) == 0;
-      const int cell = pairs ? 2 * (wt & 3) : wt & 7, row0 = pairs ? wt >> 2 : wt >> 3;
-      const uint8_t* a_src = a_blk + row0 * kg + 4 * cell;
-      const uint8_t* b_src = b_blk + row0 * kg + 4 * cell;
-      const int dst0 = row0 * kRowW + cell;
-      auto fetch = [&](int c) {
-        uint32_t* sa = sf_stage + (c & 1) * CF::kSfBufWords + dst0;
-        uint32_t* sb = sf_stage + (c & 1) * CF::kSfBufWords + BM * kRowW + dst0;
-        if (32 * c + 4 * cell < kg) {
-          if (pairs) {
+      const int nchunks = (kstages + kCh - 1) / kCh;
+      for (int c = 0; c < nchunks; ++c, ++gch) {
+        const uint32_t cb = gch & 1u;
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_empty[cb], ((gch >> 1) & 1u) ^ 1u, abort_flag,
+                                               FGQ_DEVERR_SF_SLOT))) {
+          ok = false;
+          break;
+        }
+        uint8_t* tiles = sf_stage + cb * CF::kSfBufBytes;
+        const int byte = 32 * c + 4 * c8;
+        if (byte < kg) {
 #pragma unroll
-            for (int i = 0; i < kNA / 2; ++i)
-              if (row0 + 32 * i < a_rows) cp_async8(sa + 32 * i * kRowW, a_src + 32 * i * kg + 32 * c);
+          for (int i = 0; i < 8; ++i) {  // A rows m = r + 32 kq, r = wq + 4 i
+            const int r = wq + 4 * i, m = r + 32 * kq;
+            if (m < a_rows) cp_async4(tiles + c8 * CF::kSfTile + 16 * r + 4 * kq, a_blk + m * kg + byte);
+          }
 #pragma unroll
-            for (int i = 0; i < kNB / 2; ++i) cp_async8(sb + 32 * i * kRowW, b_src + 32 * i * kg + 32 * c);
-          } else {
-#pragma unroll
-            for (int i = 0; i < kNA; ++i)
-              if (row0 + 16 * i < a_rows) cp_async4(sa + 16 * i * kRowW, a_src + 16 * i * kg + 32 * c);
-#pragma unroll
-            for (int i = 0; i < kNB; ++i) cp_async4(sb + 16 * i * kRowW, b_src + 16 * i * kg + 32 * c);
+          for (int i = 0; i < BN / 16; ++i) {  // B columns n = 128 h + 32 kq + r
+            const int r = wq + 4 * (i % 8), h = i / 8, n = 128 * h + 32 * kq + r;
+            cp_async4(tiles + (8 + c8 * (BN / 128) + h) * CF::kSfTile + 16 * r + 4 * kq,
+                      b_blk + n * kg + byte);
           }
         }
         cp_async_commit();
-      };
-      // wa: the warp's rows' cells; wb[8 w + j]: cell w of column group j,
-      // which sits at TMEM column 8 w + j of the slot's B part (consecutive)
-      auto store = [&](const uint32_t (&wa)[kCells], const uint32_t (&wb)[8 * kCells]) -> bool {
-        const uint32_t r = g_it % kSlots;
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&sf_empty[r], ((g_it / kSlots) & 1u) ^ 1u,
-                                               abort_flag, FGQ_DEVERR_SF_SLOT)))
-          return false;
-        tc_fence_after();
-        const uint32_t ca = tmem_base + t_lane + kSfaCol0 + kSfaSlot * r + static_cast<uint32_t>(q);
-        const uint32_t cb = tmem_base + t_lane + kSfbCol0 + kSfbSlot * r;
-#pragma unroll
-        for (int j = 0; j < kCells; ++j) tmem_st_32x32b_x1(ca + 4 * j, wa[j]);
-        if constexpr (kCells == 4)
-          tmem_st_32x32b_x32(cb, wb);
-        else
-          tmem_st_32x32b_x16(cb, wb);
-        tmem_wait_st();
-        tc_fence_before();
+        cp_async_wait_all();
+        fence_proxy_async();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sf_full[r]);
-        ++g_it;
-        return true;
-      };
-      // every warp has read the previous tile's last chunk (which may sit
-      // in buffer 0) before any warp refills buffer 0
-      named_barrier_sync(kSfBarrier, 128);
-      fetch(0);
-      cp_async_wait_all();
-      named_barrier_sync(kSfBarrier, 128);
-      for (int c = 0; c < nchunks; ++c) {
-        const uint32_t* sa = sf_stage + (c & 1) * CF::kSfBufWords + (32 * q + lane) * kRowW;
-        const uint32_t* sb = sf_stage + (c & 1) * CF::kSfBufWords + BM * kRowW + lane * kRowW;
-#pragma unroll 1
-        for (int st = 0; st < kCh && kCh * c + st < kstages && ok; ++st) {
-          // cell pairs as 8-byte loads (rows of 10 words: no bank conflict
-          // within a half warp)
-          uint32_t wa[kCells], wb[8 * kCells];
-#pragma unroll
-          for (int w = 0; w < kCells; w += 2) {
-            const uint2 a2 = *reinterpret_cast<const uint2*>(sa + kCells * st + w);
-            wa[w] = a2.x;
-            wa[w + 1] = a2.y;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int jj = j < BN / 32 ? j : j - BN / 32;  // BN = 128: columns 4-7 repeat 0-3
-              const uint2 b2 = *reinterpret_cast<const uint2*>(sb + 32 * jj * kRowW + kCells * st + w);
-              wb[8 * w + j] = b2.x;
-              wb[8 * (w + 1) + j] = b2.y;
-            }
-          }
-          ok = store(wa, wb);
-          // chunk c + 1 goes into buffer (c + 1) & 1, which held chunk
-          // c - 1: every warp finished reading it before the last barrier
-          if (st == 0 && c + 1 < nchunks) fetch(c + 1);
-        }
-        if (c + 1 < nchunks) {
-          cp_async_wait_all();
-          named_barrier_sync(kSfBarrier, 128);
-        }
+        if (lane == 0) mbar_arrive(&sf_full[cb]);
       }
     }
   } else if (warp >= 8) {
@@ -580,15 +549,19 @@ cudaError_t launch_fp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B, co
                        int64_t N, int64_t K, int out_bf16, cudaStream_t stream,
                        const DeviceInfo& dev) {
   if (M == 0 || N == 0) return cudaSuccess;
+  // 128-column tiles: six operand stages, or fewer as the factor ring needs
+  constexpr int kNarrow = Fp4Fmt<NV>::kSlots - Fp4Fmt<NV>::kChunkStages + 1 < 6
+                              ? Fp4Fmt<NV>::kSlots - Fp4Fmt<NV>::kChunkStages + 1
+                              : 6;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
   const int64_t tiles256 = ((M + BM - 1) / BM) * (N / 256);
   const bool wide = (N % 256 == 0) && tiles256 >= dev.sm_count;
   if (out_bf16) {
     return wide ? launch_mxf4_cfg<256, 4, true, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, stream, dev)
-                : launch_mxf4_cfg<128, 6, true, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, stream, dev);
+                : launch_mxf4_cfg<128, kNarrow, true, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, stream, dev);
   }
   return wide ? launch_mxf4_cfg<256, 4, false, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, stream, dev)
-              : launch_mxf4_cfg<128, 6, false, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, stream, dev);
+              : launch_mxf4_cfg<128, kNarrow, false, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, stream, dev);
 }
 
 }  // namespace
