@@ -118,3 +118,84 @@ def test_product_path_has_no_oracle_dependency():
                 src = fh.read()
             assert not re.search(r"^\s*(import|from)\s+fine_grained_fp8_gb300\b", src, re.M), f
             assert "libfgq" not in src, f
+
+
+@pytest.mark.parametrize("args", [
+    (0, 256, 128, 128, P, P, 0, None),       # null x
+    (P, 200, 128, 128, P, P, 0, None),       # M % 128
+    (P, 256, 100, 128, P, P, 0, None),       # K % 128
+    (P, 256, 128, 120, P, P, 0, None),       # ldx < K
+    (P, 256, 128, 128, P + 8, P, 0, None),   # xqt misaligned
+    (P, 256, 128, 128, P, P, 5, None),       # bad mode
+])
+def test_quant_128x1_rejects(fgq, args):
+    assert _lib.fgq_quant_act_128x1(*args) == _lib.FGQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args", [
+    (0, 4, 64, 64, P, P, None),              # null x
+    (P, 4, 48, 64, P, P, None),              # K % 32
+    (P, -1, 64, 64, P, P, None),             # R < 0
+    (P, 4, 64, 60, P, P, None),              # ldx < K
+    (P + 2, 4, 64, 64, P, P, None),          # x misaligned
+    (P, 4, 64, 64, P + 2, P, None),          # xq misaligned
+])
+def test_quant_mxfp4_rejects(fgq, args):
+    assert _lib.fgq_quant_mxfp4_1x32(*args) == _lib.FGQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args", [
+    (0, 4, 64, 64, P, None),                 # null x
+    (P, 4, 40, 64, P, None),                 # K % 16
+    (P, 4, 64, 64, 0, None),                 # null g
+    (P, 4, 64, 60, P, None),                 # ldx < K
+    (P, 4, 64, 64, P + 2, None),             # g misaligned
+])
+def test_nvfp4_global_scale_rejects(fgq, args):
+    assert _lib.fgq_nvfp4_global_scale(*args) == _lib.FGQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args", [
+    (0, 4, 64, 64, P, P, P, None),           # null x
+    (P, 4, 40, 64, P, P, P, None),           # K % 16
+    (P, 4, 64, 64, 0, P, P, None),           # null g
+    (P, 4, 64, 64, P, P + 2, P, None),       # xq misaligned
+    (P, 4, 64, 68, P, P, P, None),           # ldx % 8
+])
+def test_quant_nvfp4_rejects(fgq, args):
+    assert _lib.fgq_quant_nvfp4_1x16(*args) == _lib.FGQ_ERR_INVALID_ARG
+
+
+def test_fp4_quantizers_empty_is_ok(fgq):
+    assert _lib.fgq_quant_mxfp4_1x32(0, 0, 64, 64, 0, 0, None) == _lib.FGQ_OK
+    assert _lib.fgq_quant_nvfp4_1x16(0, 0, 64, 64, 0, 0, 0, None) == _lib.FGQ_OK
+
+
+@pytest.mark.parametrize("args", [
+    (0, P, P, P, P, 256, 128, 256, 256, 0, None),      # null A
+    (P, P, P, P, P, 256, 128, 256, 192, 0, None),      # K % 128
+    (P, P, P, P, P, 256, 128, 192, 256, 0, None),      # N % 128
+    (P, P, P, P, P, 200, 128, 256, 256, 0, None),      # ldc < N
+    (P, P, P, P, P, 256, 128, 256, 256, 3, None),      # bad out dtype
+    (P + 8, P, P, P, P, 256, 128, 256, 256, 0, None),  # A misaligned
+    (P, P + 2, P, P, P, 256, 128, 256, 256, 0, None),  # sA misaligned
+])
+def test_gemm_mxfp4_rejects(fgq, args):
+    assert _lib.fgq_gemm_mxfp4(*args) == _lib.FGQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args", [
+    (P, P, 0, P, P, P, P, 256, 128, 256, 256, 0, None),      # null gA
+    (P, P, P, P, P, 0, P, 256, 128, 256, 256, 0, None),      # null gB
+    (P, P, P, P, P, P, P, 256, 128, 256, 192, 0, None),      # K % 128
+    (P, P, P, P, P, P, P, 256, 128, 256, 256, 2, None),      # bad out dtype
+    (P, P, P + 2, P, P, P, P, 256, 128, 256, 256, 0, None),  # gA misaligned
+    (P, P, P, P, P, P, P + 4, 256, 128, 256, 256, 0, None),  # C misaligned
+])
+def test_gemm_nvfp4_rejects(fgq, args):
+    assert _lib.fgq_gemm_nvfp4(*args) == _lib.FGQ_ERR_INVALID_ARG
+
+
+def test_fp4_gemms_empty_is_ok(fgq):
+    assert _lib.fgq_gemm_mxfp4(0, 0, 0, 0, 0, 256, 0, 256, 256, 0, None) == _lib.FGQ_OK
+    assert _lib.fgq_gemm_nvfp4(0, 0, 0, 0, 0, 0, 0, 256, 0, 256, 256, 0, None) == _lib.FGQ_OK
