@@ -18,8 +18,8 @@
 //
 // Same structure as the power-of-two FP8 kernel (gemm_mx.cu): persistent
 // CTAs on 128 x BN tiles, warp 0 TMA producer (one 128-byte stage = 256
-// elements of K), warp 1 MMA issuer (four MMAs per stage), warps 4-7 write
-// the factors into a TMEM ring (one slot per stage), warps 8-15 epilogue.
+// elements of K), warp 1 MMA issuer (factor copies, four MMAs per stage),
+// warps 4-7 stage the factors in shared memory, warps 8-15 epilogue.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
