@@ -350,9 +350,59 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+namespace {
+
+// Recently encoded descriptors, keyed by everything the encoding depends
+// on (base address, rows, K, box rows).  A descriptor holds no device
+// state, only the address and geometry, so an entry stays valid even if
+// the memory behind it is freed and reallocated at the same address.
+struct MapCacheEntry {
+  const void* base;
+  int64_t rows, K;
+  int box_rows;
+  bool valid;
+  CUtensorMap map;
+};
+constexpr int kMapCacheSize = 64;
+MapCacheEntry g_map_cache[kMapCacheSize];
+int g_map_cache_next = 0;
+std::mutex g_map_cache_mu;
+
+bool encode_k_major_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                        int box_rows);
+
+}  // namespace
+
 // K-major E4M3 operand [rows, K] (row stride K bytes), box 128 (K) x box_rows,
-// 128-byte swizzle, out-of-range rows read as zero.
+// 128-byte swizzle, out-of-range rows read as zero.  Served from a small
+// cache of recent descriptors (the host-side encoding then runs once per
+// operand, not once per call).
 bool make_k_major_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
+  {
+    std::lock_guard<std::mutex> lock(g_map_cache_mu);
+    for (const MapCacheEntry& e : g_map_cache)
+      if (e.valid && e.base == base && e.rows == rows && e.K == K && e.box_rows == box_rows) {
+        *map = e.map;
+        return true;
+      }
+  }
+  if (!encode_k_major_map(map, base, rows, K, box_rows)) return false;
+  std::lock_guard<std::mutex> lock(g_map_cache_mu);
+  MapCacheEntry& e = g_map_cache[g_map_cache_next];
+  g_map_cache_next = (g_map_cache_next + 1) % kMapCacheSize;
+  e.base = base;
+  e.rows = rows;
+  e.K = K;
+  e.box_rows = box_rows;
+  e.map = *map;
+  e.valid = true;
+  return true;
+}
+
+namespace {
+
+bool encode_k_major_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                        int box_rows) {
   auto encode = tensor_map_encoder();
   if (!encode) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
@@ -365,6 +415,8 @@ bool make_k_major_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
   return r == CUDA_SUCCESS;
 }
 
+}  // namespace
+
 namespace {
 
 template <int BN, int STAGES, bool OUT_BF16>
@@ -373,27 +425,25 @@ cudaError_t launch_cfg(const uint8_t* A, const float* sA, const uint8_t* B, cons
                        const DeviceInfo& dev) {
   using CF = Cfg<BN, STAGES>;
   auto kern = gemm_fp8_blockscaled_kernel<BN, STAGES, OUT_BF16>;
-  static bool attr_set[64] = {};
+  static bool ready[64] = {};
   static std::mutex mu;
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (dev.device < 64 && !attr_set[dev.device]) {
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    if (!ready[dev.device]) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(CF::kSmemBytes));
       if (e != cudaSuccess) return e;
-      attr_set[dev.device] = true;
+      // The setmaxnreg split assumes every thread is launched with
+      // kLaunchRegs registers; with fewer the epilogue's increase could
+      // never be granted.
+      cudaFuncAttributes attr;
+      e = cudaFuncGetAttributes(&attr, kern);
+      if (e != cudaSuccess) return e;
+      if (attr.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+      ready[dev.device] = true;
     }
   }
-  // The setmaxnreg split assumes every thread is launched with kLaunchRegs
-  // registers; with fewer the epilogue's increase could never be granted.
-  static int launch_regs = -1;
-  if (launch_regs < 0) {
-    cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, kern);
-    if (e != cudaSuccess) return e;
-    launch_regs = attr.numRegs;
-  }
-  if (launch_regs != kLaunchRegs) return cudaErrorInvalidConfiguration;
   CUtensorMap ta, tb;
   if (!make_k_major_map(&ta, A, M, K, BM) || !make_k_major_map(&tb, B, N, K, BN))
     return cudaErrorInvalidValue;

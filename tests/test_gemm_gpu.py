@@ -5,10 +5,13 @@ accumulator satisfies
     |C - C_ref| <= 2e-3 * sum_k |a_hat[m,k]| |b_hat[k,n]|
 where C_ref is the fp64 product of the dequantised operands; a bf16 output
 may differ from that accumulator by its own rounding, half a bf16 ulp
-(2^-8 of the value), which the bf16 cases add to the bound.  Small cases
-are compared element by element against the full oracle; full-size cases
-on sampled outputs the oracle computes one by one, plus a full-matrix check
-of the same bound against an fp32 torch product of dequantised operands.
+(2^-8 of the value), which the bf16 cases add to the bound.  Every case is
+compared element by element against the oracle on the whole output; the
+full-size ones spread the oracle over the host's cores (oracle.threads).
+The workloads' own configurations (tiny, outlier, large prefill, skinny)
+run the whole path: the GPU quantizers on the workload's inputs, checked
+bit for bit against the oracle's codes and scales, then the GPU GEMM on
+those codes.
 """
 import numpy as np
 import pytest
@@ -16,6 +19,7 @@ import torch
 
 import fgq_inputs
 import oracle
+from oracle.threads import gemm_dequant_parallel
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +45,7 @@ def _run(fgq, ops, out_dtype, mode_name, out=None):
 
 
 def _check_full(c_gpu, aq, sa, bq, sb):
-    cref, tref = oracle.gemm_dequant(aq, sa, bq, sb)
+    cref, tref = gemm_dequant_parallel(aq, sa, bq, sb)
     c = c_gpu.float().cpu().numpy().astype(np.float64)
     ok, ratio = oracle.gemm_within_tolerance(c, cref, tref, TOL,
                                              out_bf16=c_gpu.dtype == torch.bfloat16)
@@ -49,47 +53,20 @@ def _check_full(c_gpu, aq, sa, bq, sb):
     return ratio
 
 
-def _check_sampled(c_gpu, aq, sa, bq, sb, n_samples=3000, seed=0):
-    M, N = c_gpu.shape
-    rng = np.random.default_rng(seed)
-    rows = rng.integers(0, M, n_samples)
-    cols = rng.integers(0, N, n_samples)
-    # always include the corners and the last (possibly ragged) rows
-    rows = np.concatenate([rows, [0, 0, M - 1, M - 1]])
-    cols = np.concatenate([cols, [0, N - 1, 0, N - 1]])
-    cref, tref = oracle.gemm_dequant_at(aq, sa, bq, sb, rows, cols)
-    c = c_gpu.float().cpu().numpy()[rows, cols].astype(np.float64)
-    ok, ratio = oracle.gemm_within_tolerance(c, cref, tref, TOL,
-                                             out_bf16=c_gpu.dtype == torch.bfloat16)
-    assert ok, f"sampled max |err|/T = {ratio:.3e} exceeds {TOL}"
-    return ratio
-
-
-def _check_full_vs_torch(c_gpu, ops):
-    """Every element against an fp32 (no TF32) torch product of the
-    dequantised operands, with the same bound."""
-    aq, sa, bq, sb = ops
-    M, K = aq.shape
-    N = bq.shape[0]
-    old = torch.backends.cuda.matmul.allow_tf32
-    torch.backends.cuda.matmul.allow_tf32 = False
-    try:
-        ah = aq.view(torch.float8_e4m3fn).float() * sa.repeat_interleave(128, dim=1)
-        bh = bq.view(torch.float8_e4m3fn).float() * sb.t().repeat_interleave(128, 0).repeat_interleave(128, 1)
-        cref = ah @ bh.t()
-        tref = ah.abs() @ bh.abs().t()
-    finally:
-        torch.backends.cuda.matmul.allow_tf32 = old
-    err = (c_gpu.float() - cref).abs()
-    # the fp32 reference itself carries K * 2^-24 relative error of T; a bf16
-    # output adds its own rounding (half an ulp: 2^-8 of the value)
-    bound = TOL * tref + K * 2.0 ** -24 * tref
-    if c_gpu.dtype == torch.bfloat16:
-        bound = bound + 2.0 ** -8 * (cref.abs() + bound)
-    assert torch.isfinite(c_gpu.float()).all()
-    worst = (err / tref.clamp_min(1e-30)).max().item()
-    assert bool((err <= bound).all()), f"max |err|/T = {worst:.3e}"
-    return worst
+def _gpu_quantized(fgq, a, b, mode, dev):
+    """The GPU quantizers on the workload's bf16 inputs, their codes and
+    scales checked bit for bit against the oracle's; returns the device
+    operands and the oracle's host operands (weight codes logical [K, N])."""
+    name, mid = mode
+    aq, sa = fgq.quant_act_1x128(a.to(dev), name)
+    bq, sb = fgq.quant_w_128x128(b.to(dev), name)
+    torch.cuda.synchronize()
+    host = _oracle_operands(a, b, mid)
+    got = (aq.cpu().numpy(), sa.cpu().numpy(), np.ascontiguousarray(bq.cpu().numpy().T),
+           sb.cpu().numpy())
+    for g, h, what in zip(got, host, ("A codes", "A scales", "B codes", "B scales")):
+        assert np.array_equal(g.view(np.uint8), h.view(np.uint8)), f"GPU {what} differ from the oracle"
+    return (aq, sa, bq, sb), host
 
 
 MODES = [("fp32", oracle.MODE_FP32), ("ue8m0", oracle.MODE_UE8M0)]
@@ -103,12 +80,21 @@ def test_tiny_config(fgq, cuda_dev):
     _check_full(c, *host)
 
 
+def test_tiny_config_whole_path(fgq, cuda_dev):
+    """The tiny workload through the GPU quantizers and the GEMM."""
+    a, b = fgq_inputs.tiny(seed=0)
+    ops, host = _gpu_quantized(fgq, a, b, MODES[0], cuda_dev)
+    c = _run(fgq, ops, torch.float32, "fp32")
+    _check_full(c, *host)
+
+
 @pytest.mark.parametrize("mode", MODES, ids=lambda m: m[0])
 def test_outlier_config(fgq, cuda_dev, mode):
-    """M = N = K = 1024, N(0, 1) with 0.1% of entries x100, fp32 C."""
+    """M = N = K = 1024, N(0, 1) with 0.1% of entries x100, fp32 C: the GPU
+    quantizers on the workload's own inputs, then the GEMM."""
     a, b = fgq_inputs.outlier_gemm(1024, seed=0)
-    host = _oracle_operands(a, b, mode[1])
-    c = _run(fgq, _to_dev(*host, cuda_dev), torch.float32, mode[0])
+    ops, host = _gpu_quantized(fgq, a, b, mode, cuda_dev)
+    c = _run(fgq, ops, torch.float32, mode[0])
     _check_full(c, *host)
 
 
@@ -167,28 +153,24 @@ def test_end_to_end_quantize_then_gemm(fgq, cuda_dev, mode):
 @pytest.mark.parametrize("mode", MODES, ids=lambda m: m[0])
 def test_large_prefill_full_size(fgq, cuda_dev, mode):
     """A [4096, 7168] N(0,1), B [7168, 7168] N(0,0.02^2), bf16 C, through the
-    GPU quantizers, in the configuration the benchmark times."""
+    GPU quantizers, in the configuration the benchmark times; every one of
+    the 29.4 M outputs against the oracle."""
     a, b = fgq_inputs.large_prefill(seed=0)
-    aq, sa = fgq.quant_act_1x128(a.to(cuda_dev), mode[0])
-    bq, sb = fgq.quant_w_128x128(b.to(cuda_dev), mode[0])
-    c = _run(fgq, (aq, sa, bq, sb), torch.bfloat16, mode[0])
-    host = (aq.cpu().numpy(), sa.cpu().numpy(), np.ascontiguousarray(bq.cpu().numpy().T),
-            sb.cpu().numpy())
-    oq, osa = oracle.quant_act_1x128(a, mode[1])
-    assert np.array_equal(host[0], oq) and np.array_equal(host[1], osa)
-    _check_sampled(c, *host, n_samples=4000)
-    _check_full_vs_torch(c, (aq, sa, bq, sb))
+    ops, host = _gpu_quantized(fgq, a, b, mode, cuda_dev)
+    c = _run(fgq, ops, torch.bfloat16, mode[0])
+    _check_full(c, *host)
 
 
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: m[0])
 @pytest.mark.parametrize("M", [16, 64, 256])
-def test_skinny_full_size(fgq, cuda_dev, M):
-    """M x N=24576 x K=1536, bf16 C (the low-M path)."""
+def test_skinny_full_size(fgq, cuda_dev, mode, M):
+    """M x N=24576 x K=1536, bf16 C (the low-M paths): the GPU quantizers on
+    the workload's own inputs, then the GEMM, every output against the
+    oracle."""
     a, b = fgq_inputs.skinny(M, seed=0)
-    host = _oracle_operands(a, b, oracle.MODE_FP32)
-    ops = _to_dev(*host, cuda_dev)
-    c = _run(fgq, ops, torch.bfloat16, "fp32")
-    _check_sampled(c, *host, n_samples=4000, seed=M)
-    _check_full_vs_torch(c, ops)
+    ops, host = _gpu_quantized(fgq, a, b, mode, cuda_dev)
+    c = _run(fgq, ops, torch.bfloat16, mode[0])
+    _check_full(c, *host)
 
 
 def test_repeat_calls_are_deterministic(fgq, cuda_dev):

@@ -15,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import fgq_inputs
 import oracle
 from golden_io import e4m3_codes, quant_groups
 
@@ -624,3 +625,19 @@ def test_nvfp4_gemm_matches_numpy_page_dequant():
     af = a.float().numpy().astype(np.float64)
     d = np.repeat(float(ga) * torch.from_numpy(sa.copy()).view(torch.float8_e4m3fn).double().numpy(), 16, axis=1)
     assert np.all(np.abs(ah - af) <= 2.0 * d + 1e-300)
+
+
+def test_parallel_gemm_reference_is_the_whole_matrix_call():
+    """oracle.threads only slices the output by column blocks and runs the
+    oracle on each slice: its (C, T) equal one whole-matrix call bit for
+    bit, for any slice width and thread count."""
+    from oracle.threads import gemm_dequant_parallel
+    a = fgq_inputs.outlier((70, 384), 1e-2, 100.0, seed=21)
+    b = fgq_inputs.exponent_spread((384, 640), 6, 128, seed=22)
+    aq, sa = oracle.quant_act_1x128(a)
+    bq, sb = oracle.quant_w_128x128(b)
+    c, t = oracle.gemm_dequant(aq, sa, bq, sb)
+    for workers, per in ((1, 1), (3, 1), (4, 2), (2, 5)):
+        cp, tp = gemm_dequant_parallel(aq, sa, bq, sb, workers=workers, blocks_per_task=per)
+        assert np.array_equal(cp.view(np.uint64), c.view(np.uint64))
+        assert np.array_equal(tp.view(np.uint64), t.view(np.uint64))

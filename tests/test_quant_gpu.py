@@ -203,5 +203,31 @@ def test_full_size_skinny_weight(fgq, cuda_dev, mode):
     _assert_w_parity(fgq, w, mode, cuda_dev)
 
 
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: m[0])
+def test_tiny_config_quantizers(fgq, cuda_dev, mode):
+    """The tiny workload's own inputs: A [128, 256] and B [256, 128], N(0, 1)."""
+    a, b = fgq_inputs.tiny(seed=0)
+    _assert_act_parity(fgq, a, mode, cuda_dev)
+    _assert_w_parity(fgq, b, mode, cuda_dev)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: m[0])
+def test_outlier_config_quantizers(fgq, cuda_dev, mode):
+    """The outlier workload's own inputs, both scale modes: A and B [1024,
+    1024] N(0, 1) with 0.1% of entries x100 at seeded positions."""
+    a, b = fgq_inputs.outlier_gemm(1024, seed=0)
+    _assert_act_parity(fgq, a, mode, cuda_dev)
+    _assert_w_parity(fgq, b, mode, cuda_dev)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: m[0])
+@pytest.mark.parametrize("M", [16, 64, 256])
+def test_skinny_config_activations(fgq, cuda_dev, mode, M):
+    """The skinny sweep's own activations, A [M, 1536] N(0, 1) (its weight
+    is covered by test_full_size_skinny_weight)."""
+    a, _ = fgq_inputs.skinny(M, seed=0)
+    _assert_act_parity(fgq, a, mode, cuda_dev)
+
+
 def test_no_device_error(fgq, cuda_dev):
     assert fgq.device_error() == 0
