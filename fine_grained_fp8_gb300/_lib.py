@@ -23,6 +23,9 @@ FGQ_SCALE_UE8M0 = 1
 FGQ_OUT_F32 = 0
 FGQ_OUT_BF16 = 1
 
+# Size of the fixed array behind fgq_gemm_fp8_blockscaled_splitk_noalloc.
+FGQ_NOALLOC_SCRATCH_BYTES = 16 << 20
+
 # Every symbol include/fgq.h declares, with (restype, argtypes).
 _vp = ctypes.c_void_p
 _i64 = ctypes.c_int64

@@ -191,7 +191,8 @@ fgq_status fgq_gemm_fp8_blockscaled_ex(const uint8_t* A, const float* sA, const 
   const int bf16 = out == FGQ_OUT_BF16 ? 1 : 0;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M <= kLowMDirect)
-    return from_cuda(fgq::launch_gemm_lowm(A, sA, B, sB, C, ldc, M, N, K, bf16, 1, nullptr, s, dev));
+    return from_cuda(
+        fgq::launch_gemm_lowm(A, sA, B, sB, C, ldc, M, N, K, bf16, false, nullptr, s, dev));
   // power-of-two scales: applied by the tensor core, no promotion step
   if (mode == FGQ_SCALE_UE8M0)
     return from_cuda(fgq::launch_gemm_mx(A, sA, B, sB, C, ldc, M, N, K, bf16, s, dev));
@@ -285,9 +286,8 @@ fgq_status fgq_gemm_fp8_blockscaled_splitk(const uint8_t* A, const float* sA, co
   if (!workspace || !aligned(workspace, 16) ||
       workspace_bytes < fgq::lowm_workspace_bytes(M, N, K, dev.sm_count))
     return FGQ_ERR_INVALID_ARG;
-  const int splits = fgq::lowm_splits(M, N, K, dev.sm_count);
   return from_cuda(fgq::launch_gemm_lowm(A, sA, B, sB, C, ldc, M, N, K, out == FGQ_OUT_BF16 ? 1 : 0,
-                                         splits, workspace, static_cast<cudaStream_t>(stream), dev));
+                                         true, workspace, static_cast<cudaStream_t>(stream), dev));
 }
 
 fgq_status fgq_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const uint8_t* B,
@@ -314,15 +314,15 @@ fgq_status fgq_gemm_fp8_blockscaled_splitk_noalloc(const uint8_t* A, const float
   void* scratch = nullptr;
   if (fgq::noalloc_scratch(dev, &scratch) != cudaSuccess) return FGQ_ERR_CUDA;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int splits = fgq::lowm_splits(M, N, K, dev.sm_count);
-  if (splits > 1) {
-    // the per-tile counters must start at zero; an earlier call that gave
-    // up on a wait may have left them otherwise (they lie inside `need`)
-    const size_t counter_bytes = static_cast<size_t>(N / 128) * sizeof(unsigned int);
-    if (cudaMemsetAsync(scratch, 0, counter_bytes, s) != cudaSuccess) return FGQ_ERR_CUDA;
+  const size_t zero = fgq::lowm_workspace_zero_bytes(M, N, K, dev.sm_count);
+  if (zero > 0) {
+    // the stream-K counters and flags must start at zero; an earlier call
+    // that gave up on a wait may have left them otherwise (they lie inside
+    // `need`)
+    if (cudaMemsetAsync(scratch, 0, zero, s) != cudaSuccess) return FGQ_ERR_CUDA;
   }
   return from_cuda(fgq::launch_gemm_lowm(A, sA, B, sB, C, ldc, M, N, K, out == FGQ_OUT_BF16 ? 1 : 0,
-                                         splits, scratch, s, dev));
+                                         true, scratch, s, dev));
 }
 
 const char* fgq_status_string(fgq_status status) {

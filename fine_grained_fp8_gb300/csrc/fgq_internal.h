@@ -16,6 +16,7 @@
 #define FGQ_DEVERR_SF_SLOT 0x20u        // scale-factor writer waiting for a free TMEM slot
 #define FGQ_DEVERR_MMA_SF 0x40u         // MMA issuer waiting for scale factors in TMEM
 #define FGQ_DEVERR_SELFTEST 0x80u       // the self-test's wait on a barrier nothing completes
+#define FGQ_DEVERR_SK_FLAG 0x100u       // stream-K fix-up waiting for another CTA's partial tile
 
 namespace fgq {
 
@@ -104,13 +105,16 @@ cudaError_t launch_gemm_lowm_fused(const void* a16, int64_t lda, const uint8_t* 
 // first call for each device).
 cudaError_t noalloc_scratch(const DeviceInfo& dev, void** ptr);
 
-// Low-M GEMM (M <= 256): split count and workspace size for a problem, and
-// the launch (splits == 1 needs no workspace).
-int lowm_splits(int64_t M, int64_t N, int64_t K, int sm_count);
+// Low-M GEMM (M <= 256).  With stream_k, the tiles left after the last
+// whole wave are shared out by K chunks (stream-K) and the workspace holds
+// the partial tiles: lowm_workspace_bytes of it, whose first
+// lowm_workspace_zero_bytes must be zero before a call (every completed call
+// leaves them zero).  Without, whole tiles only and no workspace.
 size_t lowm_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count);
+size_t lowm_workspace_zero_bytes(int64_t M, int64_t N, int64_t K, int sm_count);
 cudaError_t launch_gemm_lowm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                              void* C, int64_t ldc, int64_t M, int64_t N, int64_t K, int out_bf16,
-                             int splits, void* workspace, cudaStream_t stream,
+                             bool stream_k, void* workspace, cudaStream_t stream,
                              const DeviceInfo& dev);
 
 }  // namespace fgq

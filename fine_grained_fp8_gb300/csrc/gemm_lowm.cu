@@ -8,24 +8,35 @@
 //     weight rows (n), its N dimension over the M rows of A padded to MP
 //     (16..256).  The partial of a 128-K chunk lands in TMEM as
 //     [128 lanes = n] x [MP columns = m]; no MMA rows are spent on padding.
-//   - Split-K: a work unit is (128-column tile of C, range of K chunks).
-//     With S > 1 splits every unit writes its fp32 partial tile to a
-//     workspace; the last unit of a tile to finish (per-tile arrival
-//     counter) adds the S partials in split order and writes C, then resets
-//     the counter to zero, so the result does not depend on timing and the
-//     workspace is ready for the next call.
-//   - Persistent CTAs over units; warp 0 = TMA producer, warp 1 = MMA
-//     issuer, warps 4-11 = promotion epilogue (each warp: 32 n-rows x MP/2
-//     columns), the same roles and bounded waits as gemm.cu.
+//   - Scheduling ("Persistent kernel (grid = SM count, internal tile loop)",
+//     §Scheduler: linear and stream-K).  The work is 128-column tiles of C,
+//     each a run of K chunks.  Whole waves of tiles go to the CTAs one tile
+//     each (data-parallel).  When a workspace is given, the tiles left over
+//     after the last whole wave are not given out whole (that would leave
+//     most SMs idle for a whole tile time): their K chunks, laid end to end,
+//     are cut into equal contiguous ranges, one per CTA (stream-K), so every
+//     CTA streams about the same number of weight chunks.  A range that
+//     covers part of a tile yields a partial tile.
+//   - Stream-K fix-up: each partial tile's CTA bumps the tile's arrival
+//     counter first.  The last to arrive keeps its partial in registers,
+//     waits (bounded) for the others' ready flags, adds the partials in the
+//     order of the CTAs' ranges (a fixed order, so results are
+//     deterministic), writes C and resets the counter and flags; the others
+//     write their partial to their own workspace slot and raise their flag.
+//     A waiting CTA only waits for CTAs that have already arrived, i.e.
+//     finished their chunks, so the wait always ends.
+//   - Warp 0 = TMA producer, warp 1 = MMA issuer, warps 4-11 = promotion
+//     epilogue (each warp: 32 n-rows x MP/2 columns), the same roles and
+//     bounded waits as gemm.cu.
 //   - Batched promotion: the partials of kBatch = 256 / MP consecutive K
 //     chunks go to adjacent TMEM slices of one of two slots, and the
 //     epilogue waits once per batch, promotes its chunks with the next
 //     slice's load in flight, and hands the slot back.  With the tensor
 //     core filling the other slot meanwhile, the per-chunk wait and load
 //     latency of the epilogue is off the weight stream's critical path.
-// The per-(row, chunk) scales sA[m, c] are staged in shared memory in
-// windows of 16 chunks, transposed ([chunk][m]), so the epilogue reads them
-// as broadcast values.
+// The products sA[m, c] * sB[c, n/128] of a tile are staged in shared
+// memory in windows of 16 chunks ([chunk][m]), so the epilogue reads them
+// as broadcast values and promotes with one FMA per element.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -46,8 +57,8 @@ constexpr int kCtlWarps = 4;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (kCtlWarps + kEpiWarps);
 constexpr int kLaunchRegs = 168;
-constexpr uint32_t kCtlRegs = 56;
-constexpr uint32_t kEpiRegs = 224;
+constexpr uint32_t kCtlRegs = 104;
+constexpr uint32_t kEpiRegs = 200;
 constexpr uint32_t kEpiBarrier = 1;      // named barrier of the 256 epilogue threads
 constexpr uint32_t kQuantBarrier = 2;    // named barrier closing the in-kernel quantization
 constexpr int kQuantWarps = 11;          // warps 1-11 quantize A (warp 0 streams the weight)
@@ -149,17 +160,115 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
   return r;
 }
 
-// Unit u -> (n tile, split); the splits of a tile are adjacent in u so they
-// run at about the same time.
+// The work of one CTA: its stream-K range first, then its whole tiles.
+//   - Tiles [0, dp_tiles) run whole: CTA b takes tiles b, b + G, b + 2G, ...
+//   - The chunks of tiles [dp_tiles, n_tiles), laid end to end (sk_chunks of
+//     them), are split among CTAs [0, sk_ctas): CTA b takes the chunks
+//     [b * sk_chunks / sk_ctas, (b + 1) * sk_chunks / sk_ctas).  The host
+//     keeps sk_ctas <= sk_chunks, so every range is non-empty.
+// Item i of a CTA is (tile, chunk range [c0, c1), j): j is the stream-K
+// tile index (tile - dp_tiles) of a partial tile, -1 for a whole one.  The
+// partial of CTA b for stream-K tile j goes to workspace slot b + j (slots
+// are distinct: a CTA's tiles increase, and the next CTA starts at or after
+// its last tile).
 struct LowSched {
-  int n_tiles, splits, total, chunks_per_split, kchunks;
-  __device__ __forceinline__ void unit(int u, int& nt, int& sp, int& c0, int& c1) const {
-    nt = u / splits;
-    sp = u - nt * splits;
-    c0 = sp * chunks_per_split;
-    c1 = min(c0 + chunks_per_split, kchunks);
+  int n_tiles, kchunks, dp_tiles, sk_ctas;
+  long long sk_chunks;
+
+  // One CTA's list, worked out once (the only divisions); item() then takes
+  // constant time without dividing.
+  struct Cta {
+    int n_items, nsk;
+    int j_first, c_first;  // first stream-K tile and its first chunk
+    int j_last, c_last;    // last stream-K tile and the end of its range
+  };
+  __device__ __forceinline__ Cta cta(int b, int G) const {
+    Cta w{};
+    if (b < sk_ctas) {
+      const long long s0 = static_cast<long long>(b) * sk_chunks / sk_ctas;
+      const long long s1 = static_cast<long long>(b + 1) * sk_chunks / sk_ctas;
+      if (s1 > s0) {
+        w.j_first = static_cast<int>(s0 / kchunks);
+        w.c_first = static_cast<int>(s0 - static_cast<long long>(w.j_first) * kchunks);
+        w.j_last = static_cast<int>((s1 - 1) / kchunks);
+        w.c_last = static_cast<int>(s1 - static_cast<long long>(w.j_last) * kchunks);
+        w.nsk = w.j_last - w.j_first + 1;
+      }
+    }
+    w.n_items = w.nsk + (b < dp_tiles ? (dp_tiles - 1 - b) / G + 1 : 0);
+    return w;
+  }
+  __device__ __forceinline__ void item(const Cta& w, int b, int G, int i, int& tile, int& c0,
+                                       int& c1, int& j) const {
+    if (i < w.nsk) {
+      const int jj = w.j_first + i;
+      c0 = i == 0 ? w.c_first : 0;
+      c1 = jj == w.j_last ? w.c_last : kchunks;
+      tile = dp_tiles + jj;
+      j = (c0 == 0 && c1 == kchunks) ? -1 : jj;
+    } else {
+      tile = b + (i - w.nsk) * G;
+      c0 = 0;
+      c1 = kchunks;
+      j = -1;
+    }
+  }
+  // The CTAs whose ranges meet stream-K tile j: b_lo .. b_hi (the largest b
+  // with b * sk_chunks / sk_ctas <= x is ((x + 1) * sk_ctas - 1) / sk_chunks).
+  __device__ __forceinline__ void seg_ctas(int j, int& b_lo, int& b_hi) const {
+    const long long x0 = static_cast<long long>(j) * kchunks, x1 = x0 + kchunks - 1;
+    b_lo = static_cast<int>(((x0 + 1) * sk_ctas - 1) / sk_chunks);
+    b_hi = static_cast<int>(((x1 + 1) * sk_ctas - 1) / sk_chunks);
+    if (b_hi > sk_ctas - 1) b_hi = sk_ctas - 1;
   }
 };
+
+// acc[off + jj] += p[jj] * c[jj] for jj < W, with c the staged multipliers
+// (read as float4 broadcasts); with A quantized in the kernel the staged
+// values are sA alone and the multiplier is c[jj] * sb, the same product.
+template <int W, bool MUL_SB, int HALFW>
+__device__ __forceinline__ void promote_cols(float (&acc)[HALFW], int off, const uint32_t* p,
+                                             const float* c, float sb) {
+  const float4* c4 = reinterpret_cast<const float4*>(c);
+#pragma unroll
+  for (int v = 0; v < W / 4; ++v) {
+    const float4 m = c4[v];
+    const float mm[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      acc[off + 4 * v + t] =
+          fmaf(__uint_as_float(p[4 * v + t]), MUL_SB ? mm[t] * sb : mm[t], acc[off + 4 * v + t]);
+  }
+}
+
+__device__ __forceinline__ void st_release_u32(unsigned int* p, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait (bounded) until another CTA has raised *flag.  Gives up after
+// FGQ_WAIT_NS of %globaltimer time, or when another warp of this CTA already
+// gave up, recording FGQ_DEVERR_SK_FLAG and setting the abort flag.
+__device__ __forceinline__ bool wait_flag(const unsigned int* flag, volatile int* abort) {
+  if (ld_acquire_u32(flag) != 0u) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_acquire_u32(flag) != 0u) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > FGQ_WAIT_NS) {
+        record_error(FGQ_DEVERR_SK_FLAG);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
 
 // FUSE = 0: A comes quantized (codes by TMA per stage, scales sA).  FUSE =
 // kScaleFp32 + 1 or kScaleUe8m0 + 1: A comes as bf16 (a16, row stride lda)
@@ -172,9 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_lowm_kernel(const __grid_constant__ CUtensorMap tmap_w,   // Wq [N, K], box 128 x BN rows
                      const __grid_constant__ CUtensorMap tmap_a,   // Aq [M, K], box 128 x MP rows
                      const float* __restrict__ sA, const float* __restrict__ sB, void* __restrict__ C,
-                     int64_t ldc, int M, int N, int K, int splits, int chunks_per_split,
-                     float* __restrict__ partial,      // [splits][M][N] fp32 (splits > 1)
-                     unsigned int* __restrict__ counters,  // [N / 128], zero between calls
+                     int64_t ldc, int M, int N, int K, LowSched sched,
+                     float* __restrict__ partial,          // [slots][M][128] fp32 (stream-K)
+                     unsigned int* __restrict__ counters,  // [stream-K tiles], zero between calls
+                     unsigned int* __restrict__ flags,     // [slots], zero between calls
                      const uint16_t* __restrict__ a16, int64_t lda) {
   using CF = LowCfg<MP>;
   constexpr int STAGES = CF::STAGES;
@@ -201,13 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  LowSched sched;
-  sched.n_tiles = N / BN;
-  sched.splits = splits;
-  sched.total = sched.n_tiles * splits;
-  sched.chunks_per_split = chunks_per_split;
-  sched.kchunks = K / BK;
   const int kchunks = sched.kchunks;
+  const int G = static_cast<int>(gridDim.x);
+  const LowSched::Cta cw = sched.cta(blockIdx.x, G);
+  const int n_items = cw.n_items;
   const int nb = N / 128;
 
   if (threadIdx.x == 0) {
@@ -298,9 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < sched.total && ok; u += gridDim.x) {
-          int nt, sp, c0, c1;
-          sched.unit(u, nt, sp, c0, c1);
+        for (int i = 0; i < n_items && ok; ++i) {
+          int nt, c0, c1, jsk;
+          sched.item(cw, blockIdx.x, G, i, nt, c0, c1, jsk);
           for (int kc = c0; kc < c1; ++kc, ++it) {
             if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, FGQ_DEVERR_PRODUCER_EMPTY)) {
               ok = false;
@@ -330,9 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < sched.total && ok; u += gridDim.x) {
-          int nt, sp, c0, c1;
-          sched.unit(u, nt, sp, c0, c1);
+        for (int i = 0; i < n_items && ok; ++i) {
+          int nt, c0, c1, jsk;
+          sched.item(cw, blockIdx.x, G, i, nt, c0, c1, jsk);
           for (int kc = c0; kc < c1; ++kc) {
             const int j = (kc - c0) % kBatch;
             const uint32_t slot = bt & 1u;
@@ -384,9 +491,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int m0 = half * HALF;                     // first column (row of A) of this warp
     uint32_t bt = 0;  // batches consumed
     bool ok = true;
-    for (int u = blockIdx.x; u < sched.total && ok; u += gridDim.x) {
-      int nt, sp, c0, c1;
-      sched.unit(u, nt, sp, c0, c1);
+    for (int i = 0; i < n_items && ok; ++i) {
+      int nt, c0, c1, jsk;
+      sched.item(cw, blockIdx.x, G, i, nt, c0, c1, jsk);
       const int n = nt * BN + r_in_tile;
 
       float acc[HALF];
@@ -395,18 +502,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok_unit = true;
       for (int kb = c0; kb < c1; kb += kBatch, ++bt) {
         const int nbt = min(kBatch, c1 - kb);
-        // Stage sA[m, window] transposed as [chunk][m] (zero for m >= M) at
-        // the start of every window of kScaleWindow chunks (a whole number
-        // of batches).  Every epilogue warp runs every batch (a warp that
-        // gave up on a wait only skips the work), so all of them reach
-        // these barriers.
+        // Stage the window's multipliers sA[m, c] * sB[c, nt] as [chunk][m]
+        // (zero for m >= M) at the start of every window of kScaleWindow
+        // chunks (a whole number of batches).  Every epilogue warp runs every
+        // batch (a warp that gave up on a wait only skips the work), so all
+        // of them reach these barriers.  With A quantized in the kernel the
+        // staged values are sA alone (all chunks), and sB is applied below.
         const int w0 = FUSE ? kb : (kb - c0) % kScaleWindow;  // row of sm_sa for chunk kb
         if (!FUSE && w0 == 0) {
           named_barrier_sync(kEpiBarrier, 32 * kEpiWarps);  // earlier readers done
           const int nck = min(kScaleWindow, c1 - kb);
-          for (int i = et; i < nck * MP; i += 32 * kEpiWarps) {
-            const int c = i / MP, m = i - c * MP;
-            sm_sa[i] = m < M ? __ldg(sA + static_cast<int64_t>(m) * kchunks + kb + c) : 0.0f;
+          for (int e = et; e < nck * MP; e += 32 * kEpiWarps) {
+            const int c = e / MP, m = e - c * MP;
+            sm_sa[e] = m < M ? __ldg(sA + static_cast<int64_t>(m) * kchunks + kb + c) *
+                                   __ldg(sB + static_cast<int64_t>(kb + c) * nb + nt)
+                             : 0.0f;
           }
           named_barrier_sync(kEpiBarrier, 32 * kEpiWarps);
         }
@@ -429,41 +539,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int p = 0; p < P; ++p) {
               const int j = j0 + p < nbt ? j0 + p : nbt - 1;  // repeat the last in-range chunk
-              sbv[p] = __ldg(sB + static_cast<int64_t>(kb + j) * nb + nt);
+              sbv[p] = FUSE ? __ldg(sB + static_cast<int64_t>(kb + j) * nb + nt) : 1.0f;
               tmem_ld_cols_to<LW>(taddr + j * MP, r + p * LW);
             }
             tmem_wait_ld_regs64(r);
 #pragma unroll
             for (int p = 0; p < P; ++p) {
-              if (j0 + p < nbt) {
-                const float* sa_c = sm_sa + (w0 + j0 + p) * MP + m0;
-#pragma unroll
-                for (int jj = 0; jj < LW; ++jj)
-                  acc[jj] = fmaf(__uint_as_float(r[p * LW + jj]), sa_c[jj] * sbv[p], acc[jj]);
-              }
+              if (j0 + p < nbt)
+                promote_cols<LW, FUSE != 0>(acc, 0, r + p * LW, sm_sa + (w0 + j0 + p) * MP + m0,
+                                            sbv[p]);
             }
           }
+        } else if (NLD == 2) {
+          for (int j = 0; j < nbt; ++j) {  // both halves in flight, one wait
+            const float sb = FUSE ? __ldg(sB + static_cast<int64_t>(kb + j) * nb + nt) : 1.0f;
+            const float* cm = sm_sa + (w0 + j) * MP + m0;
+            uint32_t r[64];
+            tmem_ld_cols_to<LW>(taddr + j * MP, r);
+            tmem_ld_cols_to<LW>(taddr + j * MP + LW, r + LW);
+            tmem_wait_ld_regs64(r);
+            promote_cols<2 * LW, FUSE != 0>(acc, 0, r, cm, sb);
+          }
         } else {
+          // a 128-column accumulator: two 32-column loads alternate, the next
+          // one in flight while the current one is promoted
           for (int j = 0; j < nbt; ++j) {
-            const float sb = __ldg(sB + static_cast<int64_t>(kb + j) * nb + nt);
-            const float* sa_c = sm_sa + (w0 + j) * MP + m0;
-            if (NLD == 2) {  // both halves in flight, one wait
-              uint32_t r[64];
-              tmem_ld_cols_to<LW>(taddr + j * MP, r);
-              tmem_ld_cols_to<LW>(taddr + j * MP + LW, r + LW);
-              tmem_wait_ld_regs64(r);
+            const float sb = FUSE ? __ldg(sB + static_cast<int64_t>(kb + j) * nb + nt) : 1.0f;
+            const float* cm = sm_sa + (w0 + j) * MP + m0;
+            uint32_t ra[32], rb[32];
+            tmem_ld_cols_to<32>(taddr + j * MP, ra);
+            tmem_wait_ld_regs(ra);
 #pragma unroll
-              for (int jj = 0; jj < 2 * LW; ++jj)
-                acc[jj] = fmaf(__uint_as_float(r[jj]), sa_c[jj] * sb, acc[jj]);
-            } else {  // a 128-column accumulator leaves room for one load at a time
-#pragma unroll
-              for (int q = 0; q < NLD; ++q) {
-                uint32_t r[32];
-                tmem_ld_cols_to<LW>(taddr + j * MP + q * LW, r);
-                tmem_wait_ld_regs(r);
-#pragma unroll
-                for (int jj = 0; jj < LW; ++jj)
-                  acc[q * LW + jj] = fmaf(__uint_as_float(r[jj]), sa_c[q * LW + jj] * sb, acc[q * LW + jj]);
+            for (int q = 0; q < NLD; ++q) {
+              if (q + 1 < NLD) tmem_ld_cols_to<32>(taddr + j * MP + 32 * (q + 1), q % 2 == 0 ? rb : ra);
+              if (q % 2 == 0)
+                promote_cols<32, FUSE != 0>(acc, 32 * q, ra, cm + 32 * q, sb);
+              else
+                promote_cols<32, FUSE != 0>(acc, 32 * q, rb, cm + 32 * q, sb);
+              if (q + 1 < NLD) {
+                if (q % 2 == 0)
+                  tmem_wait_ld_regs(rb);
+                else
+                  tmem_wait_ld_regs(ra);
               }
             }
           }
@@ -473,14 +590,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive_relaxed(&tempty[slot]);
       }
-      // Every epilogue warp reaches this barrier once per unit, whether it
+      // Every epilogue warp reaches this barrier once per item, whether it
       // finished its chunks or gave up on a wait; continue only together.
       ok = named_barrier_and(kEpiBarrier, 32 * kEpiWarps, ok_unit);
       if (!ok) break;
 
       // (Loops over acc are unrolled with per-element guards so that acc
       // stays in registers.)
-      if (splits == 1) {
+      if (jsk < 0) {  // a whole tile
 #pragma unroll
         for (int j = 0; j < HALF; ++j) {
           const int m = m0 + j;
@@ -493,35 +610,81 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         continue;  // the staged scales were last read before the barrier above
       }
-      // Split-K: publish this unit's partial, then the last unit of the tile
-      // sums the partials in split order.
-      float* my = partial + static_cast<int64_t>(sp) * M * N;
-#pragma unroll
-      for (int j = 0; j < HALF; ++j) {
-        const int m = m0 + j;
-        if (m < M) my[static_cast<int64_t>(m) * N + n] = acc[j];
-      }
-      __threadfence();
-      named_barrier_sync(kEpiBarrier, 32 * kEpiWarps);
+
+      // ---- stream-K fix-up of a partial tile ----
+      // Partial layout of a slot: [HALF/4 groups][256 threads][4 floats], so
+      // that every epilogue thread moves its own values with 16-byte
+      // accesses and a warp's accesses are 512 contiguous bytes.
+      int b_lo, b_hi;
+      sched.seg_ctas(jsk, b_lo, b_hi);
       if (et == 0) {
-        const unsigned int prev = atomicAdd(&counters[nt], 1u);
-        *last_flag = (prev == static_cast<unsigned int>(splits - 1)) ? 1 : 0;
+        const unsigned int prev = atomicAdd(&counters[jsk], 1u);
+        *last_flag = prev == static_cast<unsigned int>(b_hi - b_lo) ? 1 : 0;
       }
       named_barrier_sync(kEpiBarrier, 32 * kEpiWarps);
-      if (*last_flag) {
+      const bool last = *last_flag != 0;
+      if (!last) {
+        float4* my = reinterpret_cast<float4*>(partial) +
+                     static_cast<int64_t>(blockIdx.x + jsk) * (HALF / 4) * 256 + et;
+#pragma unroll
+        for (int g = 0; g < HALF / 4; ++g)
+          __stcg(my + g * 256, make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]));
         __threadfence();
-        for (int j = 0; j < HALF; ++j) {
-          const int m = m0 + j;
-          if (m >= M) break;
-          float sum = 0.0f;
-          for (int q = 0; q < splits; ++q)
-            sum += __ldcg(partial + (static_cast<int64_t>(q) * M + m) * N + n);
-          if (OUT_BF16)
-            static_cast<uint16_t*>(C)[static_cast<int64_t>(m) * ldc + n] = f32_to_bf16_rn(sum);
-          else
-            static_cast<float*>(C)[static_cast<int64_t>(m) * ldc + n] = sum;
+        named_barrier_sync(kEpiBarrier, 32 * kEpiWarps);
+        if (et == 0) st_release_u32(&flags[blockIdx.x + jsk], 1u);
+        continue;
+      }
+      // The last to arrive: every other CTA of this tile has arrived, so it
+      // has finished its chunks and is writing its partial; wait for its
+      // flag (bounded), then add the partials in CTA order.
+      bool ready = true;
+      if (et == 0) {
+        for (int b = b_lo; b <= b_hi && ready; ++b)
+          if (b != static_cast<int>(blockIdx.x)) ready = wait_flag(&flags[b + jsk], abort_flag);
+      }
+      ok = named_barrier_and(kEpiBarrier, 32 * kEpiWarps, ready);
+      if (!ok) break;
+      __threadfence();
+      constexpr int GW = HALF / 4 < 4 ? HALF / 4 : 4;  // groups of 4 values in flight together
+#pragma unroll
+      for (int g0 = 0; g0 < HALF / 4; g0 += GW) {
+        float sum[4 * GW];
+#pragma unroll
+        for (int t = 0; t < 4 * GW; ++t) sum[t] = 0.0f;
+        for (int b = b_lo; b <= b_hi; ++b) {
+          if (b == static_cast<int>(blockIdx.x)) {
+#pragma unroll
+            for (int t = 0; t < 4 * GW; ++t) sum[t] += acc[4 * g0 + t];
+          } else {
+            const float4* src = reinterpret_cast<const float4*>(partial) +
+                                static_cast<int64_t>(b + jsk) * (HALF / 4) * 256 + et;
+            float4 v[GW];
+#pragma unroll
+            for (int g = 0; g < GW; ++g) v[g] = __ldcg(src + (g0 + g) * 256);
+#pragma unroll
+            for (int g = 0; g < GW; ++g) {
+              sum[4 * g] += v[g].x;
+              sum[4 * g + 1] += v[g].y;
+              sum[4 * g + 2] += v[g].z;
+              sum[4 * g + 3] += v[g].w;
+            }
+          }
         }
-        if (et == 0) counters[nt] = 0u;  // ready for the next call
+#pragma unroll
+        for (int t = 0; t < 4 * GW; ++t) {
+          const int m = m0 + 4 * g0 + t;
+          if (m < M) {
+            if (OUT_BF16)
+              static_cast<uint16_t*>(C)[static_cast<int64_t>(m) * ldc + n] = f32_to_bf16_rn(sum[t]);
+            else
+              static_cast<float*>(C)[static_cast<int64_t>(m) * ldc + n] = sum[t];
+          }
+        }
+      }
+      if (et == 0) {  // ready for the next call
+        for (int b = b_lo; b <= b_hi; ++b)
+          if (b != static_cast<int>(blockIdx.x)) flags[b + jsk] = 0u;
+        counters[jsk] = 0u;
       }
     }
   }
@@ -535,17 +698,74 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+constexpr int kMinChunksPerRange = 4;  // shortest stream-K range worth a fix-up
+
+int mp_for(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256; }
+
+// The schedule of one problem and the workspace it needs.
+struct LowPlan {
+  LowSched sched;
+  int grid;
+  int slots;               // partial-tile slots (stream-K)
+  size_t counter_bytes;    // per stream-K tile arrival counters (zero between calls)
+  size_t flag_bytes;       // per slot ready flags (zero between calls)
+  size_t partial_bytes;    // slots x MP x 128 fp32
+};
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+LowPlan lowm_plan(int64_t M, int64_t N, int64_t K, int sm_count, bool stream_k) {
+  const int T = static_cast<int>(N / BN), kc = static_cast<int>(K / BK);
+  const long long W = static_cast<long long>(T) * kc;
+  const int mp = mp_for(M);
+  const int G = static_cast<int>(W < sm_count ? W : sm_count);
+  int dp = T, sk = 0;
+  if (stream_k && G > 0) {
+    dp = (T / G) * G;
+    const int L = T - dp;
+    const long long skc = static_cast<long long>(L) * kc;
+    if (L > 0) {
+      // Larger partial tiles cost more to add up, so wide ones are split
+      // among fewer CTAs.
+      const long long smax = mp <= 64 ? (1ll << 40) : (mp == 128 ? 4 : 2);
+      long long s = G;
+      if (s > L * smax) s = L * smax;
+      const long long by_len = skc / kMinChunksPerRange;
+      if (s > (by_len > 0 ? by_len : 1)) s = by_len > 0 ? by_len : 1;
+      if (skc % s == 0 && (skc / s) % kc == 0) s = 0;  // whole tiles: nothing to split
+      if (s == 0) dp = T;
+      sk = static_cast<int>(s);
+    }
+  }
+  LowPlan p{};
+  p.sched.n_tiles = T;
+  p.sched.kchunks = kc;
+  p.sched.dp_tiles = dp;
+  p.sched.sk_ctas = sk;
+  p.sched.sk_chunks = static_cast<long long>(T - dp) * kc;
+  if (dp == T)
+    p.grid = T < sm_count ? T : sm_count;
+  else
+    p.grid = dp > 0 ? G : sk;
+  const int L = T - dp;
+  p.slots = sk > 0 ? sk + L - 1 : 0;
+  p.counter_bytes = sk > 0 ? round256(static_cast<size_t>(L) * sizeof(unsigned int)) : 0;
+  p.flag_bytes = sk > 0 ? round256(static_cast<size_t>(p.slots) * sizeof(unsigned int)) : 0;
+  p.partial_bytes = static_cast<size_t>(p.slots) * mp * BN * sizeof(float);
+  return p;
+}
+
 template <int MP, bool OUT_BF16>
 cudaError_t launch_lowm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
-                        void* C, int64_t ldc, int M, int N, int K, int splits, float* partial,
-                        unsigned int* counters, cudaStream_t stream, const DeviceInfo& dev) {
+                        void* C, int64_t ldc, int M, int N, int K, const LowPlan& plan,
+                        void* workspace, cudaStream_t stream, const DeviceInfo& dev) {
   using CF = LowCfg<MP>;
   auto kern = gemm_lowm_kernel<MP, OUT_BF16, 0>;
   static std::mutex mu;
   static bool ready[64] = {};
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (dev.device >= 64) return cudaErrorInvalidDevice;
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     if (!ready[dev.device]) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(CF::kSmemBytes));
@@ -561,16 +781,22 @@ cudaError_t launch_lowm(const uint8_t* A, const float* sA, const uint8_t* B, con
   CUtensorMap tw, ta;
   if (!make_k_major_map(&tw, B, N, K, BN) || !make_k_major_map(&ta, A, M, K, MP))
     return cudaErrorInvalidValue;
-  const int kchunks = K / BK;
-  const int cps = (kchunks + splits - 1) / splits;
-  const int units = (N / BN) * splits;
-  const int grid = units < dev.sm_count ? units : dev.sm_count;
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), CF::kSmemBytes, stream, tw, ta, sA, sB, C,
-                    ldc, M, N, K, splits, cps, partial, counters,
+  unsigned int* counters = nullptr;
+  unsigned int* flags = nullptr;
+  float* partial = nullptr;
+  if (plan.sched.sk_ctas > 0) {
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    counters = reinterpret_cast<unsigned int*>(w);
+    flags = reinterpret_cast<unsigned int*>(w + plan.counter_bytes);
+    partial = reinterpret_cast<float*>(w + plan.counter_bytes + plan.flag_bytes);
+  }
+  return launch_pdl(kern, dim3(plan.grid), dim3(kThreads), CF::kSmemBytes, stream, tw, ta, sA, sB,
+                    C, ldc, M, N, K, plan.sched, partial, counters, flags,
                     static_cast<const uint16_t*>(nullptr), int64_t{0});
 }
 
-// A as bf16, quantized inside the kernel (FUSE = scale mode + 1); no split.
+// A as bf16, quantized inside the kernel (FUSE = scale mode + 1); whole
+// tiles only.
 template <int MP, bool OUT_BF16, int FUSE>
 cudaError_t launch_lowm_fused(const uint16_t* a16, int64_t lda, const uint8_t* B, const float* sB,
                               void* C, int64_t ldc, int M, int N, int K, cudaStream_t stream,
@@ -583,7 +809,7 @@ cudaError_t launch_lowm_fused(const uint16_t* a16, int64_t lda, const uint8_t* B
   static bool ready[64] = {};
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (dev.device >= 64) return cudaErrorInvalidDevice;
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     if (!ready[dev.device]) {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            kMaxSmemOptin);
@@ -597,57 +823,39 @@ cudaError_t launch_lowm_fused(const uint16_t* a16, int64_t lda, const uint8_t* B
   }
   CUtensorMap tw, ta_unused = {};
   if (!make_k_major_map(&tw, B, N, K, BN)) return cudaErrorInvalidValue;
-  const int kchunks = K / BK;
-  const int units = N / BN;
-  const int grid = units < dev.sm_count ? units : dev.sm_count;
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, stream, tw, ta_unused,
-                    static_cast<const float*>(nullptr), sB, C, ldc, M, N, K, 1, kchunks,
-                    static_cast<float*>(nullptr), static_cast<unsigned int*>(nullptr), a16, lda);
+  const LowPlan plan = lowm_plan(M, N, K, dev.sm_count, false);
+  return launch_pdl(kern, dim3(plan.grid), dim3(kThreads), smem, stream, tw, ta_unused,
+                    static_cast<const float*>(nullptr), sB, C, ldc, M, N, K, plan.sched,
+                    static_cast<float*>(nullptr), static_cast<unsigned int*>(nullptr),
+                    static_cast<unsigned int*>(nullptr), a16, lda);
 }
 
 template <bool OUT_BF16>
 cudaError_t dispatch_mp(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
-                        void* C, int64_t ldc, int M, int N, int K, int splits, float* partial,
-                        unsigned int* counters, cudaStream_t stream, const DeviceInfo& dev) {
+                        void* C, int64_t ldc, int M, int N, int K, const LowPlan& plan,
+                        void* workspace, cudaStream_t stream, const DeviceInfo& dev) {
   if (M <= 16)
-    return launch_lowm<16, OUT_BF16>(A, sA, B, sB, C, ldc, M, N, K, splits, partial, counters,
-                                     stream, dev);
+    return launch_lowm<16, OUT_BF16>(A, sA, B, sB, C, ldc, M, N, K, plan, workspace, stream, dev);
   if (M <= 32)
-    return launch_lowm<32, OUT_BF16>(A, sA, B, sB, C, ldc, M, N, K, splits, partial, counters,
-                                     stream, dev);
+    return launch_lowm<32, OUT_BF16>(A, sA, B, sB, C, ldc, M, N, K, plan, workspace, stream, dev);
   if (M <= 64)
-    return launch_lowm<64, OUT_BF16>(A, sA, B, sB, C, ldc, M, N, K, splits, partial, counters,
-                                     stream, dev);
+    return launch_lowm<64, OUT_BF16>(A, sA, B, sB, C, ldc, M, N, K, plan, workspace, stream, dev);
   if (M <= 128)
-    return launch_lowm<128, OUT_BF16>(A, sA, B, sB, C, ldc, M, N, K, splits, partial, counters,
-                                      stream, dev);
-  return launch_lowm<256, OUT_BF16>(A, sA, B, sB, C, ldc, M, N, K, splits, partial, counters,
-                                    stream, dev);
+    return launch_lowm<128, OUT_BF16>(A, sA, B, sB, C, ldc, M, N, K, plan, workspace, stream, dev);
+  return launch_lowm<256, OUT_BF16>(A, sA, B, sB, C, ldc, M, N, K, plan, workspace, stream, dev);
 }
 
 }  // namespace
 
-int lowm_splits(int64_t M, int64_t N, int64_t K, int sm_count) {
-  // Split K only when the tiles alone leave SMs idle: enough units for about
-  // one per SM, each at least kMinChunksPerUnit chunks long (a split costs a
-  // partial-tile store and a fixed reduction step).
-  constexpr int64_t kMinChunksPerUnit = 4;
-  const int64_t kchunks = K / BK, n_tiles = N / BN;
-  int64_t s = (sm_count + n_tiles - 1) / n_tiles;
-  if (s > kchunks / kMinChunksPerUnit) s = kchunks / kMinChunksPerUnit;
-  if (s < 1) s = 1;
-  // every split non-empty
-  const int64_t cps = (kchunks + s - 1) / s;
-  s = (kchunks + cps - 1) / cps;
-  (void)M;
-  return static_cast<int>(s);
+size_t lowm_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count) {
+  const LowPlan p = lowm_plan(M, N, K, sm_count, true);
+  if (p.sched.sk_ctas == 0) return 256;  // never touched; a non-empty buffer keeps the contract simple
+  return p.counter_bytes + p.flag_bytes + p.partial_bytes;
 }
 
-size_t lowm_workspace_bytes(int64_t M, int64_t N, int64_t K, int sm_count) {
-  const int s = lowm_splits(M, N, K, sm_count);
-  const size_t counters = static_cast<size_t>(N / BN) * sizeof(unsigned int);
-  if (s <= 1) return 256;  // never touched; a non-empty buffer keeps the contract simple
-  return ((counters + 255) / 256) * 256 + static_cast<size_t>(s) * M * N * sizeof(float);
+size_t lowm_workspace_zero_bytes(int64_t M, int64_t N, int64_t K, int sm_count) {
+  const LowPlan p = lowm_plan(M, N, K, sm_count, true);
+  return p.counter_bytes + p.flag_bytes;
 }
 
 size_t lowm_fused_smem_bytes(int64_t M, int64_t K) {
@@ -684,20 +892,14 @@ cudaError_t launch_gemm_lowm_fused(const void* a16, int64_t lda, const uint8_t* 
 
 cudaError_t launch_gemm_lowm(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
                              void* C, int64_t ldc, int64_t M, int64_t N, int64_t K, int out_bf16,
-                             int splits, void* workspace, cudaStream_t stream,
+                             bool stream_k, void* workspace, cudaStream_t stream,
                              const DeviceInfo& dev) {
   if (M == 0) return cudaSuccess;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
-  unsigned int* counters = static_cast<unsigned int*>(workspace);
-  float* partial = nullptr;
-  if (splits > 1) {
-    const size_t cbytes = ((static_cast<size_t>(N / BN) * sizeof(unsigned int) + 255) / 256) * 256;
-    partial = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + cbytes);
-  }
-  return out_bf16 ? dispatch_mp<true>(A, sA, B, sB, C, ldc, m, n, k, splits, partial, counters,
-                                      stream, dev)
-                  : dispatch_mp<false>(A, sA, B, sB, C, ldc, m, n, k, splits, partial, counters,
-                                       stream, dev);
+  const LowPlan plan = lowm_plan(M, N, K, dev.sm_count, stream_k);
+  if (plan.sched.sk_ctas > 0 && workspace == nullptr) return cudaErrorInvalidValue;
+  return out_bf16 ? dispatch_mp<true>(A, sA, B, sB, C, ldc, m, n, k, plan, workspace, stream, dev)
+                  : dispatch_mp<false>(A, sA, B, sB, C, ldc, m, n, k, plan, workspace, stream, dev);
 }
 
 }  // namespace fgq
@@ -717,20 +919,53 @@ static __device__ __align__(256) unsigned char g_splitk_scratch[FGQ_NOALLOC_SCRA
 
 }  // namespace
 
+// Unique id of the current context (cuCtxGetId), so that a cached symbol
+// address is looked up again once the context it came from is gone (after
+// cudaDeviceReset the module is loaded again and may sit elsewhere).
+cudaError_t current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+  if (get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  return cudaSuccess;
+}
+
 cudaError_t noalloc_scratch(const DeviceInfo& dev, void** ptr) {
   // The array's name in host code is only a host-side stand-in for the
-  // symbol, so its device address is looked up once per device, with that
-  // device current (the caller made it current).
+  // symbol, so its device address is looked up with the device current
+  // (the caller made it current): once per device, and again whenever the
+  // device's context has changed since (a device reset).
   static std::mutex mu;
   static void* addr[64] = {};
+  static unsigned long long ctx_of[64] = {};
   if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  unsigned long long ctx = 0;
+  cudaError_t e = current_context_id(&ctx);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev.device] == nullptr) {
+  if (addr[dev.device] == nullptr || ctx_of[dev.device] != ctx) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_splitk_scratch);
+    e = cudaGetSymbolAddress(&p, g_splitk_scratch);
     if (e != cudaSuccess) return e;
     if (p == nullptr) return cudaErrorInvalidSymbol;
     addr[dev.device] = p;
+    ctx_of[dev.device] = ctx;
   }
   *ptr = addr[dev.device];
   return cudaSuccess;

@@ -171,23 +171,25 @@ fgq_status fgq_gemm_fp8_blockscaled_ex(const uint8_t* A, const float* sA, const 
                                        int64_t N, int64_t K, int out, int mode, void* stream);
 
 /*
- * Block-scaled FP8 GEMM with split-K for few rows of A, using a caller-owned
- * workspace.  Same arguments and result as fgq_gemm_fp8_blockscaled_ex.
+ * Block-scaled FP8 GEMM with stream-K scheduling for few rows of A, using a
+ * caller-owned workspace ("Persistent kernel" page, §Scheduler: stream-K).
+ * Same arguments and result as fgq_gemm_fp8_blockscaled_ex.
  *
- * For M <= 256 the K chunks of each 128-column tile of C are divided among
- * several CTAs (about four work units per SM); each writes its fp32 partial
- * tile to the workspace and the last one to finish adds the partials in a
- * fixed order and writes C, so results are deterministic and identical
- * across calls.  For M > 256 this is fgq_gemm_fp8_blockscaled_ex and the
- * workspace is not touched.  (The weight streaming that bounds this regime
- * is the same; split-K only balances it over every SM.)
+ * For M <= 256: whole waves of 128-column tiles of C run one tile per SM;
+ * the K chunks of the tiles left over after the last whole wave are laid
+ * end to end and cut into equal contiguous ranges, one per SM, so every SM
+ * streams about the same share of the weight.  A range that covers part of
+ * a tile leaves an fp32 partial tile; the last CTA of that tile to finish
+ * adds the partials in a fixed order (that of the ranges) and writes C, so
+ * results are deterministic and identical across calls.  For M > 256 this
+ * is fgq_gemm_fp8_blockscaled_ex and the workspace is not touched.
  *
  *   workspace        device memory of at least the size that
  *                    fgq_gemm_splitk_workspace_size returns for (M, N, K) on
  *                    the current device, 16-byte aligned, owned by the
  *                    caller.  It must be zero-filled before its first use;
  *                    every call that returns FGQ_OK leaves it ready for the
- *                    next (its per-tile counters back at zero).  After a
+ *                    next (its per-tile counters and flags back at zero).  After a
  *                    call whose kernel gave up on a wait
  *                    (FGQ_ERR_DEVICE_TIMEOUT from fgq_device_error) zero it
  *                    again.  Calls that share a workspace must not overlap
@@ -305,7 +307,8 @@ fgq_status fgq_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const float* gA,
                           int64_t ldc, int64_t M, int64_t N, int64_t K, int out, void* stream);
 
 /* Workspace bytes fgq_gemm_fp8_blockscaled_splitk needs for (M, N, K) on the
- * current device (depends on its SM count).  Same size checks as the GEMM. */
+ * current device (depends on its SM count; 256 when the problem has no
+ * partial tiles).  Same size checks as the GEMM. */
 fgq_status fgq_gemm_splitk_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes);
 
 /* Size of the fixed scratch array behind fgq_gemm_fp8_blockscaled_splitk_noalloc. */
@@ -328,10 +331,14 @@ fgq_status fgq_gemm_splitk_workspace_size(int64_t M, int64_t N, int64_t K, size_
  *     anything is launched.
  *   - The first call on each device looks up the array's device address;
  *     make that first call before capturing any stream on that device.
- *   - Every call that splits K clears the part of the array that must
- *     start at zero (the per-tile counters) on `stream` before its kernel
- *     runs; the rest keeps the previous call's partial results, which are
- *     always overwritten before they are read.
+ *     A device reset (cudaDeviceReset) discards the device's context and
+ *     with it that address; the first call afterwards looks it up again
+ *     (the lookup is keyed by the context's id), so make that call before
+ *     any capture as well.
+ *   - Every call with partial tiles clears the part of the array that must
+ *     start at zero (the per-tile counters and ready flags) on `stream`
+ *     before its kernel runs; the rest keeps the previous call's partial
+ *     results, which are always overwritten before they are read.
  *   - All calls on a device share the one array: calls that can overlap on
  *     the GPU (different streams without ordering between them) race and
  *     give wrong results.  Order them, e.g. issue them on one stream.

@@ -79,7 +79,7 @@ def test_quant_w_rejects(fgq, args):
     assert _lib.fgq_quant_w_128x128(*args) == _lib.FGQ_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("args", [
+GEMM_BAD_ARGS = [
     (0, P, P, P, P, 128, 128, 128, 128, 0, 0, None),      # null A
     (P, P, P, P, P, 128, 128, 128, 100, 0, 0, None),      # K % 128
     (P, P, P, P, P, 128, 128, 100, 128, 0, 0, None),      # N % 128
@@ -91,9 +91,29 @@ def test_quant_w_rejects(fgq, args):
     (P, P, P, P, P, 128, 128, 128, 128, 2, 0, None),      # bad out dtype
     (P, P, P, P, P, 128, 128, 128, 128, 0, 3, None),      # bad mode
     (P, P, P, P, P, 128, -1, 128, 128, 0, 0, None),       # M < 0
-])
+    (P, 0, P, P, P, 128, 128, 128, 128, 0, 0, None),      # null sA
+    (P, P, P, 0, P, 128, 128, 128, 128, 0, 0, None),      # null sB
+    (P, P, P, P, 0, 128, 128, 128, 128, 0, 0, None),      # null C
+    (P, P + 2, P, P, P, 128, 128, 128, 128, 0, 0, None),  # sA misaligned
+]
+
+
+@pytest.mark.parametrize("args", GEMM_BAD_ARGS)
 def test_gemm_rejects(fgq, args):
     assert _lib.fgq_gemm_fp8_blockscaled_ex(*args) == _lib.FGQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args", GEMM_BAD_ARGS)
+def test_gemm_noalloc_rejects(fgq, args):
+    """The entry point without a workspace runs the same checks, all before
+    any device call."""
+    assert _lib.fgq_gemm_fp8_blockscaled_splitk_noalloc(*args) == _lib.FGQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args", GEMM_BAD_ARGS)
+def test_gemm_splitk_rejects(fgq, args):
+    a = args[:-1] + (P, 1 << 20) + args[-1:]
+    assert _lib.fgq_gemm_fp8_blockscaled_splitk(*a) == _lib.FGQ_ERR_INVALID_ARG
 
 
 def test_gemm_plain_signature_rejects(fgq):
