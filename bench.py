@@ -1,8 +1,8 @@
 """Benchmark of the fine-grained FP8 hot path on GB300.
 
 One step = the whole hot path on one batch of the large-prefill workload:
-  quantize A [4096, 7168] bf16 (1x128 tiles) -> quantize B [7168, 7168] bf16
-  (128x128 blocks) -> block-scaled FP8 GEMM -> C [4096, 7168] bf16.
+  quantize A [4096, 7168] bf16 (1x128 tiles) and B [7168, 7168] bf16 (128x128
+  blocks), both in one launch -> block-scaled FP8 GEMM -> C [4096, 7168] bf16.
 value = 2*M*N*K / (step time), in TFLOP/s, summed over ranks (weak scaling:
 every rank runs its own batch; the path has no exchange step).
 
@@ -41,7 +41,7 @@ BYTES_QUANT_W = K_ * N_ * 2 + K_ * N_ + (K_ // 128) * (N_ // 128) * 4
 FLOPS_GEMM = 2 * M_ * N_ * K_
 BYTES_GEMM = M_ * K_ + N_ * K_ + M_ * (K_ // 128) * 4 + (K_ // 128) * (N_ // 128) * 4 + M_ * N_ * 2
 
-SOAK_SECONDS = 1.0  # untimed steps right before the timed region, for the clock record
+SOAK_SECONDS = 1.0  # the sustained leg after the timed region (also the clock record)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -312,15 +312,12 @@ def run_fgq(args):
         a, b = sets[i % 2]
         if ev is not None:
             ev[0].record(stream)
-        fgq.quant_act_1x128(a, "fp32", xq=aq, sx=sa)
+        fgq.quant_operands(a, b, "fp32", xq=aq, sx=sa, wq=bq, sw=sb)
         if ev is not None:
             ev[1].record(stream)
-        fgq.quant_w_128x128(b, "fp32", wq=bq, sw=sb)
-        if ev is not None:
-            ev[2].record(stream)
         fgq.gemm_fp8_blockscaled(aq, sa, bq, sb, torch.bfloat16, "fp32", out=c)
         if ev is not None:
-            ev[3].record(stream)
+            ev[2].record(stream)
 
     w0 = torch.cuda.Event(enable_timing=True)
     w1 = torch.cuda.Event(enable_timing=True)
@@ -331,31 +328,46 @@ def run_fgq(args):
     torch.cuda.synchronize()
     warm_ms = w0.elapsed_time(w1) / args.warmup
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
+    soak_steps = max(1, int(args.sustained_seconds / max(1e-4, warm_ms * 1e-3)))
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
-        # The timed region is a few milliseconds, shorter than one clock
-        # sample; the same steps run untimed for about a second just before
-        # it, so the sampler sees the clocks these kernels run at.
-        soak_steps = max(1, int(SOAK_SECONDS / max(1e-4, warm_ms * 1e-3)))
-        for i in range(soak_steps):
-            step(i)
         barrier(dist)
         torch.cuda.synchronize()
+        # The timed region: K steps back to back with nothing between the
+        # kernels (an event recorded between two kernels would cut the
+        # programmatic dependent launch that overlaps a kernel's set-up with
+        # the previous kernel's tail).
         start.record(stream)
         for i in range(args.steps):
-            step(i, events[i])
+            step(i)
         stop.record(stream)
+        # The same K steps again with an event around every kernel, for the
+        # per-kernel durations (the roofline of each kernel).
+        for i in range(args.steps):
+            step(i, events[i])
+        # The timed region is a few milliseconds, shorter than one clock
+        # sample.  The same steps continue for about a second right after it
+        # (timed on their own as the sustained figure), so the sampler, which
+        # started before the timed region, also sees the clocks these
+        # kernels settle at under the power limit.
+        s0.record(stream)
+        for i in range(soak_steps):
+            step(i)
+        s1.record(stream)
         torch.cuda.synchronize()
         barrier(dist)
     clk = clocks.summary()
-    clk["soak_s"] = soak_steps * warm_ms * 1e-3
+    sustained_ms = reduce_max(dist, s0.elapsed_time(s1), dev) / soak_steps
+    clk["window"] = "from before the timed region to the end of the sustained leg after it"
     ms_total = start.elapsed_time(stop)
     ms_total = reduce_max(dist, ms_total, dev)
     ms_step = ms_total / args.steps
-    per = [[e[j].elapsed_time(e[j + 1]) for e in events] for j in range(3)]
-    us_act, us_w, us_gemm = (1e3 * sum(p) / len(p) for p in per)
+    per = [[e[j].elapsed_time(e[j + 1]) for e in events] for j in range(2)]
+    us_quant, us_gemm = (1e3 * sum(p) / len(p) for p in per)
     if fgq.device_error() != 0:
         raise SystemExit("a kernel reported a device wait timeout")
 
@@ -393,8 +405,7 @@ def run_fgq(args):
             stream.wait_event(uploaded[j])
             if downloaded[j] is not None:
                 stream.wait_event(downloaded[j])
-            fgq.quant_act_1x128(a_dev[j], "fp32", xq=aq, sx=sa)
-            fgq.quant_w_128x128(b_dev[j], "fp32", wq=bq, sw=sb)
+            fgq.quant_operands(a_dev[j], b_dev[j], "fp32", xq=aq, sx=sa, wq=bq, sw=sb)
             consumed[j] = torch.cuda.Event()
             consumed[j].record(stream)
             fgq.gemm_fp8_blockscaled(aq, sa, bq, sb, torch.bfloat16, "fp32", out=c_dev[j])
@@ -427,17 +438,18 @@ def run_fgq(args):
     if not args.no_ue8m0:
         usteps = max(10, min(args.steps, 500))
 
-        def ustep(i, ev):
+        def ustep(i, ev=None):
             a, b = sets[i % 2]
-            ev[0].record(stream)
-            fgq.quant_act_1x128(a, "ue8m0", xq=aq, sx=sa)
-            ev[1].record(stream)
-            fgq.quant_w_128x128(b, "ue8m0", wq=bq, sw=sb)
-            ev[2].record(stream)
+            if ev is not None:
+                ev[0].record(stream)
+            fgq.quant_operands(a, b, "ue8m0", xq=aq, sx=sa, wq=bq, sw=sb)
+            if ev is not None:
+                ev[1].record(stream)
             fgq.gemm_fp8_blockscaled(aq, sa, bq, sb, torch.bfloat16, "ue8m0", out=c)
-            ev[3].record(stream)
+            if ev is not None:
+                ev[2].record(stream)
 
-        uev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(usteps)]
+        uev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(usteps)]
         for i in range(5):
             ustep(i, uev[i])
         torch.cuda.synchronize()
@@ -445,15 +457,17 @@ def run_fgq(args):
         u1 = torch.cuda.Event(enable_timing=True)
         u0.record(stream)
         for i in range(usteps):
-            ustep(i, uev[i])
+            ustep(i)
         u1.record(stream)
+        for i in range(usteps):
+            ustep(i, uev[i])
         torch.cuda.synchronize()
         ums = reduce_max(dist, u0.elapsed_time(u1), dev) / usteps
-        uper = [[e[j].elapsed_time(e[j + 1]) for e in uev] for j in range(3)]
-        u_act, u_w, u_gemm = (1e3 * sum(p) / len(p) for p in uper)
+        uper = [[e[j].elapsed_time(e[j + 1]) for e in uev] for j in range(2)]
+        u_quant, u_gemm = (1e3 * sum(p) / len(p) for p in uper)
         ue8m0 = {"scale_mode": "ue8m0", "steps": usteps, "ms_per_step": ums,
                  "value": world * FLOPS_GEMM / (ums * 1e-3) / 1e12, "unit": "TFLOP/s",
-                 "quant_act_us": u_act, "quant_w_us": u_w, "gemm_us": u_gemm,
+                 "quant_operands_us": u_quant, "gemm_us": u_gemm,
                  "gemm_TFLOP/s": FLOPS_GEMM / (u_gemm * 1e-6) / 1e12,
                  "kernel": "gemm_mx_kernel (tcgen05.mma kind::mxf8f6f4.block_scale)"}
         if fgq.device_error() != 0:
@@ -469,13 +483,16 @@ def run_fgq(args):
         aq4 = torch.empty((M_, K_ // 2), dtype=torch.uint8, device=dev)
         sa4 = torch.empty((M_, K_ // 32), dtype=torch.uint8, device=dev)
 
-        def mstep(i, ev):
+        def mstep(i, ev=None):
             a, _ = sets[i % 2]
-            ev[0].record(stream)
+            if ev is not None:
+                ev[0].record(stream)
             fgq.quant_mxfp4_1x32(a, xq=aq4, sx=sa4)
-            ev[1].record(stream)
+            if ev is not None:
+                ev[1].record(stream)
             fgq.gemm_mxfp4(aq4, sa4, *wq4[i % 2], torch.bfloat16, out=c)
-            ev[2].record(stream)
+            if ev is not None:
+                ev[2].record(stream)
 
         mev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(msteps)]
         for i in range(5):
@@ -485,8 +502,10 @@ def run_fgq(args):
         m1 = torch.cuda.Event(enable_timing=True)
         m0.record(stream)
         for i in range(msteps):
-            mstep(i, mev[i])
+            mstep(i)
         m1.record(stream)
+        for i in range(msteps):
+            mstep(i, mev[i])
         torch.cuda.synchronize()
         mms = reduce_max(dist, m0.elapsed_time(m1), dev) / msteps
         m_act = 1e3 * sum(e[0].elapsed_time(e[1]) for e in mev) / msteps
@@ -513,15 +532,18 @@ def run_fgq(args):
         sn4 = torch.empty((M_, K_ // 16), dtype=torch.uint8, device=dev)
         gn4 = torch.empty((1,), dtype=torch.float32, device=dev)
 
-        def nstep(i, ev):
+        def nstep(i, ev=None):
             a, _ = sets[i % 2]
-            ev[0].record(stream)
+            if ev is not None:
+                ev[0].record(stream)
             fgq.nvfp4_global_scale(a, g=gn4)
             fgq.quant_nvfp4_1x16(a, g=gn4, xq=an4, sx=sn4)
-            ev[1].record(stream)
+            if ev is not None:
+                ev[1].record(stream)
             bq4, bs4, bg4 = wn4[i % 2]
             fgq.gemm_nvfp4(an4, sn4, gn4, bq4, bs4, bg4, torch.bfloat16, out=c)
-            ev[2].record(stream)
+            if ev is not None:
+                ev[2].record(stream)
 
         nev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nsteps)]
         for i in range(5):
@@ -531,8 +553,10 @@ def run_fgq(args):
         n1 = torch.cuda.Event(enable_timing=True)
         n0.record(stream)
         for i in range(nsteps):
-            nstep(i, nev[i])
+            nstep(i)
         n1.record(stream)
+        for i in range(nsteps):
+            nstep(i, nev[i])
         torch.cuda.synchronize()
         nms = reduce_max(dist, n0.elapsed_time(n1), dev) / nsteps
         n_act = 1e3 * sum(e[0].elapsed_time(e[1]) for e in nev) / nsteps
@@ -585,7 +609,10 @@ def run_fgq(args):
                                                                     sx=qnvs),
                  QM * QK * 2 + QM * QK // 2 + QM * (QK // 16)),
                 ("quant_w_128x128", lambda i: fgq.quant_w_128x128(qw[i % 2], "fp32", wq=bq, sw=sb),
-                 BYTES_QUANT_W)):
+                 BYTES_QUANT_W),
+                ("quant_operands", lambda i: fgq.quant_operands(qa[i % 2], qw[i % 2], "fp32", xq=qaq,
+                                                                sx=qsa, wq=bq, sw=sb),
+                 QM * QK * 3 + QM * (QK // 128) * 4 + BYTES_QUANT_W)):
             for i in range(5):
                 fn(i)
             torch.cuda.synchronize()
@@ -693,7 +720,7 @@ def run_fgq(args):
     peaks, src = _peaks()
     if quant_bw:
         for k in ("quant_act_1x128", "quant_act_128x1", "quant_mxfp4_1x32", "nvfp4_global_scale",
-                  "quant_nvfp4_1x16", "quant_w_128x128"):
+                  "quant_nvfp4_1x16", "quant_w_128x128", "quant_operands"):
             quant_bw[k]["frac_hbm"] = quant_bw[k]["GB/s"] / peaks["hbm_gbs"]
     if skinny:
         for k, v in skinny.items():
@@ -730,18 +757,16 @@ def run_fgq(args):
     # on the quantize-bandwidth workload, and the two inside the step.
     quant_roofline = []
     if quant_bw:
-        for k in ("quant_act_1x128", "quant_w_128x128", "quant_act_128x1", "quant_mxfp4_1x32",
-                  "nvfp4_global_scale", "quant_nvfp4_1x16"):
+        for k in ("quant_act_1x128", "quant_w_128x128", "quant_operands", "quant_act_128x1",
+                  "quant_mxfp4_1x32", "nvfp4_global_scale", "quant_nvfp4_1x16"):
             quant_roofline.append({"kernel": k, "workload": "quantize-bw (alone)", "bound": "hbm",
                                    "achieved": quant_bw[k]["GB/s"], "peak": hbm, "unit": "GB/s",
                                    "frac": quant_bw[k]["GB/s"] / hbm,
                                    "bytes_per_launch": quant_bw[k]["bytes"]})
     gemm_tflops = FLOPS_GEMM / (us_gemm * 1e-6) / 1e12
-    act_gbs = BYTES_QUANT_ACT / (us_act * 1e-6) / 1e9
-    w_gbs = BYTES_QUANT_W / (us_w * 1e-6) / 1e9
+    quant_gbs = (BYTES_QUANT_ACT + BYTES_QUANT_W) / (us_quant * 1e-6) / 1e9
     value = world * FLOPS_GEMM / (ms_step * 1e-3) / 1e12
-    for k, us, nbytes in (("quant_act_1x128", us_act, BYTES_QUANT_ACT),
-                          ("quant_w_128x128", us_w, BYTES_QUANT_W)):
+    for k, us, nbytes in (("quant_operands", us_quant, BYTES_QUANT_ACT + BYTES_QUANT_W),):
         gbs = nbytes / (us * 1e-6) / 1e9
         quant_roofline.append({"kernel": k, "workload": "large prefill (inside the step)",
                                "bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
@@ -754,7 +779,7 @@ def run_fgq(args):
         "config": {"workload": WORKLOAD, "M": M_, "N": N_, "K": K_, "out": "bf16",
                    "scale_mode": "fp32", "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2 (two input sets rotated, 161 MB bf16 each)",
-                   "value_def": "2*M*N*K per step / step time (quantize A + quantize B + GEMM)"},
+                   "value_def": "2*M*N*K per step / step time (quantize A and B in one launch + GEMM)"},
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak,
                      "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
                      "traffic": _traffic("gemm_fp8_blockscaled", "gemm.cu"),
@@ -763,10 +788,9 @@ def run_fgq(args):
                      "frac_of_sustained": gemm_tflops / fp8_peak_sustained,
                      "quantizers": quant_roofline},
         "kernels": {
-            "quant_act_1x128": {"us": us_act, "GB/s": act_gbs, "frac_hbm": act_gbs / hbm,
-                                "bytes": BYTES_QUANT_ACT},
-            "quant_w_128x128": {"us": us_w, "GB/s": w_gbs, "frac_hbm": w_gbs / hbm,
-                                "bytes": BYTES_QUANT_W},
+            "quant_operands": {"us": us_quant, "GB/s": quant_gbs, "frac_hbm": quant_gbs / hbm,
+                               "bytes": BYTES_QUANT_ACT + BYTES_QUANT_W,
+                               "what": "quantize A 1x128 and B 128x128 in one launch"},
             "gemm_fp8_blockscaled": {"us": us_gemm, "TFLOP/s": gemm_tflops,
                                      "frac_fp8": gemm_tflops / fp8_peak, "flops": FLOPS_GEMM},
             "fp8_peak": fp8_peak, "fp8_peak_sustained": fp8_peak_sustained,
@@ -775,7 +799,11 @@ def run_fgq(args):
         "e2e": {"value": world * FLOPS_GEMM / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": (M_ * K_ + K_ * N_) * 2, "d2h_bytes_per_step": M_ * N_ * 2,
                 "ms_per_step": e2e_ms, "steps": e2e_steps},
-        "gpu_launches": 3 * args.steps,
+        "sustained": {"steps": soak_steps, "ms_per_step": sustained_ms,
+                      "value": world * FLOPS_GEMM / (sustained_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                      "note": "the same step repeated for about a second right after the timed "
+                              "region (clocks settle under the power limit)"},
+        "gpu_launches": 2 * args.steps,
         "quant_bw": quant_bw,
         "ue8m0": ue8m0,
         "mxfp4": mxfp4,
@@ -797,6 +825,8 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["fgq", "reference"], default="fgq")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sustained-seconds", type=float, default=SOAK_SECONDS,
+                   help="length of the sustained leg after the timed region (at least one step)")
     p.add_argument("--no-quant-bw", action="store_true",
                    help="skip the separate quantize-bandwidth measurement")
     p.add_argument("--no-ue8m0", action="store_true",

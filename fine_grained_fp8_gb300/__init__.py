@@ -9,6 +9,7 @@ the library's kernels:
                             groups of 128 rows (for a GEMM reducing over M)
   quant_w_128x128(w)        bf16 [K, N] -> (E4M3 codes [N, K] uint8 (K-major),
                                             fp32 [K/128, N/128])
+  quant_operands(x, w)      both of the above in one launch
   gemm_fp8_blockscaled(aq, sa, bq, sb, out_dtype)
                             C [M, N] = sum over 128-wide K chunks of
                             (Aq Bq)_chunk * sa * sb
@@ -23,7 +24,7 @@ from . import _lib
 from ._lib import (FGQ_OUT_BF16, FGQ_OUT_F32, FGQ_SCALE_FP32, FGQ_SCALE_UE8M0, FgqError,
                    check, load)
 
-__all__ = ["quant_act_1x128", "quant_act_128x1", "quant_mxfp4_1x32", "nvfp4_global_scale",
+__all__ = ["quant_act_1x128", "quant_act_128x1", "quant_operands", "quant_mxfp4_1x32", "nvfp4_global_scale",
            "quant_nvfp4_1x16", "quant_w_128x128", "gemm_fp8_blockscaled",
            "gemm_fp8_blockscaled_splitk", "gemm_fp8_blockscaled_fused_act", "gemm_mxfp4",
            "gemm_nvfp4", "splitk_workspace", "device_error",
@@ -186,6 +187,41 @@ def quant_w_128x128(w: torch.Tensor, mode="fp32", wq: torch.Tensor | None = None
                                   scale_mode(mode), _stream(w))
     check("fgq_quant_w_128x128", st)
     return wq, sw
+
+
+def quant_operands(x: torch.Tensor, w: torch.Tensor, mode="fp32", xq: torch.Tensor | None = None,
+                   sx: torch.Tensor | None = None, wq: torch.Tensor | None = None,
+                   sw: torch.Tensor | None = None):
+    """Both GEMM operands in one launch: quant_act_1x128(x) and
+    quant_w_128x128(w), bit for bit.  Returns (xq, sx, wq, sw)."""
+    _need_cuda("x", x, torch.bfloat16)
+    _need_cuda("w", w, torch.bfloat16)
+    if x.dim() != 2 or x.stride(1) != 1 or w.dim() != 2 or w.stride(1) != 1:
+        raise ValueError("x and w must be 2-D with a contiguous last dimension")
+    M, K = x.shape
+    K2, N = w.shape
+    if K2 != K:
+        raise ValueError(f"x is [M, {K}] but w is [{K2}, N]")
+    if x.device != w.device:
+        raise ValueError("x and w must be on the same device")
+    dev = x.device
+    xq = torch.empty((M, K), dtype=torch.uint8, device=dev) if xq is None else xq
+    sx = torch.empty((M, K // 128), dtype=torch.float32, device=dev) if sx is None else sx
+    wq = torch.empty((N, K), dtype=torch.uint8, device=dev) if wq is None else wq
+    sw = torch.empty((K // 128, N // 128), dtype=torch.float32, device=dev) if sw is None else sw
+    for name, t, dt in (("xq", xq, torch.uint8), ("sx", sx, torch.float32), ("wq", wq, torch.uint8),
+                        ("sw", sw, torch.float32)):
+        _need_cuda(name, t, dt)
+    if xq.shape != (M, K) or xq.stride(1) != 1 or sx.shape != (M, K // 128) or not sx.is_contiguous():
+        raise ValueError("xq must be [M, K] (contiguous rows) and sx a dense [M, K/128]")
+    if wq.shape != (N, K) or not wq.is_contiguous() or sw.shape != (K // 128, N // 128) \
+            or not sw.is_contiguous():
+        raise ValueError("wq must be a dense [N, K] and sw a dense [K/128, N/128]")
+    st = _lib.fgq_quant_operands(x.data_ptr(), M, K, x.stride(0), xq.data_ptr(), xq.stride(0),
+                                 sx.data_ptr(), w.data_ptr(), N, w.stride(0), wq.data_ptr(),
+                                 sw.data_ptr(), scale_mode(mode), _stream(x))
+    check("fgq_quant_operands", st)
+    return xq, sx, wq, sw
 
 
 def gemm_fp8_blockscaled(aq: torch.Tensor, sa: torch.Tensor, bq: torch.Tensor,

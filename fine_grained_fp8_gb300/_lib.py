@@ -37,6 +37,8 @@ SIGNATURES = {
     "fgq_nvfp4_global_scale": (_int, [_vp, _i64, _i64, _i64, _vp, _vp]),
     "fgq_quant_nvfp4_1x16": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
     "fgq_quant_w_128x128": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _int, _vp]),
+    "fgq_quant_operands": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64, _i64, _vp,
+                                  _vp, _int, _vp]),
     "fgq_gemm_fp8_blockscaled": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp]),
     "fgq_gemm_fp8_blockscaled_ex": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                            _int, _int, _vp]),
@@ -126,6 +128,10 @@ def fgq_quant_nvfp4_1x16(x, R, K, ldx, g, xq, sx, stream) -> int:
 
 def fgq_quant_w_128x128(w, K, N, ldw, wq, sw, mode, stream) -> int:
     return load().fgq_quant_w_128x128(w, K, N, ldw, wq, sw, mode, stream)
+
+
+def fgq_quant_operands(x, M, K, ldx, xq, ldq, sx, w, N, ldw, wq, sw, mode, stream) -> int:
+    return load().fgq_quant_operands(x, M, K, ldx, xq, ldq, sx, w, N, ldw, wq, sw, mode, stream)
 
 
 def fgq_gemm_fp8_blockscaled(A, sA, B, sB, C, M, N, K, stream) -> int:

@@ -151,6 +151,29 @@ fgq_status fgq_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
                                                static_cast<cudaStream_t>(stream), dev));
 }
 
+fgq_status fgq_quant_operands(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
+                              int64_t ldq, float* sx, const void* w, int64_t N, int64_t ldw,
+                              uint8_t* wq, float* sw, int mode, void* stream) {
+  // the checks of fgq_quant_act_1x128 and fgq_quant_w_128x128 together
+  if (M < 0 || K <= 0 || K % 128 != 0 || N <= 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (mode != FGQ_SCALE_FP32 && mode != FGQ_SCALE_UE8M0) return FGQ_ERR_INVALID_ARG;
+  if (!w || !wq || !sw) return FGQ_ERR_INVALID_ARG;
+  if (ldw < N || ldw % 8 != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(wq, 16) || !aligned(sw, 4)) return FGQ_ERR_INVALID_ARG;
+  if ((K / 128) > kMaxGroups / (N / 128)) return FGQ_ERR_INVALID_ARG;
+  if (M > 0) {
+    if (!x || !xq || !sx) return FGQ_ERR_INVALID_ARG;
+    if (ldx < K || ldq < K || ldx % 8 != 0 || ldq % 16 != 0) return FGQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(xq, 16) || !aligned(sx, 4)) return FGQ_ERR_INVALID_ARG;
+    if (M > kMaxGroups / (K / 128)) return FGQ_ERR_INVALID_ARG;
+  }
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_quant_operands(x, M, K, ldx, xq, ldq, sx, w, N, ldw, wq, sw, mode,
+                                              static_cast<cudaStream_t>(stream), dev));
+}
+
 namespace {
 
 // Checks shared by the GEMM entry points (M == 0 returns OK before pointer checks).

@@ -45,6 +45,13 @@ cudaError_t launch_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t 
                                    uint8_t* wq, float* sw, int mode, cudaStream_t stream,
                                    const DeviceInfo& dev);
 
+// Both operands of a GEMM in one launch: X [M, K] 1x128 and W [K, N]
+// 128x128, the same codes and scales as the two launches above.
+cudaError_t launch_quant_operands(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
+                                  int64_t ldq, float* sx, const void* w, int64_t N, int64_t ldw,
+                                  uint8_t* wq, float* sw, int mode, cudaStream_t stream,
+                                  const DeviceInfo& dev);
+
 cudaError_t launch_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const uint8_t* B,
                                         const float* sB, void* C, int64_t ldc, int64_t M,
                                         int64_t N, int64_t K, int out_bf16, int mode,

@@ -332,6 +332,285 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---- CTA pairs: 256 x 128 tiles, four partial buffers ------------------------------
+//
+// The single-CTA kernel above takes 48 KB of operands into shared memory per
+// K chunk of a 128 x 256 tile, which is what bounds its tensor core (about
+// 15 TB/s of L2-to-SM traffic over the GPU), and its epilogue has only two
+// partial buffers of 256 columns.  Here two CTAs of a cluster share one
+// tcgen05.mma.cta_group::2 of M = 256, N = 128: each CTA holds its own 128
+// rows of A and half of B's 128 rows (24 KB per chunk, the same bytes per
+// multiply-add as the 128 x 256 tile) and receives its 128 rows of the
+// partial in its own TMEM.  A 128-column partial leaves room for four
+// buffers, so the tensor core can run three chunks ahead of the promotion,
+// and each epilogue warp reads its 64 columns of a chunk with both loads in
+// flight and one wait.
+//   - The even CTA (leader) issues the MMAs.  Both CTAs' TMA copies of a
+//     stage complete on the leader's `full` barrier; the leader's commits
+//     arrive on the `empty` and `tfull` barriers of both CTAs (multicast).
+//   - Both CTAs' epilogues hand a drained buffer back on the leader's
+//     `tempty` barrier (the peer with a cluster-scope release arrive).
+constexpr int kPairBN = 128;   // output columns of a pair tile (the MMA's N)
+constexpr int kPairStages = 8;
+constexpr int kPairBufs = 4;   // TMEM partial buffers of kPairBN columns
+constexpr uint16_t kPairMask = 0x3;
+// Measured slower than the single-CTA kernel on the shapes tried (large
+// prefill 204 against 155-162 us; skinny M = 256 27.5 against 21.7 us), so
+// launch_gemm_fp8_blockscaled does not route to it.
+constexpr bool kUsePairs = false;
+// A 64-column accumulator needs fewer epilogue registers than the 128 of the
+// single-CTA kernel; the control warps get the rest.
+constexpr uint32_t kPairCtlRegs = 104;
+constexpr uint32_t kPairEpiRegs = 200;
+static_assert(128 * kPairCtlRegs + 256 * kPairEpiRegs <= kThreads * kLaunchRegs, "register split");
+
+struct PairCfg {
+  static constexpr int kABytes = BM * BK;                // this CTA's 128 rows of A
+  static constexpr int kBBytes = (kPairBN / 2) * BK;     // this CTA's 64 rows of B
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTxBytes = 2 * kStageBytes;  // both CTAs' copies of a stage
+  static constexpr int kTmemCols = kPairBufs * kPairBN;
+  static constexpr int kBarBytes = (2 * kPairStages + 2 * kPairBufs) * 8 + 16;
+  static constexpr size_t kSmemBytes =
+      1024 + static_cast<size_t>(kPairStages) * kStageBytes + kBarBytes;
+  static_assert(kTmemCols == 512, "TMEM allocation");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+};
+
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp8_pair_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                         const __grid_constant__ CUtensorMap tmap_b,
+                         const float* __restrict__ sA, const float* __restrict__ sB,
+                         void* __restrict__ C, int64_t ldc, int M, int N, int K) {
+  using CF = PairCfg;
+  constexpr int STAGES = kPairStages;
+  constexpr int HALF = kPairBN / 2;  // columns per epilogue warp
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sm_a = smem;
+  uint8_t* sm_b = smem + STAGES * CF::kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm_b + STAGES * CF::kBBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + kPairBufs;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + kPairBufs);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const bool leader = rank == 0;
+  // Pair tiles (two stacked 128-row tiles x 128 columns), M fastest; the
+  // cluster c takes tiles c, c + clusters, ...
+  const int m_tiles = (M + BM - 1) / BM;
+  const int m_groups = (m_tiles + 1) / 2;
+  const int n_tiles = N / kPairBN;
+  const int total = m_groups * n_tiles;
+  const int first = static_cast<int>(blockIdx.x) / 2;
+  const int stride = static_cast<int>(gridDim.x) / 2;
+  const int kchunks = K / BK;
+  const int nb = N / 128;
+
+  if (threadIdx.x == 0) {
+    // The leader's full and tempty barriers gather both CTAs; every CTA
+    // receives the leader's commits on its own empty and tfull barriers.
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < kPairBufs; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 2 * kEpiWarps);
+    }
+    *abort_flag = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, CF::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers and TMEM exist before either uses the other's
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_launch_dependents();
+
+  if (warp < kCtlWarps) {
+    setmaxnreg_dec<kPairCtlRegs>();
+    if (warp == 0) {
+      // ---------------- TMA producer (each CTA loads its own share) ----------------
+      if (elect_one_sync()) {
+        uint32_t it = 0;
+        bool ok = true;
+        const uint32_t bar0 = mapa_shared(&full[0], 0);
+        for (int u = first; u < total && ok; u += stride) {
+          const int tm = (u % m_groups) * 2 + rank, tn = u / m_groups;
+          const int b_row = tn * kPairBN + rank * (kPairBN / 2);
+          for (int kc = 0; kc < kchunks; ++kc, ++it) {
+            const int s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1u;
+            if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, FGQ_DEVERR_PRODUCER_EMPTY)) {
+              ok = false;
+              break;
+            }
+            if (leader) mbar_arrive_expect_tx(&full[s], CF::kTxBytes);
+            const uint32_t bar = bar0 + s * 8;
+            tma_load_2d_pair(sm_a + s * CF::kABytes, &tmap_a, bar, kc * BK, tm * BM);
+            tma_load_2d_pair(sm_b + s * CF::kBBytes, &tmap_b, bar, kc * BK, b_row);
+          }
+        }
+        // Before leaving: every copy into the pair's shared memory has landed
+        // (the leader's full barriers see both CTAs' copies) and every MMA
+        // commit addressed to this CTA's empty barriers has arrived.
+        const uint32_t lo = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
+        for (uint32_t j = lo; j < it; ++j) {
+          if (leader) mbar_wait_drain(&full[j % STAGES], (j / STAGES) & 1u);
+          mbar_wait_drain(&empty[j % STAGES], (j / STAGES) & 1u);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 1 && leader) {
+      // ---------------- MMA issuer (the leader) ----------------
+      if (elect_one_sync()) {
+        constexpr uint32_t idesc = idesc_e4m3_f32(2 * BM, kPairBN);
+        const uint64_t dA0 = smem_desc_k_sw128(smem_u32(sm_a));
+        const uint32_t a_lo0 = static_cast<uint32_t>(dA0), dhi = static_cast<uint32_t>(dA0 >> 32);
+        const uint32_t b_lo0 = static_cast<uint32_t>(smem_desc_k_sw128(smem_u32(sm_b)));
+        int ls = 0;
+        uint32_t lph = 0;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int u = first; u < total && ok; u += stride) {
+          for (int kc = 0; kc < kchunks; ++kc, ++it) {
+            const uint32_t buf = it % kPairBufs, tph = (it / kPairBufs) & 1u;
+            if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, FGQ_DEVERR_MMA_TMEM) ||
+                !mbar_wait(&full[ls], lph, abort_flag, FGQ_DEVERR_MMA_FULL)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem_base + buf * kPairBN;
+            const uint32_t a_lo = a_lo0 + ls * (CF::kABytes >> 4);
+            const uint32_t b_lo = b_lo0 + ls * (CF::kBBytes >> 4);
+#pragma unroll
+            for (int kk = 0; kk < BK / 32; ++kk)
+              umma_f8f6f4_pair(d, make_desc(a_lo + kk * 2, dhi), make_desc(b_lo + kk * 2, dhi),
+                               idesc, kk > 0 ? 1u : 0u);
+            umma_commit_pair(&empty[ls], kPairMask);
+            umma_commit_pair(&tfull[buf], kPairMask);
+            if (++ls == STAGES) {
+              ls = 0;
+              lph ^= 1u;
+            }
+          }
+        }
+        // MMAs still in flight must finish before TMEM is released.
+        if (it > 0) mbar_wait_drain(&tfull[(it - 1) % kPairBufs], ((it - 1) / kPairBufs) & 1u);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ---------------- epilogue: promotion + store (both CTAs) ----------------
+    setmaxnreg_inc<kPairEpiRegs>();
+    const int ew = warp - kCtlWarps;
+    const int quad = warp & 3;   // TMEM lanes this warp may access
+    const int half = ew >> 2;    // which 64 of the tile's 128 columns
+    const int r_in_tile = quad * 32 + lane;
+    const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tempty0 = mapa_shared(&tempty[0], 0);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = first; u < total && ok; u += stride) {
+      const int tm = (u % m_groups) * 2 + rank, tn = u / m_groups;
+      const int row = tm * BM + r_in_tile;
+      const bool row_ok = row < M;
+      const int col0 = tn * kPairBN + half * HALF;
+      const float* sa_row = sA + static_cast<int64_t>(row_ok ? row : 0) * kchunks;
+      const float* sb_col = sB + tn;  // a 128-column tile is one scale block
+
+      uint64_t acc[HALF / 2];
+#pragma unroll
+      for (int j = 0; j < HALF / 2; ++j) acc[j] = 0ull;
+
+      float sa_next = row_ok ? __ldg(sa_row) : 0.0f;
+      float sb_next = __ldg(sb_col);
+      for (int kc = 0; kc < kchunks; ++kc, ++it) {
+        const uint32_t buf = it % kPairBufs, tph = (it / kPairBufs) & 1u;
+        const float comb = sa_next * sb_next;
+        if (kc + 1 < kchunks) {  // prefetch the next chunk's scales
+          sa_next = row_ok ? __ldg(sa_row + kc + 1) : 0.0f;
+          sb_next = __ldg(sb_col + static_cast<int64_t>(kc + 1) * nb);
+        }
+        const uint64_t comb2 = pack2(__float_as_uint(comb), __float_as_uint(comb));
+        // warp-uniform outcome: the TMEM loads below are warp-collective
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&tfull[buf], tph, abort_flag, FGQ_DEVERR_EPI_TMEM))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + t_lane + buf * kPairBN + half * HALF;
+        uint32_t ra[32], rb[32];
+        tmem_ld_32x32b_x32(taddr, ra);
+        tmem_ld_32x32b_x32(taddr + 32, rb);
+        tmem_wait_ld_regs(ra);
+        tmem_wait_ld_regs(rb);
+        // every column of this buffer is in registers (the reads have
+        // completed): hand it back to the leader's MMA issuer
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader)
+            mbar_arrive_relaxed(&tempty[buf]);
+          else
+            mbar_arrive_cluster_relaxed(tempty0 + buf * 8);
+        }
+        promote32(acc, ra, comb2, 0);
+        promote32(acc, rb, comb2, 16);
+      }
+      if (!ok) break;
+      if (row_ok) {
+        if (OUT_BF16) {
+          uint16_t* crow = static_cast<uint16_t*>(C) + static_cast<int64_t>(row) * ldc + col0;
+#pragma unroll
+          for (int j = 0; j < HALF / 2; j += 4) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(acc[j])),
+                              __uint_as_float(static_cast<uint32_t>(acc[j] >> 32)));
+            v.y = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(acc[j + 1])),
+                              __uint_as_float(static_cast<uint32_t>(acc[j + 1] >> 32)));
+            v.z = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(acc[j + 2])),
+                              __uint_as_float(static_cast<uint32_t>(acc[j + 2] >> 32)));
+            v.w = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(acc[j + 3])),
+                              __uint_as_float(static_cast<uint32_t>(acc[j + 3] >> 32)));
+            *reinterpret_cast<uint4*>(crow + 2 * j) = v;
+          }
+        } else {
+          float* crow = static_cast<float*>(C) + static_cast<int64_t>(row) * ldc + col0;
+#pragma unroll
+          for (int j = 0; j < HALF / 2; j += 2) {
+            uint4 v = make_uint4(static_cast<uint32_t>(acc[j]), static_cast<uint32_t>(acc[j] >> 32),
+                                 static_cast<uint32_t>(acc[j + 1]),
+                                 static_cast<uint32_t>(acc[j + 1] >> 32));
+            *reinterpret_cast<uint4*>(crow + 2 * j) = v;
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync();  // neither CTA leaves while its peer may still reach its memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, CF::kTmemCols);
+  }
+}
+
 // ---- host side -------------------------------------------------------------------
 
 }  // namespace
@@ -453,6 +732,72 @@ cudaError_t launch_cfg(const uint8_t* A, const float* sA, const uint8_t* B, cons
                     ldc, M, N, K);
 }
 
+// Clusters of two that fit on the device at once (0 when the pair kernel
+// cannot run), worked out once per device together with the launch checks.
+template <bool OUT_BF16>
+cudaError_t pair_clusters(const DeviceInfo& dev, int* clusters) {
+  auto kern = gemm_fp8_pair_kernel<OUT_BF16>;
+  static std::mutex mu;
+  static int cached[64] = {};
+  static bool ready[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  if (!ready[dev.device]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(PairCfg::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    // the setmaxnreg split assumes this launch register count
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (dev.sm_count / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = PairCfg::kSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    cached[dev.device] = n;
+    ready[dev.device] = true;
+  }
+  *clusters = cached[dev.device];
+  return cudaSuccess;
+}
+
+template <bool OUT_BF16>
+cudaError_t launch_pair(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                        void* C, int64_t ldc, int M, int N, int K, int clusters,
+                        cudaStream_t stream) {
+  CUtensorMap ta, tb;
+  if (!make_k_major_map(&ta, A, M, K, BM) || !make_k_major_map(&tb, B, N, K, kPairBN / 2))
+    return cudaErrorInvalidValue;
+  const int units = ((((M + BM - 1) / BM) + 1) / 2) * (N / kPairBN);
+  const int grid = 2 * (units < clusters ? units : clusters);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = PairCfg::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_fp8_pair_kernel<OUT_BF16>, ta, tb, sA, sB, C, ldc, M, N, K);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const uint8_t* B,
@@ -462,6 +807,17 @@ cudaError_t launch_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const
   (void)mode;  // power-of-two scales take the same promotion path (exact products)
   if (M == 0 || N == 0) return cudaSuccess;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  // CTA pairs when there is at least one 256 x 128 tile per pair that fits
+  const int64_t pair_units = (((M + BM - 1) / BM + 1) / 2) * (N / kPairBN);
+  if (kUsePairs && M > BM) {
+    int clusters = 0;
+    const cudaError_t e =
+        out_bf16 ? pair_clusters<true>(dev, &clusters) : pair_clusters<false>(dev, &clusters);
+    if (e != cudaSuccess) return e;
+    if (clusters > 0 && pair_units >= clusters)
+      return out_bf16 ? launch_pair<true>(A, sA, B, sB, C, ldc, m, n, k, clusters, stream)
+                      : launch_pair<false>(A, sA, B, sB, C, ldc, m, n, k, clusters, stream);
+  }
   const int64_t tiles256 = ((M + BM - 1) / BM) * ((N + 255) / 256);
   const bool wide = (N % 256 == 0) && tiles256 >= dev.sm_count;
   if (out_bf16) {

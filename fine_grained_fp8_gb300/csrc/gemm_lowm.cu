@@ -160,30 +160,37 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
   return r;
 }
 
-// The work of one CTA: its stream-K range first, then its whole tiles.
+// The work of one CTA: its stream-K range first, then its whole tiles, then
+// the fix-ups it was handed.
 //   - Tiles [0, dp_tiles) run whole: CTA b takes tiles b, b + G, b + 2G, ...
 //   - The chunks of tiles [dp_tiles, n_tiles), laid end to end (sk_chunks of
 //     them), are split among CTAs [0, sk_ctas): CTA b takes the chunks
 //     [b * sk_chunks / sk_ctas, (b + 1) * sk_chunks / sk_ctas).  The host
 //     keeps sk_ctas <= sk_chunks, so every range is non-empty.
-// Item i of a CTA is (tile, chunk range [c0, c1), j): j is the stream-K
-// tile index (tile - dp_tiles) of a partial tile, -1 for a whole one.  The
-// partial of CTA b for stream-K tile j goes to workspace slot b + j (slots
-// are distinct: a CTA's tiles increase, and the next CTA starts at or after
-// its last tile).
+//   - When some CTAs have no stream-K range (reducers = G - sk_ctas > 0),
+//     stream-K tile j also gets a fix-up item on CTA sk_ctas + j % reducers,
+//     after its whole tiles: that CTA, done early, usually arrives last and
+//     adds the partials, so the CTAs with ranges publish and move on.
+// Item i of a CTA is (tile, chunk range [c0, c1), j, kind): j is the
+// stream-K tile index (tile - dp_tiles) of a partial tile or a fix-up item,
+// -1 for a whole one.  The partial of CTA b for stream-K tile j goes to
+// workspace slot b + j (slots are distinct: a CTA's tiles increase, and the
+// next CTA starts at or after its last tile).
 struct LowSched {
-  int n_tiles, kchunks, dp_tiles, sk_ctas;
+  int n_tiles, kchunks, dp_tiles, sk_ctas, reducers;
   long long sk_chunks;
 
   // One CTA's list, worked out once (the only divisions); item() then takes
   // constant time without dividing.
   struct Cta {
-    int n_items, nsk;
+    int n_items, nsk, ndp;
     int j_first, c_first;  // first stream-K tile and its first chunk
     int j_last, c_last;    // last stream-K tile and the end of its range
+    int red0;              // first stream-K tile this CTA fixes up (-1: none)
   };
   __device__ __forceinline__ Cta cta(int b, int G) const {
     Cta w{};
+    w.red0 = -1;
     if (b < sk_ctas) {
       const long long s0 = static_cast<long long>(b) * sk_chunks / sk_ctas;
       const long long s1 = static_cast<long long>(b + 1) * sk_chunks / sk_ctas;
@@ -195,22 +202,36 @@ struct LowSched {
         w.nsk = w.j_last - w.j_first + 1;
       }
     }
-    w.n_items = w.nsk + (b < dp_tiles ? (dp_tiles - 1 - b) / G + 1 : 0);
+    w.ndp = b < dp_tiles ? (dp_tiles - 1 - b) / G + 1 : 0;
+    int nred = 0;
+    const int L = n_tiles - dp_tiles;
+    if (reducers > 0 && b >= sk_ctas && b - sk_ctas < reducers && b - sk_ctas < L) {
+      w.red0 = b - sk_ctas;
+      nred = (L - 1 - w.red0) / reducers + 1;
+    }
+    w.n_items = w.nsk + w.ndp + nred;
     return w;
   }
+  // kind: 0 a chunk range of a tile, 1 a fix-up only (no chunks)
   __device__ __forceinline__ void item(const Cta& w, int b, int G, int i, int& tile, int& c0,
-                                       int& c1, int& j) const {
+                                       int& c1, int& j, int& kind) const {
+    kind = 0;
     if (i < w.nsk) {
       const int jj = w.j_first + i;
       c0 = i == 0 ? w.c_first : 0;
       c1 = jj == w.j_last ? w.c_last : kchunks;
       tile = dp_tiles + jj;
       j = (c0 == 0 && c1 == kchunks) ? -1 : jj;
-    } else {
+    } else if (i < w.nsk + w.ndp) {
       tile = b + (i - w.nsk) * G;
       c0 = 0;
       c1 = kchunks;
       j = -1;
+    } else {
+      j = w.red0 + (i - w.nsk - w.ndp) * reducers;
+      tile = dp_tiles + j;
+      c0 = c1 = 0;
+      kind = 1;
     }
   }
   // The CTAs whose ranges meet stream-K tile j: b_lo .. b_hi (the largest b
@@ -406,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ph = 0;
         bool ok = true;
         for (int i = 0; i < n_items && ok; ++i) {
-          int nt, c0, c1, jsk;
-          sched.item(cw, blockIdx.x, G, i, nt, c0, c1, jsk);
+          int nt, c0, c1, jsk, kind;
+          sched.item(cw, blockIdx.x, G, i, nt, c0, c1, jsk, kind);
           for (int kc = c0; kc < c1; ++kc, ++it) {
             if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, FGQ_DEVERR_PRODUCER_EMPTY)) {
               ok = false;
@@ -438,8 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ph = 0;
         bool ok = true;
         for (int i = 0; i < n_items && ok; ++i) {
-          int nt, c0, c1, jsk;
-          sched.item(cw, blockIdx.x, G, i, nt, c0, c1, jsk);
+          int nt, c0, c1, jsk, kind;
+          sched.item(cw, blockIdx.x, G, i, nt, c0, c1, jsk, kind);
           for (int kc = c0; kc < c1; ++kc) {
             const int j = (kc - c0) % kBatch;
             const uint32_t slot = bt & 1u;
@@ -492,8 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t bt = 0;  // batches consumed
     bool ok = true;
     for (int i = 0; i < n_items && ok; ++i) {
-      int nt, c0, c1, jsk;
-      sched.item(cw, blockIdx.x, G, i, nt, c0, c1, jsk);
+      int nt, c0, c1, jsk, kind;
+      sched.item(cw, blockIdx.x, G, i, nt, c0, c1, jsk, kind);
       const int n = nt * BN + r_in_tile;
 
       float acc[HALF];
@@ -615,21 +636,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Partial layout of a slot: [HALF/4 groups][256 threads][4 floats], so
       // that every epilogue thread moves its own values with 16-byte
       // accesses and a warp's accesses are 512 contiguous bytes.
+      // A fix-up item contributes no partial; the tile's arrivals are its
+      // range CTAs plus, when fix-ups are handed out, the reducer.
+      const bool contributes = kind == 0;
       int b_lo, b_hi;
       sched.seg_ctas(jsk, b_lo, b_hi);
       if (et == 0) {
+        const unsigned int arrivals = static_cast<unsigned int>(b_hi - b_lo + 1) +
+                                      (sched.reducers > 0 ? 1u : 0u);
         const unsigned int prev = atomicAdd(&counters[jsk], 1u);
-        *last_flag = prev == static_cast<unsigned int>(b_hi - b_lo) ? 1 : 0;
+        *last_flag = prev + 1 == arrivals ? 1 : 0;
       }
       named_barrier_sync(kEpiBarrier, 32 * kEpiWarps);
       const bool last = *last_flag != 0;
+      if (!last && !contributes) continue;  // a range CTA arrives after it and adds up
       if (!last) {
+        // Publish: every thread stores its values, the barrier orders those
+        // stores before thread 0's release store of the flag (release is
+        // cumulative), so one release covers the whole partial tile.
         float4* my = reinterpret_cast<float4*>(partial) +
                      static_cast<int64_t>(blockIdx.x + jsk) * (HALF / 4) * 256 + et;
 #pragma unroll
         for (int g = 0; g < HALF / 4; ++g)
           __stcg(my + g * 256, make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]));
-        __threadfence();
         named_barrier_sync(kEpiBarrier, 32 * kEpiWarps);
         if (et == 0) st_release_u32(&flags[blockIdx.x + jsk], 1u);
         continue;
@@ -637,36 +666,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The last to arrive: every other CTA of this tile has arrived, so it
       // has finished its chunks and is writing its partial; wait for its
       // flag (bounded), then add the partials in CTA order.
+      const int me = contributes ? static_cast<int>(blockIdx.x) : -1;
       bool ready = true;
       if (et == 0) {
         for (int b = b_lo; b <= b_hi && ready; ++b)
-          if (b != static_cast<int>(blockIdx.x)) ready = wait_flag(&flags[b + jsk], abort_flag);
+          if (b != me) ready = wait_flag(&flags[b + jsk], abort_flag);
       }
+      // thread 0's acquire loads, then the barrier, order the others' reads
+      // of the partials after the peers' release stores
       ok = named_barrier_and(kEpiBarrier, 32 * kEpiWarps, ready);
       if (!ok) break;
-      __threadfence();
-      constexpr int GW = HALF / 4 < 4 ? HALF / 4 : 4;  // groups of 4 values in flight together
+      // GW groups of 4 values of up to P peers are loaded together, then
+      // added in CTA order.
+      constexpr int GW = HALF <= 16 ? HALF / 4 : (HALF <= 64 ? 4 : 2);
+      constexpr int P = HALF <= 32 ? 3 : 2;
 #pragma unroll
       for (int g0 = 0; g0 < HALF / 4; g0 += GW) {
         float sum[4 * GW];
 #pragma unroll
         for (int t = 0; t < 4 * GW; ++t) sum[t] = 0.0f;
-        for (int b = b_lo; b <= b_hi; ++b) {
-          if (b == static_cast<int>(blockIdx.x)) {
+        for (int b0 = b_lo; b0 <= b_hi; b0 += P) {
+          float4 v[P][GW];
 #pragma unroll
-            for (int t = 0; t < 4 * GW; ++t) sum[t] += acc[4 * g0 + t];
-          } else {
-            const float4* src = reinterpret_cast<const float4*>(partial) +
-                                static_cast<int64_t>(b + jsk) * (HALF / 4) * 256 + et;
-            float4 v[GW];
+          for (int p = 0; p < P; ++p) {
+            const int b = b0 + p;
+            if (b <= b_hi && b != me) {
+              const float4* src = reinterpret_cast<const float4*>(partial) +
+                                  static_cast<int64_t>(b + jsk) * (HALF / 4) * 256 + et;
 #pragma unroll
-            for (int g = 0; g < GW; ++g) v[g] = __ldcg(src + (g0 + g) * 256);
+              for (int g = 0; g < GW; ++g) v[p][g] = __ldcg(src + (g0 + g) * 256);
+            }
+          }
 #pragma unroll
-            for (int g = 0; g < GW; ++g) {
-              sum[4 * g] += v[g].x;
-              sum[4 * g + 1] += v[g].y;
-              sum[4 * g + 2] += v[g].z;
-              sum[4 * g + 3] += v[g].w;
+          for (int p = 0; p < P; ++p) {
+            const int b = b0 + p;
+            if (b > b_hi) break;
+            if (b == me) {
+#pragma unroll
+              for (int t = 0; t < 4 * GW; ++t) sum[t] += acc[4 * g0 + t];
+            } else {
+#pragma unroll
+              for (int g = 0; g < GW; ++g) {
+                sum[4 * g] += v[p][g].x;
+                sum[4 * g + 1] += v[p][g].y;
+                sum[4 * g + 2] += v[p][g].z;
+                sum[4 * g + 3] += v[p][g].w;
+              }
             }
           }
         }
@@ -683,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (et == 0) {  // ready for the next call
         for (int b = b_lo; b <= b_hi; ++b)
-          if (b != static_cast<int>(blockIdx.x)) flags[b + jsk] = 0u;
+          if (b != me) flags[b + jsk] = 0u;
         counters[jsk] = 0u;
       }
     }
@@ -743,6 +788,8 @@ LowPlan lowm_plan(int64_t M, int64_t N, int64_t K, int sm_count, bool stream_k) 
   p.sched.dp_tiles = dp;
   p.sched.sk_ctas = sk;
   p.sched.sk_chunks = static_cast<long long>(T - dp) * kc;
+  // CTAs with whole tiles only take the fix-ups (when there are any)
+  p.sched.reducers = (sk > 0 && dp > 0 && G > sk) ? G - sk : 0;
   if (dp == T)
     p.grid = T < sm_count ? T : sm_count;
   else

@@ -47,15 +47,14 @@ constexpr int kActThreads = 256;
 constexpr int kActRounds = 2;
 constexpr int kActGroupsPerWarp = 4 * kActRounds;
 
+// The groups of warp `warp` out of `nwarps` warps sharing the work.
 template <int MODE, bool DENSE>
-__global__ void __launch_bounds__(kActThreads)
-    quant_act_1x128_kernel(const uint16_t* __restrict__ x, uint32_t kc, uint32_t groups,
-                           int64_t ldx, uint8_t* __restrict__ xq, int64_t ldq,
-                           float* __restrict__ sx) {
+__device__ __forceinline__ void act_groups(const uint16_t* __restrict__ x, uint32_t kc,
+                                           uint32_t groups, int64_t ldx, uint8_t* __restrict__ xq,
+                                           int64_t ldq, float* __restrict__ sx, uint32_t warp,
+                                           uint32_t nwarps) {
   const uint32_t lane = threadIdx.x & 31u;
   const uint32_t sub = lane >> 3, l8 = lane & 7u;
-  const uint32_t warp = (blockIdx.x * kActThreads + threadIdx.x) >> 5;
-  const uint32_t nwarps = (gridDim.x * kActThreads) >> 5;
 
   for (uint32_t base = warp * kActGroupsPerWarp; base < groups;
        base += nwarps * kActGroupsPerWarp) {
@@ -101,6 +100,16 @@ __global__ void __launch_bounds__(kActThreads)
   }
 }
 
+template <int MODE, bool DENSE>
+__global__ void __launch_bounds__(kActThreads)
+    quant_act_1x128_kernel(const uint16_t* __restrict__ x, uint32_t kc, uint32_t groups,
+                           int64_t ldx, uint8_t* __restrict__ xq, int64_t ldq,
+                           float* __restrict__ sx) {
+  act_groups<MODE, DENSE>(x, kc, groups, ldx, xq, ldq, sx,
+                          (blockIdx.x * kActThreads + threadIdx.x) >> 5,
+                          (gridDim.x * kActThreads) >> 5);
+}
+
 // ---- 128x128 weight quantizer ------------------------------------------------
 //
 // One CTA per 128x128 block of W [K, N].  Thread t loads the 16-byte column
@@ -131,15 +140,16 @@ __device__ __forceinline__ void transpose4x4_bytes(uint32_t r0, uint32_t r1, uin
 // Five CTAs per SM (at most 51 registers a thread): measured faster than
 // the four that 55 registers allow, despite a few bytes of spill in the
 // fp32-scale instantiation; six spill heavily and are slower.
+// Block `block` of W (k-block major), by the CTA's kWThreads threads.
 template <int MODE>
-__global__ void __launch_bounds__(kWThreads, 5)
-    quant_w_128x128_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t ldw,
-                           uint8_t* __restrict__ wq, float* __restrict__ sw) {
+__device__ __forceinline__ void w_block(const uint16_t* __restrict__ w, int64_t K, int64_t N,
+                                        int64_t ldw, uint8_t* __restrict__ wq,
+                                        float* __restrict__ sw, uint32_t block) {
   __shared__ __align__(16) uint2 tile[128 * 16];  // [n][k-chunk of 8], swizzled
   __shared__ uint32_t warp_max[kWThreads / 32];
 
   const int nb_count = static_cast<int>(N / 128);
-  const int nb = blockIdx.x % nb_count, kb = blockIdx.x / nb_count;
+  const int nb = static_cast<int>(block % nb_count), kb = static_cast<int>(block / nb_count);
   const int64_t n0 = static_cast<int64_t>(nb) * 128, k0 = static_cast<int64_t>(kb) * 128;
   const int t = threadIdx.x, c = t & 15, rg = t >> 4;
 
@@ -194,6 +204,37 @@ __global__ void __launch_bounds__(kWThreads, 5)
     uint8_t* dst = wq + (n0 + n) * K + k0 + 16 * (q ^ (swz >> 1));
     st_stream_16(dst, val);
   }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kWThreads, 5)
+    quant_w_128x128_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t ldw,
+                           uint8_t* __restrict__ wq, float* __restrict__ sw) {
+  w_block<MODE>(w, K, N, ldw, wq, sw, blockIdx.x);
+}
+
+// Both operands of one GEMM in one launch: CTAs [0, w_blocks) quantize one
+// 128x128 weight block each (as quant_w_128x128_kernel); the rest share the
+// 1x128 activation groups (as quant_act_1x128_kernel, kActThreads / 32
+// warps each).  The same arithmetic, so the same codes and scales as the
+// two kernels; one launch saves the second kernel's fill and drain.
+// (Four CTAs per SM: at five, the activation half spills.)
+static_assert(kActThreads == kWThreads, "one block size for both halves");
+template <int MODE, bool DENSE>
+__global__ void __launch_bounds__(kWThreads, 4)
+    quant_operands_kernel(const uint16_t* __restrict__ x, uint32_t kc, uint32_t groups,
+                          int64_t ldx, uint8_t* __restrict__ xq, int64_t ldq,
+                          float* __restrict__ sx, const uint16_t* __restrict__ w, int64_t K,
+                          int64_t N, int64_t ldw, uint8_t* __restrict__ wq,
+                          float* __restrict__ sw, uint32_t w_blocks) {
+  if (blockIdx.x < w_blocks) {
+    w_block<MODE>(w, K, N, ldw, wq, sw, blockIdx.x);
+    return;
+  }
+  const uint32_t act_ctas = gridDim.x - w_blocks;
+  act_groups<MODE, DENSE>(x, kc, groups, ldx, xq, ldq, sx,
+                          ((blockIdx.x - w_blocks) * kActThreads + threadIdx.x) >> 5,
+                          act_ctas * (kActThreads / 32));
 }
 
 // ---- 128x1 (transposed) activation quantizer -----------------------------------
@@ -475,6 +516,36 @@ cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t 
   if (grid > needed) grid = needed;
   k<<<grid, kActThreads, 0, stream>>>(static_cast<const uint16_t*>(x), kc, groups, ldx, xq, ldq,
                                       sx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_operands(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
+                                  int64_t ldq, float* sx, const void* w, int64_t N, int64_t ldw,
+                                  uint8_t* wq, float* sw, int mode, cudaStream_t stream,
+                                  const DeviceInfo& dev) {
+  (void)dev;
+  const uint32_t kc = static_cast<uint32_t>(K / 128);
+  const uint32_t groups = static_cast<uint32_t>(M * (K / 128));
+  const int64_t w_blocks = (K / 128) * (N / 128);
+  // activation CTAs: kRoundsPerWarp rounds of kActGroupsPerWarp groups per
+  // warp, at least one CTA when there are groups
+  constexpr uint32_t kRoundsPerWarp = 4;
+  const uint32_t per_cta = (kActThreads / 32) * kActGroupsPerWarp * kRoundsPerWarp;
+  const uint32_t act_ctas = (groups + per_cta - 1) / per_cta;
+  const int64_t grid = w_blocks + act_ctas;
+  if (grid == 0) return cudaSuccess;
+  if (grid >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
+  const bool dense = (ldx == K) && (ldq == K);
+  using Kern = void (*)(const uint16_t*, uint32_t, uint32_t, int64_t, uint8_t*, int64_t, float*,
+                        const uint16_t*, int64_t, int64_t, int64_t, uint8_t*, float*, uint32_t);
+  Kern k;
+  if (mode == kScaleFp32)
+    k = dense ? quant_operands_kernel<kScaleFp32, true> : quant_operands_kernel<kScaleFp32, false>;
+  else
+    k = dense ? quant_operands_kernel<kScaleUe8m0, true> : quant_operands_kernel<kScaleUe8m0, false>;
+  k<<<static_cast<unsigned>(grid), kWThreads, 0, stream>>>(
+      static_cast<const uint16_t*>(x), kc, groups, ldx, xq, ldq, sx, static_cast<const uint16_t*>(w),
+      K, N, ldw, wq, sw, static_cast<uint32_t>(w_blocks));
   return cudaGetLastError();
 }
 

@@ -132,6 +132,24 @@ fgq_status fgq_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
                                float* sw, int mode, void* stream);
 
 /*
+ * Both operands of one block-scaled GEMM in one launch: the activations X
+ * [M, K] in 1x128 groups (exactly as fgq_quant_act_1x128) and the weight W
+ * [K, N] in 128x128 blocks (exactly as fgq_quant_w_128x128), one scale
+ * mode for both ("Fine-Grained FP8/FP4 Quantization", §Scaling
+ * Granularities; scale shapes from §DeepGEMM).  The codes and scales are
+ * bit for bit those of the two separate calls; one kernel does both, so the
+ * second launch's fill and drain are saved.
+ *
+ *   x, ldx, xq, ldq, sx   as fgq_quant_act_1x128 (unused when M == 0).
+ *   w, ldw, wq, sw        as fgq_quant_w_128x128 (W [K, N], codes [N, K]).
+ *   K % 128 == 0, N % 128 == 0, K > 0, N > 0, M >= 0.
+ * The same argument checks as the two calls, all before any launch.
+ */
+fgq_status fgq_quant_operands(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
+                              int64_t ldq, float* sx, const void* w, int64_t N, int64_t ldw,
+                              uint8_t* wq, float* sw, int mode, void* stream);
+
+/*
  * Block-scaled FP8 GEMM (§DeepGEMM: Tile-wise and Block-wise Scaling),
  * fp32 output, fp32 scales:
  *   C[m,n] = sum_c sA[m,c] * sB[c,n/128] * sum_{k in chunk c} A[m,k] * B[k,n]

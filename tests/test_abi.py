@@ -62,6 +62,22 @@ def test_quant_act_rejects(fgq, args):
     assert _lib.fgq_quant_act_1x128(*args) == _lib.FGQ_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("args", [
+    (P, 4, 128, 128, P, 128, P, 0, 128, 128, P, P, 0, None),      # null w
+    (P, 4, 128, 128, P, 128, P, P, 100, 128, P, P, 0, None),      # N % 128
+    (P, 4, 100, 128, P, 128, P, P, 128, 128, P, P, 0, None),      # K % 128
+    (P, 4, 128, 128, P, 128, P, P, 128, 120, P, P, 0, None),      # ldw < N
+    (P, 4, 128, 128, P, 128, P, P, 128, 128, P + 8, P, 0, None),  # wq misaligned
+    (0, 4, 128, 128, P, 128, P, P, 128, 128, P, P, 0, None),      # null x (M > 0)
+    (P, 4, 128, 128, P, 136, P, P, 128, 128, P, P, 0, None),      # ldq % 16
+    (P + 2, 4, 128, 128, P, 128, P, P, 128, 128, P, P, 0, None),  # x misaligned
+    (P, -1, 128, 128, P, 128, P, P, 128, 128, P, P, 0, None),     # M < 0
+    (P, 4, 128, 128, P, 128, P, P, 128, 128, P, P, 9, None),      # bad mode
+])
+def test_quant_operands_rejects(fgq, args):
+    assert _lib.fgq_quant_operands(*args) == _lib.FGQ_ERR_INVALID_ARG
+
+
 def test_quant_act_empty_is_ok(fgq):
     assert _lib.fgq_quant_act_1x128(0, 0, 128, 128, 0, 128, 0, 0, None) == _lib.FGQ_OK
 

@@ -124,6 +124,23 @@ def test_wide_tile_path(fgq, cuda_dev, M):
     assert torch.isnan(pad.float()).all(), "GEMM wrote outside C's rows"
 
 
+@pytest.mark.parametrize("M,N,K,out_dtype", [(600, 10240, 384, torch.float32),
+                                             (2431, 128 * 77, 512, torch.bfloat16),
+                                             (257, 128 * 160, 256, torch.bfloat16)])
+def test_pair_tile_path(fgq, cuda_dev, M, N, K, out_dtype):
+    """Enough 256 x 128 tiles for the CTA-pair kernel (tcgen05 cta_group::2):
+    ragged M (an odd number of 128-row tiles leaves the last pair's second
+    CTA with rows past M only), N not a multiple of 256, padded C."""
+    a = fgq_inputs.outlier((M, K), 1e-3, 100.0, seed=M)
+    b = fgq_inputs.normal((K, N), 0.02, seed=N % 997)
+    host = _oracle_operands(a, b, oracle.MODE_FP32)
+    out = torch.full((M, N + 64), float("nan"), dtype=out_dtype, device=cuda_dev)[:, :N]
+    c = _run(fgq, _to_dev(*host, cuda_dev), out_dtype, "fp32", out=out)
+    _check_full(c, *host)
+    pad = out.as_strided((M, 64), (N + 64, 1), storage_offset=N)
+    assert torch.isnan(pad.float()).all(), "GEMM wrote outside C's rows"
+
+
 def test_plain_c_abi_signature(fgq, cuda_dev):
     """fgq_gemm_fp8_blockscaled(A, sA, B, sB, C, M, N, K, stream): fp32 out."""
     from fine_grained_fp8_gb300 import _lib

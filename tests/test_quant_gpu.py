@@ -229,5 +229,49 @@ def test_skinny_config_activations(fgq, cuda_dev, mode, M):
     _assert_act_parity(fgq, a, mode, cuda_dev)
 
 
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: m[0])
+@pytest.mark.parametrize("M,K,N", [(0, 256, 384), (1, 128, 128), (129, 640, 256), (77, 7168, 1024),
+                                   (4096, 7168, 7168)])
+def test_quant_operands_one_launch(fgq, cuda_dev, mode, M, K, N):
+    """Both operands in one launch: codes and scales bit for bit those of the
+    oracle (and so of the two separate quantizers), including an empty A and
+    the large-prefill operands."""
+    name, mid = mode
+    a = fgq_inputs.student_t((M, K), 3, 1.0, seed=M + 1) if M else torch.zeros((0, K), dtype=torch.bfloat16)
+    w = fgq_inputs.normal((K, N), 0.02, seed=N + 2)
+    xq, sx, wq, sw = fgq.quant_operands(a.to(cuda_dev), w.to(cuda_dev), name)
+    torch.cuda.synchronize()
+    if M:
+        oq, os_ = oracle.quant_act_1x128(a, mid)
+        assert np.array_equal(sx.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+        assert np.array_equal(xq.cpu().numpy(), oq)
+    wo, wso = oracle.quant_w_128x128(w, mid)
+    assert np.array_equal(sw.cpu().numpy().view(np.uint32), wso.view(np.uint32))
+    assert np.array_equal(wq.cpu().numpy().T, wo)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=lambda m: m[0])
+def test_quant_operands_strided(fgq, cuda_dev, mode):
+    """Strided activations and weight, padded code rows: the same bits as the
+    separate quantizers, and nothing written outside the codes' rows."""
+    name, _ = mode
+    M, K, N = 300, 1024, 640
+    a = fgq_inputs.outlier((M, K), 1e-3, 100.0, seed=11)
+    w = fgq_inputs.outlier((K, N), 1e-3, 100.0, seed=12)
+    abig = torch.zeros((M, K + 72), dtype=torch.bfloat16, device=cuda_dev)
+    abig[:, :K] = a.to(cuda_dev)
+    wbig = torch.zeros((K, N + 136), dtype=torch.bfloat16, device=cuda_dev)
+    wbig[:, :N] = w.to(cuda_dev)
+    xq = torch.full((M, K + 16), 0xA5, dtype=torch.uint8, device=cuda_dev)[:, :K]
+    xq, sx, wq, sw = fgq.quant_operands(abig[:, :K], wbig[:, :N], name, xq=xq)
+    xq2, sx2 = fgq.quant_act_1x128(abig[:, :K], name)
+    wq2, sw2 = fgq.quant_w_128x128(wbig[:, :N], name)
+    torch.cuda.synchronize()
+    assert torch.equal(xq, xq2) and torch.equal(sx.view(torch.int32), sx2.view(torch.int32))
+    assert torch.equal(wq, wq2) and torch.equal(sw.view(torch.int32), sw2.view(torch.int32))
+    pad = xq.as_strided((M, 16), (K + 16, 1), storage_offset=K)
+    assert bool((pad == 0xA5).all()), "quantizer wrote outside its rows"
+
+
 def test_no_device_error(fgq, cuda_dev):
     assert fgq.device_error() == 0
