@@ -476,6 +476,96 @@ __host__ __device__ constexpr uint32_t idesc_mx_e4m3_ue8m0(int m, int n) {
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// ---- coalesced row stores ----------------------------------------------------------
+
+// A warp's output rows, one per lane (lane l holds RB bytes of row l as RB/4
+// 32-bit words in column order), stored to global memory so that each store
+// instruction writes whole contiguous row segments instead of 16 bytes of
+// 32 different rows.  The rows pass through `stage`, an SB-byte per-warp
+// shared-memory buffer (16-byte aligned): in each round RR = SB / RB lanes
+// write their rows into it (16-byte units XOR-swizzled by the row so the
+// writes do not collide in a bank), then all 32 lanes read it back in
+// row-major order and store 16 bytes at a time.  Row l goes to
+// row0 + l * stride; only rows l < rows are stored.  Every lane of the warp
+// must call it.
+template <int RB, int SB = 2048>
+__device__ __forceinline__ void warp_store_rows(uint8_t* stage, const uint32_t (&words)[RB / 4],
+                                                uint8_t* row0, int64_t stride, int rows) {
+  static_assert(RB % 64 == 0 && RB <= SB && (SB == 1024 || SB == 2048), "row and stage bytes");
+  constexpr int RU = RB / 16;          // 16-byte units per row
+  constexpr int RR = SB / RB;          // rows per round
+  constexpr int NL = SB / 512;         // 16-byte loads per lane per round
+  constexpr int SW = RU < 8 ? RU - 1 : 7;
+  static_assert(32 % RR == 0, "rounds");
+  const int lane = threadIdx.x & 31;
+  const uint32_t st0 = smem_u32(stage);
+#pragma unroll
+  for (int k = 0; k < 32 / RR; ++k) {
+    if (lane / RR == k) {
+      const int rl = lane % RR;
+#pragma unroll
+      for (int u = 0; u < RU; ++u)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         st0 + rl * RB + ((u ^ (rl & SW)) * 16)),
+                     "r"(words[4 * u]), "r"(words[4 * u + 1]), "r"(words[4 * u + 2]),
+                     "r"(words[4 * u + 3])
+                     : "memory");
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < NL; ++j) {
+      const int q = lane + 32 * j;
+      const int rl = q / RU, u = q % RU;
+      uint4 v;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "r"(st0 + rl * RB + ((u ^ (rl & SW)) * 16))
+                   : "memory");
+      const int r = k * RR + rl;
+      if (r < rows) *reinterpret_cast<uint4*>(row0 + r * stride + u * 16) = v;
+    }
+    __syncwarp();
+  }
+}
+
+// One 32-byte store (a whole sector) of eight 32-bit words; dst 32-byte
+// aligned.
+__device__ __forceinline__ void st_global_32B(void* dst, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// Two fp32 -> packed bf16x2 (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 32 accumulator columns of the warp's 32 rows (lane = row; r holds fp32
+// bits), converted (bf16 rounds to nearest even) and stored through the
+// warp's staging buffer: rows row0 .. row0 + 31 (those below row0 + rows),
+// columns col .. col + 31 of C (leading dimension ldc elements).
+template <bool OUT_BF16, int SB = 2048>
+__device__ __forceinline__ void warp_store32(uint8_t* stage, const uint32_t (&r)[32], void* C,
+                                             int64_t ldc, int row0, int col, int rows) {
+  if (OUT_BF16) {
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) w[j] = cvt_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+    warp_store_rows<64, SB>(stage, w,
+                            reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(C) +
+                                                       static_cast<int64_t>(row0) * ldc + col),
+                            ldc * 2, rows);
+  } else {
+    warp_store_rows<128, SB>(stage, r,
+                             reinterpret_cast<uint8_t*>(static_cast<float*>(C) +
+                                                        static_cast<int64_t>(row0) * ldc + col),
+                             ldc * 4, rows);
+  }
+}
+
 // Read (and optionally clear) this translation unit's copy of the device
 // error word.  Each unit with kernels that record errors exports a wrapper
 // around this; the C ABI reports the OR of all of them.

@@ -60,6 +60,7 @@ struct Cfg {
   static constexpr int kBarBytes = (2 * STAGES + 2 * kNBuf) * 8 + 16;
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes + kBarBytes;
   static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation must be a power of 2");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 // Bounded wait used while unwinding; ignores the abort flag.
@@ -95,7 +96,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_blockscaled_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                 const __grid_constant__ CUtensorMap tmap_b,
                                 const float* __restrict__ sA, const float* __restrict__ sB,
-                                void* __restrict__ C, int64_t ldc, int M, int N, int K) {
+                                void* __restrict__ C, int64_t ldc, int M, int N, int K,
+                                int wide_stores) {
   using CF = Cfg<BN, STAGES>;
   constexpr uint32_t NBUF = CF::kNBuf;
   constexpr int HALF = BN / 2;     // columns per epilogue warp
@@ -293,7 +295,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (row_ok && cols_ok) {
+      // Store with 32-byte stores, one whole sector of the row per lane and
+      // instruction.  (With 16-byte stores the C store took about 23 us of
+      // the large-prefill GEMM: the next tile's MMAs waited for the TMEM
+      // buffers while the epilogue stored.  Staging the rows through shared
+      // memory for fully coalesced stores measured no better here: the
+      // staging buffer takes 16 KB of the L1 the scale loads use.)
+      // wide_stores: C and its row pitch are 32-byte aligned (the host
+      // checks); otherwise 16-byte stores.
+      if (row_ok && cols_ok && !wide_stores) {
         if (OUT_BF16) {
           uint16_t* crow = static_cast<uint16_t*>(C) + static_cast<int64_t>(row) * ldc + col0;
 #pragma unroll
@@ -317,6 +327,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  static_cast<uint32_t>(acc[j + 1]),
                                  static_cast<uint32_t>(acc[j + 1] >> 32));
             *reinterpret_cast<uint4*>(crow + 2 * j) = v;
+          }
+        }
+      } else if (row_ok && cols_ok) {
+        if (OUT_BF16) {
+          uint16_t* crow = static_cast<uint16_t*>(C) + static_cast<int64_t>(row) * ldc + col0;
+#pragma unroll
+          for (int j = 0; j < HALF / 2; j += 8) {
+            uint32_t w[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              w[q] = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(acc[j + q])),
+                                 __uint_as_float(static_cast<uint32_t>(acc[j + q] >> 32)));
+            st_global_32B(crow + 2 * j, w);
+          }
+        } else {
+          float* crow = static_cast<float*>(C) + static_cast<int64_t>(row) * ldc + col0;
+#pragma unroll
+          for (int j = 0; j < HALF / 2; j += 4) {
+            const uint32_t w[8] = {
+                static_cast<uint32_t>(acc[j]),         static_cast<uint32_t>(acc[j] >> 32),
+                static_cast<uint32_t>(acc[j + 1]),     static_cast<uint32_t>(acc[j + 1] >> 32),
+                static_cast<uint32_t>(acc[j + 2]),     static_cast<uint32_t>(acc[j + 2] >> 32),
+                static_cast<uint32_t>(acc[j + 3]),     static_cast<uint32_t>(acc[j + 3] >> 32)};
+            st_global_32B(crow + 2 * j, w);
           }
         }
       }
@@ -728,8 +762,12 @@ cudaError_t launch_cfg(const uint8_t* A, const float* sA, const uint8_t* B, cons
     return cudaErrorInvalidValue;
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
+  // 32-byte stores need every row segment 32-byte aligned: C itself and the
+  // row pitch (column offsets are multiples of 128 elements)
+  const int64_t pitch = ldc * (OUT_BF16 ? 2 : 4);
+  const int wide = (reinterpret_cast<uintptr_t>(C) % 32 == 0 && pitch % 32 == 0) ? 1 : 0;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), CF::kSmemBytes, stream, ta, tb, sA, sB, C,
-                    ldc, M, N, K);
+                    ldc, M, N, K, wide);
 }
 
 // Clusters of two that fit on the device at once (0 when the pair kernel

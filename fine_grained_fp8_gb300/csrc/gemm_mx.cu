@@ -57,8 +57,10 @@ struct MxCfg {
   static constexpr int kBBytes = BN * BK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kNumBars = 2 * STAGES + 2 * kSlots + 2 * kNAcc + 1;
+  static constexpr int kStoreBytes = kEpiWarps * 2048;  // per-warp staging of C rows
   static constexpr size_t kSmemBytes =
-      1024 + static_cast<size_t>(STAGES) * kStageBytes + kNumBars * 8 + 16;
+      1024 + static_cast<size_t>(STAGES) * kStageBytes + kStoreBytes + kNumBars * 8 + 16;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(kNAcc * BN <= static_cast<int>(kSfaCol0), "accumulators overlap the scale ring");
   static_assert(BN / 32 <= 8, "B factors of one slot take BN/32 <= 8 columns");
 };
@@ -74,37 +76,9 @@ __device__ __forceinline__ bool mx_wait_drain(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
-__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 // UE8M0 code of a power-of-two fp32 scale 2^e, e in [-127, 127]: its biased
 // exponent field (2^-127 is the subnormal 0x00400000, whose field is 0).
 __device__ __forceinline__ uint32_t ue8m0_code(float s) { return (__float_as_uint(s) >> 23) & 0xFFu; }
-
-// 32 accumulator columns of one row: convert and store (16-byte stores).
-template <bool OUT_BF16>
-__device__ __forceinline__ void store32(void* C, int64_t ldc, int row, int col,
-                                        const uint32_t (&r)[32]) {
-  if (OUT_BF16) {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(C) + row * ldc + col);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint4 v;
-      v.x = bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
-      v.y = bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
-      v.z = bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
-      v.w = bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
-      dst[j] = v;
-    }
-  } else {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(C) + row * ldc + col);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) dst[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-  }
-}
 
 template <int BN, int STAGES, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -122,7 +96,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sm_a = smem;
   uint8_t* sm_b = smem + STAGES * CF::kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm_b + STAGES * CF::kBBytes);
+  uint8_t* sm_st = sm_b + STAGES * CF::kBBytes;  // C row staging, 2 KB per epilogue warp
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm_st + CF::kStoreBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* sf_full = empty + STAGES;
   uint64_t* sf_empty = sf_full + kSlots;
@@ -306,10 +281,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = ew >> 2;
     const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
     uint32_t t_it = 0;
+    uint8_t* stage = sm_st + ew * 2048;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t_it) {
       const int tm = tile % m_tiles, tn = tile / m_tiles;
-      const int row = tm * BM + 32 * q + lane;
-      const bool row_ok = row < M;
+      const int row0 = tm * BM + 32 * q;  // the warp's first row
       const int col0 = tn * BN + half * HALF;
       const uint32_t buf = t_it % NACC, aph = (t_it / NACC) & 1u;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[buf], aph, abort_flag, FGQ_DEVERR_EPI_TMEM)))
@@ -332,12 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
-        if (row_ok) {
-          if (j % 2 == 0)
-            store32<OUT_BF16>(C, ldc, row, col0 + 32 * j, ra);
-          else
-            store32<OUT_BF16>(C, ldc, row, col0 + 32 * j, rb);
-        }
+        // the warp's rows go out through its staging buffer (whole row
+        // segments per store instruction)
+        if (j % 2 == 0)
+          warp_store32<OUT_BF16>(stage, ra, C, ldc, row0, col0 + 32 * j, M - row0);
+        else
+          warp_store32<OUT_BF16>(stage, rb, C, ldc, row0, col0 + 32 * j, M - row0);
         if (j + 1 < NLD) {
           if (j % 2 == 0)
             tmem_wait_ld_regs(rb);

@@ -84,8 +84,9 @@ struct Mxf4Cfg {
   static constexpr int kSfTile = 528;
   static constexpr int kTilesB = 8 * (BN / 128);
   static constexpr int kSfBufBytes = (8 + kTilesB) * kSfTile;
+  static constexpr int kStoreBytes = kEpiWarps * 1024;  // per-warp staging of C rows
   static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes +
-                                       2 * kSfBufBytes + kNumBars * 8 + 16;
+                                       2 * kSfBufBytes + kStoreBytes + kNumBars * 8 + 16;
   // At the first stage s of a chunk the issuer, past the full[] wait of
   // stage s (whose TMA waited for the MMAs of stage s - STAGES), copies the
   // factors of stages s .. s + kChunkStages - 1; the slot of stage s + j last
@@ -164,34 +165,6 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// 32 accumulator columns of one row: convert and store (16-byte stores).
-template <bool OUT_BF16>
-__device__ __forceinline__ void store32(void* C, int64_t ldc, int row, int col,
-                                        const uint32_t (&r)[32]) {
-  if (OUT_BF16) {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(C) + row * ldc + col);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint4 v;
-      v.x = bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
-      v.y = bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
-      v.z = bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
-      v.w = bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
-      dst[j] = v;
-    }
-  } else {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(C) + row * ldc + col);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) dst[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-  }
-}
-
 template <int BN, int STAGES, bool OUT_BF16, bool NV>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_mxf4_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -215,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm_a = smem;
   uint8_t* sm_b = smem + STAGES * CF::kABytes;
   uint8_t* sf_stage = sm_b + STAGES * CF::kBBytes;  // two chunk buffers of factor tiles
-  uint64_t* full = reinterpret_cast<uint64_t*>(sf_stage + 2 * CF::kSfBufBytes);
+  uint8_t* sm_st = sf_stage + 2 * CF::kSfBufBytes;   // C row staging, 1 KB per epilogue warp
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm_st + CF::kStoreBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* sf_full = empty + STAGES;
   uint64_t* sf_empty = sf_full + 2;
@@ -462,10 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     uint32_t t_it = 0;
+    uint8_t* stage = sm_st + (warp - 8) * 1024;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t_it) {
       const int tm = tile % m_tiles, tn = tile / m_tiles;
-      const int row = tm * BM + 32 * q + lane;
-      const bool row_ok = row < M;
+      const int row0 = tm * BM + 32 * q;  // the warp's first row
       const int col0 = tn * BN + half * HALF;
       const uint32_t buf = t_it % NACC, aph = (t_it / NACC) & 1u;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[buf], aph, abort_flag, FGQ_DEVERR_EPI_TMEM)))
@@ -488,14 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
-        if (row_ok) {
-          if (j % 2 == 0) {
-            scale32(ra);
-            store32<OUT_BF16>(C, ldc, row, col0 + 32 * j, ra);
-          } else {
-            scale32(rb);
-            store32<OUT_BF16>(C, ldc, row, col0 + 32 * j, rb);
-          }
+        // the warp's rows go out through its staging buffer (whole row
+        // segments per store instruction)
+        if (j % 2 == 0) {
+          scale32(ra);
+          warp_store32<OUT_BF16, 1024>(stage, ra, C, ldc, row0, col0 + 32 * j, M - row0);
+        } else {
+          scale32(rb);
+          warp_store32<OUT_BF16, 1024>(stage, rb, C, ldc, row0, col0 + 32 * j, M - row0);
         }
         if (j + 1 < NLD) {
           if (j % 2 == 0)

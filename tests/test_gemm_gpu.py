@@ -141,6 +141,28 @@ def test_pair_tile_path(fgq, cuda_dev, M, N, K, out_dtype):
     assert torch.isnan(pad.float()).all(), "GEMM wrote outside C's rows"
 
 
+@pytest.mark.parametrize("out_dtype,pad", [(torch.bfloat16, 8), (torch.float32, 4)],
+                         ids=["bf16", "f32"])
+@pytest.mark.parametrize("M,N", [(1000, 4096), (2432, 2048)], ids=["tile128", "tile256"])
+def test_c_rows_16_byte_aligned_only(fgq, cuda_dev, out_dtype, pad, M, N):
+    """C whose start and row pitch are 16-byte but not 32-byte aligned (the
+    ABI's minimum): the kernel falls back from 32-byte to 16-byte stores."""
+    K = 256
+    a = fgq_inputs.normal((M, K), 1.0, seed=31)
+    b = fgq_inputs.normal((K, N), 0.02, seed=32)
+    host = _oracle_operands(a, b, oracle.MODE_FP32)
+    ldc = N + pad
+    esz = 2 if out_dtype == torch.bfloat16 else 4
+    buf = torch.full((M * ldc + 64,), float("nan"), dtype=out_dtype, device=cuda_dev)
+    off = 16 // esz  # start 16 bytes past a 512-byte boundary
+    out = buf.as_strided((M, N), (ldc, 1), storage_offset=off)
+    assert (out.data_ptr() % 32) == 16 and (ldc * esz) % 32 == 16
+    c = _run(fgq, _to_dev(*host, cuda_dev), out_dtype, "fp32", out=out)
+    _check_full(c, *host)
+    pad_view = buf.as_strided((M, pad), (ldc, 1), storage_offset=off + N)
+    assert torch.isnan(pad_view.float()).all(), "GEMM wrote outside C's rows"
+
+
 def test_plain_c_abi_signature(fgq, cuda_dev):
     """fgq_gemm_fp8_blockscaled(A, sA, B, sB, C, M, N, K, stream): fp32 out."""
     from fine_grained_fp8_gb300 import _lib
