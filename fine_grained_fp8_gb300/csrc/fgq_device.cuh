@@ -157,6 +157,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// The same bounded wait with acquire semantics at cluster scope: for a
+// barrier that CTAs of the cluster arrive on with release.cluster after
+// writing this CTA's shared memory.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort, unsigned int site) {
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((it & 63u) == 63u) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > FGQ_WAIT_NS) {
+        record_error(site);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // ---- TMA ---------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {

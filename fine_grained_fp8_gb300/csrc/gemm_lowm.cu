@@ -92,6 +92,11 @@ struct LowCfg {
            fused_scale_bytes(kchunks) + kBarBytes + 16;
   }
   static_assert(kScaleWindow % kBatch == 0, "a batch never straddles a scale window");
+  // Cluster-pair split (below): the receive buffer of the peer's partial tile
+  // and its barrier, after the control words.
+  static constexpr int kRecvBytes = MP * BN * 4;
+  static constexpr size_t kPairSmemBytes = kSmemBytes + 64 + kRecvBytes;
+  static_assert(MP > 64 || kPairSmemBytes <= 232448, "shared memory per CTA (pairs)");
 };
 
 // Loads of W consecutive TMEM columns into r[0..W-1] (r points into a
@@ -179,6 +184,11 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
 struct LowSched {
   int n_tiles, kchunks, dp_tiles, sk_ctas, reducers;
   long long sk_chunks;
+  // Cluster-pair split (no workspace): the tiles [dp_tiles, dp_tiles +
+  // pair_tiles) are split in K between the two CTAs of cluster c (tile
+  // dp_tiles + c): rank 0 takes chunks [0, kchunks / 2), rank 1 the rest and
+  // sends its partial to rank 0 through distributed shared memory.
+  int pair_tiles;
 
   // One CTA's list, worked out once (the only divisions); item() then takes
   // constant time without dividing.
@@ -191,7 +201,15 @@ struct LowSched {
   __device__ __forceinline__ Cta cta(int b, int G) const {
     Cta w{};
     w.red0 = -1;
-    if (b < sk_ctas) {
+    if (pair_tiles > 0) {
+      const int c = b >> 1, r = b & 1, h = kchunks / 2;
+      if (c < pair_tiles) {
+        w.nsk = 1;
+        w.j_first = w.j_last = c;
+        w.c_first = r ? h : 0;
+        w.c_last = r ? kchunks : h;
+      }
+    } else if (b < sk_ctas) {
       const long long s0 = static_cast<long long>(b) * sk_chunks / sk_ctas;
       const long long s1 = static_cast<long long>(b + 1) * sk_chunks / sk_ctas;
       if (s1 > s0) {
@@ -222,6 +240,7 @@ struct LowSched {
       c1 = jj == w.j_last ? w.c_last : kchunks;
       tile = dp_tiles + jj;
       j = (c0 == 0 && c1 == kchunks) ? -1 : jj;
+      if (pair_tiles > 0) kind = 2;  // half of a tile split within the cluster
     } else if (i < w.nsk + w.ndp) {
       tile = b + (i - w.nsk) * G;
       c0 = 0;
@@ -297,7 +316,10 @@ __device__ __forceinline__ bool wait_flag(const unsigned int* flag, volatile int
 // fgq_quant_act_1x128, into shared memory that holds all of A's K chunks
 // (codes in the 128-byte-swizzled layout a TMA load would write) and their
 // scales for the whole kernel.
-template <int MP, bool OUT_BF16, int FUSE>
+// PAIR: launched in clusters of two with the cluster-pair split of the
+// schedule (sched.pair_tiles); the receive buffer and its barrier follow the
+// control words in shared memory.
+template <int MP, bool OUT_BF16, int FUSE, bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_lowm_kernel(const __grid_constant__ CUtensorMap tmap_w,   // Wq [N, K], box 128 x BN rows
                      const __grid_constant__ CUtensorMap tmap_a,   // Aq [M, K], box 128 x MP rows
@@ -330,6 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  uint64_t* recv_bar = reinterpret_cast<uint64_t*>(tmem_slot + 4);  // 8-byte aligned
+  float* recv = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(recv_bar + 1) + 15) & ~static_cast<uintptr_t>(15));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kchunks = sched.kchunks;
@@ -348,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[b], kEpiWarps);
     }
     mbar_init(drain, 1);
+    if (PAIR) mbar_init(recv_bar, 32 * kEpiWarps);  // every epilogue thread of the peer
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tmap_w);
@@ -358,7 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();  // the peer's receive barrier exists before anyone arrives on it
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // Everything above (barrier set-up, TMEM allocation) may overlap the
@@ -618,6 +647,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // (Loops over acc are unrolled with per-element guards so that acc
       // stays in registers.)
+      if (PAIR && kind == 2) {
+        // Half of a tile split within the cluster: rank 1 sends its partial
+        // into rank 0's receive buffer (distributed shared memory, layout
+        // [HALF/4][256 threads][4]); rank 0 adds it to its own (rank 0's
+        // half plus rank 1's: a fixed order) and writes C.
+        if (blockIdx.x & 1) {
+          const uint32_t dst = mapa_shared(recv, 0) + static_cast<uint32_t>(et) * 16;
+#pragma unroll
+          for (int g = 0; g < HALF / 4; ++g)
+            asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + g * 4096),
+                         "f"(acc[4 * g]), "f"(acc[4 * g + 1]), "f"(acc[4 * g + 2]), "f"(acc[4 * g + 3])
+                         : "memory");
+          mbar_arrive_cluster(mapa_shared(recv_bar, 0));  // release: orders the stores above
+        } else {
+          ok = named_barrier_and(kEpiBarrier, 32 * kEpiWarps,
+                                 mbar_wait_cluster(recv_bar, 0, abort_flag, FGQ_DEVERR_SK_FLAG));
+          if (!ok) break;
+          const float4* src = reinterpret_cast<const float4*>(recv) + et;
+#pragma unroll
+          for (int g = 0; g < HALF / 4; ++g) {
+            const float4 v = src[g * 256];
+            const float pv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const int m = m0 + 4 * g + t;
+              if (m < M) {
+                const float sum = acc[4 * g + t] + pv[t];
+                if (OUT_BF16)
+                  static_cast<uint16_t*>(C)[static_cast<int64_t>(m) * ldc + n] = f32_to_bf16_rn(sum);
+                else
+                  static_cast<float*>(C)[static_cast<int64_t>(m) * ldc + n] = sum;
+              }
+            }
+          }
+        }
+        continue;
+      }
       if (jsk < 0) {  // a whole tile
 #pragma unroll
         for (int j = 0; j < HALF; ++j) {
@@ -736,7 +802,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();  // neither CTA leaves while its peer may still reach its memory
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, CF::kTmemCols);
@@ -751,6 +820,7 @@ int mp_for(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <=
 struct LowPlan {
   LowSched sched;
   int grid;
+  bool pairs;              // clusters of two with the cluster-pair split
   int slots;               // partial-tile slots (stream-K)
   size_t counter_bytes;    // per stream-K tile arrival counters (zero between calls)
   size_t flag_bytes;       // per slot ready flags (zero between calls)
@@ -788,17 +858,48 @@ LowPlan lowm_plan(int64_t M, int64_t N, int64_t K, int sm_count, bool stream_k) 
   p.sched.dp_tiles = dp;
   p.sched.sk_ctas = sk;
   p.sched.sk_chunks = static_cast<long long>(T - dp) * kc;
+  p.sched.pair_tiles = 0;
   // CTAs with whole tiles only take the fix-ups (when there are any)
   p.sched.reducers = (sk > 0 && dp > 0 && G > sk) ? G - sk : 0;
   if (dp == T)
     p.grid = T < sm_count ? T : sm_count;
   else
     p.grid = dp > 0 ? G : sk;
+  p.pairs = false;
   const int L = T - dp;
   p.slots = sk > 0 ? sk + L - 1 : 0;
   p.counter_bytes = sk > 0 ? round256(static_cast<size_t>(L) * sizeof(unsigned int)) : 0;
   p.flag_bytes = sk > 0 ? round256(static_cast<size_t>(p.slots) * sizeof(unsigned int)) : 0;
   p.partial_bytes = static_cast<size_t>(p.slots) * mp * BN * sizeof(float);
+  return p;
+}
+
+// Whole tiles, except that the tiles left after the last whole wave of G =
+// 2 * clusters CTAs (or all tiles, when there are at most G / 2 of them) are
+// split in K between the two CTAs of a cluster, when that leaves each
+// cluster at most one such tile.  Falls back to lowm_plan(..., false).
+LowPlan lowm_plan_pairs(int64_t M, int64_t N, int64_t K, int sm_count, int clusters) {
+  LowPlan p = lowm_plan(M, N, K, sm_count, false);
+  const int T = static_cast<int>(N / BN), kc = static_cast<int>(K / BK);
+  const int G = 2 * clusters;
+  if (clusters < 1 || kc < 2 || mp_for(M) > 64) return p;
+  int dp, L;
+  if (T <= clusters) {
+    dp = 0;
+    L = T;
+  } else if (T > G && T % G != 0 && T % G <= clusters) {
+    L = T % G;
+    dp = T - L;
+  } else {
+    return p;
+  }
+  p.sched.dp_tiles = dp;
+  p.sched.pair_tiles = L;
+  p.sched.sk_ctas = 0;
+  p.sched.sk_chunks = 0;
+  p.sched.reducers = 0;
+  p.grid = dp > 0 ? G : 2 * L;
+  p.pairs = true;
   return p;
 }
 
@@ -842,6 +943,90 @@ cudaError_t launch_lowm(const uint8_t* A, const float* sA, const uint8_t* B, con
                     static_cast<const uint16_t*>(nullptr), int64_t{0});
 }
 
+// The cluster-pair variant: clusters of two that fit at once (cached per
+// device; 0 when it cannot run), then the launch.
+template <int MP, bool OUT_BF16>
+cudaError_t lowm_pair_clusters(const DeviceInfo& dev, int* clusters) {
+  using CF = LowCfg<MP>;
+  auto kern = gemm_lowm_kernel<MP, OUT_BF16, 0, true>;
+  static std::mutex mu;
+  static int cached[64] = {};
+  static bool ready[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  if (!ready[dev.device]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(CF::kPairSmemBytes));
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (dev.sm_count / 2));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = CF::kPairSmemBytes;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    cached[dev.device] = n;
+    ready[dev.device] = true;
+  }
+  *clusters = cached[dev.device];
+  return cudaSuccess;
+}
+
+template <int MP, bool OUT_BF16>
+cudaError_t launch_lowm_pair(const uint8_t* A, const float* sA, const uint8_t* B,
+                             const float* sB, void* C, int64_t ldc, int M, int N, int K,
+                             const LowPlan& plan, cudaStream_t stream) {
+  using CF = LowCfg<MP>;
+  CUtensorMap tw, ta;
+  if (!make_k_major_map(&tw, B, N, K, BN) || !make_k_major_map(&ta, A, M, K, MP))
+    return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = dim3(plan.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = CF::kPairSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemm_lowm_kernel<MP, OUT_BF16, 0, true>, tw, ta, sA, sB, C, ldc,
+                            M, N, K, plan.sched, static_cast<float*>(nullptr),
+                            static_cast<unsigned int*>(nullptr),
+                            static_cast<unsigned int*>(nullptr),
+                            static_cast<const uint16_t*>(nullptr), int64_t{0});
+}
+
+// Whole tiles with the cluster-pair split of the tail when it applies.
+template <int MP, bool OUT_BF16>
+cudaError_t launch_lowm_auto(const uint8_t* A, const float* sA, const uint8_t* B,
+                             const float* sB, void* C, int64_t ldc, int M, int N, int K,
+                             bool pairs_allowed, cudaStream_t stream, const DeviceInfo& dev) {
+  int clusters = 0;
+  if (pairs_allowed) {
+    const cudaError_t e = lowm_pair_clusters<MP, OUT_BF16>(dev, &clusters);
+    if (e != cudaSuccess) return e;
+  }
+  const LowPlan plan = lowm_plan_pairs(M, N, K, dev.sm_count, clusters);
+  if (plan.pairs) return launch_lowm_pair<MP, OUT_BF16>(A, sA, B, sB, C, ldc, M, N, K, plan, stream);
+  return launch_lowm<MP, OUT_BF16>(A, sA, B, sB, C, ldc, M, N, K, plan, nullptr, stream, dev);
+}
+
 // A as bf16, quantized inside the kernel (FUSE = scale mode + 1); whole
 // tiles only.
 template <int MP, bool OUT_BF16, int FUSE>
@@ -870,7 +1055,53 @@ cudaError_t launch_lowm_fused(const uint16_t* a16, int64_t lda, const uint8_t* B
   }
   CUtensorMap tw, ta_unused = {};
   if (!make_k_major_map(&tw, B, N, K, BN)) return cudaErrorInvalidValue;
-  const LowPlan plan = lowm_plan(M, N, K, dev.sm_count, false);
+  // The same schedule as the GEMM on quantized activations (launch_lowm_auto
+  // with the same cluster count), so that the two give the same bits: the
+  // tail split within clusters of two when the receive buffer fits next to
+  // the resident activations.
+  LowPlan plan = lowm_plan(M, N, K, dev.sm_count, false);
+  const size_t pair_smem = smem + 64 + CF::kRecvBytes;
+  if (pair_smem <= static_cast<size_t>(kMaxSmemOptin)) {
+    int clusters = 0;
+    cudaError_t e = lowm_pair_clusters<MP, OUT_BF16>(dev, &clusters);
+    if (e != cudaSuccess) return e;
+    plan = lowm_plan_pairs(M, N, K, dev.sm_count, clusters);
+    if (plan.pairs) {
+      auto pkern = gemm_lowm_kernel<MP, OUT_BF16, FUSE, true>;
+      static std::mutex pmu;
+      static bool pready[64] = {};
+      {
+        std::lock_guard<std::mutex> lock(pmu);
+        if (!pready[dev.device]) {
+          e = cudaFuncSetAttribute(pkern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmemOptin);
+          if (e != cudaSuccess) return e;
+          cudaFuncAttributes fa;
+          e = cudaFuncGetAttributes(&fa, pkern);
+          if (e != cudaSuccess) return e;
+          if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+          pready[dev.device] = true;
+        }
+      }
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[2];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
+      cfg.gridDim = dim3(plan.grid);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = pair_smem;
+      cfg.stream = stream;
+      cfg.attrs = attr;
+      cfg.numAttrs = 2;
+      return cudaLaunchKernelEx(&cfg, pkern, tw, ta_unused, static_cast<const float*>(nullptr), sB,
+                                C, ldc, M, N, K, plan.sched, static_cast<float*>(nullptr),
+                                static_cast<unsigned int*>(nullptr),
+                                static_cast<unsigned int*>(nullptr), a16, lda);
+    }
+  }
   return launch_pdl(kern, dim3(plan.grid), dim3(kThreads), smem, stream, tw, ta_unused,
                     static_cast<const float*>(nullptr), sB, C, ldc, M, N, K, plan.sched,
                     static_cast<float*>(nullptr), static_cast<unsigned int*>(nullptr),
@@ -914,6 +1145,12 @@ bool lowm_fused_fits(int64_t M, int64_t K) {
   return M >= 1 && M <= 32 && K / BK <= 4096 && lowm_fused_smem_bytes(M, K) <= kMaxSmemOptin;
 }
 
+// The fused kernel also has room for the cluster-pair receive buffer.
+bool lowm_fused_pair_fits(int64_t M, int64_t K) {
+  const size_t recv = M <= 16 ? LowCfg<16>::kRecvBytes : LowCfg<32>::kRecvBytes;
+  return lowm_fused_fits(M, K) && lowm_fused_smem_bytes(M, K) + 64 + recv <= kMaxSmemOptin;
+}
+
 cudaError_t launch_gemm_lowm_fused(const void* a16, int64_t lda, const uint8_t* B, const float* sB,
                                    void* C, int64_t ldc, int64_t M, int64_t N, int64_t K,
                                    int out_bf16, int mode, cudaStream_t stream,
@@ -943,6 +1180,20 @@ cudaError_t launch_gemm_lowm(const uint8_t* A, const float* sA, const uint8_t* B
                              const DeviceInfo& dev) {
   if (M == 0) return cudaSuccess;
   const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  if (!stream_k && M <= 64) {
+    // No workspace: whole tiles, the tail split within clusters of two.
+    // For M <= 32 the split is taken only where the GEMM that quantizes its
+    // activations itself can take it too, so that both give the same bits.
+    const bool pairs = M > 32 || !lowm_fused_fits(M, K) || lowm_fused_pair_fits(M, K);
+    if (M <= 16)
+      return out_bf16 ? launch_lowm_auto<16, true>(A, sA, B, sB, C, ldc, m, n, k, pairs, stream, dev)
+                      : launch_lowm_auto<16, false>(A, sA, B, sB, C, ldc, m, n, k, pairs, stream, dev);
+    if (M <= 32)
+      return out_bf16 ? launch_lowm_auto<32, true>(A, sA, B, sB, C, ldc, m, n, k, pairs, stream, dev)
+                      : launch_lowm_auto<32, false>(A, sA, B, sB, C, ldc, m, n, k, pairs, stream, dev);
+    return out_bf16 ? launch_lowm_auto<64, true>(A, sA, B, sB, C, ldc, m, n, k, pairs, stream, dev)
+                    : launch_lowm_auto<64, false>(A, sA, B, sB, C, ldc, m, n, k, pairs, stream, dev);
+  }
   const LowPlan plan = lowm_plan(M, N, K, dev.sm_count, stream_k);
   if (plan.sched.sk_ctas > 0 && workspace == nullptr) return cudaErrorInvalidValue;
   return out_bf16 ? dispatch_mp<true>(A, sA, B, sB, C, ldc, m, n, k, plan, workspace, stream, dev)

@@ -166,7 +166,13 @@ fgq_status fgq_quant_operands(const void* x, int64_t M, int64_t K, int64_t ldx, 
  * Each 128-wide K chunk is one tensor-core partial product in TMEM, which is
  * scaled by sA * sB and added into an fp32 accumulator (the page's
  * promotion step, done by the epilogue warps).  For M <= 32 the operands
- * are swapped so the tensor core's 128-row side runs over the weight.
+ * are swapped so the tensor core's 128-row side runs over the weight, and
+ * the 128-column tiles of C left after the last whole wave over the SMs
+ * (all of them, when there are at most one per pair of SMs) are split in
+ * two halves of K between the two CTAs of a cluster, the halves added
+ * through distributed shared memory in a fixed order (deterministic, no
+ * workspace).  Results for M <= 32 are the same bits as
+ * fgq_gemm_fp8_blockscaled_fused_act on the unquantized activations.
  */
 fgq_status fgq_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const uint8_t* B,
                                     const float* sB, float* C, int64_t M, int64_t N,

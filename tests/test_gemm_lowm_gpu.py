@@ -170,5 +170,26 @@ def test_stream_k_shapes(fgq, cuda_dev, M, N, K, mode):
     assert fgq.device_error() == 0
 
 
+# The default entry point's cluster-pair split (no workspace): the tiles
+# after the last whole wave, or all tiles when there are at most one per
+# cluster, are split in K within clusters of two (odd chunk counts split
+# unevenly); other shapes run whole tiles.  For a GB300's 152 SMs.
+PAIR_SHAPES = [(16, 128 * 192, 1536), (32, 128 * 155, 640), (9, 128 * 3, 3 * 128),
+               (16, 128 * 76, 256), (16, 128 * 252, 256), (16, 1024, 128), (30, 128 * 40, 8 * 128)]
+
+
+@pytest.mark.parametrize("M,N,K", PAIR_SHAPES)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_lowm_cluster_pair_split(fgq, cuda_dev, M, N, K, out_dtype):
+    host = _operands(M, N, K, seed=N % 991 + M)
+    ops = _dev(*host, cuda_dev)
+    c1 = fgq.gemm_fp8_blockscaled(*ops, out_dtype=out_dtype)
+    c2 = fgq.gemm_fp8_blockscaled(*ops, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    _check(c1, host)
+    assert torch.equal(c1, c2), "the split result changed between calls"
+    assert fgq.device_error() == 0
+
+
 def test_no_device_error_after_lowm(fgq, cuda_dev):
     assert fgq.device_error() == 0
