@@ -16,6 +16,9 @@ What each function follows ("Fine-Grained FP8/FP4 Quantization" page):
   ue8m0_*           §Blackwell: Native Block Scaling (2^(e-127), 4 per word)
   gemm_*            §DeepGEMM: C += partial * scale_A * scale_B per
                     128-wide K chunk, i.e. the fp64 dequantised product.
+  fp4_scale_tiles   the FP4 block scales in the library's tiled storage
+                    layout (a permutation; its definition is in the
+                    docstring).
 
 Parity is pinned for every function (tests/test_oracle_pins.py); nothing
 here is "parity unpinned".
@@ -333,6 +336,32 @@ def gemm_nvfp4_at(aq, sa, ga, bq, sb, gb, rows, cols):
     if rc != 0:
         raise ValueError(f"oracle gemm_nvfp4_at failed ({rc})")
     return c, t
+
+
+def fp4_scale_tiles(s):
+    """FP4 block-scale codes s uint8 [R, F] (F % 4 == 0: MXFP4 F = K/32,
+    NVFP4 F = K/16) in the tiled layout the FP4 GEMM's tensor-map loads
+    take.  The layout is this library's storage format, not the page's: it
+    follows from how the block-scaled MMA reads its factors (row m of a
+    128-row tile at TMEM lane m, column m / 32; four factor bytes per
+    32-bit cell, §Blackwell: Native Block Scaling) and from the copy that
+    puts a 32-row x 16-byte shared-memory tile into all four lane quarters.
+
+    Every code s[r, f] goes to byte
+        ((r // 128) * (F // 4) + f // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + f % 4
+    of a uint8 array of ceil(R / 128) * 128 * F bytes; the bytes of rows
+    R .. (multiple of 128) - 1 are zero here.  A pure permutation: no
+    arithmetic on the codes."""
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    R, F = s.shape
+    if F % 4 != 0:
+        raise ValueError("fp4_scale_tiles: F must be a multiple of 4")
+    out = np.zeros(((R + 127) // 128) * 128 * F, dtype=np.uint8)
+    r = np.arange(R, dtype=np.int64)[:, None]
+    f = np.arange(F, dtype=np.int64)[None, :]
+    off = ((r // 128) * (F // 4) + f // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + f % 4
+    out[off] = s
+    return out
 
 
 def quant_w_128x128(w_bf16, mode: int = MODE_FP32):

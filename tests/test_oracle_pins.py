@@ -641,3 +641,43 @@ def test_parallel_gemm_reference_is_the_whole_matrix_call():
         cp, tp = gemm_dequant_parallel(aq, sa, bq, sb, workers=workers, blocks_per_task=per)
         assert np.array_equal(cp.view(np.uint64), c.view(np.uint64))
         assert np.array_equal(tp.view(np.uint64), t.view(np.uint64))
+
+
+def test_fp4_scale_tiles_by_hand():
+    """Positions worked out by hand from the tiled layout's definition
+    (512-byte tiles of 128 rows x 4 factor bytes; in a tile, row r at
+    16 (r % 32) + 4 ((r % 128) / 32), factor byte f at + f % 4)."""
+    R, F = 130, 8
+    r = np.arange(R)[:, None]
+    f = np.arange(F)[None, :]
+    s = ((7 * r + 3 * f + 1) % 251).astype(np.uint8)
+    t = oracle.fp4_scale_tiles(s)
+    assert t.shape == (2 * 128 * F,)
+    cases = {(0, 0): 0, (1, 0): 16, (32, 0): 4, (64, 4): 520, (33, 5): 533,
+             (127, 3): 511, (129, 7): 1555, (128, 0): 1024, (96, 2): 14}
+    for (rr, ff), off in cases.items():
+        assert t[off] == s[rr, ff], (rr, ff, off)
+    # rows 130..255 of the second row tile are padding: zero
+    assert t[1024 + 2 * 16] == 0 and t[1024 + 31 * 16 + 3 * 4 + 3] == 0
+
+
+def test_fp4_scale_tiles_is_a_permutation_matching_the_tensor_core_reading():
+    """Every code lands exactly once, and read as [row tile, cell, lane i,
+    quarter j, byte b] the tiles give code s[128 tile + 32 j + i, 4 cell + b]:
+    the factor of row m sits in lane m % 32 of quarter m / 32."""
+    R, F = 256, 12
+    s = np.arange(R * F, dtype=np.int64).reshape(R, F)
+    lo = (s % 256).astype(np.uint8)
+    hi = (s // 256).astype(np.uint8)
+    tl, th = oracle.fp4_scale_tiles(lo), oracle.fp4_scale_tiles(hi)
+    back = tl.astype(np.int64) + 256 * th.astype(np.int64)
+    assert np.array_equal(np.sort(back), np.arange(R * F))
+    v = back.reshape(R // 128, F // 4, 32, 4, 4)
+    for rb in range(R // 128):
+        for c in range(F // 4):
+            for i in (0, 5, 31):
+                for j in range(4):
+                    m = 128 * rb + 32 * j + i
+                    assert list(v[rb, c, i, j]) == list(s[m, 4 * c:4 * c + 4])
+    with pytest.raises(ValueError):
+        oracle.fp4_scale_tiles(np.zeros((4, 6), dtype=np.uint8))
