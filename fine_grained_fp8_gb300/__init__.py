@@ -27,7 +27,9 @@ from ._lib import (FGQ_OUT_BF16, FGQ_OUT_F32, FGQ_SCALE_FP32, FGQ_SCALE_UE8M0, F
 __all__ = ["quant_act_1x128", "quant_act_128x1", "quant_operands", "quant_mxfp4_1x32", "nvfp4_global_scale",
            "quant_nvfp4_1x16", "quant_w_128x128", "gemm_fp8_blockscaled",
            "gemm_fp8_blockscaled_splitk", "gemm_fp8_blockscaled_fused_act", "gemm_mxfp4",
-           "gemm_nvfp4", "splitk_workspace", "device_error",
+           "gemm_nvfp4", "fp4_scale_tiles_bytes", "fp4_scales_to_tiles",
+           "quant_mxfp4_1x32_tiled", "quant_nvfp4_1x16_tiled", "gemm_mxfp4_tiled",
+           "gemm_nvfp4_tiled", "splitk_workspace", "device_error",
            "FgqError", "load", "FGQ_SCALE_FP32", "FGQ_SCALE_UE8M0", "FGQ_OUT_F32",
            "FGQ_OUT_BF16", "scale_mode"]
 
@@ -338,6 +340,141 @@ def gemm_nvfp4(aq: torch.Tensor, sa: torch.Tensor, ga: torch.Tensor, bq: torch.T
                              FGQ_OUT_BF16 if out_dtype == torch.bfloat16 else FGQ_OUT_F32,
                              _stream(aq))
     check("fgq_gemm_nvfp4", st)
+    return out
+
+
+def fp4_scale_tiles_bytes(R: int, F: int) -> int:
+    """Bytes of FP4 block scales for R rows of F factor bytes (F = K/32 for
+    MXFP4, K/16 for NVFP4) in the tiled layout: ceil(R/128) * 128 * F."""
+    st, n = _lib.fgq_fp4_scale_tiles_bytes(R, F)
+    check("fgq_fp4_scale_tiles_bytes", st)
+    return n
+
+
+def fp4_scales_to_tiles(s: torch.Tensor, tiles: torch.Tensor | None = None) -> torch.Tensor:
+    """Row-major FP4 block scales s [R, F] uint8 (F % 4 == 0) in the tiled
+    layout the _tiled GEMMs take: a 1-D uint8 tensor of
+    fp4_scale_tiles_bytes(R, F) bytes (pad rows left as they are)."""
+    _need_cuda("s", s, torch.uint8)
+    if s.dim() != 2 or not s.is_contiguous():
+        raise ValueError("s must be a dense [R, F]")
+    R, F = s.shape
+    n = fp4_scale_tiles_bytes(R, F)
+    if tiles is None:
+        tiles = torch.empty((n,), dtype=torch.uint8, device=s.device)
+    _need_cuda("tiles", tiles, torch.uint8)
+    if tiles.numel() != n or not tiles.is_contiguous():
+        raise ValueError(f"tiles must be a dense uint8 tensor of {n} bytes")
+    st = _lib.fgq_fp4_scales_to_tiles(s.data_ptr(), R, F, tiles.data_ptr(), _stream(s))
+    check("fgq_fp4_scales_to_tiles", st)
+    return tiles
+
+
+def _tiles_out(t, n, dev, name):
+    if t is None:
+        t = torch.empty((n,), dtype=torch.uint8, device=dev)
+    _need_cuda(name, t, torch.uint8)
+    if t.numel() != n or not t.is_contiguous():
+        raise ValueError(f"{name} must be a dense uint8 tensor of {n} bytes")
+    return t
+
+
+def quant_mxfp4_1x32_tiled(x: torch.Tensor, xq: torch.Tensor | None = None,
+                           s_tiles: torch.Tensor | None = None):
+    """quant_mxfp4_1x32 with the scales in the tiled layout: returns (xq
+    [R, K/2], scale tiles as a 1-D uint8 tensor).  K % 128 == 0."""
+    _need_cuda("x", x, torch.bfloat16)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with a contiguous last dimension")
+    R, K = x.shape
+    if xq is None:
+        xq = torch.empty((R, K // 2), dtype=torch.uint8, device=x.device)
+    _need_cuda("xq", xq, torch.uint8)
+    if xq.shape != (R, K // 2) or not xq.is_contiguous():
+        raise ValueError("xq must be a dense [R, K/2]")
+    tiles = _tiles_out(s_tiles, fp4_scale_tiles_bytes(R, K // 32), x.device, "s_tiles")
+    st = _lib.fgq_quant_mxfp4_1x32_tiled(x.data_ptr(), R, K, x.stride(0), xq.data_ptr(),
+                                         tiles.data_ptr(), _stream(x))
+    check("fgq_quant_mxfp4_1x32_tiled", st)
+    return xq, tiles
+
+
+def quant_nvfp4_1x16_tiled(x: torch.Tensor, g: torch.Tensor | None = None,
+                           xq: torch.Tensor | None = None, s_tiles: torch.Tensor | None = None):
+    """quant_nvfp4_1x16 with the scales in the tiled layout: returns (xq
+    [R, K/2], scale tiles as a 1-D uint8 tensor, g).  K % 64 == 0."""
+    _need_cuda("x", x, torch.bfloat16)
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be 2-D with a contiguous last dimension")
+    R, K = x.shape
+    if g is None:
+        g = nvfp4_global_scale(x)
+    _need_cuda("g", g, torch.float32)
+    if xq is None:
+        xq = torch.empty((R, K // 2), dtype=torch.uint8, device=x.device)
+    _need_cuda("xq", xq, torch.uint8)
+    if xq.shape != (R, K // 2) or not xq.is_contiguous():
+        raise ValueError("xq must be a dense [R, K/2]")
+    tiles = _tiles_out(s_tiles, fp4_scale_tiles_bytes(R, K // 16), x.device, "s_tiles")
+    st = _lib.fgq_quant_nvfp4_1x16_tiled(x.data_ptr(), R, K, x.stride(0), g.data_ptr(),
+                                         xq.data_ptr(), tiles.data_ptr(), _stream(x))
+    check("fgq_quant_nvfp4_1x16_tiled", st)
+    return xq, tiles, g
+
+
+def _fp4_tiled_operands(aq, sa, bq, sb, per):
+    for name, t in (("aq", aq), ("sa", sa), ("bq", bq), ("sb", sb)):
+        _need_cuda(name, t, torch.uint8)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    M, K = aq.shape[0], 2 * aq.shape[1]
+    N = bq.shape[0]
+    if bq.shape != (N, K // 2):
+        raise ValueError("shape mismatch: aq [M, K/2], bq [N, K/2]")
+    if K % per != 0 or (K // per) % 4 != 0:
+        raise ValueError("K must give a whole number of 4-byte factor cells")
+    if sa.numel() != fp4_scale_tiles_bytes(M, K // per) or \
+            sb.numel() != fp4_scale_tiles_bytes(N, K // per):
+        raise ValueError("sa / sb must be scale tiles of fp4_scale_tiles_bytes(rows, K/%d)" % per)
+    return M, N, K
+
+
+def gemm_mxfp4_tiled(aq: torch.Tensor, sa: torch.Tensor, bq: torch.Tensor, sb: torch.Tensor,
+                     out_dtype=torch.float32, out: torch.Tensor | None = None) -> torch.Tensor:
+    """gemm_mxfp4 with sa and sb as scale tiles (quant_mxfp4_1x32_tiled or
+    fp4_scales_to_tiles)."""
+    M, N, K = _fp4_tiled_operands(aq, sa, bq, sb, 32)
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=aq.device)
+    _need_cuda("out", out, out_dtype)
+    if out.shape != (M, N) or out.stride(1) != 1:
+        raise ValueError("out must be [M, N] with contiguous rows")
+    st = _lib.fgq_gemm_mxfp4_tiled(aq.data_ptr(), sa.data_ptr(), bq.data_ptr(), sb.data_ptr(),
+                                   out.data_ptr(), out.stride(0), M, N, K,
+                                   FGQ_OUT_BF16 if out_dtype == torch.bfloat16 else FGQ_OUT_F32,
+                                   _stream(aq))
+    check("fgq_gemm_mxfp4_tiled", st)
+    return out
+
+
+def gemm_nvfp4_tiled(aq: torch.Tensor, sa: torch.Tensor, ga: torch.Tensor, bq: torch.Tensor,
+                     sb: torch.Tensor, gb: torch.Tensor, out_dtype=torch.float32,
+                     out: torch.Tensor | None = None) -> torch.Tensor:
+    """gemm_nvfp4 with sa and sb as scale tiles (quant_nvfp4_1x16_tiled or
+    fp4_scales_to_tiles)."""
+    M, N, K = _fp4_tiled_operands(aq, sa, bq, sb, 16)
+    _need_cuda("ga", ga, torch.float32)
+    _need_cuda("gb", gb, torch.float32)
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=aq.device)
+    _need_cuda("out", out, out_dtype)
+    if out.shape != (M, N) or out.stride(1) != 1:
+        raise ValueError("out must be [M, N] with contiguous rows")
+    st = _lib.fgq_gemm_nvfp4_tiled(aq.data_ptr(), sa.data_ptr(), ga.data_ptr(), bq.data_ptr(),
+                                   sb.data_ptr(), gb.data_ptr(), out.data_ptr(), out.stride(0), M,
+                                   N, K, FGQ_OUT_BF16 if out_dtype == torch.bfloat16 else FGQ_OUT_F32,
+                                   _stream(aq))
+    check("fgq_gemm_nvfp4_tiled", st)
     return out
 
 

@@ -48,6 +48,13 @@ SIGNATURES = {
     "fgq_gemm_mxfp4": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _vp]),
     "fgq_gemm_nvfp4": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int,
                               _vp]),
+    "fgq_gemm_mxfp4_tiled": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _vp]),
+    "fgq_gemm_nvfp4_tiled": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                    _int, _vp]),
+    "fgq_quant_mxfp4_1x32_tiled": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp]),
+    "fgq_quant_nvfp4_1x16_tiled": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "fgq_fp4_scale_tiles_bytes": (_int, [_i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
+    "fgq_fp4_scales_to_tiles": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "fgq_gemm_fp8_blockscaled_fused_act": (_int, [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                                   _int, _int, _vp]),
     "fgq_gemm_fp8_blockscaled_splitk_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
@@ -165,6 +172,32 @@ def fgq_gemm_mxfp4(A, sA, B, sB, C, ldc, M, N, K, out, stream) -> int:
 
 def fgq_gemm_nvfp4(A, sA, gA, B, sB, gB, C, ldc, M, N, K, out, stream) -> int:
     return load().fgq_gemm_nvfp4(A, sA, gA, B, sB, gB, C, ldc, M, N, K, out, stream)
+
+
+def fgq_gemm_mxfp4_tiled(A, sA, B, sB, C, ldc, M, N, K, out, stream) -> int:
+    return load().fgq_gemm_mxfp4_tiled(A, sA, B, sB, C, ldc, M, N, K, out, stream)
+
+
+def fgq_gemm_nvfp4_tiled(A, sA, gA, B, sB, gB, C, ldc, M, N, K, out, stream) -> int:
+    return load().fgq_gemm_nvfp4_tiled(A, sA, gA, B, sB, gB, C, ldc, M, N, K, out, stream)
+
+
+def fgq_quant_mxfp4_1x32_tiled(x, R, K, ldx, xq, s_tiles, stream) -> int:
+    return load().fgq_quant_mxfp4_1x32_tiled(x, R, K, ldx, xq, s_tiles, stream)
+
+
+def fgq_quant_nvfp4_1x16_tiled(x, R, K, ldx, g, xq, s_tiles, stream) -> int:
+    return load().fgq_quant_nvfp4_1x16_tiled(x, R, K, ldx, g, xq, s_tiles, stream)
+
+
+def fgq_fp4_scale_tiles_bytes(R, F):
+    n = ctypes.c_size_t(0)
+    st = load().fgq_fp4_scale_tiles_bytes(R, F, ctypes.byref(n))
+    return st, int(n.value)
+
+
+def fgq_fp4_scales_to_tiles(s, R, F, tiles, stream) -> int:
+    return load().fgq_fp4_scales_to_tiles(s, R, F, tiles, stream)
 
 
 def fgq_gemm_splitk_workspace_size(M, N, K):

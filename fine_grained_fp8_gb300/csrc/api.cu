@@ -104,7 +104,22 @@ fgq_status fgq_quant_mxfp4_1x32(const void* x, int64_t R, int64_t K, int64_t ldx
   fgq::DeviceInfo dev;
   fgq_status st = get_device(&dev);
   if (st != FGQ_OK) return st;
-  return from_cuda(fgq::launch_quant_mxfp4_1x32(x, R, K, ldx, xq, sx,
+  return from_cuda(fgq::launch_quant_mxfp4_1x32(x, R, K, ldx, xq, sx, false,
+                                                static_cast<cudaStream_t>(stream), dev));
+}
+
+fgq_status fgq_quant_mxfp4_1x32_tiled(const void* x, int64_t R, int64_t K, int64_t ldx,
+                                      uint8_t* xq, uint8_t* s_tiles, void* stream) {
+  if (R < 0 || K <= 0 || K % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (R == 0) return FGQ_OK;
+  if (!x || !xq || !s_tiles) return FGQ_ERR_INVALID_ARG;
+  if (ldx < K || ldx % 8 != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(xq, 4)) return FGQ_ERR_INVALID_ARG;
+  if (R > kMaxGroups / (K / 32)) return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_quant_mxfp4_1x32(x, R, K, ldx, xq, s_tiles, true,
                                                 static_cast<cudaStream_t>(stream), dev));
 }
 
@@ -132,7 +147,7 @@ fgq_status fgq_quant_nvfp4_1x16(const void* x, int64_t R, int64_t K, int64_t ldx
   fgq::DeviceInfo dev;
   fgq_status st = get_device(&dev);
   if (st != FGQ_OK) return st;
-  return from_cuda(fgq::launch_quant_nvfp4_1x16(x, R, K, ldx, g, xq, sx,
+  return from_cuda(fgq::launch_quant_nvfp4_1x16(x, R, K, ldx, g, xq, sx, false,
                                                 static_cast<cudaStream_t>(stream), dev));
 }
 
@@ -245,6 +260,41 @@ fgq_status fgq_gemm_fp8_blockscaled_fused_act(const void* A, int64_t lda, const 
                                                static_cast<cudaStream_t>(stream), dev));
 }
 
+fgq_status fgq_quant_nvfp4_1x16_tiled(const void* x, int64_t R, int64_t K, int64_t ldx,
+                                      const float* g, uint8_t* xq, uint8_t* s_tiles, void* stream) {
+  if (R < 0 || K <= 0 || K % 64 != 0) return FGQ_ERR_INVALID_ARG;
+  if (R == 0) return FGQ_OK;
+  if (!x || !g || !xq || !s_tiles) return FGQ_ERR_INVALID_ARG;
+  if (ldx < K || ldx % 8 != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(g, 4) || !aligned(xq, 4)) return FGQ_ERR_INVALID_ARG;
+  if (R > kMaxGroups / (K / 16)) return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_quant_nvfp4_1x16(x, R, K, ldx, g, xq, s_tiles, true,
+                                                static_cast<cudaStream_t>(stream), dev));
+}
+
+fgq_status fgq_fp4_scale_tiles_bytes(int64_t R, int64_t F, size_t* bytes) {
+  if (!bytes || R < 0 || F <= 0 || F % 4 != 0) return FGQ_ERR_INVALID_ARG;
+  if (R >= (int64_t{1} << 31) || F >= (int64_t{1} << 31)) return FGQ_ERR_INVALID_ARG;
+  *bytes = static_cast<size_t>((R + 127) / 128) * 128u * static_cast<size_t>(F);
+  return FGQ_OK;
+}
+
+fgq_status fgq_fp4_scales_to_tiles(const uint8_t* s, int64_t R, int64_t F, uint8_t* tiles,
+                                   void* stream) {
+  if (R < 0 || F <= 0 || F % 4 != 0) return FGQ_ERR_INVALID_ARG;
+  if (R >= (int64_t{1} << 31) || F >= (int64_t{1} << 31)) return FGQ_ERR_INVALID_ARG;
+  if (R == 0) return FGQ_OK;
+  if (!s || !tiles || !aligned(s, 4) || !aligned(tiles, 4)) return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_fp4_scales_to_tiles(s, R, F, tiles, static_cast<cudaStream_t>(stream),
+                                                   dev));
+}
+
 fgq_status fgq_gemm_mxfp4(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
                           const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
                           int64_t K, int out, void* stream) {
@@ -285,6 +335,51 @@ fgq_status fgq_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const float* gA,
   return from_cuda(fgq::launch_gemm_nvf4(A, sA, gA, B, sB, gB, C, ldc, M, N, K,
                                          out == FGQ_OUT_BF16 ? 1 : 0,
                                          static_cast<cudaStream_t>(stream), dev));
+}
+
+fgq_status fgq_gemm_mxfp4_tiled(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                                const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
+                                int64_t K, int out, void* stream) {
+  if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (out != FGQ_OUT_F32 && out != FGQ_OUT_BF16) return FGQ_ERR_INVALID_ARG;
+  if (M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31) || K >= (int64_t{1} << 31))
+    return FGQ_ERR_INVALID_ARG;
+  if (M == 0) return FGQ_OK;
+  if (!A || !sA || !B || !sB || !C) return FGQ_ERR_INVALID_ARG;
+  const int64_t vec = (out == FGQ_OUT_F32) ? 4 : 8;
+  if (ldc < N || ldc % vec != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(sA, 16) ||
+      !aligned(sB, 16))
+    return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_gemm_mxf4_tiled(A, sA, B, sB, C, ldc, M, N, K,
+                                               out == FGQ_OUT_BF16 ? 1 : 0,
+                                               static_cast<cudaStream_t>(stream), dev));
+}
+
+fgq_status fgq_gemm_nvfp4_tiled(const uint8_t* A, const uint8_t* sA, const float* gA,
+                                const uint8_t* B, const uint8_t* sB, const float* gB, void* C,
+                                int64_t ldc, int64_t M, int64_t N, int64_t K, int out,
+                                void* stream) {
+  if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (out != FGQ_OUT_F32 && out != FGQ_OUT_BF16) return FGQ_ERR_INVALID_ARG;
+  if (M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31) || K >= (int64_t{1} << 31))
+    return FGQ_ERR_INVALID_ARG;
+  if (M == 0) return FGQ_OK;
+  if (!A || !sA || !gA || !B || !sB || !gB || !C) return FGQ_ERR_INVALID_ARG;
+  const int64_t vec = (out == FGQ_OUT_F32) ? 4 : 8;
+  if (ldc < N || ldc % vec != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(sA, 16) ||
+      !aligned(sB, 16) || !aligned(gA, 4) || !aligned(gB, 4))
+    return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_gemm_nvf4_tiled(A, sA, gA, B, sB, gB, C, ldc, M, N, K,
+                                               out == FGQ_OUT_BF16 ? 1 : 0,
+                                               static_cast<cudaStream_t>(stream), dev));
 }
 
 fgq_status fgq_gemm_splitk_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {

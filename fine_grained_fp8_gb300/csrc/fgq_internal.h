@@ -38,8 +38,11 @@ cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t 
                                    float* sxt, int mode, cudaStream_t stream,
                                    const DeviceInfo& dev);
 
+// MXFP4 1x32 quantizer; with `tiled` the scales go out in the tiled FP4
+// scale layout (K % 128 == 0) instead of row-major [R, K/32].
 cudaError_t launch_quant_mxfp4_1x32(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* xq,
-                                    uint8_t* sx, cudaStream_t stream, const DeviceInfo& dev);
+                                    uint8_t* sx, bool tiled, cudaStream_t stream,
+                                    const DeviceInfo& dev);
 
 cudaError_t launch_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
                                    uint8_t* wq, float* sw, int mode, cudaStream_t stream,
@@ -77,11 +80,26 @@ cudaError_t launch_gemm_nvf4(const uint8_t* A, const uint8_t* sA, const float* g
                              const uint8_t* B, const uint8_t* sB, const float* gb, void* C,
                              int64_t ldc, int64_t M, int64_t N, int64_t K, int out_bf16,
                              cudaStream_t stream, const DeviceInfo& dev);
+// The same two GEMMs on block scales in the tiled FP4 scale layout, loaded
+// by the tensor-map engine (16-byte aligned scale tiles).
+cudaError_t launch_gemm_mxf4_tiled(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                                   const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
+                                   int64_t K, int out_bf16, cudaStream_t stream,
+                                   const DeviceInfo& dev);
+cudaError_t launch_gemm_nvf4_tiled(const uint8_t* A, const uint8_t* sA, const float* ga,
+                                   const uint8_t* B, const uint8_t* sB, const float* gb, void* C,
+                                   int64_t ldc, int64_t M, int64_t N, int64_t K, int out_bf16,
+                                   cudaStream_t stream, const DeviceInfo& dev);
+// Row-major FP4 block scales [R, F] (F % 4 == 0) into the tiled layout.
+cudaError_t launch_fp4_scales_to_tiles(const uint8_t* s, int64_t R, int64_t F, uint8_t* tiles,
+                                       cudaStream_t stream, const DeviceInfo& dev);
 cudaError_t launch_nvfp4_global_scale(const void* x, int64_t R, int64_t K, int64_t ldx, float* g,
                                       cudaStream_t stream, const DeviceInfo& dev);
+// NVFP4 1x16 quantizer; with `tiled` the scales go out in the tiled FP4
+// scale layout (K % 64 == 0) instead of row-major [R, K/16].
 cudaError_t launch_quant_nvfp4_1x16(const void* x, int64_t R, int64_t K, int64_t ldx,
-                                    const float* g, uint8_t* xq, uint8_t* sx, cudaStream_t stream,
-                                    const DeviceInfo& dev);
+                                    const float* g, uint8_t* xq, uint8_t* sx, bool tiled,
+                                    cudaStream_t stream, const DeviceInfo& dev);
 
 // Each kernel translation unit keeps its own device error word; these read
 // (and optionally clear) one unit's word.
@@ -93,6 +111,11 @@ cudaError_t read_device_error_mxf4(uint32_t* word, bool clear);
 // TMA descriptor of a K-major E4M3 operand [rows, K] with a 128 (K) x
 // box_rows box, 128-byte swizzle, zero fill outside the tensor.
 bool make_k_major_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows);
+
+// TMA descriptor of FP4 scale tiles in the tiled layout: `tiles` 512-byte
+// tiles, read box_tiles consecutive tiles at a time (no swizzle, zero fill
+// past the end).
+bool make_scale_tile_map(CUtensorMap* map, const void* base, int64_t tiles, int box_tiles);
 
 // Low-M GEMM that quantizes bf16 A (1x128, scale mode `mode`) in the kernel
 // and keeps all of it in shared memory: M <= 32 and K small enough for

@@ -673,6 +673,7 @@ struct MapCacheEntry {
   const void* base;
   int64_t rows, K;
   int box_rows;
+  int kind;  // 0: K-major operand, 1: FP4 scale tiles
   bool valid;
   CUtensorMap map;
 };
@@ -683,6 +684,34 @@ std::mutex g_map_cache_mu;
 
 bool encode_k_major_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
                         int box_rows);
+bool encode_scale_tile_map(CUtensorMap* map, const void* base, int64_t tiles, int box_tiles);
+
+bool cached_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows,
+                int kind) {
+  {
+    std::lock_guard<std::mutex> lock(g_map_cache_mu);
+    for (const MapCacheEntry& e : g_map_cache)
+      if (e.valid && e.kind == kind && e.base == base && e.rows == rows && e.K == K &&
+          e.box_rows == box_rows) {
+        *map = e.map;
+        return true;
+      }
+  }
+  const bool ok = kind == 0 ? encode_k_major_map(map, base, rows, K, box_rows)
+                            : encode_scale_tile_map(map, base, rows, box_rows);
+  if (!ok) return false;
+  std::lock_guard<std::mutex> lock(g_map_cache_mu);
+  MapCacheEntry& e = g_map_cache[g_map_cache_next];
+  g_map_cache_next = (g_map_cache_next + 1) % kMapCacheSize;
+  e.base = base;
+  e.rows = rows;
+  e.K = K;
+  e.box_rows = box_rows;
+  e.kind = kind;
+  e.map = *map;
+  e.valid = true;
+  return true;
+}
 
 }  // namespace
 
@@ -691,28 +720,30 @@ bool encode_k_major_map(CUtensorMap* map, const void* base, int64_t rows, int64_
 // cache of recent descriptors (the host-side encoding then runs once per
 // operand, not once per call).
 bool make_k_major_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
-  {
-    std::lock_guard<std::mutex> lock(g_map_cache_mu);
-    for (const MapCacheEntry& e : g_map_cache)
-      if (e.valid && e.base == base && e.rows == rows && e.K == K && e.box_rows == box_rows) {
-        *map = e.map;
-        return true;
-      }
-  }
-  if (!encode_k_major_map(map, base, rows, K, box_rows)) return false;
-  std::lock_guard<std::mutex> lock(g_map_cache_mu);
-  MapCacheEntry& e = g_map_cache[g_map_cache_next];
-  g_map_cache_next = (g_map_cache_next + 1) % kMapCacheSize;
-  e.base = base;
-  e.rows = rows;
-  e.K = K;
-  e.box_rows = box_rows;
-  e.map = *map;
-  e.valid = true;
-  return true;
+  return cached_map(map, base, rows, K, box_rows, 0);
+}
+
+// FP4 scale tiles: 512-byte tiles seen as rows of 128 32-bit words, box of
+// box_tiles rows, no swizzle, zero fill past the last tile.  Cached like
+// the operand descriptors.
+bool make_scale_tile_map(CUtensorMap* map, const void* base, int64_t tiles, int box_tiles) {
+  return cached_map(map, base, tiles, 0, box_tiles, 1);
 }
 
 namespace {
+
+bool encode_scale_tile_map(CUtensorMap* map, const void* base, int64_t tiles, int box_tiles) {
+  auto encode = tensor_map_encoder();
+  if (!encode) return false;
+  cuuint64_t dims[2] = {128u, static_cast<cuuint64_t>(tiles)};
+  cuuint64_t strides[1] = {512u};
+  cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_tiles)};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides,
+                      box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 bool encode_k_major_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
                         int box_rows) {

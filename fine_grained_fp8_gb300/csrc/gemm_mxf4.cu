@@ -490,6 +490,426 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---- block scales in the tiled layout ----------------------------------------
+//
+// The same two products with the block scales stored in the tiled FP4 scale
+// layout: 512-byte tiles of 128 rows x 4 factor bytes, row r of a tile at
+// byte 16 (r % 32) + 4 ((r % 128) / 32).  Each such tile is exactly the
+// 32-row x 16-byte shared-memory tile tcgen05.cp.32x128b.warpx4 spreads
+// over the four lane quarters, so the factors need no gathering: the
+// producer loads a stage's factor tiles with the tensor-map engine next to
+// its operand tiles (one `full` barrier for both), and the issuer copies
+// them into a TMEM slot before the stage's MMAs.  There are no
+// factor-writer warps.
+//
+// PAIR: 256 x BN tiles on clusters of two CTAs.  Each CTA holds 128 rows of
+// A and BN/2 of the tile's BN columns of B, and the even CTA (leader)
+// issues tcgen05.mma.cta_group::2 (M = 256), so each SM takes in A plus
+// half of B per stage for the MMA work a single CTA needs A plus all of B
+// for.  Each CTA loads the factor tiles of its own rows of A and of all BN
+// columns of B (the MMA reads, in each CTA's TMEM, its own rows' A factors
+// and every column's B factors); the leader's tcgen05.cp.cta_group::2
+// copies each CTA's tiles into that CTA's TMEM.  Both CTAs' tensor-map
+// copies complete on the leader's `full` barrier; the leader's commits
+// arrive on the `empty` and `acc_full` barriers of both CTAs (multicast);
+// both epilogues hand the accumulator back on the leader's `acc_empty`
+// (the peer with a relaxed cluster arrive after tcgen05.wait::ld, when its
+// reads have completed).
+template <bool NV>
+struct Fp4TiledFmt {
+  static constexpr int kCells = NV ? 4 : 2;     // factor tiles per 128 rows per stage
+  static constexpr int kSlots = NV ? 5 : 10;    // TMEM factor slots, one per stage in flight
+  static constexpr uint32_t kSfaSlot = 4 * kCells, kSfbSlot = 8 * kCells;
+  static constexpr uint32_t kSfaCol0 = 256;     // after the accumulators
+  static constexpr uint32_t kSfbCol0 = kSfaCol0 + kSfaSlot * kSlots;
+};
+
+template <bool PAIR, int BN, bool NV>
+struct TiledCfg {
+  using F = Fp4TiledFmt<NV>;
+  static constexpr int kNAcc = BN == 128 ? 2 : 1;
+  static constexpr int kABytes = BM * BK;                    // this CTA's 128 rows of A
+  static constexpr int kBRows = PAIR ? BN / 2 : BN;          // this CTA's rows of B
+  static constexpr int kBBytes = kBRows * BK;
+  static constexpr int kSfABytes = F::kCells * 512;
+  static constexpr int kSfBBytes = (BN / 128) * F::kCells * 512;
+  static constexpr int kSfBytes = kSfABytes + kSfBBytes;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfBytes;
+  static constexpr uint32_t kTxBytes = (PAIR ? 2 : 1) * kStageBytes;
+  static constexpr int kStoreBytes = kEpiWarps * 1024;
+  static constexpr int kFit = (232448 - 1024 - kStoreBytes - 256) / kStageBytes;
+  static constexpr int STAGES = kFit < F::kSlots ? kFit : F::kSlots;
+  static constexpr int kNumBars = 2 * STAGES + 2 * kNAcc + 1;
+  static constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * kStageBytes +
+                                       kStoreBytes + kNumBars * 8 + 16;
+  // the slot of stage s last served stage s - kSlots <= s - STAGES, whose
+  // MMAs completed before the copy into full[s]'s buffer was issued
+  static_assert(F::kSlots >= STAGES && STAGES >= 3, "stages");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(kNAcc * BN <= static_cast<int>(F::kSfaCol0), "accumulators overlap the scale ring");
+  static_assert(F::kSfbCol0 % 8 == 0 && F::kSfbCol0 + F::kSfbSlot * F::kSlots <= kTmemCols,
+                "scale ring within TMEM");
+  static_assert(kBBytes % 1024 == 0 && kSfBytes % 512 == 0, "tile alignment");
+};
+
+__device__ __forceinline__ void umma_mxf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t sfa_tmem,
+                                               uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t sfa_tmem,
+                                               uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// tcgen05.cp issued by the leader of a pair: each CTA's tile at this
+// shared-memory offset into the same TMEM columns of that CTA.
+__device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+template <bool PAIR, bool NV>
+__device__ __forceinline__ void fp4_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t sfa, uint32_t sfb, uint32_t acc) {
+  if constexpr (PAIR) {
+    if constexpr (NV)
+      umma_nvf4_pair(d, a, b, idesc, sfa, sfb, acc);
+    else
+      umma_mxf4_pair(d, a, b, idesc, sfa, sfb, acc);
+  } else {
+    if constexpr (NV)
+      umma_nvf4(d, a, b, idesc, sfa, sfb, acc);
+    else
+      umma_mxf4(d, a, b, idesc, sfa, sfb, acc);
+  }
+}
+
+template <bool PAIR, int BN, bool OUT_BF16, bool NV>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp4_tiled_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                          const __grid_constant__ CUtensorMap tmap_b,
+                          const __grid_constant__ CUtensorMap tmap_sa,
+                          const __grid_constant__ CUtensorMap tmap_sb,
+                          const float* __restrict__ ga, const float* __restrict__ gb,
+                          void* __restrict__ C, int64_t ldc, int M, int N, int K) {
+  using CF = TiledCfg<PAIR, BN, NV>;
+  using F = Fp4TiledFmt<NV>;
+  constexpr int STAGES = CF::STAGES;
+  constexpr int kSlots = F::kSlots;
+  constexpr int kCells = F::kCells;
+  constexpr int NACC = CF::kNAcc;
+  constexpr int G = PAIR ? 2 : 1;  // CTAs per tile
+  constexpr int HALF = BN / 2;     // columns per epilogue warp
+  constexpr int NLD = HALF / 32;   // 32-column loads per warp and tile
+  constexpr uint16_t kMask = 0x3;
+  static_assert(NLD >= 2, "the load pipeline assumes at least two loads");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sm_a = smem;
+  uint8_t* sm_b = sm_a + STAGES * CF::kABytes;
+  uint8_t* sm_sf = sm_b + STAGES * CF::kBBytes;  // per stage: A factor tiles, then B's
+  uint8_t* sm_st = sm_sf + STAGES * CF::kSfBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm_st + CF::kStoreBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint64_t* acc_empty = acc_full + NACC;
+  uint64_t* drain = acc_empty + NACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = rank == 0;
+  // tiles of G stacked 128-row tiles x BN columns, M fastest; a cluster (a
+  // CTA) takes tiles first, first + stride, ...
+  const int m_tiles = (M + BM - 1) / BM;
+  const int m_units = (m_tiles + G - 1) / G;
+  const int total = m_units * (N / BN);
+  const int first = static_cast<int>(blockIdx.x) / G;
+  const int stride = static_cast<int>(gridDim.x) / G;
+  const int kstages = (K + 255) / 256;
+  const bool half_last = (K % 256) != 0;
+  const int cpr = K / (NV ? 64 : 128);  // factor tiles per 128 rows (one per 4 factor bytes)
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < NACC; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], G * kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+    tma_prefetch_desc(&tmap_sa);
+    tma_prefetch_desc(&tmap_sb);
+  }
+  if (warp == 1) {
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_slot, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
+  }
+  tc_fence_before();
+  if constexpr (PAIR)
+    cluster_sync();  // both CTAs' barriers and TMEM exist before either uses the other's
+  else
+    __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    // ---------------- TMA producer (operands and factor tiles) ----------------
+    if (elect_one_sync()) {
+      uint32_t it = 0;
+      bool ok = true;
+      const uint32_t bar0 = PAIR ? mapa_shared(&full[0], 0) : smem_u32(&full[0]);
+      for (int u = first; u < total && ok; u += stride) {
+        const int tm = (u % m_units) * G + rank, tn = u / m_units;
+        const int b_row = tn * BN + rank * CF::kBRows;
+        for (int kc = 0; kc < kstages; ++kc, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, FGQ_DEVERR_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full[s], CF::kTxBytes);
+          uint8_t* sf = sm_sf + s * CF::kSfBytes;
+          const int t0 = kc * kCells;  // first factor tile of this stage within a row tile
+          if constexpr (PAIR) {
+            const uint32_t bar = bar0 + s * 8;
+            tma_load_2d_pair(sm_a + s * CF::kABytes, &tmap_a, bar, kc * BK, tm * BM);
+            tma_load_2d_pair(sm_b + s * CF::kBBytes, &tmap_b, bar, kc * BK, b_row);
+            tma_load_2d_pair(sf, &tmap_sa, bar, 0, tm * cpr + t0);
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              tma_load_2d_pair(sf + CF::kSfABytes + h * kCells * 512, &tmap_sb, bar, 0,
+                               (tn * (BN / 128) + h) * cpr + t0);
+          } else {
+            tma_load_2d(sm_a + s * CF::kABytes, &tmap_a, &full[s], kc * BK, tm * BM);
+            tma_load_2d(sm_b + s * CF::kBBytes, &tmap_b, &full[s], kc * BK, b_row);
+            tma_load_2d(sf, &tmap_sa, &full[s], 0, tm * cpr + t0);
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              tma_load_2d(sf + CF::kSfABytes + h * kCells * 512, &tmap_sb, &full[s], 0,
+                          (tn * (BN / 128) + h) * cpr + t0);
+          }
+        }
+      }
+      // Before leaving: every copy into this CTA's (the pair's) shared memory
+      // has landed, and for a pair every commit addressed to this CTA's empty
+      // barriers has arrived.
+      const uint32_t lo = it > static_cast<uint32_t>(STAGES) ? it - STAGES : 0u;
+      for (uint32_t j = lo; j < it; ++j) {
+        if (leader) mxf4_wait_drain(&full[j % STAGES], (j / STAGES) & 1u);
+        if (PAIR) mxf4_wait_drain(&empty[j % STAGES], (j / STAGES) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1 && leader) {
+    // ---------------- MMA issuer (the leader of a pair) ----------------
+    if (elect_one_sync()) {
+      constexpr uint32_t idesc0 = idesc_fp4(G * BM, BN, NV);
+      constexpr uint32_t kId2 = (2u << 29) | (2u << 4);  // factor bytes 2-3 of A and B
+      const uint64_t dA0 = smem_desc_k_sw128(smem_u32(sm_a));
+      const uint32_t a_lo0 = static_cast<uint32_t>(dA0), dhi = static_cast<uint32_t>(dA0 >> 32);
+      const uint32_t b_lo0 = static_cast<uint32_t>(smem_desc_k_sw128(smem_u32(sm_b)));
+      const uint32_t sf0 = smem_u32(sm_sf);
+      int ls = 0;
+      uint32_t lph = 0, g_it = 0, t_it = 0;
+      bool ok = true;
+      for (int u = first; u < total && ok; u += stride, ++t_it) {
+        const uint32_t buf = t_it % NACC, aph = (t_it / NACC) & 1u;
+        if (!mbar_wait(&acc_empty[buf], aph ^ 1u, abort_flag, FGQ_DEVERR_MMA_TMEM)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + buf * BN;
+        for (int kc = 0; kc < kstages; ++kc, ++g_it) {
+          if (!mbar_wait(&full[ls], lph, abort_flag, FGQ_DEVERR_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t r = g_it % kSlots;
+          const uint32_t sfa = tmem_base + F::kSfaCol0 + F::kSfaSlot * r;
+          const uint32_t sfb = tmem_base + F::kSfbCol0 + F::kSfbSlot * r;
+          // the stage's factor tiles into slot r: A tile w to columns 4 w ..
+          // 4 w + 3, B tile w of columns 128 h .. 128 h + 127 to 8 w + 4 h ..
+          // + 3 (in order before the MMAs that read them)
+          const uint32_t sfs = sf0 + ls * CF::kSfBytes;
+#pragma unroll
+          for (int w = 0; w < kCells; ++w) {
+            const uint64_t da = sf_tile_desc(sfs + w * 512);
+            if constexpr (PAIR)
+              tmem_cp_32x128b_x4_pair(sfa + 4 * w, da);
+            else
+              tmem_cp_32x128b_x4(sfa + 4 * w, da);
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h) {
+              const uint64_t db = sf_tile_desc(sfs + CF::kSfABytes + (h * kCells + w) * 512);
+              if constexpr (PAIR)
+                tmem_cp_32x128b_x4_pair(sfb + 8 * w + 4 * h, db);
+              else
+                tmem_cp_32x128b_x4(sfb + 8 * w + 4 * h, db);
+            }
+          }
+          const uint32_t a_lo = a_lo0 + ls * (CF::kABytes >> 4);
+          const uint32_t b_lo = b_lo0 + ls * (CF::kBBytes >> 4);
+          // four K = 64 MMAs (32 bytes of each row apart); a final half stage
+          // has two.  MXFP4: factor bytes 0-1 and 2-3 of tile 0, then of
+          // tile 1.  NVFP4: tile kk for MMA kk.
+          const bool full_stage = kc + 1 < kstages || !half_last;
+          if constexpr (NV) {
+            fp4_mma<PAIR, NV>(d, make_desc(a_lo, dhi), make_desc(b_lo, dhi), idesc0, sfa, sfb,
+                              kc > 0 ? 1u : 0u);
+            fp4_mma<PAIR, NV>(d, make_desc(a_lo + 2, dhi), make_desc(b_lo + 2, dhi), idesc0,
+                              sfa + 4, sfb + 8, 1u);
+            if (full_stage) {
+              fp4_mma<PAIR, NV>(d, make_desc(a_lo + 4, dhi), make_desc(b_lo + 4, dhi), idesc0,
+                                sfa + 8, sfb + 16, 1u);
+              fp4_mma<PAIR, NV>(d, make_desc(a_lo + 6, dhi), make_desc(b_lo + 6, dhi), idesc0,
+                                sfa + 12, sfb + 24, 1u);
+            }
+          } else {
+            fp4_mma<PAIR, NV>(d, make_desc(a_lo, dhi), make_desc(b_lo, dhi), idesc0, sfa, sfb,
+                              kc > 0 ? 1u : 0u);
+            fp4_mma<PAIR, NV>(d, make_desc(a_lo + 2, dhi), make_desc(b_lo + 2, dhi),
+                              idesc0 | kId2, sfa, sfb, 1u);
+            if (full_stage) {
+              fp4_mma<PAIR, NV>(d, make_desc(a_lo + 4, dhi), make_desc(b_lo + 4, dhi), idesc0,
+                                sfa + 4, sfb + 8, 1u);
+              fp4_mma<PAIR, NV>(d, make_desc(a_lo + 6, dhi), make_desc(b_lo + 6, dhi),
+                                idesc0 | kId2, sfa + 4, sfb + 8, 1u);
+            }
+          }
+          if constexpr (PAIR)
+            umma_commit_pair(&empty[ls], kMask);
+          else
+            umma_commit(&empty[ls]);
+          if (++ls == STAGES) {
+            ls = 0;
+            lph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if constexpr (PAIR)
+          umma_commit_pair(&acc_full[buf], kMask);
+        else
+          umma_commit(&acc_full[buf]);
+      }
+      // Every MMA this thread issued must finish before TMEM is released.
+      if constexpr (PAIR)
+        umma_commit_pair(drain, 0x1);
+      else
+        umma_commit(drain);
+      mxf4_wait_drain(drain, 0);
+    }
+    __syncwarp();
+  } else if (warp >= 8) {
+    // ---------------- epilogue (each CTA its own 128 rows) ----------------
+    const int ew = warp - 8;
+    const int q = warp & 3;
+    const int half = ew >> 2;
+    const uint32_t t_lane = static_cast<uint32_t>(32 * q) << 16;
+    const uint32_t acc_empty0 = PAIR ? mapa_shared(&acc_empty[0], 0) : 0u;
+    float alpha = 1.0f;
+    if constexpr (NV) alpha = __fmul_rn(__ldg(ga), __ldg(gb));
+    auto scale32 = [&](uint32_t (&r)[32]) {
+      if constexpr (NV) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), alpha));
+      }
+    };
+    uint32_t t_it = 0;
+    uint8_t* stage = sm_st + ew * 1024;
+    for (int u = first; u < total; u += stride, ++t_it) {
+      const int tm = (u % m_units) * G + rank, tn = u / m_units;
+      const int row0 = tm * BM + 32 * q;
+      const int col0 = tn * BN + half * HALF;
+      const uint32_t buf = t_it % NACC, aph = (t_it / NACC) & 1u;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[buf], aph, abort_flag, FGQ_DEVERR_EPI_TMEM)))
+        break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + t_lane + buf * BN + half * HALF;
+      uint32_t ra[32], rb[32];
+      tmem_ld_32x32b_x32(taddr, ra);
+      tmem_wait_ld_regs(ra);
+#pragma unroll
+      for (int j = 0; j < NLD; ++j) {
+        if (j + 1 < NLD) {
+          if (j % 2 == 0)
+            tmem_ld_32x32b_x32(taddr + 32 * (j + 1), rb);
+          else
+            tmem_ld_32x32b_x32(taddr + 32 * (j + 1), ra);
+        } else {
+          // the whole accumulator is in registers: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (PAIR && !leader)
+              mbar_arrive_cluster_relaxed(acc_empty0 + buf * 8);
+            else
+              mbar_arrive_relaxed(&acc_empty[buf]);
+          }
+        }
+        if (j % 2 == 0) {
+          scale32(ra);
+          warp_store32<OUT_BF16, 1024>(stage, ra, C, ldc, row0, col0 + 32 * j, M - row0);
+        } else {
+          scale32(rb);
+          warp_store32<OUT_BF16, 1024>(stage, rb, C, ldc, row0, col0 + 32 * j, M - row0);
+        }
+        if (j + 1 < NLD) {
+          if (j % 2 == 0)
+            tmem_wait_ld_regs(rb);
+          else
+            tmem_wait_ld_regs(ra);
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  if constexpr (PAIR) {
+    cluster_sync();  // neither CTA leaves while its peer may still reach its memory
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+  } else {
+    __syncthreads();
+    if (warp == 1) {
+      tc_fence_after();
+      tmem_dealloc(tmem_base, kTmemCols);
+    }
+  }
+}
+
 template <int BN, int STAGES, bool OUT_BF16, bool NV>
 cudaError_t launch_mxf4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B, const uint8_t* sB,
                           const float* ga, const float* gb, void* C, int64_t ldc, int M, int N,
@@ -515,6 +935,117 @@ cudaError_t launch_mxf4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* 
   const int grid = tiles < dev.sm_count ? tiles : dev.sm_count;
   return launch_pdl(kern, dim3(grid), dim3(kThreads), CF::kSmemBytes, stream, ta, tb, sA, sB, ga,
                     gb, C, ldc, M, N, K);
+}
+
+// Tiled-scale kernel set-up, once per device and configuration: the shared
+// memory attribute, and for pairs the clusters of two that fit at once (0
+// when the pair kernel cannot run).
+template <bool PAIR, int BN, bool OUT_BF16, bool NV>
+cudaError_t tiled_setup(const DeviceInfo& dev, int* clusters) {
+  using CF = TiledCfg<PAIR, BN, NV>;
+  auto kern = gemm_fp4_tiled_kernel<PAIR, BN, OUT_BF16, NV>;
+  static std::mutex mu;
+  static int cached[64] = {};
+  static bool ready[64] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  if (!ready[dev.device]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(CF::kSmemBytes));
+    if (e != cudaSuccess) return e;
+    int n = 1;
+    if (PAIR) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * (dev.sm_count / 2));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = CF::kSmemBytes;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+    }
+    cached[dev.device] = n;
+    ready[dev.device] = true;
+  }
+  *clusters = cached[dev.device];
+  return cudaSuccess;
+}
+
+template <bool PAIR, int BN, bool OUT_BF16, bool NV>
+cudaError_t launch_tiled_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                             const uint8_t* sB, const float* ga, const float* gb, void* C,
+                             int64_t ldc, int M, int N, int K, int clusters, cudaStream_t stream,
+                             const DeviceInfo& dev) {
+  using CF = TiledCfg<PAIR, BN, NV>;
+  constexpr int G = PAIR ? 2 : 1;
+  CUtensorMap ta, tb, tsa, tsb;
+  // operand rows of K/2 bytes (two E2M1 per byte); factor tiles: one per
+  // 128 rows and 4 factor bytes, K/128 (MXFP4) or K/64 (NVFP4) per row tile
+  const int64_t cpr = K / (NV ? 64 : 128);
+  const int64_t a_tiles = (M + BM - 1) / BM * cpr, b_tiles = N / 128 * cpr;
+  if (!make_k_major_map(&ta, A, M, K / 2, BM) || !make_k_major_map(&tb, B, N, K / 2, CF::kBRows) ||
+      !make_scale_tile_map(&tsa, sA, a_tiles, Fp4TiledFmt<NV>::kCells) ||
+      !make_scale_tile_map(&tsb, sB, b_tiles, Fp4TiledFmt<NV>::kCells))
+    return cudaErrorInvalidValue;
+  const int units = ((M + BM - 1) / BM + G - 1) / G * (N / BN);
+  const int cap = PAIR ? clusters : dev.sm_count;
+  const int grid = G * (units < cap ? units : cap);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na++].val.programmaticStreamSerializationAllowed = 1;
+  if (PAIR) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na++].val.clusterDim.z = 1;
+  }
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = CF::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, gemm_fp4_tiled_kernel<PAIR, BN, OUT_BF16, NV>, ta, tb, tsa, tsb,
+                            ga, gb, C, ldc, M, N, K);
+}
+
+// Configuration choice for tiled scales: CTA pairs once A has two row tiles,
+// on 256-column tiles when there is at least one per cluster, else
+// 128-column ones; a single CTA per 128 x 128 tile for one row tile.
+template <bool OUT_BF16, bool NV>
+cudaError_t launch_fp4_tiled(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                             const uint8_t* sB, const float* ga, const float* gb, void* C,
+                             int64_t ldc, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+                             const DeviceInfo& dev) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  const int m = static_cast<int>(M), n = static_cast<int>(N), k = static_cast<int>(K);
+  const int64_t m_tiles = (M + BM - 1) / BM;
+  if (m_tiles >= 2) {
+    int c256 = 0, c128 = 0;
+    cudaError_t e = tiled_setup<true, 256, OUT_BF16, NV>(dev, &c256);
+    if (e != cudaSuccess) return e;
+    e = tiled_setup<true, 128, OUT_BF16, NV>(dev, &c128);
+    if (e != cudaSuccess) return e;
+    const int64_t groups = (m_tiles + 1) / 2;
+    if (N % 256 == 0 && c256 > 0 && groups * (N / 256) >= c256)
+      return launch_tiled_cfg<true, 256, OUT_BF16, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, c256,
+                                                       stream, dev);
+    if (c128 > 0)
+      return launch_tiled_cfg<true, 128, OUT_BF16, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, c128,
+                                                       stream, dev);
+  }
+  int one = 0;
+  const cudaError_t e = tiled_setup<false, 128, OUT_BF16, NV>(dev, &one);
+  if (e != cudaSuccess) return e;
+  return launch_tiled_cfg<false, 128, OUT_BF16, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, 0, stream,
+                                                    dev);
 }
 
 template <bool NV>
@@ -551,6 +1082,24 @@ cudaError_t launch_gemm_nvf4(const uint8_t* A, const uint8_t* sA, const float* g
                              int64_t ldc, int64_t M, int64_t N, int64_t K, int out_bf16,
                              cudaStream_t stream, const DeviceInfo& dev) {
   return launch_fp4<true>(A, sA, B, sB, ga, gb, C, ldc, M, N, K, out_bf16, stream, dev);
+}
+
+cudaError_t launch_gemm_mxf4_tiled(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                                   const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
+                                   int64_t K, int out_bf16, cudaStream_t stream,
+                                   const DeviceInfo& dev) {
+  return out_bf16 ? launch_fp4_tiled<true, false>(A, sA, B, sB, nullptr, nullptr, C, ldc, M, N, K,
+                                                  stream, dev)
+                  : launch_fp4_tiled<false, false>(A, sA, B, sB, nullptr, nullptr, C, ldc, M, N, K,
+                                                   stream, dev);
+}
+
+cudaError_t launch_gemm_nvf4_tiled(const uint8_t* A, const uint8_t* sA, const float* ga,
+                                   const uint8_t* B, const uint8_t* sB, const float* gb, void* C,
+                                   int64_t ldc, int64_t M, int64_t N, int64_t K, int out_bf16,
+                                   cudaStream_t stream, const DeviceInfo& dev) {
+  return out_bf16 ? launch_fp4_tiled<true, true>(A, sA, B, sB, ga, gb, C, ldc, M, N, K, stream, dev)
+                  : launch_fp4_tiled<false, true>(A, sA, B, sB, ga, gb, C, ldc, M, N, K, stream, dev);
 }
 
 cudaError_t read_device_error_mxf4(uint32_t* word, bool clear) {

@@ -90,7 +90,16 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
 constexpr int kNvThreads = 256;
 constexpr int kNvRounds = 2;
 
-template <bool DENSE>
+// Byte of factor f of row r in the tiled FP4 scale layout (F factor bytes a
+// row, F % 4 == 0): 512-byte tiles of 128 rows x 4 factor bytes, tile
+// (r / 128, f / 4); in a tile, row r at 16 (r % 32) + 4 ((r % 128) / 32),
+// the byte at + f % 4.
+__device__ __forceinline__ uint64_t nv_tile_offset(uint32_t r, uint32_t f, uint32_t F) {
+  return (static_cast<uint64_t>(r >> 7) * (F >> 2) + (f >> 2)) * 512u + (r & 31u) * 16u +
+         ((r >> 5) & 3u) * 4u + (f & 3u);
+}
+
+template <bool DENSE, bool TILED>
 __global__ void __launch_bounds__(kNvThreads)
     quant_nvfp4_1x16_kernel(const uint16_t* __restrict__ x, uint32_t kb, uint32_t blocks,
                             int64_t ldx, const float* __restrict__ gptr, uint8_t* __restrict__ xq,
@@ -166,7 +175,14 @@ __global__ void __launch_bounds__(kNvThreads)
         }
         // row-major [R, K/2]: block b covers bytes 8 b .. 8 b + 7
         *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(b[u]) * 8 + 4 * l2) = packed;
-        if (l2 == 0) sx[b[u]] = static_cast<uint8_t>(sc);
+        if (l2 == 0) {
+          if (TILED) {
+            const uint32_t r = b[u] / kb;
+            sx[nv_tile_offset(r, b[u] - r * kb, kb)] = static_cast<uint8_t>(sc);
+          } else {
+            sx[b[u]] = static_cast<uint8_t>(sc);
+          }
+        }
       }
     }
   }
@@ -200,13 +216,14 @@ cudaError_t launch_nvfp4_global_scale(const void* x, int64_t R, int64_t K, int64
 }
 
 cudaError_t launch_quant_nvfp4_1x16(const void* x, int64_t R, int64_t K, int64_t ldx,
-                                    const float* g, uint8_t* xq, uint8_t* sx, cudaStream_t stream,
-                                    const DeviceInfo& dev) {
+                                    const float* g, uint8_t* xq, uint8_t* sx, bool tiled,
+                                    cudaStream_t stream, const DeviceInfo& dev) {
   const uint32_t kb = static_cast<uint32_t>(K / 16);
   const uint32_t blocks = static_cast<uint32_t>(R * (K / 16));
   if (blocks == 0) return cudaSuccess;
   const bool dense = ldx == K;
-  auto k = dense ? quant_nvfp4_1x16_kernel<true> : quant_nvfp4_1x16_kernel<false>;
+  auto k = dense ? (tiled ? quant_nvfp4_1x16_kernel<true, true> : quant_nvfp4_1x16_kernel<true, false>)
+                 : (tiled ? quant_nvfp4_1x16_kernel<false, true> : quant_nvfp4_1x16_kernel<false, false>);
   int per_sm = 0;
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kNvThreads, 0);
   if (err != cudaSuccess) return err;
@@ -216,6 +233,34 @@ cudaError_t launch_quant_nvfp4_1x16(const void* x, int64_t R, int64_t K, int64_t
   uint32_t grid = static_cast<uint32_t>(dev.sm_count) * static_cast<uint32_t>(per_sm);
   if (grid > needed) grid = needed;
   k<<<grid, kNvThreads, 0, stream>>>(static_cast<const uint16_t*>(x), kb, blocks, ldx, g, xq, sx);
+  return cudaGetLastError();
+}
+
+// Row-major FP4 block scales [R, F] (F % 4 == 0) into the tiled layout:
+// one 4-byte cell (four factor bytes of one row) per thread, read and
+// written whole (a cell's four bytes stay together in the tiled layout).
+__global__ void __launch_bounds__(256)
+    fp4_scales_to_tiles_kernel(const uint32_t* __restrict__ s, uint32_t cells_per_row,
+                               uint64_t cells, uint32_t* __restrict__ tiles) {
+  for (uint64_t i = blockIdx.x * 256ull + threadIdx.x; i < cells; i += gridDim.x * 256ull) {
+    const uint32_t r = static_cast<uint32_t>(i / cells_per_row);
+    const uint32_t c = static_cast<uint32_t>(i - static_cast<uint64_t>(r) * cells_per_row);
+    const uint64_t word = (static_cast<uint64_t>(r >> 7) * cells_per_row + c) * 128u +
+                          (r & 31u) * 4u + ((r >> 5) & 3u);
+    tiles[word] = __ldg(s + i);
+  }
+}
+
+cudaError_t launch_fp4_scales_to_tiles(const uint8_t* s, int64_t R, int64_t F, uint8_t* tiles,
+                                       cudaStream_t stream, const DeviceInfo& dev) {
+  const uint64_t cells = static_cast<uint64_t>(R) * static_cast<uint64_t>(F / 4);
+  if (cells == 0) return cudaSuccess;
+  uint64_t grid = (cells + 255) / 256;
+  const uint64_t cap = static_cast<uint64_t>(dev.sm_count) * 8;
+  if (grid > cap) grid = cap;
+  fp4_scales_to_tiles_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
+      reinterpret_cast<const uint32_t*>(s), static_cast<uint32_t>(F / 4), cells,
+      reinterpret_cast<uint32_t*>(tiles));
   return cudaGetLastError();
 }
 

@@ -402,7 +402,17 @@ __device__ __forceinline__ uint32_t mx_scale_code(uint32_t mag_bits) {
   return man != 0 ? e + 1 : e;
 }
 
-template <bool DENSE>
+// Byte of factor f of row r in the tiled FP4 scale layout (F factor bytes a
+// row, F % 4 == 0): 512-byte tiles of 128 rows x 4 factor bytes, tile
+// (r / 128, f / 4); in a tile, row r at 16 (r % 32) + 4 ((r % 128) / 32),
+// the byte at + f % 4.  A tile is the 32-row x 16-byte shared-memory tile
+// the FP4 GEMM copies into TMEM (row m of A lands at lane m, column m / 32).
+__device__ __forceinline__ uint64_t fp4_tile_offset(uint32_t r, uint32_t f, uint32_t F) {
+  return (static_cast<uint64_t>(r >> 7) * (F >> 2) + (f >> 2)) * 512u + (r & 31u) * 16u +
+         ((r >> 5) & 3u) * 4u + (f & 3u);
+}
+
+template <bool DENSE, bool TILED>
 __global__ void __launch_bounds__(kMxThreads)
     quant_mxfp4_1x32_kernel(const uint16_t* __restrict__ x, uint32_t kg, uint32_t groups,
                             int64_t ldx, uint8_t* __restrict__ xq, uint8_t* __restrict__ sx) {
@@ -449,7 +459,14 @@ __global__ void __launch_bounds__(kMxThreads)
         const uint32_t packed = cvt_e2m1x8(y);
         // row-major [R, K/2]: group g covers bytes 16 g .. 16 g + 15
         *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(g[u]) * 16 + 4 * l4) = packed;
-        if (l4 == 0) sx[g[u]] = static_cast<uint8_t>(code);
+        if (l4 == 0) {
+          if (TILED) {
+            const uint32_t r = g[u] / kg;
+            sx[fp4_tile_offset(r, g[u] - r * kg, kg)] = static_cast<uint8_t>(code);
+          } else {
+            sx[g[u]] = static_cast<uint8_t>(code);
+          }
+        }
       }
     }
   }
@@ -458,12 +475,14 @@ __global__ void __launch_bounds__(kMxThreads)
 }  // namespace
 
 cudaError_t launch_quant_mxfp4_1x32(const void* x, int64_t R, int64_t K, int64_t ldx, uint8_t* xq,
-                                    uint8_t* sx, cudaStream_t stream, const DeviceInfo& dev) {
+                                    uint8_t* sx, bool tiled, cudaStream_t stream,
+                                    const DeviceInfo& dev) {
   const uint32_t kg = static_cast<uint32_t>(K / 32);
   const uint32_t groups = static_cast<uint32_t>(R * (K / 32));
   if (groups == 0) return cudaSuccess;
   const bool dense = ldx == K;
-  auto k = dense ? quant_mxfp4_1x32_kernel<true> : quant_mxfp4_1x32_kernel<false>;
+  auto k = dense ? (tiled ? quant_mxfp4_1x32_kernel<true, true> : quant_mxfp4_1x32_kernel<true, false>)
+                 : (tiled ? quant_mxfp4_1x32_kernel<false, true> : quant_mxfp4_1x32_kernel<false, false>);
   int per_sm = 0;
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kMxThreads, 0);
   if (err != cudaSuccess) return err;

@@ -330,6 +330,57 @@ fgq_status fgq_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const float* gA,
                           const uint8_t* B, const uint8_t* sB, const float* gB, void* C,
                           int64_t ldc, int64_t M, int64_t N, int64_t K, int out, void* stream);
 
+/*
+ * Tiled FP4 block-scale layout.  The FP4 GEMMs below with the _tiled suffix
+ * take their block scales in this layout, which the tensor-map engine loads
+ * without gathering; it is this library's storage format (the page gives
+ * none).  For R rows of F factor bytes (F = K/32 for MXFP4, K/16 for NVFP4,
+ * F % 4 == 0) the code of row r, factor f sits at byte
+ *     ((r / 128) * (F / 4) + f / 4) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + f % 4
+ * of a buffer of ceil(R / 128) * 128 * F bytes: 512-byte tiles of 128 rows x
+ * 4 factor bytes, each the 32-row x 16-byte tile the tensor core's factor
+ * copy spreads over a 128-row TMEM tile (row m at lane m, column m / 32;
+ * "Fine-Grained FP8/FP4 Quantization", §Blackwell: Native Block Scaling).
+ * The bytes of rows R .. up to the next multiple of 128 are padding: no
+ * call here writes them, and they reach no stored output.
+ *
+ * fgq_fp4_scale_tiles_bytes: that buffer size.  F % 4 == 0, F > 0, R >= 0.
+ * fgq_fp4_scales_to_tiles: row-major codes s [R, F] (4-byte aligned) into
+ *   the tiled layout at `tiles` (4-byte aligned, the size above); device
+ *   buffers, asynchronous on `stream`.  A pure permutation.
+ */
+fgq_status fgq_fp4_scale_tiles_bytes(int64_t R, int64_t F, size_t* bytes);
+fgq_status fgq_fp4_scales_to_tiles(const uint8_t* s, int64_t R, int64_t F, uint8_t* tiles,
+                                   void* stream);
+
+/*
+ * fgq_quant_mxfp4_1x32 and fgq_quant_nvfp4_1x16 with the scales written in
+ * the tiled layout (s_tiles: fgq_fp4_scale_tiles_bytes(R, K/32 or K/16)
+ * bytes, padding untouched) instead of row-major.  Codes, scales and
+ * arguments otherwise as those calls; K % 128 == 0 (MXFP4) or
+ * K % 64 == 0 (NVFP4).
+ */
+fgq_status fgq_quant_mxfp4_1x32_tiled(const void* x, int64_t R, int64_t K, int64_t ldx,
+                                      uint8_t* xq, uint8_t* s_tiles, void* stream);
+fgq_status fgq_quant_nvfp4_1x16_tiled(const void* x, int64_t R, int64_t K, int64_t ldx,
+                                      const float* g, uint8_t* xq, uint8_t* s_tiles, void* stream);
+
+/*
+ * fgq_gemm_mxfp4 and fgq_gemm_nvfp4 with sA and sB in the tiled layout
+ * (16-byte aligned; sA for the M rows of A, sB for the N rows of the
+ * transposed weight).  Same products, same arguments and limits otherwise.
+ * The tensor-map engine loads each stage's factor tiles with its operand
+ * tiles; once A has two 128-row tiles, pairs of CTAs (a cluster of two)
+ * share each 256-row tile, each loading half of the weight tile.
+ */
+fgq_status fgq_gemm_mxfp4_tiled(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                                const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
+                                int64_t K, int out, void* stream);
+fgq_status fgq_gemm_nvfp4_tiled(const uint8_t* A, const uint8_t* sA, const float* gA,
+                                const uint8_t* B, const uint8_t* sB, const float* gB, void* C,
+                                int64_t ldc, int64_t M, int64_t N, int64_t K, int out,
+                                void* stream);
+
 /* Workspace bytes fgq_gemm_fp8_blockscaled_splitk needs for (M, N, K) on the
  * current device (depends on its SM count; 256 when the problem has no
  * partial tiles).  Same size checks as the GEMM. */

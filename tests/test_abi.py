@@ -235,3 +235,61 @@ def test_gemm_nvfp4_rejects(fgq, args):
 def test_fp4_gemms_empty_is_ok(fgq):
     assert _lib.fgq_gemm_mxfp4(0, 0, 0, 0, 0, 256, 0, 256, 256, 0, None) == _lib.FGQ_OK
     assert _lib.fgq_gemm_nvfp4(0, 0, 0, 0, 0, 0, 0, 256, 0, 256, 256, 0, None) == _lib.FGQ_OK
+
+
+@pytest.mark.parametrize("args", [
+    (0, 4, 128, 128, P, P, None),            # null x
+    (P, 4, 96, 128, P, P, None),             # K % 128
+    (P, 4, 128, 120, P, P, None),            # ldx < K
+    (P, 4, 128, 128, P + 2, P, None),        # xq misaligned
+    (P, 4, 128, 128, P, 0, None),            # null scale tiles
+])
+def test_quant_mxfp4_tiled_rejects(fgq, args):
+    assert _lib.fgq_quant_mxfp4_1x32_tiled(*args) == _lib.FGQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args", [
+    (0, 4, 64, 64, P, P, P, None),           # null x
+    (P, 4, 48, 64, P, P, P, None),           # K % 64
+    (P, 4, 64, 64, 0, P, P, None),           # null g
+    (P, 4, 64, 64, P, P, 0, None),           # null scale tiles
+])
+def test_quant_nvfp4_tiled_rejects(fgq, args):
+    assert _lib.fgq_quant_nvfp4_1x16_tiled(*args) == _lib.FGQ_ERR_INVALID_ARG
+
+
+def test_fp4_scale_tiles_bytes(fgq):
+    assert _lib.fgq_fp4_scale_tiles_bytes(130, 8) == (_lib.FGQ_OK, 256 * 8)
+    assert _lib.fgq_fp4_scale_tiles_bytes(0, 4) == (_lib.FGQ_OK, 0)
+    assert _lib.fgq_fp4_scale_tiles_bytes(4, 6)[0] == _lib.FGQ_ERR_INVALID_ARG
+    assert _lib.fgq_fp4_scale_tiles_bytes(-1, 4)[0] == _lib.FGQ_ERR_INVALID_ARG
+    assert _lib.fgq_fp4_scales_to_tiles(P, 4, 6, P, None) == _lib.FGQ_ERR_INVALID_ARG
+    assert _lib.fgq_fp4_scales_to_tiles(P + 2, 4, 8, P, None) == _lib.FGQ_ERR_INVALID_ARG
+    assert _lib.fgq_fp4_scales_to_tiles(0, 0, 8, 0, None) == _lib.FGQ_OK
+
+
+@pytest.mark.parametrize("args", [
+    (0, P, P, P, P, 256, 128, 256, 256, 0, None),      # null A
+    (P, P, P, P, P, 256, 128, 256, 192, 0, None),      # K % 128
+    (P, P, P, P, P, 256, 128, 192, 256, 0, None),      # N % 128
+    (P, P + 4, P, P, P, 256, 128, 256, 256, 0, None),  # sA not 16-byte aligned
+    (P, P, P, P + 8, P, 256, 128, 256, 256, 0, None),  # sB not 16-byte aligned
+])
+def test_gemm_mxfp4_tiled_rejects(fgq, args):
+    assert _lib.fgq_gemm_mxfp4_tiled(*args) == _lib.FGQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args", [
+    (P, P, 0, P, P, P, P, 256, 128, 256, 256, 0, None),      # null gA
+    (P, P + 4, P, P, P, P, P, 256, 128, 256, 256, 0, None),  # sA not 16-byte aligned
+    (P, P, P, P, P, P, P, 256, 128, 256, 192, 0, None),      # K % 128
+])
+def test_gemm_nvfp4_tiled_rejects(fgq, args):
+    assert _lib.fgq_gemm_nvfp4_tiled(*args) == _lib.FGQ_ERR_INVALID_ARG
+
+
+def test_fp4_tiled_empty_is_ok(fgq):
+    assert _lib.fgq_gemm_mxfp4_tiled(0, 0, 0, 0, 0, 256, 0, 256, 256, 0, None) == _lib.FGQ_OK
+    assert _lib.fgq_gemm_nvfp4_tiled(0, 0, 0, 0, 0, 0, 0, 256, 0, 256, 256, 0, None) == _lib.FGQ_OK
+    assert _lib.fgq_quant_mxfp4_1x32_tiled(0, 0, 128, 128, 0, 0, None) == _lib.FGQ_OK
+    assert _lib.fgq_quant_nvfp4_1x16_tiled(0, 0, 64, 64, 0, 0, 0, None) == _lib.FGQ_OK

@@ -68,3 +68,44 @@ def test_mxfp4_every_bf16_magnitude(fgq, cuda_dev):
 def test_mxfp4_full_size(fgq, cuda_dev):
     x = fgq_inputs.student_t((4096, 7168), 3, 1.0, seed=6)
     _check(fgq, x, cuda_dev)
+
+
+def _defined(R, F):
+    """The bytes of the tiled layout that hold a code (not row padding)."""
+    return oracle.fp4_scale_tiles(np.ones((R, F), np.uint8)) == 1
+
+
+@pytest.mark.parametrize("R,K,pad", [(1, 128, 0), (7, 384, 8), (130, 1024, 0), (33, 7168, 64),
+                                     (256, 256, 0)])
+def test_mxfp4_tiled_scales_match_oracle(fgq, cuda_dev, R, K, pad):
+    """The tiled-scale quantizer: codes as the row-major one, scales bit for
+    bit the oracle's scales in the tiled layout; and the relayout of the
+    row-major scales gives the same tiles."""
+    x_cpu = fgq_inputs.outlier((R, K), 1e-2, 100.0, seed=R + K + 1)
+    if pad:
+        big = torch.zeros((R, K + pad), dtype=torch.bfloat16)
+        big[:, :K] = x_cpu
+        x = big.to(cuda_dev)[:, :K]
+    else:
+        x = x_cpu.to(cuda_dev)
+    q, t = fgq.quant_mxfp4_1x32_tiled(x)
+    q2, s2 = fgq.quant_mxfp4_1x32(x)
+    t2 = fgq.fp4_scales_to_tiles(s2)
+    torch.cuda.synchronize()
+    qo, so = oracle.quant_mxfp4_1x32(x_cpu)
+    to = oracle.fp4_scale_tiles(so)
+    mask = _defined(R, K // 32)
+    assert np.array_equal(q.cpu().numpy(), qo)
+    assert np.array_equal(t.cpu().numpy()[mask], to[mask])
+    assert np.array_equal(t2.cpu().numpy()[mask], to[mask])
+    assert fgq.device_error() == 0
+
+
+@pytest.mark.parametrize("R,F", [(1, 4), (129, 8), (300, 12), (4096, 224)])
+def test_fp4_scales_to_tiles_matches_oracle(fgq, cuda_dev, R, F):
+    s = np.random.default_rng(R * F).integers(0, 256, (R, F), dtype=np.uint8)
+    t = fgq.fp4_scales_to_tiles(torch.from_numpy(s).to(cuda_dev))
+    torch.cuda.synchronize()
+    assert t.numel() == fgq.fp4_scale_tiles_bytes(R, F) == ((R + 127) // 128) * 128 * F
+    mask = _defined(R, F)
+    assert np.array_equal(t.cpu().numpy()[mask], oracle.fp4_scale_tiles(s)[mask])

@@ -95,3 +95,26 @@ def test_nvfp4_all_zero_tensor(fgq, cuda_dev):
 def test_nvfp4_full_size(fgq, cuda_dev):
     x = fgq_inputs.student_t((4096, 7168), 3, 1.0, seed=6)
     _check(fgq, x, cuda_dev)
+
+
+def _defined(R, F):
+    """The bytes of the tiled layout that hold a code (not row padding)."""
+    return oracle.fp4_scale_tiles(np.ones((R, F), np.uint8)) == 1
+
+
+@pytest.mark.parametrize("R,K,pad", [(1, 64, 0), (7, 384, 8), (130, 1024, 0), (33, 7168, 64),
+                                     (256, 192, 0)])
+def test_nvfp4_tiled_scales_match_oracle(fgq, cuda_dev, R, K, pad):
+    """The tiled-scale quantizer: global scale and codes as the row-major
+    one, block scales bit for bit the oracle's in the tiled layout."""
+    x_cpu = fgq_inputs.outlier((R, K), 1e-2, 100.0, seed=R + K + 2)
+    x = _dev(x_cpu, cuda_dev, pad)
+    q, t, g = fgq.quant_nvfp4_1x16_tiled(x)
+    torch.cuda.synchronize()
+    go = oracle.nvfp4_global_scale(x_cpu)
+    assert np.float32(g.cpu().numpy()[0]).view(np.uint32) == np.float32(go).view(np.uint32)
+    qo, so, _ = oracle.quant_nvfp4_1x16(x_cpu, g=go)
+    mask = _defined(R, K // 16)
+    assert np.array_equal(q.cpu().numpy(), qo)
+    assert np.array_equal(t.cpu().numpy()[mask], oracle.fp4_scale_tiles(so)[mask])
+    assert fgq.device_error() == 0
