@@ -171,6 +171,22 @@ def reduce_max(dist, value: float, device) -> float:
     return float(t.item())
 
 
+def _event_us(fn, stream, n: int) -> float:
+    """Mean device time of fn() in microseconds: CUDA events around n calls
+    on `stream`, after three untimed ones."""
+    import torch
+    for _ in range(3):
+        fn()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        fn()
+    e1.record(stream)
+    e1.synchronize()
+    return 1e3 * e0.elapsed_time(e1) / n
+
+
 def barrier(dist):
     if dist is not None:
         dist.barrier()
@@ -475,22 +491,23 @@ def run_fgq(args):
 
     # MXFP4 on the same workload: A quantized (E2M1, UE8M0 per 32) every step,
     # the weight quantized once as its transpose [N, K] (inference), and the
-    # block-scaled FP4 GEMM (tcgen05.mma kind::mxf4).
+    # block-scaled FP4 GEMM (tcgen05.mma kind::mxf4), with the block scales
+    # in the tiled layout (written so by the quantizer, loaded by TMA).
     mxfp4 = None
     if not args.no_mxfp4:
         msteps = max(10, min(args.steps, 500))
-        wq4 = [fgq.quant_mxfp4_1x32(b.t().contiguous()) for _, b in sets]
+        wq4 = [fgq.quant_mxfp4_1x32_tiled(b.t().contiguous()) for _, b in sets]
         aq4 = torch.empty((M_, K_ // 2), dtype=torch.uint8, device=dev)
-        sa4 = torch.empty((M_, K_ // 32), dtype=torch.uint8, device=dev)
+        sa4 = torch.empty((fgq.fp4_scale_tiles_bytes(M_, K_ // 32),), dtype=torch.uint8, device=dev)
 
         def mstep(i, ev=None):
             a, _ = sets[i % 2]
             if ev is not None:
                 ev[0].record(stream)
-            fgq.quant_mxfp4_1x32(a, xq=aq4, sx=sa4)
+            fgq.quant_mxfp4_1x32_tiled(a, xq=aq4, s_tiles=sa4)
             if ev is not None:
                 ev[1].record(stream)
-            fgq.gemm_mxfp4(aq4, sa4, *wq4[i % 2], torch.bfloat16, out=c)
+            fgq.gemm_mxfp4_tiled(aq4, sa4, *wq4[i % 2], torch.bfloat16, out=c)
             if ev is not None:
                 ev[2].record(stream)
 
@@ -510,13 +527,20 @@ def run_fgq(args):
         mms = reduce_max(dist, m0.elapsed_time(m1), dev) / msteps
         m_act = 1e3 * sum(e[0].elapsed_time(e[1]) for e in mev) / msteps
         m_gemm = 1e3 * sum(e[1].elapsed_time(e[2]) for e in mev) / msteps
-        mxfp4 = {"format": "MXFP4 (E2M1, UE8M0 scale per 32, both operands along K)",
+        # the same GEMM on row-major scales (factor-writer warps), for comparison
+        sa4r = fgq.quant_mxfp4_1x32(sets[0][0])
+        wq4r = fgq.quant_mxfp4_1x32(sets[0][1].t().contiguous())
+        m_rm = _event_us(lambda: fgq.gemm_mxfp4(*sa4r, *wq4r, torch.bfloat16, out=c), stream, 20)
+        mxfp4 = {"format": "MXFP4 (E2M1, UE8M0 scale per 32, both operands along K; "
+                           "block scales in the tiled layout)",
                  "steps": msteps, "ms_per_step": mms,
                  "value": world * FLOPS_GEMM / (mms * 1e-3) / 1e12, "unit": "TFLOP/s",
                  "quant_act_us": m_act, "gemm_us": m_gemm,
                  "gemm_TFLOP/s": FLOPS_GEMM / (m_gemm * 1e-6) / 1e12,
-                 "kernel": "gemm_mxf4_kernel (tcgen05.mma kind::mxf4.block_scale)"}
-        del wq4, aq4, sa4
+                 "gemm_rowmajor_scales_us": m_rm,
+                 "kernel": "gemm_fp4_tiled_kernel<pair, 256> (tcgen05.mma.cta_group::2 "
+                           "kind::mxf4.block_scale)"}
+        del wq4, aq4, sa4, sa4r, wq4r
         if fgq.device_error() != 0:
             raise SystemExit("a kernel reported a device wait timeout")
 
@@ -527,9 +551,9 @@ def run_fgq(args):
     nvfp4 = None
     if not args.no_nvfp4:
         nsteps = max(10, min(args.steps, 500))
-        wn4 = [fgq.quant_nvfp4_1x16(b.t().contiguous()) for _, b in sets]
+        wn4 = [fgq.quant_nvfp4_1x16_tiled(b.t().contiguous()) for _, b in sets]
         an4 = torch.empty((M_, K_ // 2), dtype=torch.uint8, device=dev)
-        sn4 = torch.empty((M_, K_ // 16), dtype=torch.uint8, device=dev)
+        sn4 = torch.empty((fgq.fp4_scale_tiles_bytes(M_, K_ // 16),), dtype=torch.uint8, device=dev)
         gn4 = torch.empty((1,), dtype=torch.float32, device=dev)
 
         def nstep(i, ev=None):
@@ -537,11 +561,11 @@ def run_fgq(args):
             if ev is not None:
                 ev[0].record(stream)
             fgq.nvfp4_global_scale(a, g=gn4)
-            fgq.quant_nvfp4_1x16(a, g=gn4, xq=an4, sx=sn4)
+            fgq.quant_nvfp4_1x16_tiled(a, g=gn4, xq=an4, s_tiles=sn4)
             if ev is not None:
                 ev[1].record(stream)
             bq4, bs4, bg4 = wn4[i % 2]
-            fgq.gemm_nvfp4(an4, sn4, gn4, bq4, bs4, bg4, torch.bfloat16, out=c)
+            fgq.gemm_nvfp4_tiled(an4, sn4, gn4, bq4, bs4, bg4, torch.bfloat16, out=c)
             if ev is not None:
                 ev[2].record(stream)
 
@@ -561,14 +585,19 @@ def run_fgq(args):
         nms = reduce_max(dist, n0.elapsed_time(n1), dev) / nsteps
         n_act = 1e3 * sum(e[0].elapsed_time(e[1]) for e in nev) / nsteps
         n_gemm = 1e3 * sum(e[1].elapsed_time(e[2]) for e in nev) / nsteps
+        an4r = fgq.quant_nvfp4_1x16(sets[0][0])
+        wn4r = fgq.quant_nvfp4_1x16(sets[0][1].t().contiguous())
+        n_rm = _event_us(lambda: fgq.gemm_nvfp4(*an4r, *wn4r, torch.bfloat16, out=c), stream, 20)
         nvfp4 = {"format": "NVFP4 (E2M1, E4M3 scale per 16 and an fp32 per-tensor scale, "
-                           "both operands along K)",
+                           "both operands along K; block scales in the tiled layout)",
                  "steps": nsteps, "ms_per_step": nms,
                  "value": world * FLOPS_GEMM / (nms * 1e-3) / 1e12, "unit": "TFLOP/s",
                  "quant_act_us": n_act, "gemm_us": n_gemm,
                  "gemm_TFLOP/s": FLOPS_GEMM / (n_gemm * 1e-6) / 1e12,
-                 "kernel": "gemm_mxf4_kernel<..., NV> (tcgen05.mma kind::mxf4nvf4.block_scale.scale_vec::4X)"}
-        del wn4, an4, sn4, gn4
+                 "gemm_rowmajor_scales_us": n_rm,
+                 "kernel": "gemm_fp4_tiled_kernel<pair, 256, NV> (tcgen05.mma.cta_group::2 "
+                           "kind::mxf4nvf4.block_scale.scale_vec::4X)"}
+        del wn4, an4, sn4, gn4, an4r, wn4r
         if fgq.device_error() != 0:
             raise SystemExit("a kernel reported a device wait timeout")
 
@@ -594,6 +623,8 @@ def run_fgq(args):
         qsat = torch.empty((QK, QM // 128), dtype=torch.float32, device=dev)
         qnv = torch.empty((QM, QK // 2), dtype=torch.uint8, device=dev)
         qnvs = torch.empty((QM, QK // 16), dtype=torch.uint8, device=dev)
+        qmxt = torch.empty((fgq.fp4_scale_tiles_bytes(QM, QK // 32),), dtype=torch.uint8, device=dev)
+        qnvt = torch.empty((fgq.fp4_scale_tiles_bytes(QM, QK // 16),), dtype=torch.uint8, device=dev)
         qg = [fgq.nvfp4_global_scale(qa[i]) for i in range(2)]
         qg_out = torch.empty((1,), dtype=torch.float32, device=dev)
         for name, fn, nbytes in (
@@ -603,10 +634,16 @@ def run_fgq(args):
                  QM * QK * 3 + QK * (QM // 128) * 4),
                 ("quant_mxfp4_1x32", lambda i: fgq.quant_mxfp4_1x32(qa[i % 2], xq=qmx, sx=qmxs),
                  QM * QK * 2 + QM * QK // 2 + QM * (QK // 32)),
+                ("quant_mxfp4_1x32_tiled",
+                 lambda i: fgq.quant_mxfp4_1x32_tiled(qa[i % 2], xq=qmx, s_tiles=qmxt),
+                 QM * QK * 2 + QM * QK // 2 + QM * (QK // 32)),
                 ("nvfp4_global_scale", lambda i: fgq.nvfp4_global_scale(qa[i % 2], g=qg_out),
                  QM * QK * 2 + 4),
                 ("quant_nvfp4_1x16", lambda i: fgq.quant_nvfp4_1x16(qa[i % 2], g=qg[i % 2], xq=qnv,
                                                                     sx=qnvs),
+                 QM * QK * 2 + QM * QK // 2 + QM * (QK // 16)),
+                ("quant_nvfp4_1x16_tiled",
+                 lambda i: fgq.quant_nvfp4_1x16_tiled(qa[i % 2], g=qg[i % 2], xq=qnv, s_tiles=qnvt),
                  QM * QK * 2 + QM * QK // 2 + QM * (QK // 16)),
                 ("quant_w_128x128", lambda i: fgq.quant_w_128x128(qw[i % 2], "fp32", wq=bq, sw=sb),
                  BYTES_QUANT_W),
@@ -719,8 +756,9 @@ def run_fgq(args):
 
     peaks, src = _peaks()
     if quant_bw:
-        for k in ("quant_act_1x128", "quant_act_128x1", "quant_mxfp4_1x32", "nvfp4_global_scale",
-                  "quant_nvfp4_1x16", "quant_w_128x128", "quant_operands"):
+        for k in ("quant_act_1x128", "quant_act_128x1", "quant_mxfp4_1x32",
+                  "quant_mxfp4_1x32_tiled", "nvfp4_global_scale", "quant_nvfp4_1x16",
+                  "quant_nvfp4_1x16_tiled", "quant_w_128x128", "quant_operands"):
             quant_bw[k]["frac_hbm"] = quant_bw[k]["GB/s"] / peaks["hbm_gbs"]
     if skinny:
         for k, v in skinny.items():
@@ -739,13 +777,13 @@ def run_fgq(args):
         mxfp4["peak_fp4"] = fp4_peak
         mxfp4["frac_fp4"] = mxfp4["gemm_TFLOP/s"] / fp4_peak
         mxfp4["peak_source"] = f"{src}: 6 x bf16_tflops (burst; nominal 13.5 / 2.25 PFLOP/s)"
-        mxfp4["traffic"] = _traffic("gemm_mxf4", "gemm_mxf4.cu")
+        mxfp4["traffic"] = _traffic("gemm_mxf4_tiled", "gemm_mxf4.cu")
     if nvfp4:
         fp4_peak = 6.0 * peaks["bf16_tflops"]
         nvfp4["peak_fp4"] = fp4_peak
         nvfp4["frac_fp4"] = nvfp4["gemm_TFLOP/s"] / fp4_peak
         nvfp4["peak_source"] = f"{src}: 6 x bf16_tflops (burst; nominal 13.5 / 2.25 PFLOP/s)"
-        nvfp4["traffic"] = _traffic("gemm_nvf4", "gemm_mxf4.cu")
+        nvfp4["traffic"] = _traffic("gemm_nvf4_tiled", "gemm_mxf4.cu")
     if ue8m0:
         ue8m0["frac_fp8"] = ue8m0["gemm_TFLOP/s"] / fp8_peak
         ue8m0["peak_fp8"] = fp8_peak
@@ -758,7 +796,8 @@ def run_fgq(args):
     quant_roofline = []
     if quant_bw:
         for k in ("quant_act_1x128", "quant_w_128x128", "quant_operands", "quant_act_128x1",
-                  "quant_mxfp4_1x32", "nvfp4_global_scale", "quant_nvfp4_1x16"):
+                  "quant_mxfp4_1x32", "quant_mxfp4_1x32_tiled", "nvfp4_global_scale",
+                  "quant_nvfp4_1x16", "quant_nvfp4_1x16_tiled"):
             quant_roofline.append({"kernel": k, "workload": "quantize-bw (alone)", "bound": "hbm",
                                    "achieved": quant_bw[k]["GB/s"], "peak": hbm, "unit": "GB/s",
                                    "frac": quant_bw[k]["GB/s"] / hbm,

@@ -111,7 +111,13 @@ __global__ void __launch_bounds__(kNvThreads)
   constexpr uint32_t kPerWarp = 16 * kNvRounds;
   const float g = __ldg(gptr);
   const float d6 = __fmul_rn(6.0f, g);
-  for (uint32_t base = warp * kPerWarp; base < blocks; base += nwarps * kPerWarp) {
+  // Tiled scales: the row and block index of `base`, advanced by the loop's
+  // stride without a division per iteration.
+  const uint32_t step = nwarps * kPerWarp;
+  const uint32_t step_r = TILED ? step / kb : 0u, step_f = TILED ? step - step_r * kb : 0u;
+  uint32_t r_base = TILED ? (warp * kPerWarp) / kb : 0u;
+  uint32_t f_base = TILED ? warp * kPerWarp - r_base * kb : 0u;
+  for (uint32_t base = warp * kPerWarp; base < blocks; base += step) {
     uint4 v[kNvRounds];
     uint32_t b[kNvRounds];
 #pragma unroll
@@ -175,14 +181,32 @@ __global__ void __launch_bounds__(kNvThreads)
         }
         // row-major [R, K/2]: block b covers bytes 8 b .. 8 b + 7
         *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(b[u]) * 8 + 4 * l2) = packed;
-        if (l2 == 0) {
-          if (TILED) {
-            const uint32_t r = b[u] / kb;
-            sx[nv_tile_offset(r, b[u] - r * kb, kb)] = static_cast<uint8_t>(sc);
-          } else {
-            sx[b[u]] = static_cast<uint8_t>(sc);
+        if (!TILED && l2 == 0) sx[b[u]] = static_cast<uint8_t>(sc);
+      }
+      if (TILED) {
+        // Four consecutive blocks (subs 4j .. 4j + 3) are one 4-byte cell of
+        // one row (kb % 4 == 0 and the blocks start at a multiple of 4): the
+        // cell's first lane gathers the codes and stores the cell whole.
+        const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, sc, 2);
+        const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, sc, 4);
+        const uint32_t c3 = __shfl_down_sync(0xFFFFFFFFu, sc, 6);
+        if ((lane & 7u) == 0 && b[u] < blocks) {
+          uint32_t r = r_base, f = f_base + 16 * u + (lane >> 1);
+          while (f >= kb) {  // at most 28 / kb + 1 times
+            f -= kb;
+            ++r;
           }
+          *reinterpret_cast<uint32_t*>(sx + nv_tile_offset(r, f, kb)) =
+              sc | (c1 << 8) | (c2 << 16) | (c3 << 24);
         }
+      }
+    }
+    if (TILED) {
+      r_base += step_r;
+      f_base += step_f;
+      if (f_base >= kb) {
+        f_base -= kb;
+        ++r_base;
       }
     }
   }

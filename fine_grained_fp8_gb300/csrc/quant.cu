@@ -421,7 +421,13 @@ __global__ void __launch_bounds__(kMxThreads)
   const uint32_t warp = (blockIdx.x * kMxThreads + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * kMxThreads) >> 5;
   constexpr uint32_t kPerWarp = 8 * kMxRounds;
-  for (uint32_t base = warp * kPerWarp; base < groups; base += nwarps * kPerWarp) {
+  // Tiled scales: the row and factor index of `base`, advanced by the
+  // loop's stride without a division per iteration.
+  const uint32_t step = nwarps * kPerWarp;
+  const uint32_t step_r = TILED ? step / kg : 0u, step_f = TILED ? step - step_r * kg : 0u;
+  uint32_t r_base = TILED ? (warp * kPerWarp) / kg : 0u;
+  uint32_t f_base = TILED ? warp * kPerWarp - r_base * kg : 0u;
+  for (uint32_t base = warp * kPerWarp; base < groups; base += step) {
     uint4 v[kMxRounds];
     uint32_t g[kMxRounds];
 #pragma unroll
@@ -459,14 +465,32 @@ __global__ void __launch_bounds__(kMxThreads)
         const uint32_t packed = cvt_e2m1x8(y);
         // row-major [R, K/2]: group g covers bytes 16 g .. 16 g + 15
         *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(g[u]) * 16 + 4 * l4) = packed;
-        if (l4 == 0) {
-          if (TILED) {
-            const uint32_t r = g[u] / kg;
-            sx[fp4_tile_offset(r, g[u] - r * kg, kg)] = static_cast<uint8_t>(code);
-          } else {
-            sx[g[u]] = static_cast<uint8_t>(code);
+        if (!TILED && l4 == 0) sx[g[u]] = static_cast<uint8_t>(code);
+      }
+      if (TILED) {
+        // Four consecutive groups (subs 4j .. 4j + 3) are one 4-byte cell of
+        // one row (kg % 4 == 0 and the groups start at a multiple of 4): the
+        // cell's first lane gathers the codes and stores the cell whole.
+        const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, code, 4);
+        const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, code, 8);
+        const uint32_t c3 = __shfl_down_sync(0xFFFFFFFFu, code, 12);
+        if ((lane & 15u) == 0 && g[u] < groups) {
+          uint32_t r = r_base, f = f_base + 8 * u + (lane >> 2);
+          while (f >= kg) {  // at most 12 / kg + 1 times
+            f -= kg;
+            ++r;
           }
+          *reinterpret_cast<uint32_t*>(sx + fp4_tile_offset(r, f, kg)) =
+              code | (c1 << 8) | (c2 << 16) | (c3 << 24);
         }
+      }
+    }
+    if (TILED) {
+      r_base += step_r;
+      f_base += step_f;
+      if (f_base >= kg) {
+        f_base -= kg;
+        ++r_base;
       }
     }
   }

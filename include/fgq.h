@@ -356,7 +356,7 @@ fgq_status fgq_fp4_scales_to_tiles(const uint8_t* s, int64_t R, int64_t F, uint8
 /*
  * fgq_quant_mxfp4_1x32 and fgq_quant_nvfp4_1x16 with the scales written in
  * the tiled layout (s_tiles: fgq_fp4_scale_tiles_bytes(R, K/32 or K/16)
- * bytes, padding untouched) instead of row-major.  Codes, scales and
+ * bytes, 4-byte aligned, padding untouched) instead of row-major.  Codes, scales and
  * arguments otherwise as those calls; K % 128 == 0 (MXFP4) or
  * K % 64 == 0 (NVFP4).
  */
