@@ -354,7 +354,7 @@ def fp4_scale_tiles_bytes(R: int, F: int) -> int:
 def fp4_scales_to_tiles(s: torch.Tensor, tiles: torch.Tensor | None = None) -> torch.Tensor:
     """Row-major FP4 block scales s [R, F] uint8 (F % 4 == 0) in the tiled
     layout the _tiled GEMMs take: a 1-D uint8 tensor of
-    fp4_scale_tiles_bytes(R, F) bytes (pad rows left as they are)."""
+    fp4_scale_tiles_bytes(R, F) bytes (pad rows written as zeros)."""
     _need_cuda("s", s, torch.uint8)
     if s.dim() != 2 or not s.is_contiguous():
         raise ValueError("s must be a dense [R, F]")

@@ -114,7 +114,7 @@ fgq_status fgq_quant_mxfp4_1x32_tiled(const void* x, int64_t R, int64_t K, int64
   if (R == 0) return FGQ_OK;
   if (!x || !xq || !s_tiles) return FGQ_ERR_INVALID_ARG;
   if (ldx < K || ldx % 8 != 0) return FGQ_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || !aligned(xq, 4) || !aligned(s_tiles, 4)) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(xq, 4) || !aligned(s_tiles, 16)) return FGQ_ERR_INVALID_ARG;
   if (R > kMaxGroups / (K / 32)) return FGQ_ERR_INVALID_ARG;
   fgq::DeviceInfo dev;
   fgq_status st = get_device(&dev);
@@ -266,7 +266,7 @@ fgq_status fgq_quant_nvfp4_1x16_tiled(const void* x, int64_t R, int64_t K, int64
   if (R == 0) return FGQ_OK;
   if (!x || !g || !xq || !s_tiles) return FGQ_ERR_INVALID_ARG;
   if (ldx < K || ldx % 8 != 0) return FGQ_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || !aligned(g, 4) || !aligned(xq, 4) || !aligned(s_tiles, 4))
+  if (!aligned(x, 16) || !aligned(g, 4) || !aligned(xq, 4) || !aligned(s_tiles, 16))
     return FGQ_ERR_INVALID_ARG;
   if (R > kMaxGroups / (K / 16)) return FGQ_ERR_INVALID_ARG;
   fgq::DeviceInfo dev;

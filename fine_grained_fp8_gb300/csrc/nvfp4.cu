@@ -90,16 +90,56 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
 constexpr int kNvThreads = 256;
 constexpr int kNvRounds = 2;
 
-// Byte of factor f of row r in the tiled FP4 scale layout (F factor bytes a
-// row, F % 4 == 0): 512-byte tiles of 128 rows x 4 factor bytes, tile
-// (r / 128, f / 4); in a tile, row r at 16 (r % 32) + 4 ((r % 128) / 32),
-// the byte at + f % 4.
-__device__ __forceinline__ uint64_t nv_tile_offset(uint32_t r, uint32_t f, uint32_t F) {
-  return (static_cast<uint64_t>(r >> 7) * (F >> 2) + (f >> 2)) * 512u + (r & 31u) * 16u +
-         ((r >> 5) & 3u) * 4u + (f & 3u);
+// One block of 16 elements over two lanes (8 each, v) under the global
+// scale g (d6 = fl32(6 g)): the block's E4M3 scale code (the same in both
+// lanes) and this lane's eight E2M1 codes.
+__device__ __forceinline__ uint32_t nv_block(const uint4& v, float g, float d6, uint32_t* out) {
+  uint32_t mx = absmax_pairs(v);
+  mx = __vmaxu2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+  const float amax = __uint_as_float(max(mx & 0xFFFFu, mx >> 16) << 16);
+  const uint32_t sc = e4m3_code(__fdiv_rn(amax, d6));
+  const float d = __fmul_rn(g, e4m3_value(sc));
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t packed = 0;
+  if (d == 0.0f) {
+    // signed zeros: code 8 where the bf16 sign bit is set
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+      packed |= (((w[p] >> 12) & 0x8u) | ((w[p] >> 24) & 0x80u)) << (8 * p);
+  } else {
+    float ylo[8], yhi[8];
+    const float r = __frcp_rn(d);
+    const float2 r2 = make_float2(r, r);
+    const float2 lo2 = make_float2(1.0f - 0x1p-20f, 1.0f - 0x1p-20f);
+    const float2 hi2 = make_float2(1.0f + 0x1p-20f, 1.0f + 0x1p-20f);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float2 q = mul2(bf16x2_to_f32x2(w[p]), r2);
+      const float2 ql = mul2(q, lo2), qh = mul2(q, hi2);
+      ylo[2 * p] = ql.x;
+      ylo[2 * p + 1] = ql.y;
+      yhi[2 * p] = qh.x;
+      yhi[2 * p + 1] = qh.y;
+    }
+    // the two ends of the bracket; equal codes are the code of y too
+    packed = cvt_e2m1x8(ylo);
+    if (!(d >= 0x1p-126f) || packed != cvt_e2m1x8(yhi)) {
+      // rare: recompute the lane's eight quotients exactly
+      float y[8];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const float2 f = bf16x2_to_f32x2(w[p]);
+        y[2 * p] = __fdiv_rn(f.x, d);
+        y[2 * p + 1] = __fdiv_rn(f.y, d);
+      }
+      packed = cvt_e2m1x8(y);
+    }
+  }
+  *out = packed;
+  return sc;
 }
 
-template <bool DENSE, bool TILED>
+template <bool DENSE>
 __global__ void __launch_bounds__(kNvThreads)
     quant_nvfp4_1x16_kernel(const uint16_t* __restrict__ x, uint32_t kb, uint32_t blocks,
                             int64_t ldx, const float* __restrict__ gptr, uint8_t* __restrict__ xq,
@@ -111,13 +151,7 @@ __global__ void __launch_bounds__(kNvThreads)
   constexpr uint32_t kPerWarp = 16 * kNvRounds;
   const float g = __ldg(gptr);
   const float d6 = __fmul_rn(6.0f, g);
-  // Tiled scales: the row and block index of `base`, advanced by the loop's
-  // stride without a division per iteration.
-  const uint32_t step = nwarps * kPerWarp;
-  const uint32_t step_r = TILED ? step / kb : 0u, step_f = TILED ? step - step_r * kb : 0u;
-  uint32_t r_base = TILED ? (warp * kPerWarp) / kb : 0u;
-  uint32_t f_base = TILED ? warp * kPerWarp - r_base * kb : 0u;
-  for (uint32_t base = warp * kPerWarp; base < blocks; base += step) {
+  for (uint32_t base = warp * kPerWarp; base < blocks; base += nwarps * kPerWarp) {
     uint4 v[kNvRounds];
     uint32_t b[kNvRounds];
 #pragma unroll
@@ -137,78 +171,68 @@ __global__ void __launch_bounds__(kNvThreads)
     }
 #pragma unroll
     for (int u = 0; u < kNvRounds; ++u) {
-      uint32_t mx = absmax_pairs(v[u]);
-      mx = __vmaxu2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-      const float amax = __uint_as_float(max(mx & 0xFFFFu, mx >> 16) << 16);
-      const uint32_t sc = e4m3_code(__fdiv_rn(amax, d6));
-      const float d = __fmul_rn(g, e4m3_value(sc));
+      uint32_t packed;
+      const uint32_t sc = nv_block(v[u], g, d6, &packed);
       if (b[u] < blocks) {
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        uint32_t packed = 0;
-        if (d == 0.0f) {
-          // signed zeros: code 8 where the bf16 sign bit is set
-#pragma unroll
-          for (int p = 0; p < 4; ++p)
-            packed |= (((w[p] >> 12) & 0x8u) | ((w[p] >> 24) & 0x80u)) << (8 * p);
-        } else {
-          float ylo[8], yhi[8];
-          const float r = __frcp_rn(d);
-          const float2 r2 = make_float2(r, r);
-          const float2 lo2 = make_float2(1.0f - 0x1p-20f, 1.0f - 0x1p-20f);
-          const float2 hi2 = make_float2(1.0f + 0x1p-20f, 1.0f + 0x1p-20f);
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const float2 q = mul2(bf16x2_to_f32x2(w[p]), r2);
-            const float2 ql = mul2(q, lo2), qh = mul2(q, hi2);
-            ylo[2 * p] = ql.x;
-            ylo[2 * p + 1] = ql.y;
-            yhi[2 * p] = qh.x;
-            yhi[2 * p + 1] = qh.y;
-          }
-          // the two ends of the bracket; equal codes are the code of y too
-          packed = cvt_e2m1x8(ylo);
-          if (!(d >= 0x1p-126f) || packed != cvt_e2m1x8(yhi)) {
-            // rare: recompute the lane's eight quotients exactly
-            float y[8];
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-              const float2 f = bf16x2_to_f32x2(w[p]);
-              y[2 * p] = __fdiv_rn(f.x, d);
-              y[2 * p + 1] = __fdiv_rn(f.y, d);
-            }
-            packed = cvt_e2m1x8(y);
-          }
-        }
         // row-major [R, K/2]: block b covers bytes 8 b .. 8 b + 7
         *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(b[u]) * 8 + 4 * l2) = packed;
-        if (!TILED && l2 == 0) sx[b[u]] = static_cast<uint8_t>(sc);
-      }
-      if (TILED) {
-        // Four consecutive blocks (subs 4j .. 4j + 3) are one 4-byte cell of
-        // one row (kb % 4 == 0 and the blocks start at a multiple of 4): the
-        // cell's first lane gathers the codes and stores the cell whole.
-        const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, sc, 2);
-        const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, sc, 4);
-        const uint32_t c3 = __shfl_down_sync(0xFFFFFFFFu, sc, 6);
-        if ((lane & 7u) == 0 && b[u] < blocks) {
-          uint32_t r = r_base, f = f_base + 16 * u + (lane >> 1);
-          while (f >= kb) {  // at most 28 / kb + 1 times
-            f -= kb;
-            ++r;
-          }
-          *reinterpret_cast<uint32_t*>(sx + nv_tile_offset(r, f, kb)) =
-              sc | (c1 << 8) | (c2 << 16) | (c3 << 24);
-        }
+        if (l2 == 0) sx[b[u]] = static_cast<uint8_t>(sc);
       }
     }
-    if (TILED) {
-      r_base += step_r;
-      f_base += step_f;
-      if (f_base >= kb) {
-        f_base -= kb;
-        ++r_base;
-      }
+  }
+}
+
+// The same quantizer with the scales in the tiled FP4 layout (512-byte tiles
+// of 128 rows x 4 factor bytes; 16-byte tile row i holds the cells of rows
+// 32 j + i, j = 0..3).  A warp's unit is 16-byte row i of four neighbouring
+// tiles: four rounds, round j quantizing 16 blocks (512 contiguous bytes of
+// x) of row 32 j + i; lanes 0, 8, 16 and 24 then each hold tile row i of
+// one cell and store it whole.  Rows past R read as zeros and give padding
+// codes.
+__global__ void __launch_bounds__(kNvThreads)
+    quant_nvfp4_1x16_tiled_kernel(const uint16_t* __restrict__ x, uint32_t R, uint32_t kb,
+                                  int64_t ldx, const float* __restrict__ gptr,
+                                  uint8_t* __restrict__ xq, uint8_t* __restrict__ st) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t sub = lane >> 1, l2 = lane & 1u;
+  const uint32_t warp = (blockIdx.x * kNvThreads + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * kNvThreads) >> 5;
+  const float g = __ldg(gptr);
+  const float d6 = __fmul_rn(6.0f, g);
+  const uint32_t cpr = kb >> 2;            // cells (tiles) per 128-row tile
+  const uint32_t quads = (cpr + 3u) >> 2;  // groups of four cells per 128-row tile
+  const uint32_t units = ((R + 127u) >> 7) * quads * 32u;
+  for (uint32_t unit = warp; unit < units; unit += nwarps) {
+    const uint32_t i = unit & 31u, t = unit >> 5;
+    const uint32_t rb = t / quads, cq = t - rb * quads;
+    const uint32_t blk = 16u * cq + sub;  // this lane's block within the row
+    const bool col_ok = blk < kb;         // the last cells of the four may not exist
+    uint4 v[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint32_t row = rb * 128u + 32u * jj + i;
+      v[jj] = make_uint4(0, 0, 0, 0);
+      if (row < R && col_ok)
+        v[jj] = ld_stream_16(x + static_cast<int64_t>(row) * ldx + blk * 16u + 8u * l2);
     }
+    uint32_t cell[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint32_t row = rb * 128u + 32u * jj + i;
+      uint32_t packed;
+      const uint32_t sc = nv_block(v[jj], g, d6, &packed);
+      if (row < R && col_ok)
+        *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(row) * (8u * kb) + blk * 8u +
+                                     4u * l2) = packed;
+      // lanes 8 q: the cells (blocks in lanes +0, +2, +4, +6)
+      const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, sc, 2);
+      const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, sc, 4);
+      const uint32_t c3 = __shfl_down_sync(0xFFFFFFFFu, sc, 6);
+      cell[jj] = sc | (c1 << 8) | (c2 << 16) | (c3 << 24);
+    }
+    if ((lane & 7u) == 0 && col_ok)
+      *reinterpret_cast<uint4*>(st + (static_cast<uint64_t>(rb) * cpr + 4u * cq + (lane >> 3)) * 512u +
+                                16u * i) = make_uint4(cell[0], cell[1], cell[2], cell[3]);
   }
 }
 
@@ -245,9 +269,24 @@ cudaError_t launch_quant_nvfp4_1x16(const void* x, int64_t R, int64_t K, int64_t
   const uint32_t kb = static_cast<uint32_t>(K / 16);
   const uint32_t blocks = static_cast<uint32_t>(R * (K / 16));
   if (blocks == 0) return cudaSuccess;
+  if (tiled) {
+    // one warp per 16-byte row of four neighbouring tiles (64 blocks)
+    const uint32_t units = static_cast<uint32_t>((R + 127) / 128) * ((kb / 4 + 3) / 4) * 32u;
+    int per_sm = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, quant_nvfp4_1x16_tiled_kernel, kNvThreads, 0);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+    const uint32_t per_block = kNvThreads / 32;
+    const uint32_t needed = (units + per_block - 1) / per_block;
+    uint32_t grid = static_cast<uint32_t>(dev.sm_count) * static_cast<uint32_t>(per_sm);
+    if (grid > needed) grid = needed;
+    quant_nvfp4_1x16_tiled_kernel<<<grid, kNvThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(x), static_cast<uint32_t>(R), kb, ldx, g, xq, sx);
+    return cudaGetLastError();
+  }
   const bool dense = ldx == K;
-  auto k = dense ? (tiled ? quant_nvfp4_1x16_kernel<true, true> : quant_nvfp4_1x16_kernel<true, false>)
-                 : (tiled ? quant_nvfp4_1x16_kernel<false, true> : quant_nvfp4_1x16_kernel<false, false>);
+  auto k = dense ? quant_nvfp4_1x16_kernel<true> : quant_nvfp4_1x16_kernel<false>;
   int per_sm = 0;
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kNvThreads, 0);
   if (err != cudaSuccess) return err;
@@ -260,30 +299,38 @@ cudaError_t launch_quant_nvfp4_1x16(const void* x, int64_t R, int64_t K, int64_t
   return cudaGetLastError();
 }
 
-// Row-major FP4 block scales [R, F] (F % 4 == 0) into the tiled layout:
-// one 4-byte cell (four factor bytes of one row) per thread, read and
-// written whole (a cell's four bytes stay together in the tiled layout).
+// Row-major FP4 block scales [R, F] (F % 4 == 0) into the tiled layout.  A
+// block takes one 128-row tile x 8 cells: it reads 32 contiguous bytes of
+// each of the 128 rows, transposes through shared memory, and writes the 8
+// tiles (4 KB, contiguous in the tiled layout) with whole-sector stores.
+// Rows past R are written as zeros.
 __global__ void __launch_bounds__(256)
-    fp4_scales_to_tiles_kernel(const uint32_t* __restrict__ s, uint32_t cells_per_row,
-                               uint64_t cells, uint32_t* __restrict__ tiles) {
-  for (uint64_t i = blockIdx.x * 256ull + threadIdx.x; i < cells; i += gridDim.x * 256ull) {
-    const uint32_t r = static_cast<uint32_t>(i / cells_per_row);
-    const uint32_t c = static_cast<uint32_t>(i - static_cast<uint64_t>(r) * cells_per_row);
-    const uint64_t word = (static_cast<uint64_t>(r >> 7) * cells_per_row + c) * 128u +
-                          (r & 31u) * 4u + ((r >> 5) & 3u);
-    tiles[word] = __ldg(s + i);
+    fp4_scales_to_tiles_kernel(const uint32_t* __restrict__ s, uint32_t R, uint32_t cpr,
+                               uint32_t* __restrict__ tiles) {
+  __shared__ uint32_t t[8 * 128];
+  const uint32_t cgroups = (cpr + 7u) / 8u;
+  const uint32_t rb = blockIdx.x / cgroups, c0 = (blockIdx.x - rb * cgroups) * 8u;
+  const uint32_t ncell = cpr - c0 < 8u ? cpr - c0 : 8u;
+  for (uint32_t k = threadIdx.x; k < 1024u; k += 256u) {
+    const uint32_t rr = k >> 3, cell = k & 7u;  // row in the tile, cell
+    const uint32_t r = rb * 128u + rr;
+    uint32_t w = 0;
+    if (cell < ncell && r < R) w = __ldg(s + static_cast<uint64_t>(r) * cpr + c0 + cell);
+    t[cell * 128u + (rr & 31u) * 4u + (rr >> 5)] = w;
   }
+  __syncthreads();
+  uint32_t* out = tiles + (static_cast<uint64_t>(rb) * cpr + c0) * 128u;
+  for (uint32_t k = threadIdx.x; k < ncell * 128u; k += 256u) out[k] = t[k];
 }
 
 cudaError_t launch_fp4_scales_to_tiles(const uint8_t* s, int64_t R, int64_t F, uint8_t* tiles,
                                        cudaStream_t stream, const DeviceInfo& dev) {
-  const uint64_t cells = static_cast<uint64_t>(R) * static_cast<uint64_t>(F / 4);
-  if (cells == 0) return cudaSuccess;
-  uint64_t grid = (cells + 255) / 256;
-  const uint64_t cap = static_cast<uint64_t>(dev.sm_count) * 8;
-  if (grid > cap) grid = cap;
-  fp4_scales_to_tiles_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
-      reinterpret_cast<const uint32_t*>(s), static_cast<uint32_t>(F / 4), cells,
+  (void)dev;
+  const uint32_t cpr = static_cast<uint32_t>(F / 4);
+  const uint64_t blocks = static_cast<uint64_t>((R + 127) / 128) * ((cpr + 7) / 8);
+  if (blocks == 0) return cudaSuccess;
+  fp4_scales_to_tiles_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      reinterpret_cast<const uint32_t*>(s), static_cast<uint32_t>(R), cpr,
       reinterpret_cast<uint32_t*>(tiles));
   return cudaGetLastError();
 }

@@ -402,17 +402,28 @@ __device__ __forceinline__ uint32_t mx_scale_code(uint32_t mag_bits) {
   return man != 0 ? e + 1 : e;
 }
 
-// Byte of factor f of row r in the tiled FP4 scale layout (F factor bytes a
-// row, F % 4 == 0): 512-byte tiles of 128 rows x 4 factor bytes, tile
-// (r / 128, f / 4); in a tile, row r at 16 (r % 32) + 4 ((r % 128) / 32),
-// the byte at + f % 4.  A tile is the 32-row x 16-byte shared-memory tile
-// the FP4 GEMM copies into TMEM (row m of A lands at lane m, column m / 32).
-__device__ __forceinline__ uint64_t fp4_tile_offset(uint32_t r, uint32_t f, uint32_t F) {
-  return (static_cast<uint64_t>(r >> 7) * (F >> 2) + (f >> 2)) * 512u + (r & 31u) * 16u +
-         ((r >> 5) & 3u) * 4u + (f & 3u);
+// One group of 32 elements over four lanes (8 each, v): the group's UE8M0
+// code (the same in the four lanes) and this lane's eight E2M1 codes.
+__device__ __forceinline__ uint32_t mx_group(const uint4& v, uint32_t* packed) {
+  uint32_t mx = absmax_pairs(v);
+  mx = __vmaxu2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+  mx = __vmaxu2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+  const uint32_t code = mx_scale_code(max(mx & 0xFFFFu, mx >> 16));
+  // 2^-e: exponent field 254 - code; code 0 (2^-127) gives 2^127
+  const float inv = __uint_as_float((254u - code) << 23);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float y[8];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const float2 f = bf16x2_to_f32x2(w[p]);
+    y[2 * p] = f.x * inv;
+    y[2 * p + 1] = f.y * inv;
+  }
+  *packed = cvt_e2m1x8(y);
+  return code;
 }
 
-template <bool DENSE, bool TILED>
+template <bool DENSE>
 __global__ void __launch_bounds__(kMxThreads)
     quant_mxfp4_1x32_kernel(const uint16_t* __restrict__ x, uint32_t kg, uint32_t groups,
                             int64_t ldx, uint8_t* __restrict__ xq, uint8_t* __restrict__ sx) {
@@ -421,13 +432,7 @@ __global__ void __launch_bounds__(kMxThreads)
   const uint32_t warp = (blockIdx.x * kMxThreads + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * kMxThreads) >> 5;
   constexpr uint32_t kPerWarp = 8 * kMxRounds;
-  // Tiled scales: the row and factor index of `base`, advanced by the
-  // loop's stride without a division per iteration.
-  const uint32_t step = nwarps * kPerWarp;
-  const uint32_t step_r = TILED ? step / kg : 0u, step_f = TILED ? step - step_r * kg : 0u;
-  uint32_t r_base = TILED ? (warp * kPerWarp) / kg : 0u;
-  uint32_t f_base = TILED ? warp * kPerWarp - r_base * kg : 0u;
-  for (uint32_t base = warp * kPerWarp; base < groups; base += step) {
+  for (uint32_t base = warp * kPerWarp; base < groups; base += nwarps * kPerWarp) {
     uint4 v[kMxRounds];
     uint32_t g[kMxRounds];
 #pragma unroll
@@ -447,52 +452,69 @@ __global__ void __launch_bounds__(kMxThreads)
     }
 #pragma unroll
     for (int u = 0; u < kMxRounds; ++u) {
-      uint32_t mx = absmax_pairs(v[u]);
-      mx = __vmaxu2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-      mx = __vmaxu2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-      const uint32_t code = mx_scale_code(max(mx & 0xFFFFu, mx >> 16));
-      // 2^-e: exponent field 254 - code; code 0 (2^-127) gives 2^127
-      const float inv = __uint_as_float((254u - code) << 23);
+      uint32_t packed;
+      const uint32_t code = mx_group(v[u], &packed);
       if (g[u] < groups) {
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        float y[8];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const float2 f = bf16x2_to_f32x2(w[p]);
-          y[2 * p] = f.x * inv;
-          y[2 * p + 1] = f.y * inv;
-        }
-        const uint32_t packed = cvt_e2m1x8(y);
         // row-major [R, K/2]: group g covers bytes 16 g .. 16 g + 15
         *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(g[u]) * 16 + 4 * l4) = packed;
-        if (!TILED && l4 == 0) sx[g[u]] = static_cast<uint8_t>(code);
-      }
-      if (TILED) {
-        // Four consecutive groups (subs 4j .. 4j + 3) are one 4-byte cell of
-        // one row (kg % 4 == 0 and the groups start at a multiple of 4): the
-        // cell's first lane gathers the codes and stores the cell whole.
-        const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, code, 4);
-        const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, code, 8);
-        const uint32_t c3 = __shfl_down_sync(0xFFFFFFFFu, code, 12);
-        if ((lane & 15u) == 0 && g[u] < groups) {
-          uint32_t r = r_base, f = f_base + 8 * u + (lane >> 2);
-          while (f >= kg) {  // at most 12 / kg + 1 times
-            f -= kg;
-            ++r;
-          }
-          *reinterpret_cast<uint32_t*>(sx + fp4_tile_offset(r, f, kg)) =
-              code | (c1 << 8) | (c2 << 16) | (c3 << 24);
-        }
+        if (l4 == 0) sx[g[u]] = static_cast<uint8_t>(code);
       }
     }
-    if (TILED) {
-      r_base += step_r;
-      f_base += step_f;
-      if (f_base >= kg) {
-        f_base -= kg;
-        ++r_base;
-      }
+  }
+}
+
+// The same quantizer with the scales in the tiled FP4 layout: 512-byte tiles
+// of 128 rows x 4 factor bytes; tile (r / 128, f / 4) holds, in its 16-byte
+// row i, the cells (4 factor bytes) of rows 32 j + i, j = 0..3 (the 32-row x
+// 16-byte tile the FP4 GEMM copies into TMEM).  A warp's unit is 16-byte
+// row i of two neighbouring tiles: four rounds, round j quantizing 8 groups
+// (512 contiguous bytes of x, as the row-major kernel reads them) of row
+// 32 j + i; lane 0 then holds tile row i of the first cell and lane 16 of
+// the second, each stored whole.  Consecutive warps take consecutive tile
+// rows, so the scale stores fill whole sectors.  Rows past R read as zeros
+// and give padding codes (127).
+__global__ void __launch_bounds__(kMxThreads)
+    quant_mxfp4_1x32_tiled_kernel(const uint16_t* __restrict__ x, uint32_t R, uint32_t kg,
+                                  int64_t ldx, uint8_t* __restrict__ xq,
+                                  uint8_t* __restrict__ st) {
+  const uint32_t lane = threadIdx.x & 31u;
+  const uint32_t sub = lane >> 2, l4 = lane & 3u;
+  const uint32_t warp = (blockIdx.x * kMxThreads + threadIdx.x) >> 5;
+  const uint32_t nwarps = (gridDim.x * kMxThreads) >> 5;
+  const uint32_t cpr = kg >> 2;            // cells (tiles) per 128-row tile
+  const uint32_t pairs = (cpr + 1u) >> 1;  // cell pairs per 128-row tile
+  const uint32_t units = ((R + 127u) >> 7) * pairs * 32u;
+  for (uint32_t unit = warp; unit < units; unit += nwarps) {
+    const uint32_t i = unit & 31u, t = unit >> 5;
+    const uint32_t rb = t / pairs, cp = t - rb * pairs;
+    const uint32_t grp = 8u * cp + sub;          // this lane's group within the row
+    const bool col_ok = grp < kg;                // the pair's second cell may not exist
+    uint4 v[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint32_t row = rb * 128u + 32u * jj + i;
+      v[jj] = make_uint4(0, 0, 0, 0);
+      if (row < R && col_ok)
+        v[jj] = ld_stream_16(x + static_cast<int64_t>(row) * ldx + grp * 32u + 8u * l4);
     }
+    uint32_t cell[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint32_t row = rb * 128u + 32u * jj + i;
+      uint32_t packed;
+      const uint32_t code = mx_group(v[jj], &packed);
+      if (row < R && col_ok)
+        *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(row) * (16u * kg) + grp * 16u +
+                                     4u * l4) = packed;
+      // lanes 0 and 16: the cells (groups in lanes +0, +4, +8, +12)
+      const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, code, 4);
+      const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, code, 8);
+      const uint32_t c3 = __shfl_down_sync(0xFFFFFFFFu, code, 12);
+      cell[jj] = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+    }
+    if ((lane & 15u) == 0 && col_ok)
+      *reinterpret_cast<uint4*>(st + (static_cast<uint64_t>(rb) * cpr + 2u * cp + (lane >> 4)) * 512u +
+                                16u * i) = make_uint4(cell[0], cell[1], cell[2], cell[3]);
   }
 }
 
@@ -504,9 +526,23 @@ cudaError_t launch_quant_mxfp4_1x32(const void* x, int64_t R, int64_t K, int64_t
   const uint32_t kg = static_cast<uint32_t>(K / 32);
   const uint32_t groups = static_cast<uint32_t>(R * (K / 32));
   if (groups == 0) return cudaSuccess;
+  if (tiled) {
+    // one warp per 16-byte row of two neighbouring tiles (32 groups)
+    const uint32_t units = static_cast<uint32_t>((R + 127) / 128) * ((kg / 4 + 1) / 2) * 32u;
+    int per_sm = 0;
+    cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &per_sm, quant_mxfp4_1x32_tiled_kernel, kMxThreads, 0);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) per_sm = 1;
+    const uint32_t needed = (units + kMxThreads / 32 - 1) / (kMxThreads / 32);
+    uint32_t grid = static_cast<uint32_t>(dev.sm_count) * static_cast<uint32_t>(per_sm);
+    if (grid > needed) grid = needed;
+    quant_mxfp4_1x32_tiled_kernel<<<grid, kMxThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(x), static_cast<uint32_t>(R), kg, ldx, xq, sx);
+    return cudaGetLastError();
+  }
   const bool dense = ldx == K;
-  auto k = dense ? (tiled ? quant_mxfp4_1x32_kernel<true, true> : quant_mxfp4_1x32_kernel<true, false>)
-                 : (tiled ? quant_mxfp4_1x32_kernel<false, true> : quant_mxfp4_1x32_kernel<false, false>);
+  auto k = dense ? quant_mxfp4_1x32_kernel<true> : quant_mxfp4_1x32_kernel<false>;
   int per_sm = 0;
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kMxThreads, 0);
   if (err != cudaSuccess) return err;

@@ -341,13 +341,15 @@ fgq_status fgq_gemm_nvfp4(const uint8_t* A, const uint8_t* sA, const float* gA,
  * 4 factor bytes, each the 32-row x 16-byte tile the tensor core's factor
  * copy spreads over a 128-row TMEM tile (row m at lane m, column m / 32;
  * "Fine-Grained FP8/FP4 Quantization", §Blackwell: Native Block Scaling).
- * The bytes of rows R .. up to the next multiple of 128 are padding: no
- * call here writes them, and they reach no stored output.
+ * The bytes of rows R .. up to the next multiple of 128 are padding: the
+ * calls below fill them (with the codes of zero rows, or zeros), and they
+ * reach no stored output.
  *
  * fgq_fp4_scale_tiles_bytes: that buffer size.  F % 4 == 0, F > 0, R >= 0.
  * fgq_fp4_scales_to_tiles: row-major codes s [R, F] (4-byte aligned) into
- *   the tiled layout at `tiles` (4-byte aligned, the size above); device
- *   buffers, asynchronous on `stream`.  A pure permutation.
+ *   the tiled layout at `tiles` (4-byte aligned, the size above; padding
+ *   written as zeros); device buffers, asynchronous on `stream`.  A pure
+ *   permutation of the codes.
  */
 fgq_status fgq_fp4_scale_tiles_bytes(int64_t R, int64_t F, size_t* bytes);
 fgq_status fgq_fp4_scales_to_tiles(const uint8_t* s, int64_t R, int64_t F, uint8_t* tiles,
@@ -356,7 +358,8 @@ fgq_status fgq_fp4_scales_to_tiles(const uint8_t* s, int64_t R, int64_t F, uint8
 /*
  * fgq_quant_mxfp4_1x32 and fgq_quant_nvfp4_1x16 with the scales written in
  * the tiled layout (s_tiles: fgq_fp4_scale_tiles_bytes(R, K/32 or K/16)
- * bytes, 4-byte aligned, padding untouched) instead of row-major.  Codes, scales and
+ * bytes, 16-byte aligned; padding gets the codes of zero rows) instead of
+ * row-major.  Codes, scales and
  * arguments otherwise as those calls; K % 128 == 0 (MXFP4) or
  * K % 64 == 0 (NVFP4).
  */

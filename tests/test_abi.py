@@ -243,7 +243,7 @@ def test_fp4_gemms_empty_is_ok(fgq):
     (P, 4, 128, 120, P, P, None),            # ldx < K
     (P, 4, 128, 128, P + 2, P, None),        # xq misaligned
     (P, 4, 128, 128, P, 0, None),            # null scale tiles
-    (P, 4, 128, 128, P, P + 2, None),        # scale tiles misaligned
+    (P, 4, 128, 128, P, P + 8, None),        # scale tiles not 16-byte aligned
 ])
 def test_quant_mxfp4_tiled_rejects(fgq, args):
     assert _lib.fgq_quant_mxfp4_1x32_tiled(*args) == _lib.FGQ_ERR_INVALID_ARG
@@ -254,7 +254,7 @@ def test_quant_mxfp4_tiled_rejects(fgq, args):
     (P, 4, 48, 64, P, P, P, None),           # K % 64
     (P, 4, 64, 64, 0, P, P, None),           # null g
     (P, 4, 64, 64, P, P, 0, None),           # null scale tiles
-    (P, 4, 64, 64, P, P, P + 1, None),       # scale tiles misaligned
+    (P, 4, 64, 64, P, P, P + 4, None),       # scale tiles not 16-byte aligned
 ])
 def test_quant_nvfp4_tiled_rejects(fgq, args):
     assert _lib.fgq_quant_nvfp4_1x16_tiled(*args) == _lib.FGQ_ERR_INVALID_ARG
