@@ -452,16 +452,22 @@ def run_fgq(args):
     # core (block-scaled MMA) instead of promoting every K chunk.
     ue8m0 = None
     if not args.no_ue8m0:
+        # Both operands quantized in one launch with the scales written as
+        # UE8M0 code tiles, then the code-tile GEMM (CTA pairs, factors
+        # loaded by TMA); the scale-writer kernel on fp32 scales is timed
+        # beside it for comparison.
         usteps = max(10, min(args.steps, 500))
+        uta = torch.empty((fgq.ue8m0_scale_tiles_bytes(M_, K_),), dtype=torch.uint8, device=dev)
+        utb = torch.empty((fgq.ue8m0_scale_tiles_bytes(N_, K_),), dtype=torch.uint8, device=dev)
 
         def ustep(i, ev=None):
             a, b = sets[i % 2]
             if ev is not None:
                 ev[0].record(stream)
-            fgq.quant_operands(a, b, "ue8m0", xq=aq, sx=sa, wq=bq, sw=sb)
+            fgq.quant_operands_ue8m0_tiles(a, b, xq=aq, sa_tiles=uta, wq=bq, sb_tiles=utb)
             if ev is not None:
                 ev[1].record(stream)
-            fgq.gemm_fp8_blockscaled(aq, sa, bq, sb, torch.bfloat16, "ue8m0", out=c)
+            fgq.gemm_fp8_ue8m0_tiled(aq, uta, bq, utb, torch.bfloat16, out=c)
             if ev is not None:
                 ev[2].record(stream)
 
@@ -481,11 +487,17 @@ def run_fgq(args):
         ums = reduce_max(dist, u0.elapsed_time(u1), dev) / usteps
         uper = [[e[j].elapsed_time(e[j + 1]) for e in uev] for j in range(2)]
         u_quant, u_gemm = (1e3 * sum(p) / len(p) for p in uper)
+        fgq.quant_operands(sets[0][0], sets[0][1], "ue8m0", xq=aq, sx=sa, wq=bq, sw=sb)
+        u_ex = _event_us(lambda: fgq.gemm_fp8_blockscaled(aq, sa, bq, sb, torch.bfloat16, "ue8m0",
+                                                          out=c), stream, 20)
         ue8m0 = {"scale_mode": "ue8m0", "steps": usteps, "ms_per_step": ums,
                  "value": world * FLOPS_GEMM / (ums * 1e-3) / 1e12, "unit": "TFLOP/s",
                  "quant_operands_us": u_quant, "gemm_us": u_gemm,
                  "gemm_TFLOP/s": FLOPS_GEMM / (u_gemm * 1e-6) / 1e12,
-                 "kernel": "gemm_mx_kernel (tcgen05.mma kind::mxf8f6f4.block_scale)"}
+                 "gemm_scale_writers_us": u_ex,
+                 "kernel": "gemm_fp4_tiled_kernel<pair, 256, MXF8> (tcgen05.mma.cta_group::2 "
+                           "kind::mxf8f6f4.block_scale, UE8M0 code tiles by TMA)"}
+        del uta, utb
         if fgq.device_error() != 0:
             raise SystemExit("a kernel reported a device wait timeout")
 
@@ -787,7 +799,7 @@ def run_fgq(args):
     if ue8m0:
         ue8m0["frac_fp8"] = ue8m0["gemm_TFLOP/s"] / fp8_peak
         ue8m0["peak_fp8"] = fp8_peak
-        ue8m0["traffic"] = _traffic("gemm_mx", "gemm_mx.cu")
+        ue8m0["traffic"] = _traffic("gemm_mx8_tiled", "gemm_mxf4.cu")
     if skinny and "M16" in skinny:
         skinny["M16"]["traffic_lowm"] = _traffic("gemm_lowm_m16", "gemm_lowm.cu")
     hbm = peaks["hbm_gbs"]

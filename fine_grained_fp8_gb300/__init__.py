@@ -29,7 +29,9 @@ __all__ = ["quant_act_1x128", "quant_act_128x1", "quant_operands", "quant_mxfp4_
            "gemm_fp8_blockscaled_splitk", "gemm_fp8_blockscaled_fused_act", "gemm_mxfp4",
            "gemm_nvfp4", "fp4_scale_tiles_bytes", "fp4_scales_to_tiles",
            "quant_mxfp4_1x32_tiled", "quant_nvfp4_1x16_tiled", "gemm_mxfp4_tiled",
-           "gemm_nvfp4_tiled", "splitk_workspace", "device_error",
+           "gemm_nvfp4_tiled", "ue8m0_scale_tiles_bytes", "ue8m0_scale_tiles",
+           "gemm_fp8_ue8m0_tiled", "quant_operands_ue8m0_tiles", "splitk_workspace",
+           "device_error",
            "FgqError", "load", "FGQ_SCALE_FP32", "FGQ_SCALE_UE8M0", "FGQ_OUT_F32",
            "FGQ_OUT_BF16", "scale_mode"]
 
@@ -475,6 +477,98 @@ def gemm_nvfp4_tiled(aq: torch.Tensor, sa: torch.Tensor, ga: torch.Tensor, bq: t
                                    N, K, FGQ_OUT_BF16 if out_dtype == torch.bfloat16 else FGQ_OUT_F32,
                                    _stream(aq))
     check("fgq_gemm_nvfp4_tiled", st)
+    return out
+
+
+def ue8m0_scale_tiles_bytes(R: int, K: int) -> int:
+    """Bytes of UE8M0 code tiles for R rows and reduction length K."""
+    st, n = _lib.fgq_ue8m0_scale_tiles_bytes(R, K)
+    check("fgq_ue8m0_scale_tiles_bytes", st)
+    return n
+
+
+def ue8m0_scale_tiles(s: torch.Tensor, weight: bool, tiles: torch.Tensor | None = None):
+    """UE8M0 code tiles from fp32 power-of-two scales: activation scales
+    s [M, K/128] (weight=False) or weight scales s [K/128, N/128]
+    (weight=True, one row of codes per column of the weight).  Returns a
+    1-D uint8 tensor for gemm_fp8_ue8m0_tiled."""
+    _need_cuda("s", s, torch.float32)
+    if s.dim() != 2 or not s.is_contiguous():
+        raise ValueError("s must be a dense 2-D tensor")
+    if weight:
+        K, N = 128 * s.shape[0], 128 * s.shape[1]
+        R = N
+    else:
+        R, K = s.shape[0], 128 * s.shape[1]
+    n = ue8m0_scale_tiles_bytes(R, K)
+    tiles = _tiles_out(tiles, n, s.device, "tiles")
+    if weight:
+        st = _lib.fgq_ue8m0_scale_tiles_weight(s.data_ptr(), K, N, tiles.data_ptr(), _stream(s))
+    else:
+        st = _lib.fgq_ue8m0_scale_tiles_act(s.data_ptr(), R, K, tiles.data_ptr(), _stream(s))
+    check("fgq_ue8m0_scale_tiles", st)
+    return tiles
+
+
+def quant_operands_ue8m0_tiles(x: torch.Tensor, w: torch.Tensor, xq: torch.Tensor | None = None,
+                               sa_tiles: torch.Tensor | None = None,
+                               wq: torch.Tensor | None = None,
+                               sb_tiles: torch.Tensor | None = None):
+    """quant_operands(x, w, "ue8m0") with the scales written as the UE8M0
+    code tiles gemm_fp8_ue8m0_tiled takes.  Returns (xq, sa_tiles, wq,
+    sb_tiles)."""
+    _need_cuda("x", x, torch.bfloat16)
+    _need_cuda("w", w, torch.bfloat16)
+    if x.dim() != 2 or x.stride(1) != 1 or w.dim() != 2 or w.stride(1) != 1:
+        raise ValueError("x and w must be 2-D with a contiguous last dimension")
+    M, K = x.shape
+    K2, N = w.shape
+    if K2 != K:
+        raise ValueError(f"x is [M, {K}] but w is [{K2}, N]")
+    dev = x.device
+    xq = torch.empty((M, K), dtype=torch.uint8, device=dev) if xq is None else xq
+    wq = torch.empty((N, K), dtype=torch.uint8, device=dev) if wq is None else wq
+    _need_cuda("xq", xq, torch.uint8)
+    _need_cuda("wq", wq, torch.uint8)
+    if xq.shape != (M, K) or xq.stride(1) != 1 or wq.shape != (N, K) or not wq.is_contiguous():
+        raise ValueError("xq must be [M, K] (contiguous rows) and wq a dense [N, K]")
+    sa_tiles = _tiles_out(sa_tiles, ue8m0_scale_tiles_bytes(M, K), dev, "sa_tiles")
+    sb_tiles = _tiles_out(sb_tiles, ue8m0_scale_tiles_bytes(N, K), dev, "sb_tiles")
+    st = _lib.fgq_quant_operands_ue8m0_tiles(x.data_ptr(), M, K, x.stride(0), xq.data_ptr(),
+                                             xq.stride(0), sa_tiles.data_ptr(), w.data_ptr(), N,
+                                             w.stride(0), wq.data_ptr(), sb_tiles.data_ptr(),
+                                             _stream(x))
+    check("fgq_quant_operands_ue8m0_tiles", st)
+    return xq, sa_tiles, wq, sb_tiles
+
+
+def gemm_fp8_ue8m0_tiled(aq: torch.Tensor, sa_tiles: torch.Tensor, bq: torch.Tensor,
+                         sb_tiles: torch.Tensor, out_dtype=torch.bfloat16,
+                         out: torch.Tensor | None = None) -> torch.Tensor:
+    """The power-of-two-scale FP8 GEMM with UE8M0 code tiles: aq [M, K] and
+    bq [N, K] E4M3 codes (bq as quant_w_128x128 returns it), sa_tiles and
+    sb_tiles from ue8m0_scale_tiles."""
+    for name, t in (("aq", aq), ("bq", bq), ("sa_tiles", sa_tiles), ("sb_tiles", sb_tiles)):
+        _need_cuda(name, t, torch.uint8)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    M, K = aq.shape
+    N = bq.shape[0]
+    if bq.shape != (N, K):
+        raise ValueError("shape mismatch: aq [M, K], bq [N, K]")
+    if sa_tiles.numel() != ue8m0_scale_tiles_bytes(M, K) or \
+            sb_tiles.numel() != ue8m0_scale_tiles_bytes(N, K):
+        raise ValueError("sa_tiles / sb_tiles must be ue8m0_scale_tiles of A and of the weight")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=aq.device)
+    _need_cuda("out", out, out_dtype)
+    if out.shape != (M, N) or out.stride(1) != 1:
+        raise ValueError("out must be [M, N] with contiguous rows")
+    st = _lib.fgq_gemm_fp8_ue8m0_tiled(aq.data_ptr(), sa_tiles.data_ptr(), bq.data_ptr(),
+                                       sb_tiles.data_ptr(), out.data_ptr(), out.stride(0), M, N, K,
+                                       FGQ_OUT_BF16 if out_dtype == torch.bfloat16 else FGQ_OUT_F32,
+                                       _stream(aq))
+    check("fgq_gemm_fp8_ue8m0_tiled", st)
     return out
 
 

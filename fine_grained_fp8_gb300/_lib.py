@@ -55,6 +55,13 @@ SIGNATURES = {
     "fgq_quant_nvfp4_1x16_tiled": (_int, [_vp, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
     "fgq_fp4_scale_tiles_bytes": (_int, [_i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
     "fgq_fp4_scales_to_tiles": (_int, [_vp, _i64, _i64, _vp, _vp]),
+    "fgq_ue8m0_scale_tiles_bytes": (_int, [_i64, _i64, ctypes.POINTER(ctypes.c_size_t)]),
+    "fgq_ue8m0_scale_tiles_act": (_int, [_vp, _i64, _i64, _vp, _vp]),
+    "fgq_quant_operands_ue8m0_tiles": (_int, [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64,
+                                              _i64, _vp, _vp, _vp]),
+    "fgq_ue8m0_scale_tiles_weight": (_int, [_vp, _i64, _i64, _vp, _vp]),
+    "fgq_gemm_fp8_ue8m0_tiled": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int,
+                                        _vp]),
     "fgq_gemm_fp8_blockscaled_fused_act": (_int, [_vp, _i64, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
                                                   _int, _int, _vp]),
     "fgq_gemm_fp8_blockscaled_splitk_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64,
@@ -198,6 +205,30 @@ def fgq_fp4_scale_tiles_bytes(R, F):
 
 def fgq_fp4_scales_to_tiles(s, R, F, tiles, stream) -> int:
     return load().fgq_fp4_scales_to_tiles(s, R, F, tiles, stream)
+
+
+def fgq_ue8m0_scale_tiles_bytes(R, K):
+    n = ctypes.c_size_t(0)
+    st = load().fgq_ue8m0_scale_tiles_bytes(R, K, ctypes.byref(n))
+    return st, int(n.value)
+
+
+def fgq_quant_operands_ue8m0_tiles(x, M, K, ldx, xq, ldq, sA_tiles, w, N, ldw, wq, sB_tiles,
+                                   stream) -> int:
+    return load().fgq_quant_operands_ue8m0_tiles(x, M, K, ldx, xq, ldq, sA_tiles, w, N, ldw, wq,
+                                                 sB_tiles, stream)
+
+
+def fgq_ue8m0_scale_tiles_act(sA, M, K, tiles, stream) -> int:
+    return load().fgq_ue8m0_scale_tiles_act(sA, M, K, tiles, stream)
+
+
+def fgq_ue8m0_scale_tiles_weight(sB, K, N, tiles, stream) -> int:
+    return load().fgq_ue8m0_scale_tiles_weight(sB, K, N, tiles, stream)
+
+
+def fgq_gemm_fp8_ue8m0_tiled(A, sA, B, sB, C, ldc, M, N, K, out, stream) -> int:
+    return load().fgq_gemm_fp8_ue8m0_tiled(A, sA, B, sB, C, ldc, M, N, K, out, stream)
 
 
 def fgq_gemm_splitk_workspace_size(M, N, K):

@@ -383,6 +383,86 @@ fgq_status fgq_gemm_nvfp4_tiled(const uint8_t* A, const uint8_t* sA, const float
                                                static_cast<cudaStream_t>(stream), dev));
 }
 
+fgq_status fgq_quant_operands_ue8m0_tiles(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                          uint8_t* xq, int64_t ldq, uint8_t* sA_tiles,
+                                          const void* w, int64_t N, int64_t ldw, uint8_t* wq,
+                                          uint8_t* sB_tiles, void* stream) {
+  // the checks of fgq_quant_operands, with the code tiles in place of the
+  // fp32 scale arrays
+  if (M < 0 || K <= 0 || K % 128 != 0 || N <= 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (!w || !wq || !sB_tiles) return FGQ_ERR_INVALID_ARG;
+  if (ldw < N || ldw % 8 != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(wq, 16)) return FGQ_ERR_INVALID_ARG;
+  if ((K / 128) > kMaxGroups / (N / 128)) return FGQ_ERR_INVALID_ARG;
+  if (M > 0) {
+    if (!x || !xq || !sA_tiles) return FGQ_ERR_INVALID_ARG;
+    if (ldx < K || ldq < K || ldx % 8 != 0 || ldq % 16 != 0) return FGQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(xq, 16)) return FGQ_ERR_INVALID_ARG;
+    if (M > kMaxGroups / (K / 128)) return FGQ_ERR_INVALID_ARG;
+  }
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_quant_operands(x, M, K, ldx, xq, ldq,
+                                              reinterpret_cast<float*>(sA_tiles), w, N, ldw, wq,
+                                              reinterpret_cast<float*>(sB_tiles), FGQ_SCALE_UE8M0,
+                                              static_cast<cudaStream_t>(stream), dev, true));
+}
+
+fgq_status fgq_ue8m0_scale_tiles_bytes(int64_t R, int64_t K, size_t* bytes) {
+  if (!bytes || R < 0 || K <= 0 || K % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (R >= (int64_t{1} << 31) || K >= (int64_t{1} << 31)) return FGQ_ERR_INVALID_ARG;
+  *bytes = static_cast<size_t>((R + 127) / 128) * static_cast<size_t>((K / 128 + 3) / 4) * 512u;
+  return FGQ_OK;
+}
+
+fgq_status fgq_ue8m0_scale_tiles_act(const float* sA, int64_t M, int64_t K, uint8_t* tiles,
+                                     void* stream) {
+  if (M < 0 || K <= 0 || K % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (M >= (int64_t{1} << 31) || K >= (int64_t{1} << 31)) return FGQ_ERR_INVALID_ARG;
+  if (M == 0) return FGQ_OK;
+  if (!sA || !tiles || !aligned(sA, 4) || !aligned(tiles, 16)) return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_ue8m0_scale_tiles(sA, M, K, 0, false, tiles,
+                                                 static_cast<cudaStream_t>(stream), dev));
+}
+
+fgq_status fgq_ue8m0_scale_tiles_weight(const float* sB, int64_t K, int64_t N, uint8_t* tiles,
+                                        void* stream) {
+  if (K <= 0 || N <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (N >= (int64_t{1} << 31) || K >= (int64_t{1} << 31)) return FGQ_ERR_INVALID_ARG;
+  if (!sB || !tiles || !aligned(sB, 4) || !aligned(tiles, 16)) return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_ue8m0_scale_tiles(sB, N, K, N, true, tiles,
+                                                 static_cast<cudaStream_t>(stream), dev));
+}
+
+fgq_status fgq_gemm_fp8_ue8m0_tiled(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                                    const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
+                                    int64_t K, int out, void* stream) {
+  if (M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
+  if (out != FGQ_OUT_F32 && out != FGQ_OUT_BF16) return FGQ_ERR_INVALID_ARG;
+  if (M >= (int64_t{1} << 31) || N >= (int64_t{1} << 31) || K >= (int64_t{1} << 31))
+    return FGQ_ERR_INVALID_ARG;
+  if (M == 0) return FGQ_OK;
+  if (!A || !sA || !B || !sB || !C) return FGQ_ERR_INVALID_ARG;
+  const int64_t vec = (out == FGQ_OUT_F32) ? 4 : 8;
+  if (ldc < N || ldc % vec != 0) return FGQ_ERR_INVALID_ARG;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(sA, 16) ||
+      !aligned(sB, 16))
+    return FGQ_ERR_INVALID_ARG;
+  fgq::DeviceInfo dev;
+  fgq_status st = get_device(&dev);
+  if (st != FGQ_OK) return st;
+  return from_cuda(fgq::launch_gemm_mx8_tiled(A, sA, B, sB, C, ldc, M, N, K,
+                                              out == FGQ_OUT_BF16 ? 1 : 0,
+                                              static_cast<cudaStream_t>(stream), dev));
+}
+
 fgq_status fgq_gemm_splitk_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {
   if (!bytes || M < 0 || N <= 0 || K <= 0 || K % 128 != 0 || N % 128 != 0) return FGQ_ERR_INVALID_ARG;
   fgq::DeviceInfo dev;

@@ -50,10 +50,12 @@ cudaError_t launch_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t 
 
 // Both operands of a GEMM in one launch: X [M, K] 1x128 and W [K, N]
 // 128x128, the same codes and scales as the two launches above.
+// (code_tiles: UE8M0 mode with the scales written as the UE8M0 code tiles
+// of the tiled-scale FP8 GEMM, sx and sw then being the two tile buffers.)
 cudaError_t launch_quant_operands(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
                                   int64_t ldq, float* sx, const void* w, int64_t N, int64_t ldw,
                                   uint8_t* wq, float* sw, int mode, cudaStream_t stream,
-                                  const DeviceInfo& dev);
+                                  const DeviceInfo& dev, bool code_tiles = false);
 
 cudaError_t launch_gemm_fp8_blockscaled(const uint8_t* A, const float* sA, const uint8_t* B,
                                         const float* sB, void* C, int64_t ldc, int64_t M,
@@ -90,6 +92,17 @@ cudaError_t launch_gemm_nvf4_tiled(const uint8_t* A, const uint8_t* sA, const fl
                                    const uint8_t* B, const uint8_t* sB, const float* gb, void* C,
                                    int64_t ldc, int64_t M, int64_t N, int64_t K, int out_bf16,
                                    cudaStream_t stream, const DeviceInfo& dev);
+// FP8 GEMM with power-of-two scales given as UE8M0 code tiles (the tiled
+// FP4 scale layout with F = K/128 padded to a multiple of 4): activation
+// codes per row, weight codes per column of the transposed weight.
+cudaError_t launch_gemm_mx8_tiled(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                                  const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
+                                  int64_t K, int out_bf16, cudaStream_t stream,
+                                  const DeviceInfo& dev);
+// Those code tiles from fp32 power-of-two scales: activation sA [R, K/128]
+// (weight = false) or weight sB [K/128, N/128] for R = N rows (weight = true).
+cudaError_t launch_ue8m0_scale_tiles(const float* s, int64_t R, int64_t K, int64_t N, bool weight,
+                                     uint8_t* tiles, cudaStream_t stream, const DeviceInfo& dev);
 // Row-major FP4 block scales [R, F] (F % 4 == 0) into the tiled layout.
 cudaError_t launch_fp4_scales_to_tiles(const uint8_t* s, int64_t R, int64_t F, uint8_t* tiles,
                                        cudaStream_t stream, const DeviceInfo& dev);

@@ -375,6 +375,55 @@ cudaError_t launch_gemm_mx(const uint8_t* A, const float* sA, const uint8_t* B, 
               : launch_mx_cfg<128, 6, false>(A, sA, B, sB, C, ldc, m, n, k, stream, dev);
 }
 
+// ---- UE8M0 codes in the tiled scale layout ------------------------------------
+//
+// For the tiled-scale FP8 GEMM (gemm_mxf4.cu, kind MXF8): the codes of a
+// power-of-two scale matrix laid out as the FP4 scale tiles, F = K/128 codes
+// a row padded to a multiple of 4 (padding codes 0).  Activation scales
+// sA [M, K/128] give row m's codes; weight scales sB [K/128, N/128] give
+// column n of the transposed weight the codes of its blocks, sB[c, n/128].
+// One thread per output word (a cell: four codes of one row), consecutive
+// threads writing consecutive words of a tile.
+template <bool WEIGHT>
+__global__ void __launch_bounds__(256)
+    ue8m0_scale_tiles_kernel(const float* __restrict__ s, uint32_t R, uint32_t F, uint32_t cpr,
+                             uint32_t nb, uint32_t words, uint32_t* __restrict__ tiles) {
+  for (uint32_t w = blockIdx.x * 256u + threadIdx.x; w < words; w += gridDim.x * 256u) {
+    const uint32_t tile = w >> 7, in = w & 127u;
+    const uint32_t rt = tile / cpr, c = tile - rt * cpr;
+    const uint32_t r = rt * 128u + 32u * (in & 3u) + (in >> 2);
+    uint32_t cell = 0;
+    if (r < R) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t f = 4u * c + b;
+        if (f < F) {
+          const float v = WEIGHT ? __ldg(s + static_cast<uint64_t>(f) * nb + r / 128u)
+                                 : __ldg(s + static_cast<uint64_t>(r) * F + f);
+          cell |= ue8m0_code(v) << (8 * b);
+        }
+      }
+    }
+    tiles[w] = cell;
+  }
+}
+
+cudaError_t launch_ue8m0_scale_tiles(const float* s, int64_t R, int64_t K, int64_t N, bool weight,
+                                     uint8_t* tiles, cudaStream_t stream, const DeviceInfo& dev) {
+  const uint32_t F = static_cast<uint32_t>(K / 128), cpr = (F + 3) / 4;
+  const uint64_t words = static_cast<uint64_t>((R + 127) / 128) * cpr * 128u;
+  if (words == 0) return cudaSuccess;
+  uint64_t grid = (words + 255) / 256;
+  const uint64_t cap = static_cast<uint64_t>(dev.sm_count) * 8;
+  if (grid > cap) grid = cap;
+  auto k = weight ? ue8m0_scale_tiles_kernel<true> : ue8m0_scale_tiles_kernel<false>;
+  k<<<static_cast<unsigned>(grid), 256, 0, stream>>>(s, static_cast<uint32_t>(R), F, cpr,
+                                                      static_cast<uint32_t>(N / 128),
+                                                      static_cast<uint32_t>(words),
+                                                      reinterpret_cast<uint32_t*>(tiles));
+  return cudaGetLastError();
+}
+
 cudaError_t read_device_error_mx(uint32_t* word, bool clear) {
   return read_unit_device_error(word, clear);
 }

@@ -515,18 +515,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 // both epilogues hand the accumulator back on the leader's `acc_empty`
 // (the peer with a relaxed cluster arrive after tcgen05.wait::ld, when its
 // reads have completed).
-template <bool NV>
+// The three block-scaled kinds on tiled scales: MXFP4 (E2M1, UE8M0 per 32
+// elements), NVFP4 (E2M1, E4M3 per 16) and MXF8 (E4M3 operands, one UE8M0
+// code per 128-element chunk of a row of A and per 128 x 128 block of the
+// weight: the power-of-two scales of the FP8 GEMM, applied by
+// kind::mxf8f6f4.block_scale.scale_vec::1X).  A stage is 128 bytes of
+// every row: 256 elements of K for FP4, 128 for FP8.
+constexpr int kMx4 = 0, kNv4 = 1, kMx8 = 2;
+
+template <int KIND>
 struct Fp4TiledFmt {
-  static constexpr int kCells = NV ? 4 : 2;     // factor tiles per 128 rows per stage
-  static constexpr int kSlots = NV ? 5 : 10;    // TMEM factor slots, one per stage in flight
+  // factor tiles per 128 rows per stage (MXF8: one tile serves four stages,
+  // its bytes b = 0..3 the codes of chunks 4 g + b)
+  static constexpr int kCells = KIND == kNv4 ? 4 : KIND == kMx4 ? 2 : 1;
+  static constexpr int kSlots = KIND == kNv4 ? 5 : KIND == kMx4 ? 10 : 12;
   static constexpr uint32_t kSfaSlot = 4 * kCells, kSfbSlot = 8 * kCells;
   static constexpr uint32_t kSfaCol0 = 256;     // after the accumulators
   static constexpr uint32_t kSfbCol0 = kSfaCol0 + kSfaSlot * kSlots;
 };
 
-template <bool PAIR, int BN, bool NV>
+template <bool PAIR, int BN, int KIND>
 struct TiledCfg {
-  using F = Fp4TiledFmt<NV>;
+  using F = Fp4TiledFmt<KIND>;
   static constexpr int kNAcc = BN == 128 ? 2 : 1;
   static constexpr int kABytes = BM * BK;                    // this CTA's 128 rows of A
   static constexpr int kBRows = PAIR ? BN / 2 : BN;          // this CTA's rows of B
@@ -582,23 +592,39 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 
-template <bool PAIR, bool NV>
+__device__ __forceinline__ void umma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t sfa_tmem,
+                                               uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+template <bool PAIR, int KIND>
 __device__ __forceinline__ void fp4_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
                                         uint32_t sfa, uint32_t sfb, uint32_t acc) {
   if constexpr (PAIR) {
-    if constexpr (NV)
+    if constexpr (KIND == kNv4)
       umma_nvf4_pair(d, a, b, idesc, sfa, sfb, acc);
-    else
+    else if constexpr (KIND == kMx4)
       umma_mxf4_pair(d, a, b, idesc, sfa, sfb, acc);
-  } else {
-    if constexpr (NV)
-      umma_nvf4(d, a, b, idesc, sfa, sfb, acc);
     else
+      umma_mxf8_pair(d, a, b, idesc, sfa, sfb, acc);
+  } else {
+    if constexpr (KIND == kNv4)
+      umma_nvf4(d, a, b, idesc, sfa, sfb, acc);
+    else if constexpr (KIND == kMx4)
       umma_mxf4(d, a, b, idesc, sfa, sfb, acc);
+    else
+      umma_mxf8f6f4(d, a, b, idesc, sfa, sfb, acc);
   }
 }
 
-template <bool PAIR, int BN, bool OUT_BF16, bool NV>
+template <bool PAIR, int BN, bool OUT_BF16, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp4_tiled_kernel(const __grid_constant__ CUtensorMap tmap_a,
                           const __grid_constant__ CUtensorMap tmap_b,
@@ -606,8 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __grid_constant__ CUtensorMap tmap_sb,
                           const float* __restrict__ ga, const float* __restrict__ gb,
                           void* __restrict__ C, int64_t ldc, int M, int N, int K) {
-  using CF = TiledCfg<PAIR, BN, NV>;
-  using F = Fp4TiledFmt<NV>;
+  using CF = TiledCfg<PAIR, BN, KIND>;
+  using F = Fp4TiledFmt<KIND>;
+  constexpr bool NV = KIND == kNv4, FP8 = KIND == kMx8;
   constexpr int STAGES = CF::STAGES;
   constexpr int kSlots = F::kSlots;
   constexpr int kCells = F::kCells;
@@ -642,9 +669,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int total = m_units * (N / BN);
   const int first = static_cast<int>(blockIdx.x) / G;
   const int stride = static_cast<int>(gridDim.x) / G;
-  const int kstages = (K + 255) / 256;
-  const bool half_last = (K % 256) != 0;
-  const int cpr = K / (NV ? 64 : 128);  // factor tiles per 128 rows (one per 4 factor bytes)
+  // stages of 128 bytes a row (FP4: 256 elements, the last may be half)
+  const int kstages = FP8 ? K / 128 : (K + 255) / 256;
+  const bool half_last = !FP8 && (K % 256) != 0;
+  // factor tiles per 128 rows (one per 4 factor bytes; MXF8: one per four
+  // 128-element chunks, the last padded)
+  const int cpr = FP8 ? (K / 128 + 3) / 4 : K / (NV ? 64 : 128);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -700,7 +730,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (leader) mbar_arrive_expect_tx(&full[s], CF::kTxBytes);
           uint8_t* sf = sm_sf + s * CF::kSfBytes;
-          const int t0 = kc * kCells;  // first factor tile of this stage within a row tile
+          // first factor tile of this stage within a row tile
+          const int t0 = FP8 ? kc >> 2 : kc * kCells;
           if constexpr (PAIR) {
             const uint32_t bar = bar0 + s * 8;
             tma_load_2d_pair(sm_a + s * CF::kABytes, &tmap_a, bar, kc * BK, tm * BM);
@@ -734,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1 && leader) {
     // ---------------- MMA issuer (the leader of a pair) ----------------
     if (elect_one_sync()) {
-      constexpr uint32_t idesc0 = idesc_fp4(G * BM, BN, NV);
+      constexpr uint32_t idesc0 = FP8 ? idesc_mx_e4m3_ue8m0(G * BM, BN) : idesc_fp4(G * BM, BN, NV);
       constexpr uint32_t kId2 = (2u << 29) | (2u << 4);  // factor bytes 2-3 of A and B
       const uint64_t dA0 = smem_desc_k_sw128(smem_u32(sm_a));
       const uint32_t a_lo0 = static_cast<uint32_t>(dA0), dhi = static_cast<uint32_t>(dA0 >> 32);
@@ -783,26 +814,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           // has two.  MXFP4: factor bytes 0-1 and 2-3 of tile 0, then of
           // tile 1.  NVFP4: tile kk for MMA kk.
           const bool full_stage = kc + 1 < kstages || !half_last;
-          if constexpr (NV) {
-            fp4_mma<PAIR, NV>(d, make_desc(a_lo, dhi), make_desc(b_lo, dhi), idesc0, sfa, sfb,
+          if constexpr (FP8) {
+            // four K = 32 MMAs, all reading byte kc % 4 of the slot's cells
+            const uint32_t id = static_cast<uint32_t>(kc) & 3u;
+            const uint32_t idesc = idesc0 | (id << 29) | (id << 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              fp4_mma<PAIR, KIND>(d, make_desc(a_lo + 2 * kk, dhi), make_desc(b_lo + 2 * kk, dhi),
+                                  idesc, sfa, sfb, (kc > 0 || kk > 0) ? 1u : 0u);
+          } else if constexpr (NV) {
+            fp4_mma<PAIR, KIND>(d, make_desc(a_lo, dhi), make_desc(b_lo, dhi), idesc0, sfa, sfb,
                               kc > 0 ? 1u : 0u);
-            fp4_mma<PAIR, NV>(d, make_desc(a_lo + 2, dhi), make_desc(b_lo + 2, dhi), idesc0,
+            fp4_mma<PAIR, KIND>(d, make_desc(a_lo + 2, dhi), make_desc(b_lo + 2, dhi), idesc0,
                               sfa + 4, sfb + 8, 1u);
             if (full_stage) {
-              fp4_mma<PAIR, NV>(d, make_desc(a_lo + 4, dhi), make_desc(b_lo + 4, dhi), idesc0,
+              fp4_mma<PAIR, KIND>(d, make_desc(a_lo + 4, dhi), make_desc(b_lo + 4, dhi), idesc0,
                                 sfa + 8, sfb + 16, 1u);
-              fp4_mma<PAIR, NV>(d, make_desc(a_lo + 6, dhi), make_desc(b_lo + 6, dhi), idesc0,
+              fp4_mma<PAIR, KIND>(d, make_desc(a_lo + 6, dhi), make_desc(b_lo + 6, dhi), idesc0,
                                 sfa + 12, sfb + 24, 1u);
             }
           } else {
-            fp4_mma<PAIR, NV>(d, make_desc(a_lo, dhi), make_desc(b_lo, dhi), idesc0, sfa, sfb,
+            fp4_mma<PAIR, KIND>(d, make_desc(a_lo, dhi), make_desc(b_lo, dhi), idesc0, sfa, sfb,
                               kc > 0 ? 1u : 0u);
-            fp4_mma<PAIR, NV>(d, make_desc(a_lo + 2, dhi), make_desc(b_lo + 2, dhi),
+            fp4_mma<PAIR, KIND>(d, make_desc(a_lo + 2, dhi), make_desc(b_lo + 2, dhi),
                               idesc0 | kId2, sfa, sfb, 1u);
             if (full_stage) {
-              fp4_mma<PAIR, NV>(d, make_desc(a_lo + 4, dhi), make_desc(b_lo + 4, dhi), idesc0,
+              fp4_mma<PAIR, KIND>(d, make_desc(a_lo + 4, dhi), make_desc(b_lo + 4, dhi), idesc0,
                                 sfa + 4, sfb + 8, 1u);
-              fp4_mma<PAIR, NV>(d, make_desc(a_lo + 6, dhi), make_desc(b_lo + 6, dhi),
+              fp4_mma<PAIR, KIND>(d, make_desc(a_lo + 6, dhi), make_desc(b_lo + 6, dhi),
                                 idesc0 | kId2, sfa + 4, sfb + 8, 1u);
             }
           }
@@ -940,10 +979,10 @@ cudaError_t launch_mxf4_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* 
 // Tiled-scale kernel set-up, once per device and configuration: the shared
 // memory attribute, and for pairs the clusters of two that fit at once (0
 // when the pair kernel cannot run).
-template <bool PAIR, int BN, bool OUT_BF16, bool NV>
+template <bool PAIR, int BN, bool OUT_BF16, int KIND>
 cudaError_t tiled_setup(const DeviceInfo& dev, int* clusters) {
-  using CF = TiledCfg<PAIR, BN, NV>;
-  auto kern = gemm_fp4_tiled_kernel<PAIR, BN, OUT_BF16, NV>;
+  using CF = TiledCfg<PAIR, BN, KIND>;
+  auto kern = gemm_fp4_tiled_kernel<PAIR, BN, OUT_BF16, KIND>;
   static std::mutex mu;
   static int cached[64] = {};
   static bool ready[64] = {};
@@ -976,21 +1015,24 @@ cudaError_t tiled_setup(const DeviceInfo& dev, int* clusters) {
   return cudaSuccess;
 }
 
-template <bool PAIR, int BN, bool OUT_BF16, bool NV>
+template <bool PAIR, int BN, bool OUT_BF16, int KIND>
 cudaError_t launch_tiled_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
                              const uint8_t* sB, const float* ga, const float* gb, void* C,
                              int64_t ldc, int M, int N, int K, int clusters, cudaStream_t stream,
                              const DeviceInfo& dev) {
-  using CF = TiledCfg<PAIR, BN, NV>;
+  using CF = TiledCfg<PAIR, BN, KIND>;
   constexpr int G = PAIR ? 2 : 1;
+  constexpr bool FP8 = KIND == kMx8;
   CUtensorMap ta, tb, tsa, tsb;
   // operand rows of K/2 bytes (two E2M1 per byte); factor tiles: one per
   // 128 rows and 4 factor bytes, K/128 (MXFP4) or K/64 (NVFP4) per row tile
-  const int64_t cpr = K / (NV ? 64 : 128);
+  const int64_t cpr = FP8 ? (K / 128 + 3) / 4 : K / (KIND == kNv4 ? 64 : 128);
   const int64_t a_tiles = (M + BM - 1) / BM * cpr, b_tiles = N / 128 * cpr;
-  if (!make_k_major_map(&ta, A, M, K / 2, BM) || !make_k_major_map(&tb, B, N, K / 2, CF::kBRows) ||
-      !make_scale_tile_map(&tsa, sA, a_tiles, Fp4TiledFmt<NV>::kCells) ||
-      !make_scale_tile_map(&tsb, sB, b_tiles, Fp4TiledFmt<NV>::kCells))
+  const int64_t row_bytes = FP8 ? K : K / 2;
+  if (!make_k_major_map(&ta, A, M, row_bytes, BM) ||
+      !make_k_major_map(&tb, B, N, row_bytes, CF::kBRows) ||
+      !make_scale_tile_map(&tsa, sA, a_tiles, Fp4TiledFmt<KIND>::kCells) ||
+      !make_scale_tile_map(&tsb, sB, b_tiles, Fp4TiledFmt<KIND>::kCells))
     return cudaErrorInvalidValue;
   const int units = ((M + BM - 1) / BM + G - 1) / G * (N / BN);
   const int cap = PAIR ? clusters : dev.sm_count;
@@ -1012,14 +1054,14 @@ cudaError_t launch_tiled_cfg(const uint8_t* A, const uint8_t* sA, const uint8_t*
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemm_fp4_tiled_kernel<PAIR, BN, OUT_BF16, NV>, ta, tb, tsa, tsb,
+  return cudaLaunchKernelEx(&cfg, gemm_fp4_tiled_kernel<PAIR, BN, OUT_BF16, KIND>, ta, tb, tsa, tsb,
                             ga, gb, C, ldc, M, N, K);
 }
 
 // Configuration choice for tiled scales: CTA pairs once A has two row tiles,
 // on 256-column tiles when there is at least one per cluster, else
 // 128-column ones; a single CTA per 128 x 128 tile for one row tile.
-template <bool OUT_BF16, bool NV>
+template <bool OUT_BF16, int KIND>
 cudaError_t launch_fp4_tiled(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
                              const uint8_t* sB, const float* ga, const float* gb, void* C,
                              int64_t ldc, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
@@ -1029,22 +1071,22 @@ cudaError_t launch_fp4_tiled(const uint8_t* A, const uint8_t* sA, const uint8_t*
   const int64_t m_tiles = (M + BM - 1) / BM;
   if (m_tiles >= 2) {
     int c256 = 0, c128 = 0;
-    cudaError_t e = tiled_setup<true, 256, OUT_BF16, NV>(dev, &c256);
+    cudaError_t e = tiled_setup<true, 256, OUT_BF16, KIND>(dev, &c256);
     if (e != cudaSuccess) return e;
-    e = tiled_setup<true, 128, OUT_BF16, NV>(dev, &c128);
+    e = tiled_setup<true, 128, OUT_BF16, KIND>(dev, &c128);
     if (e != cudaSuccess) return e;
     const int64_t groups = (m_tiles + 1) / 2;
     if (N % 256 == 0 && c256 > 0 && groups * (N / 256) >= c256)
-      return launch_tiled_cfg<true, 256, OUT_BF16, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, c256,
+      return launch_tiled_cfg<true, 256, OUT_BF16, KIND>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, c256,
                                                        stream, dev);
     if (c128 > 0)
-      return launch_tiled_cfg<true, 128, OUT_BF16, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, c128,
+      return launch_tiled_cfg<true, 128, OUT_BF16, KIND>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, c128,
                                                        stream, dev);
   }
   int one = 0;
-  const cudaError_t e = tiled_setup<false, 128, OUT_BF16, NV>(dev, &one);
+  const cudaError_t e = tiled_setup<false, 128, OUT_BF16, KIND>(dev, &one);
   if (e != cudaSuccess) return e;
-  return launch_tiled_cfg<false, 128, OUT_BF16, NV>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, 0, stream,
+  return launch_tiled_cfg<false, 128, OUT_BF16, KIND>(A, sA, B, sB, ga, gb, C, ldc, m, n, k, 0, stream,
                                                     dev);
 }
 
@@ -1088,18 +1130,28 @@ cudaError_t launch_gemm_mxf4_tiled(const uint8_t* A, const uint8_t* sA, const ui
                                    const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
                                    int64_t K, int out_bf16, cudaStream_t stream,
                                    const DeviceInfo& dev) {
-  return out_bf16 ? launch_fp4_tiled<true, false>(A, sA, B, sB, nullptr, nullptr, C, ldc, M, N, K,
-                                                  stream, dev)
-                  : launch_fp4_tiled<false, false>(A, sA, B, sB, nullptr, nullptr, C, ldc, M, N, K,
-                                                   stream, dev);
+  return out_bf16 ? launch_fp4_tiled<true, kMx4>(A, sA, B, sB, nullptr, nullptr, C, ldc, M, N, K,
+                                                 stream, dev)
+                  : launch_fp4_tiled<false, kMx4>(A, sA, B, sB, nullptr, nullptr, C, ldc, M, N, K,
+                                                  stream, dev);
 }
 
 cudaError_t launch_gemm_nvf4_tiled(const uint8_t* A, const uint8_t* sA, const float* ga,
                                    const uint8_t* B, const uint8_t* sB, const float* gb, void* C,
                                    int64_t ldc, int64_t M, int64_t N, int64_t K, int out_bf16,
                                    cudaStream_t stream, const DeviceInfo& dev) {
-  return out_bf16 ? launch_fp4_tiled<true, true>(A, sA, B, sB, ga, gb, C, ldc, M, N, K, stream, dev)
-                  : launch_fp4_tiled<false, true>(A, sA, B, sB, ga, gb, C, ldc, M, N, K, stream, dev);
+  return out_bf16 ? launch_fp4_tiled<true, kNv4>(A, sA, B, sB, ga, gb, C, ldc, M, N, K, stream, dev)
+                  : launch_fp4_tiled<false, kNv4>(A, sA, B, sB, ga, gb, C, ldc, M, N, K, stream, dev);
+}
+
+cudaError_t launch_gemm_mx8_tiled(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                                  const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
+                                  int64_t K, int out_bf16, cudaStream_t stream,
+                                  const DeviceInfo& dev) {
+  return out_bf16 ? launch_fp4_tiled<true, kMx8>(A, sA, B, sB, nullptr, nullptr, C, ldc, M, N, K,
+                                                 stream, dev)
+                  : launch_fp4_tiled<false, kMx8>(A, sA, B, sB, nullptr, nullptr, C, ldc, M, N, K,
+                                                  stream, dev);
 }
 
 cudaError_t read_device_error_mxf4(uint32_t* word, bool clear) {

@@ -48,7 +48,20 @@ constexpr int kActRounds = 2;
 constexpr int kActGroupsPerWarp = 4 * kActRounds;
 
 // The groups of warp `warp` out of `nwarps` warps sharing the work.
-template <int MODE, bool DENSE>
+// UE8M0 code of a power-of-two scale (its biased exponent field) at its
+// place in the code tiles of the tiled-scale FP8 GEMM: row r, chunk c of
+// F = kc chunks a row, cells of four chunks (F padded to a multiple of 4),
+// 512-byte tiles of 128 rows: byte ((r / 128) * cpr + c / 4) * 512 +
+// (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4, cpr = ceil(kc / 4).
+__device__ __forceinline__ void store_code_tile(uint8_t* tiles, uint32_t r, uint32_t c,
+                                                uint32_t cpr, float s) {
+  tiles[(static_cast<uint64_t>(r >> 7) * cpr + (c >> 2)) * 512u + (r & 31u) * 16u +
+        ((r >> 5) & 3u) * 4u + (c & 3u)] = static_cast<uint8_t>((__float_as_uint(s) >> 23) & 0xFFu);
+}
+
+// TILES (UE8M0 only): the scales go out as code tiles (sx is then the tile
+// buffer, as bytes) instead of fp32 [M, K/128].
+template <int MODE, bool DENSE, bool TILES = false>
 __device__ __forceinline__ void act_groups(const uint16_t* __restrict__ x, uint32_t kc,
                                            uint32_t groups, int64_t ldx, uint8_t* __restrict__ xq,
                                            int64_t ldq, float* __restrict__ sx, uint32_t warp,
@@ -94,7 +107,14 @@ __device__ __forceinline__ void act_groups(const uint16_t* __restrict__ x, uint3
         }
         st_stream_8(dst + 8 * l8, q0);
         st_stream_8(dst + 64 + 8 * l8, q1);
-        if (l8 == 0) sx[g[u]] = gs.s;
+        if (l8 == 0) {
+          if (TILES) {
+            const uint32_t m = g[u] / kc;
+            store_code_tile(reinterpret_cast<uint8_t*>(sx), m, g[u] - m * kc, (kc + 3) / 4, gs.s);
+          } else {
+            sx[g[u]] = gs.s;
+          }
+        }
       }
     }
   }
@@ -141,7 +161,7 @@ __device__ __forceinline__ void transpose4x4_bytes(uint32_t r0, uint32_t r1, uin
 // the four that 55 registers allow, despite a few bytes of spill in the
 // fp32-scale instantiation; six spill heavily and are slower.
 // Block `block` of W (k-block major), by the CTA's kWThreads threads.
-template <int MODE>
+template <int MODE, bool TILES = false>
 __device__ __forceinline__ void w_block(const uint16_t* __restrict__ w, int64_t K, int64_t N,
                                         int64_t ldw, uint8_t* __restrict__ wq,
                                         float* __restrict__ sw, uint32_t block) {
@@ -190,7 +210,15 @@ __device__ __forceinline__ void w_block(const uint16_t* __restrict__ w, int64_t 
     const int n = 8 * c + j;
     tile[n * 16 + (rg ^ c)] = make_uint2(lo[j], hi[j]);
   }
-  if (t == 0) sw[static_cast<int64_t>(kb) * nb_count + nb] = gs.s;
+  if (TILES) {
+    // the block's code for each of its 128 columns (rows of the transposed
+    // weight's code tiles)
+    if (t < 128)
+      store_code_tile(reinterpret_cast<uint8_t*>(sw), static_cast<uint32_t>(n0) + t,
+                      static_cast<uint32_t>(kb), static_cast<uint32_t>((K / 128 + 3) / 4), gs.s);
+  } else if (t == 0) {
+    sw[static_cast<int64_t>(kb) * nb_count + nb] = gs.s;
+  }
   __syncthreads();
 
   const uint4* tile16 = reinterpret_cast<const uint4*>(tile);
@@ -220,7 +248,7 @@ __global__ void __launch_bounds__(kWThreads, 5)
 // two kernels; one launch saves the second kernel's fill and drain.
 // (Four CTAs per SM: at five, the activation half spills.)
 static_assert(kActThreads == kWThreads, "one block size for both halves");
-template <int MODE, bool DENSE>
+template <int MODE, bool DENSE, bool TILES = false>
 __global__ void __launch_bounds__(kWThreads, 4)
     quant_operands_kernel(const uint16_t* __restrict__ x, uint32_t kc, uint32_t groups,
                           int64_t ldx, uint8_t* __restrict__ xq, int64_t ldq,
@@ -228,11 +256,11 @@ __global__ void __launch_bounds__(kWThreads, 4)
                           int64_t N, int64_t ldw, uint8_t* __restrict__ wq,
                           float* __restrict__ sw, uint32_t w_blocks) {
   if (blockIdx.x < w_blocks) {
-    w_block<MODE>(w, K, N, ldw, wq, sw, blockIdx.x);
+    w_block<MODE, TILES>(w, K, N, ldw, wq, sw, blockIdx.x);
     return;
   }
   const uint32_t act_ctas = gridDim.x - w_blocks;
-  act_groups<MODE, DENSE>(x, kc, groups, ldx, xq, ldq, sx,
+  act_groups<MODE, DENSE, TILES>(x, kc, groups, ldx, xq, ldq, sx,
                           ((blockIdx.x - w_blocks) * kActThreads + threadIdx.x) >> 5,
                           act_ctas * (kActThreads / 32));
 }
@@ -601,7 +629,7 @@ cudaError_t launch_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t 
 cudaError_t launch_quant_operands(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
                                   int64_t ldq, float* sx, const void* w, int64_t N, int64_t ldw,
                                   uint8_t* wq, float* sw, int mode, cudaStream_t stream,
-                                  const DeviceInfo& dev) {
+                                  const DeviceInfo& dev, bool code_tiles) {
   (void)dev;
   const uint32_t kc = static_cast<uint32_t>(K / 128);
   const uint32_t groups = static_cast<uint32_t>(M * (K / 128));
@@ -618,7 +646,10 @@ cudaError_t launch_quant_operands(const void* x, int64_t M, int64_t K, int64_t l
   using Kern = void (*)(const uint16_t*, uint32_t, uint32_t, int64_t, uint8_t*, int64_t, float*,
                         const uint16_t*, int64_t, int64_t, int64_t, uint8_t*, float*, uint32_t);
   Kern k;
-  if (mode == kScaleFp32)
+  if (code_tiles)
+    k = dense ? quant_operands_kernel<kScaleUe8m0, true, true>
+              : quant_operands_kernel<kScaleUe8m0, false, true>;
+  else if (mode == kScaleFp32)
     k = dense ? quant_operands_kernel<kScaleFp32, true> : quant_operands_kernel<kScaleFp32, false>;
   else
     k = dense ? quant_operands_kernel<kScaleUe8m0, true> : quant_operands_kernel<kScaleUe8m0, false>;

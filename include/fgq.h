@@ -384,6 +384,49 @@ fgq_status fgq_gemm_nvfp4_tiled(const uint8_t* A, const uint8_t* sA, const float
                                 int64_t ldc, int64_t M, int64_t N, int64_t K, int out,
                                 void* stream);
 
+/*
+ * FP8 GEMM with power-of-two scales given as UE8M0 code tiles
+ * (§Blackwell: Native Block Scaling: UE8M0 = 2^(e-127); §UE8M0 vs E4M3
+ * Scale Formats).  The product is fgq_gemm_fp8_blockscaled_ex's in
+ * FGQ_SCALE_UE8M0 mode; only the scales' storage differs.  Codes are the
+ * biased exponent fields of the fp32 power-of-two scales, laid out like the
+ * FP4 scale tiles (fgq_fp4_scales_to_tiles) with F = K/128 codes a row
+ * padded to a multiple of 4: byte ((r/128)*(F4/4) + f/4)*512 + (r%32)*16 +
+ * ((r%128)/32)*4 + f%4, F4 = 4*ceil(F/4), of ceil(R/128)*128*F4 bytes.
+ *   activation tiles: row m's codes are those of sA[m, 0..K/128);
+ *   weight tiles: row n (a column of W, a row of the transposed codes
+ *   [N, K]) holds the codes of sB[c, n/128], c = 0..K/128.
+ * The tensor-map engine loads the tiles with the operands, and once A has
+ * two 128-row tiles pairs of CTAs share each 256-row tile (each loading
+ * half of the weight tile).
+ *
+ * fgq_ue8m0_scale_tiles_bytes: that size for R rows (M or N).
+ * fgq_ue8m0_scale_tiles_act: sA fp32 [M, K/128] (powers of two, 4-byte
+ *   aligned) -> tiles (16-byte aligned).  Device buffers, async on stream.
+ * fgq_ue8m0_scale_tiles_weight: sB fp32 [K/128, N/128] -> tiles for N rows.
+ * fgq_gemm_fp8_ue8m0_tiled: A E4M3 [M, K] (row-major, dense), B E4M3 [N, K]
+ *   (the K-major weight codes of fgq_quant_w_128x128), sA and sB the
+ *   activation and weight code tiles (16-byte aligned), C as _ex.
+ *   K % 128 == 0, N % 128 == 0, M >= 0.
+ */
+fgq_status fgq_ue8m0_scale_tiles_bytes(int64_t R, int64_t K, size_t* bytes);
+/* fgq_quant_operands in FGQ_SCALE_UE8M0 mode with the scales written
+ * straight into the two code tiles (sA_tiles for the M rows of A, sB_tiles
+ * for the N columns of W; fgq_ue8m0_scale_tiles_bytes each; padding
+ * untouched) instead of fp32 arrays: the same codes as the fp32 scales'
+ * exponent fields.  Arguments and limits otherwise as fgq_quant_operands. */
+fgq_status fgq_quant_operands_ue8m0_tiles(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                          uint8_t* xq, int64_t ldq, uint8_t* sA_tiles,
+                                          const void* w, int64_t N, int64_t ldw, uint8_t* wq,
+                                          uint8_t* sB_tiles, void* stream);
+fgq_status fgq_ue8m0_scale_tiles_act(const float* sA, int64_t M, int64_t K, uint8_t* tiles,
+                                     void* stream);
+fgq_status fgq_ue8m0_scale_tiles_weight(const float* sB, int64_t K, int64_t N, uint8_t* tiles,
+                                        void* stream);
+fgq_status fgq_gemm_fp8_ue8m0_tiled(const uint8_t* A, const uint8_t* sA, const uint8_t* B,
+                                    const uint8_t* sB, void* C, int64_t ldc, int64_t M, int64_t N,
+                                    int64_t K, int out, void* stream);
+
 /* Workspace bytes fgq_gemm_fp8_blockscaled_splitk needs for (M, N, K) on the
  * current device (depends on its SM count; 256 when the problem has no
  * partial tiles).  Same size checks as the GEMM. */

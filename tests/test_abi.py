@@ -295,3 +295,30 @@ def test_fp4_tiled_empty_is_ok(fgq):
     assert _lib.fgq_gemm_nvfp4_tiled(0, 0, 0, 0, 0, 0, 0, 256, 0, 256, 256, 0, None) == _lib.FGQ_OK
     assert _lib.fgq_quant_mxfp4_1x32_tiled(0, 0, 128, 128, 0, 0, None) == _lib.FGQ_OK
     assert _lib.fgq_quant_nvfp4_1x16_tiled(0, 0, 64, 64, 0, 0, 0, None) == _lib.FGQ_OK
+
+
+def test_ue8m0_scale_tiles_calls(fgq):
+    assert _lib.fgq_ue8m0_scale_tiles_bytes(130, 640) == (_lib.FGQ_OK, 2 * 2 * 512)
+    assert _lib.fgq_ue8m0_scale_tiles_bytes(128, 7168) == (_lib.FGQ_OK, 14 * 512)
+    assert _lib.fgq_ue8m0_scale_tiles_bytes(4, 100)[0] == _lib.FGQ_ERR_INVALID_ARG
+    assert _lib.fgq_ue8m0_scale_tiles_act(P, 4, 100, P, None) == _lib.FGQ_ERR_INVALID_ARG
+    assert _lib.fgq_ue8m0_scale_tiles_act(P, 4, 128, P + 4, None) == _lib.FGQ_ERR_INVALID_ARG
+    assert _lib.fgq_ue8m0_scale_tiles_act(0, 0, 128, 0, None) == _lib.FGQ_OK
+    assert _lib.fgq_ue8m0_scale_tiles_weight(P, 128, 96, P, None) == _lib.FGQ_ERR_INVALID_ARG
+    assert _lib.fgq_ue8m0_scale_tiles_weight(0, 128, 128, P, None) == _lib.FGQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args", [
+    (0, P, P, P, P, 256, 128, 256, 256, 0, None),      # null A
+    (P, P, P, P, P, 256, 128, 256, 192, 0, None),      # K % 128
+    (P, P, P, P, P, 256, 128, 192, 256, 0, None),      # N % 128
+    (P, P + 4, P, P, P, 256, 128, 256, 256, 0, None),  # sA not 16-byte aligned
+    (P, P, P, P, P, 200, 128, 256, 256, 0, None),      # ldc < N
+    (P, P, P, P, P, 256, 128, 256, 256, 7, None),      # bad out dtype
+])
+def test_gemm_fp8_ue8m0_tiled_rejects(fgq, args):
+    assert _lib.fgq_gemm_fp8_ue8m0_tiled(*args) == _lib.FGQ_ERR_INVALID_ARG
+
+
+def test_gemm_fp8_ue8m0_tiled_empty_is_ok(fgq):
+    assert _lib.fgq_gemm_fp8_ue8m0_tiled(0, 0, 0, 0, 0, 256, 0, 256, 256, 0, None) == _lib.FGQ_OK

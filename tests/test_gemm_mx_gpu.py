@@ -137,3 +137,132 @@ def test_ue8m0_repeat_calls_are_identical(fgq, cuda_dev):
 
 def test_no_device_error_after_ue8m0(fgq, cuda_dev):
     assert fgq.device_error() == 0
+
+
+# ---- UE8M0 code tiles (fgq_gemm_fp8_ue8m0_tiled) ---------------------------------
+
+def _code_tiles(codes):
+    """UE8M0 codes [R, F] in the tiled layout: the FP4 scale tiles of the
+    oracle with F padded to a multiple of 4 (padding codes 0)."""
+    R, F = codes.shape
+    F4 = -(-F // 4) * 4
+    pad = np.zeros((R, F4), dtype=np.uint8)
+    pad[:, :F] = codes
+    return oracle.fp4_scale_tiles(pad)
+
+
+def _codes(s):
+    return np.vectorize(oracle.ue8m0_code, otypes=[np.uint8])(s.astype(np.float64))
+
+
+def _host_tiles(host):
+    """Activation code tiles (row m: codes of sA[m, :]) and weight code tiles
+    (row n: codes of sB[:, n / 128]) from the oracle's scales."""
+    aq, sa, bq, sb = host
+    N = bq.shape[1]
+    ta = _code_tiles(_codes(sa))
+    tb = _code_tiles(_codes(np.repeat(sb, 128, axis=1)[:, :N].T))
+    return ta, tb
+
+
+def _defined(R, K):
+    F = K // 128
+    F4 = -(-F // 4) * 4
+    m = np.zeros((R, F4), dtype=np.uint8)
+    m[:, :F] = 1
+    return oracle.fp4_scale_tiles(m) == 1
+
+
+@pytest.mark.parametrize("M,N,K", [(33, 384, 640), (300, 1024, 1536), (4096, 512, 7168)])
+def test_ue8m0_scale_tiles_match_oracle(fgq, cuda_dev, M, N, K):
+    a = fgq_inputs.exponent_spread((M, K), 20, 1, seed=M + 3)
+    b = fgq_inputs.exponent_spread((K, N), 20, 128, seed=M + 4)
+    host = _quant(a, b)
+    ta, tb = _host_tiles(host)
+    ga = fgq.ue8m0_scale_tiles(torch.from_numpy(host[1]).to(cuda_dev), weight=False)
+    gb = fgq.ue8m0_scale_tiles(torch.from_numpy(host[3]).to(cuda_dev), weight=True)
+    torch.cuda.synchronize()
+    ma, mb = _defined(M, K), _defined(N, K)
+    assert np.array_equal(ga.cpu().numpy()[ma], ta[ma])
+    assert np.array_equal(gb.cpu().numpy()[mb], tb[mb])
+
+
+# one row tile (single CTAs), pairs on 128- and 256-column tiles, a ragged
+# and an odd number of row tiles, K/128 not a multiple of 4 (padded code
+# cells), one chunk
+TILED_SHAPES = [(33, 384, 640), (128, 256, 128), (300, 640, 1152), (1000, 512, 1024),
+                (1100, 5120, 1536), (1280, 4096, 640), (2560, 2048, 2304)]
+
+
+@pytest.mark.parametrize("M,N,K", TILED_SHAPES)
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_ue8m0_tiled_gemm(fgq, cuda_dev, M, N, K, out_dtype):
+    """The code-tile GEMM against the oracle (sampled outputs plus the first
+    and last 256 x 256 blocks whole), and bit for bit against the UE8M0
+    path of fgq_gemm_fp8_blockscaled_ex on the same operands."""
+    a = fgq_inputs.exponent_spread((M, K), 12, 1, seed=M + K)
+    b = fgq_inputs.exponent_spread((K, N), 12, 128, seed=M + K + 1)
+    host = _quant(a, b)
+    ta, tb = _host_tiles(host)
+    ops = _dev(*host, cuda_dev)
+    c = fgq.gemm_fp8_ue8m0_tiled(ops[0], torch.from_numpy(ta).to(cuda_dev), ops[2],
+                                 torch.from_numpy(tb).to(cuda_dev), out_dtype=out_dtype)
+    c_ex = fgq.gemm_fp8_blockscaled(*ops, out_dtype=out_dtype, mode="ue8m0")
+    torch.cuda.synchronize()
+    m_last = ((M - 1) // 256) * 256
+    blocks = [(r, q) for r0, q0 in ((0, 0), (m_last, max(N - 256, 0)))
+              for r in range(r0, min(r0 + 256, M)) for q in range(q0, min(q0 + 256, N))]
+    rng = np.random.default_rng(K)
+    rows = np.concatenate([np.array([x[0] for x in blocks]), rng.integers(0, M, 2000)])
+    cols = np.concatenate([np.array([x[1] for x in blocks]), rng.integers(0, N, 2000)])
+    _check(c, host, rows, cols)
+    assert torch.equal(c, c_ex)
+    assert fgq.device_error() == 0
+
+
+def test_ue8m0_tiled_large_prefill_from_the_gpu(fgq, cuda_dev):
+    """4096 x 7168 x 7168, bf16 out, as the benchmark runs it: both operands
+    quantized in one launch (UE8M0), code tiles made on the GPU, then the
+    tiled GEMM; bit for bit the _ex UE8M0 result, and sampled outputs
+    against the oracle."""
+    M, N, K = 4096, 7168, 7168
+    a, w = fgq_inputs.large_prefill(seed=0)
+    xq, sx, wq, sw = fgq.quant_operands(a.to(cuda_dev), w.to(cuda_dev), "ue8m0")
+    ta = fgq.ue8m0_scale_tiles(sx, weight=False)
+    tb = fgq.ue8m0_scale_tiles(sw, weight=True)
+    c = fgq.gemm_fp8_ue8m0_tiled(xq, ta, wq, tb, out_dtype=torch.bfloat16)
+    c_ex = fgq.gemm_fp8_blockscaled(xq, sx, wq, sw, out_dtype=torch.bfloat16, mode="ue8m0")
+    torch.cuda.synchronize()
+    assert torch.equal(c, c_ex)
+    host = (xq.cpu().numpy(), sx.cpu().numpy(), np.ascontiguousarray(wq.cpu().numpy().T),
+            sw.cpu().numpy())
+    rng = np.random.default_rng(2)
+    rows = np.concatenate([rng.integers(0, M, 3000), [0, M - 1]])
+    cols = np.concatenate([rng.integers(0, N, 3000), [N - 1, 0]])
+    _check(c, host, rows, cols)
+    assert fgq.device_error() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 1024, 1536), (33, 384, 640), (4096, 7168, 7168)])
+def test_quant_operands_ue8m0_tiles(fgq, cuda_dev, M, N, K):
+    """The one-launch quantizer writing code tiles: codes as quant_operands
+    in UE8M0 mode, scale codes bit for bit the oracle's in the tiled layout;
+    and the tiled GEMM on them gives _ex's bits."""
+    a, w = fgq_inputs.large_prefill(seed=5, m=M, k=K, n=N)
+    xq, ta, wq, tb = fgq.quant_operands_ue8m0_tiles(a.to(cuda_dev), w.to(cuda_dev))
+    xq2, sx, wq2, sw = fgq.quant_operands(a.to(cuda_dev), w.to(cuda_dev), "ue8m0")
+    torch.cuda.synchronize()
+    assert torch.equal(xq, xq2) and torch.equal(wq, wq2)
+    host = (xq2.cpu().numpy(), sx.cpu().numpy(), np.ascontiguousarray(wq2.cpu().numpy().T),
+            sw.cpu().numpy())
+    oa, ow = oracle.quant_act_1x128(a, UE8M0), oracle.quant_w_128x128(w, UE8M0)
+    assert np.array_equal(host[1], oa[1]) and np.array_equal(host[3], ow[1])
+    ea, eb = _host_tiles(host)
+    ma, mb = _defined(M, K), _defined(N, K)
+    assert np.array_equal(ta.cpu().numpy()[ma], ea[ma])
+    assert np.array_equal(tb.cpu().numpy()[mb], eb[mb])
+    c = fgq.gemm_fp8_ue8m0_tiled(xq, ta, wq, tb, out_dtype=torch.bfloat16)
+    c_ex = fgq.gemm_fp8_blockscaled(xq2, sx, wq2, sw, out_dtype=torch.bfloat16, mode="ue8m0")
+    torch.cuda.synchronize()
+    assert torch.equal(c, c_ex)
+    assert fgq.device_error() == 0
