@@ -12,17 +12,20 @@
 //            saturating at 6; a block whose D is 0 gets signed zeros.
 // Every quotient is, or encodes exactly as, the IEEE fp32 quotient.
 //
-// Element quotients without a division: y = RN(x * RN(1/D)) has a relative
-// error below 2^-23 + 2^-48, so it lies within 3 ulps of RN(x/D) (2 from
-// the two roundings, 1/2 for RN(x/D) itself).  The bracket
-// [RN(y (1 - 2^-20)), RN(y (1 + 2^-20))] reaches at least 7.5 ulps on each
-// side of y, so it holds RN(x/D); E2M1 rounding is monotone, so when its
-// two ends encode alike every value in it does, RN(x/D) included, and the
-// code of y is the code of RN(x/D).  Otherwise (about 1 in 10^4 elements
-// on ordinary data, every exact boundary value included) the lane's eight
-// elements are recomputed with __fdiv_rn, as are blocks with a subnormal D.
-// A host test replays this over every bf16 x against divisors that put
-// quotients on and beside the E2M1 rounding boundaries.
+// Element quotients without a division: y = RN(x * r), r the hardware
+// reciprocal approximation of D (at most 1 ulp from 1/D for 2^-126 <= D <=
+// 2^125), has a relative error below 2^-22, so it lies within 4 ulps of
+// RN(x/D).  The bracket [RN(y (1 - 2^-20)), RN(y (1 + 2^-20))] reaches at
+// least 7.5 ulps on each side of y, so it holds RN(x/D); E2M1 rounding is
+// monotone, so when its two ends encode alike every value in it does,
+// RN(x/D) included, and the code of y is the code of RN(x/D).  Otherwise
+// (about 1 in 10^4 elements on ordinary data, every exact boundary value
+// included) the lane's eight elements are recomputed with __fdiv_rn, as
+// are blocks with D outside that range.  The block scale E4M3(RN(amax /
+// d6)) takes the same route with t = RN(amax * RN(1/d6)).  A host test
+// replays both over every bf16 x (amax) against divisors that put
+// quotients on and beside the rounding boundaries, for every reciprocal
+// within 1 ulp of the true one.
 //
 // Two entry points: the global scale (a max reduction of |x| with one
 // atomic per warp into the output word, then one thread turns it into g in
@@ -42,22 +45,37 @@ constexpr int kAmaxThreads = 256;
 
 // Max of the bf16 magnitude bits (non-negative bf16 patterns order like
 // their values) over 16-byte chunks of the rows; one atomicMax per warp.
+// Each thread has kAmaxLoads independent 16-byte loads in flight per round.
+constexpr int kAmaxLoads = 4;
+
+template <bool DENSE>
+__device__ __forceinline__ const uint16_t* amax_chunk(const uint16_t* x, uint64_t i,
+                                                      uint64_t chunks_per_row, int64_t ldx) {
+  if (DENSE) return x + i * 8;
+  const uint64_t r = i / chunks_per_row, c = i - r * chunks_per_row;
+  return x + static_cast<int64_t>(r) * ldx + c * 8;
+}
+
 template <bool DENSE>
 __global__ void __launch_bounds__(kAmaxThreads)
     nvfp4_amax_kernel(const uint16_t* __restrict__ x, uint64_t chunks_per_row, uint64_t chunks,
                       int64_t ldx, unsigned int* __restrict__ out) {
   uint32_t m = 0;
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kAmaxThreads;
-  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kAmaxThreads + threadIdx.x; i < chunks;
-       i += stride) {
-    const uint16_t* src;
-    if (DENSE) {
-      src = x + i * 8;
-    } else {
-      const uint64_t r = i / chunks_per_row, c = i - r * chunks_per_row;
-      src = x + static_cast<int64_t>(r) * ldx + c * 8;
+  uint64_t i = static_cast<uint64_t>(blockIdx.x) * kAmaxThreads + threadIdx.x;
+  for (; i + (kAmaxLoads - 1) * stride < chunks; i += kAmaxLoads * stride) {
+    uint4 v[kAmaxLoads];
+#pragma unroll
+    for (int u = 0; u < kAmaxLoads; ++u)
+      v[u] = ld_stream_16(amax_chunk<DENSE>(x, i + u * stride, chunks_per_row, ldx));
+#pragma unroll
+    for (int u = 0; u < kAmaxLoads; ++u) {
+      const uint32_t p = absmax_pairs(v[u]);
+      m = max(m, max(p & 0xFFFFu, p >> 16));
     }
-    const uint32_t p = absmax_pairs(ld_stream_16(src));
+  }
+  for (; i < chunks; i += stride) {
+    const uint32_t p = absmax_pairs(ld_stream_16(amax_chunk<DENSE>(x, i, chunks_per_row, ldx)));
     m = max(m, max(p & 0xFFFFu, p >> 16));
   }
   m = __reduce_max_sync(0xFFFFFFFFu, m);
@@ -78,11 +96,40 @@ __device__ __forceinline__ uint32_t e4m3_code(float t) {
   return h & 0xFFu;
 }
 
-// Value of a non-negative E4M3 code (0 .. 0x7E): m 2^-9 for exponent field
-// 0, else (1 + m/8) 2^(e - 7).
+// Value of a non-negative E4M3 code (0 .. 0x7E), through the exact
+// E4M3 -> f16 conversion (every E4M3 value is an f16 value).
 __device__ __forceinline__ float e4m3_value(uint32_t c) {
-  const uint32_t e = c >> 3, m = c & 7u;
-  return e == 0 ? static_cast<float>(m) * 0x1p-9f : __uint_as_float(((e + 120u) << 23) | (m << 20));
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(c)));
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(static_cast<uint16_t>(h2 & 0xFFFFu)));
+  return f;
+}
+
+// E4M3 codes of two non-negative floats (lo in byte 0, hi in byte 1).
+__device__ __forceinline__ uint32_t e4m3_code2(float lo, float hi) {
+  uint16_t h;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(hi), "f"(lo));
+  return h;
+}
+
+// The hardware reciprocal approximation (at most 1 ulp from 1/d for normal
+// d and 1/d; subnormal results flush to zero).
+__device__ __forceinline__ float rcp_approx(float d) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+  return r;
+}
+
+// Block scale E4M3(RN(amax / d6)): from t = RN(amax * r6) (r6 = RN(1/d6))
+// when the codes of t (1 -+ 2^-20) agree, else from the IEEE quotient.
+__device__ __forceinline__ uint32_t nv_scale_code(float amax, float d6, float r6, bool fast) {
+  if (fast) {
+    const float t = amax * r6;
+    const uint32_t c2 = e4m3_code2(t * (1.0f - 0x1p-20f), t * (1.0f + 0x1p-20f));
+    if ((c2 & 0xFFu) == (c2 >> 8)) return c2 & 0xFFu;
+  }
+  return e4m3_code(__fdiv_rn(amax, d6));
 }
 
 // One block of 16 per two lanes (8 elements, 16 bytes each), 16 blocks per
@@ -93,11 +140,12 @@ constexpr int kNvRounds = 2;
 // One block of 16 elements over two lanes (8 each, v) under the global
 // scale g (d6 = fl32(6 g)): the block's E4M3 scale code (the same in both
 // lanes) and this lane's eight E2M1 codes.
-__device__ __forceinline__ uint32_t nv_block(const uint4& v, float g, float d6, uint32_t* out) {
+__device__ __forceinline__ uint32_t nv_block(const uint4& v, float g, float d6, float r6,
+                                             bool fast6, uint32_t* out) {
   uint32_t mx = absmax_pairs(v);
   mx = __vmaxu2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
   const float amax = __uint_as_float(max(mx & 0xFFFFu, mx >> 16) << 16);
-  const uint32_t sc = e4m3_code(__fdiv_rn(amax, d6));
+  const uint32_t sc = nv_scale_code(amax, d6, r6, fast6);
   const float d = __fmul_rn(g, e4m3_value(sc));
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t packed = 0;
@@ -108,7 +156,7 @@ __device__ __forceinline__ uint32_t nv_block(const uint4& v, float g, float d6, 
       packed |= (((w[p] >> 12) & 0x8u) | ((w[p] >> 24) & 0x80u)) << (8 * p);
   } else {
     float ylo[8], yhi[8];
-    const float r = __frcp_rn(d);
+    const float r = rcp_approx(d);
     const float2 r2 = make_float2(r, r);
     const float2 lo2 = make_float2(1.0f - 0x1p-20f, 1.0f - 0x1p-20f);
     const float2 hi2 = make_float2(1.0f + 0x1p-20f, 1.0f + 0x1p-20f);
@@ -123,7 +171,7 @@ __device__ __forceinline__ uint32_t nv_block(const uint4& v, float g, float d6, 
     }
     // the two ends of the bracket; equal codes are the code of y too
     packed = cvt_e2m1x8(ylo);
-    if (!(d >= 0x1p-126f) || packed != cvt_e2m1x8(yhi)) {
+    if (!(d >= 0x1p-126f && d <= 0x1p125f) || packed != cvt_e2m1x8(yhi)) {
       // rare: recompute the lane's eight quotients exactly
       float y[8];
 #pragma unroll
@@ -151,6 +199,8 @@ __global__ void __launch_bounds__(kNvThreads)
   constexpr uint32_t kPerWarp = 16 * kNvRounds;
   const float g = __ldg(gptr);
   const float d6 = __fmul_rn(6.0f, g);
+  const bool fast6 = d6 >= 0x1p-125f && d6 <= 0x1p125f;
+  const float r6 = __frcp_rn(d6);
   for (uint32_t base = warp * kPerWarp; base < blocks; base += nwarps * kPerWarp) {
     uint4 v[kNvRounds];
     uint32_t b[kNvRounds];
@@ -172,7 +222,7 @@ __global__ void __launch_bounds__(kNvThreads)
 #pragma unroll
     for (int u = 0; u < kNvRounds; ++u) {
       uint32_t packed;
-      const uint32_t sc = nv_block(v[u], g, d6, &packed);
+      const uint32_t sc = nv_block(v[u], g, d6, r6, fast6, &packed);
       if (b[u] < blocks) {
         // row-major [R, K/2]: block b covers bytes 8 b .. 8 b + 7
         *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(b[u]) * 8 + 4 * l2) = packed;
@@ -199,6 +249,8 @@ __global__ void __launch_bounds__(kNvThreads)
   const uint32_t nwarps = (gridDim.x * kNvThreads) >> 5;
   const float g = __ldg(gptr);
   const float d6 = __fmul_rn(6.0f, g);
+  const bool fast6 = d6 >= 0x1p-125f && d6 <= 0x1p125f;
+  const float r6 = __frcp_rn(d6);
   const uint32_t cpr = kb >> 2;            // cells (tiles) per 128-row tile
   const uint32_t quads = (cpr + 3u) >> 2;  // groups of four cells per 128-row tile
   const uint32_t units = ((R + 127u) >> 7) * quads * 32u;
@@ -220,7 +272,7 @@ __global__ void __launch_bounds__(kNvThreads)
     for (int jj = 0; jj < 4; ++jj) {
       const uint32_t row = rb * 128u + 32u * jj + i;
       uint32_t packed;
-      const uint32_t sc = nv_block(v[jj], g, d6, &packed);
+      const uint32_t sc = nv_block(v[jj], g, d6, r6, fast6, &packed);
       if (row < R && col_ok)
         *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(row) * (8u * kb) + blk * 8u +
                                      4u * l2) = packed;
