@@ -266,3 +266,20 @@ def test_quant_operands_ue8m0_tiles(fgq, cuda_dev, M, N, K):
     torch.cuda.synchronize()
     assert torch.equal(c, c_ex)
     assert fgq.device_error() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(120, 384, 512), (600, 2560, 1024)], ids=["single", "pair"])
+def test_ue8m0_tiled_padded_c(fgq, cuda_dev, M, N, K):
+    """C as rows of a wider buffer (ldc > N, NaN canaries past column N)."""
+    a = fgq_inputs.exponent_spread((M, K), 8, 1, seed=M)
+    b = fgq_inputs.exponent_spread((K, N), 8, 128, seed=M + 9)
+    host = _quant(a, b)
+    ta, tb = _host_tiles(host)
+    ops = _dev(*host, cuda_dev)
+    buf = torch.full((M, N + 64), float("nan"), dtype=torch.bfloat16, device=cuda_dev)
+    c = fgq.gemm_fp8_ue8m0_tiled(ops[0], torch.from_numpy(ta).to(cuda_dev), ops[2],
+                                 torch.from_numpy(tb).to(cuda_dev), out_dtype=torch.bfloat16,
+                                 out=buf[:, :N])
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[:, N:].float()).all(), "the GEMM wrote past column N"
+    _check(c, host)

@@ -167,3 +167,18 @@ def test_mxfp4_gemm_tiled_large_prefill_from_the_gpu_quantizer(fgq, cuda_dev):
     cols = np.concatenate([np.tile(np.arange(256), 256), rng.integers(0, N, 2000), [N - 1]])
     _check(c, host, rows, cols)
     assert fgq.device_error() == 0
+
+
+@pytest.mark.parametrize("pair", [False, True], ids=["single", "pair"])
+def test_mxfp4_gemm_tiled_padded_c(fgq, cuda_dev, pair):
+    """C as rows of a wider buffer (ldc > N, NaN canaries past column N):
+    the tiled kernels write exactly the [M, N] block."""
+    M, N, K = (120, 384, 512) if not pair else (600, 2560, 512)
+    host, _ = _operands(M, N, K, seed=77 + M)
+    aq, sa, bq, sb = _dev(host, cuda_dev)
+    buf = torch.full((M, N + 64), float("nan"), dtype=torch.bfloat16, device=cuda_dev)
+    c = fgq.gemm_mxfp4_tiled(aq, _tiles(host[1], cuda_dev), bq, _tiles(host[3], cuda_dev),
+                             out_dtype=torch.bfloat16, out=buf[:, :N])
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[:, N:].float()).all(), "the GEMM wrote past column N"
+    _check(c, host)

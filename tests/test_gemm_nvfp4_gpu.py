@@ -169,3 +169,17 @@ def test_nvfp4_gemm_tiled_large_prefill_from_the_gpu_quantizer(fgq, cuda_dev):
     cols = np.concatenate([np.tile(np.arange(256), 256), rng.integers(0, N, 2000), [N - 1]])
     _check(c, host, rows, cols)
     assert fgq.device_error() == 0
+
+
+@pytest.mark.parametrize("pair", [False, True], ids=["single", "pair"])
+def test_nvfp4_gemm_tiled_padded_c(fgq, cuda_dev, pair):
+    """C as rows of a wider buffer (ldc > N, NaN canaries past column N)."""
+    M, N, K = (120, 384, 512) if not pair else (600, 2560, 512)
+    host = _operands(M, N, K, seed=77 + M)
+    aq, sa, ga, bq, sb, gb = _dev(host, cuda_dev)
+    buf = torch.full((M, N + 32), float("nan"), dtype=torch.float32, device=cuda_dev)
+    c = fgq.gemm_nvfp4_tiled(aq, _tiles(host[1], cuda_dev), ga, bq, _tiles(host[4], cuda_dev), gb,
+                             out_dtype=torch.float32, out=buf[:, :N])
+    torch.cuda.synchronize()
+    assert torch.isnan(buf[:, N:]).all(), "the GEMM wrote past column N"
+    _check(c, host)
