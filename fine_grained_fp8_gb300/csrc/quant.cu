@@ -157,9 +157,9 @@ __device__ __forceinline__ void transpose4x4_bytes(uint32_t r0, uint32_t r1, uin
   c3 = __byte_perm(t1, t3, 0x7632);
 }
 
-// Five CTAs per SM (at most 51 registers a thread): measured faster than
-// the four that 55 registers allow, despite a few bytes of spill in the
-// fp32-scale instantiation; six spill heavily and are slower.
+// Four CTAs per SM (55 registers a thread, no spill): measured 28.8 us on a
+// 7168 x 7168 weight, against 28.9-30.3 us with five (51 registers and a
+// few bytes of spill) and 35 us with six.
 // Block `block` of W (k-block major), by the CTA's kWThreads threads.
 template <int MODE, bool TILES = false>
 __device__ __forceinline__ void w_block(const uint16_t* __restrict__ w, int64_t K, int64_t N,
@@ -235,7 +235,7 @@ __device__ __forceinline__ void w_block(const uint16_t* __restrict__ w, int64_t 
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kWThreads, 5)
+__global__ void __launch_bounds__(kWThreads, 4)
     quant_w_128x128_kernel(const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t ldw,
                            uint8_t* __restrict__ wq, float* __restrict__ sw) {
   w_block<MODE>(w, K, N, ldw, wq, sw, blockIdx.x);
