@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -56,11 +57,21 @@ def _peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(text: str) -> str:
+    """A CUDA source without its comments and blank lines: what the
+    compiler sees, so that editing a comment does not retire a capture."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def _kernel_sha(name: str) -> str:
+    """First 16 hex digits of the sha256 of the kernel's unit and of
+    fgq_device.cuh, comments left out."""
     h = hashlib.sha256()
     for f in (name, "fgq_device.cuh"):
-        with open(os.path.join(ROOT, "fine_grained_fp8_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "fine_grained_fp8_gb300", "csrc", f)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -16,10 +16,18 @@
 // reads bytes 0-1 of the cell (the two 32-element blocks of one MMA), id 2
 // bytes 2-3.  4X: byte b of the cell scales the MMA's b-th 16-element block.
 //
-// Same structure as the power-of-two FP8 kernel (gemm_mx.cu): persistent
-// CTAs on 128 x BN tiles, warp 0 TMA producer (one 128-byte stage = 256
-// elements of K), warp 1 MMA issuer (factor copies, four MMAs per stage),
-// warps 4-7 stage the factors in shared memory, warps 8-15 epilogue.
+// Two kernels:
+//   - gemm_mxf4_kernel, for block scales stored row-major ([rows, K/32] or
+//     [rows, K/16]): the same structure as the power-of-two FP8 kernel
+//     (gemm_mx.cu), persistent CTAs on 128 x BN tiles, warp 0 TMA producer
+//     (one 128-byte stage = 256 elements of K), warp 1 MMA issuer (factor
+//     copies, four MMAs per stage), warps 4-7 gather the factors into
+//     shared memory, warps 8-15 epilogue;
+//   - gemm_fp4_tiled_kernel, for block scales stored as tiles the
+//     tensor-map engine loads with the operands (no factor warps), on CTA
+//     pairs once A has two row tiles.  It also serves the FP8 GEMM with
+//     power-of-two scales given as UE8M0 code tiles (kind MXF8:
+//     kind::mxf8f6f4.block_scale.scale_vec::1X, 128 elements a stage).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
