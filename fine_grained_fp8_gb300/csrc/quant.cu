@@ -630,15 +630,19 @@ cudaError_t launch_quant_operands(const void* x, int64_t M, int64_t K, int64_t l
                                   int64_t ldq, float* sx, const void* w, int64_t N, int64_t ldw,
                                   uint8_t* wq, float* sw, int mode, cudaStream_t stream,
                                   const DeviceInfo& dev, bool code_tiles) {
-  (void)dev;
   const uint32_t kc = static_cast<uint32_t>(K / 128);
   const uint32_t groups = static_cast<uint32_t>(M * (K / 128));
   const int64_t w_blocks = (K / 128) * (N / 128);
   // activation CTAs: kRoundsPerWarp rounds of kActGroupsPerWarp groups per
-  // warp, at least one CTA when there are groups
+  // warp, at least one CTA when there are groups, and at most one wave (four
+  // per SM): they run after the weight blocks, so a second, partial wave of
+  // them would be the kernel's tail (measured 45.7 against 47.4 us on the
+  // large-prefill operands)
   constexpr uint32_t kRoundsPerWarp = 4;
   const uint32_t per_cta = (kActThreads / 32) * kActGroupsPerWarp * kRoundsPerWarp;
-  const uint32_t act_ctas = (groups + per_cta - 1) / per_cta;
+  uint32_t act_ctas = (groups + per_cta - 1) / per_cta;
+  const uint32_t wave = 4u * static_cast<uint32_t>(dev.sm_count);
+  if (act_ctas > wave) act_ctas = wave;
   const int64_t grid = w_blocks + act_ctas;
   if (grid == 0) return cudaSuccess;
   if (grid >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
