@@ -413,6 +413,7 @@ cudaError_t launch_ue8m0_scale_tiles(const float* s, int64_t R, int64_t K, int64
   const uint32_t F = static_cast<uint32_t>(K / 128), cpr = (F + 3) / 4;
   const uint64_t words = static_cast<uint64_t>((R + 127) / 128) * cpr * 128u;
   if (words == 0) return cudaSuccess;
+  if (words >= (uint64_t{1} << 32)) return cudaErrorInvalidValue;  // 16 GB of tiles
   uint64_t grid = (words + 255) / 256;
   const uint64_t cap = static_cast<uint64_t>(dev.sm_count) * 8;
   if (grid > cap) grid = cap;

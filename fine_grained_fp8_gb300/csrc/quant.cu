@@ -255,6 +255,11 @@ __global__ void __launch_bounds__(kWThreads, 4)
                           float* __restrict__ sx, const uint16_t* __restrict__ w, int64_t K,
                           int64_t N, int64_t ldw, uint8_t* __restrict__ wq,
                           float* __restrict__ sw, uint32_t w_blocks) {
+  // Launched with programmatic stream serialization: the previous kernel's
+  // memory is visible after pdl_wait(); the next kernel (the GEMM) may then
+  // start its set-up, and waits for this grid itself before touching memory.
+  pdl_wait();
+  pdl_launch_dependents();
   if (blockIdx.x < w_blocks) {
     w_block<MODE, TILES>(w, K, N, ldw, wq, sw, blockIdx.x);
     return;
@@ -657,10 +662,10 @@ cudaError_t launch_quant_operands(const void* x, int64_t M, int64_t K, int64_t l
     k = dense ? quant_operands_kernel<kScaleFp32, true> : quant_operands_kernel<kScaleFp32, false>;
   else
     k = dense ? quant_operands_kernel<kScaleUe8m0, true> : quant_operands_kernel<kScaleUe8m0, false>;
-  k<<<static_cast<unsigned>(grid), kWThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(x), kc, groups, ldx, xq, ldq, sx, static_cast<const uint16_t*>(w),
-      K, N, ldw, wq, sw, static_cast<uint32_t>(w_blocks));
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(static_cast<unsigned>(grid)), dim3(kWThreads), 0, stream,
+                    static_cast<const uint16_t*>(x), kc, groups, ldx, xq, ldq, sx,
+                    static_cast<const uint16_t*>(w), K, N, ldw, wq, sw,
+                    static_cast<uint32_t>(w_blocks));
 }
 
 cudaError_t launch_quant_w_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
