@@ -126,20 +126,27 @@ template <int MODE>
 __device__ __forceinline__ uint2 encode8(uint4 v, const GroupScale& g) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t c[4];
+  if (MODE == kScaleUe8m0) {
 #pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const float2 x = bf16x2_to_f32x2(w[p]);
-    float2 q;
-    if (MODE == kScaleUe8m0) {
-      q = mul2(x, g.r2);
-    } else if (!g.exact) {
+    for (int p = 0; p < 4; ++p) {
+      const float2 q = mul2(bf16x2_to_f32x2(w[p]), g.r2);
+      c[p] = cvt_e4m3x2(q.x, q.y);
+    }
+  } else if (!g.exact) {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float2 x = bf16x2_to_f32x2(w[p]);
       const float2 q0 = mul2(x, g.r2);
       const float2 d = fma2(q0, g.ns2, x);  // x - q0 * s, exact
-      q = fma2(d, g.r2, q0);
-    } else {
-      q = make_float2(__fdiv_rn(x.x, g.s), __fdiv_rn(x.y, g.s));
+      const float2 q = fma2(d, g.r2, q0);
+      c[p] = cvt_e4m3x2(q.x, q.y);
     }
-    c[p] = cvt_e4m3x2(q.x, q.y);
+  } else {
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float2 x = bf16x2_to_f32x2(w[p]);
+      c[p] = cvt_e4m3x2(__fdiv_rn(x.x, g.s), __fdiv_rn(x.y, g.s));
+    }
   }
   // Sign bit of each code from the sign of its bf16 input (bytes 1 and 3 of
   // each input word carry the signs of its two elements).
