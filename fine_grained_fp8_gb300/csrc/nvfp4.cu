@@ -20,8 +20,8 @@
 // monotone, so when its two ends encode alike every value in it does,
 // RN(x/D) included, and the code of y is the code of RN(x/D).  Otherwise
 // (about 1 in 10^4 elements on ordinary data, every exact boundary value
-// included) the lane's eight elements are recomputed with __fdiv_rn, as
-// are blocks with D outside that range.  The block scale E4M3(RN(amax /
+// included) those eight elements are recomputed with __fdiv_rn, as are
+// blocks with D outside that range.  The block scale E4M3(RN(amax /
 // d6)) takes the same route with t = RN(amax * RN(1/d6)).  A host test
 // replays both over every bf16 x (amax) against divisors that put
 // quotients on and beside the rounding boundaries, for every reciprocal
@@ -132,37 +132,47 @@ __device__ __forceinline__ uint32_t nv_scale_code(float amax, float d6, float r6
   return e4m3_code(__fdiv_rn(amax, d6));
 }
 
-// One block of 16 per two lanes (8 elements, 16 bytes each), 16 blocks per
-// warp per round, kNvRounds rounds of loads in flight.
+// One block of 16 per thread (two 16-byte loads), 32 consecutive blocks per
+// warp per round, kNvRounds rounds of loads in flight.  A thread holds its
+// whole block, so the block's amax needs no shuffle and its scale code,
+// divisor and reciprocal are formed once for 16 elements: 57.4 us on the
+// quantize-bandwidth activations, against 68.9 us with two lanes a block.
 constexpr int kNvThreads = 256;
 constexpr int kNvRounds = 2;
 
-// One block of 16 elements over two lanes (8 each, v) under the global
-// scale g (d6 = fl32(6 g)): the block's E4M3 scale code (the same in both
-// lanes) and this lane's eight E2M1 codes.
-__device__ __forceinline__ uint32_t nv_block(const uint4& v, float g, float d6, float r6,
-                                             bool fast6, uint32_t* out) {
-  uint32_t mx = absmax_pairs(v);
-  mx = __vmaxu2(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+// One block of 16 elements (v0: elements 0-7, v1: 8-15) under the global
+// scale g (d6 = fl32(6 g), r6 = RN(1 / d6), fast6 = d6 in the reciprocal's
+// range): the block's E4M3 scale code, and its 16 E2M1 codes as two words
+// (elements 0-7 in out[0], 8-15 in out[1]).
+__device__ __forceinline__ uint32_t nv_block(const uint4& v0, const uint4& v1, float g, float d6,
+                                             float r6, bool fast6, uint32_t (&out)[2]) {
+  const uint32_t mx = __vmaxu2(absmax_pairs(v0), absmax_pairs(v1));
   const float amax = __uint_as_float(max(mx & 0xFFFFu, mx >> 16) << 16);
   const uint32_t sc = nv_scale_code(amax, d6, r6, fast6);
   const float d = __fmul_rn(g, e4m3_value(sc));
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t packed = 0;
+  const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
   if (d == 0.0f) {
     // signed zeros: code 8 where the bf16 sign bit is set
 #pragma unroll
-    for (int p = 0; p < 4; ++p)
-      packed |= (((w[p] >> 12) & 0x8u) | ((w[p] >> 24) & 0x80u)) << (8 * p);
-  } else {
+    for (int h = 0; h < 2; ++h) {
+      out[h] = 0;
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        out[h] |= (((w[4 * h + p] >> 12) & 0x8u) | ((w[4 * h + p] >> 24) & 0x80u)) << (8 * p);
+    }
+    return sc;
+  }
+  const float r = rcp_approx(d);
+  const float2 r2 = make_float2(r, r);
+  const float2 lo2 = make_float2(1.0f - 0x1p-20f, 1.0f - 0x1p-20f);
+  const float2 hi2 = make_float2(1.0f + 0x1p-20f, 1.0f + 0x1p-20f);
+  const bool in_range = d >= 0x1p-126f && d <= 0x1p125f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
     float ylo[8], yhi[8];
-    const float r = rcp_approx(d);
-    const float2 r2 = make_float2(r, r);
-    const float2 lo2 = make_float2(1.0f - 0x1p-20f, 1.0f - 0x1p-20f);
-    const float2 hi2 = make_float2(1.0f + 0x1p-20f, 1.0f + 0x1p-20f);
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-      const float2 q = mul2(bf16x2_to_f32x2(w[p]), r2);
+      const float2 q = mul2(bf16x2_to_f32x2(w[4 * h + p]), r2);
       const float2 ql = mul2(q, lo2), qh = mul2(q, hi2);
       ylo[2 * p] = ql.x;
       ylo[2 * p + 1] = ql.y;
@@ -170,21 +180,36 @@ __device__ __forceinline__ uint32_t nv_block(const uint4& v, float g, float d6, 
       yhi[2 * p + 1] = qh.y;
     }
     // the two ends of the bracket; equal codes are the code of y too
-    packed = cvt_e2m1x8(ylo);
-    if (!(d >= 0x1p-126f && d <= 0x1p125f) || packed != cvt_e2m1x8(yhi)) {
-      // rare: recompute the lane's eight quotients exactly
+    uint32_t packed = cvt_e2m1x8(ylo);
+    if (!in_range || packed != cvt_e2m1x8(yhi)) {
+      // rare: recompute these eight quotients exactly
       float y[8];
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
-        const float2 f = bf16x2_to_f32x2(w[p]);
+        const float2 f = bf16x2_to_f32x2(w[4 * h + p]);
         y[2 * p] = __fdiv_rn(f.x, d);
         y[2 * p + 1] = __fdiv_rn(f.y, d);
       }
       packed = cvt_e2m1x8(y);
     }
+    out[h] = packed;
   }
-  *out = packed;
   return sc;
+}
+
+// Block b (row b / kb, block b % kb of the row) of x, as two 16-byte loads.
+template <bool DENSE>
+__device__ __forceinline__ void nv_load(const uint16_t* x, uint32_t b, uint32_t kb, int64_t ldx,
+                                        uint4& v0, uint4& v1) {
+  const uint16_t* src;
+  if (DENSE) {
+    src = x + static_cast<uint64_t>(b) * 16;
+  } else {
+    const uint32_t r = b / kb, c = b - r * kb;
+    src = x + static_cast<int64_t>(r) * ldx + c * 16;
+  }
+  v0 = ld_stream_16(src);
+  v1 = ld_stream_16(src + 8);
 }
 
 template <bool DENSE>
@@ -193,40 +218,32 @@ __global__ void __launch_bounds__(kNvThreads)
                             int64_t ldx, const float* __restrict__ gptr, uint8_t* __restrict__ xq,
                             uint8_t* __restrict__ sx) {
   const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t sub = lane >> 1, l2 = lane & 1u;
   const uint32_t warp = (blockIdx.x * kNvThreads + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * kNvThreads) >> 5;
-  constexpr uint32_t kPerWarp = 16 * kNvRounds;
+  constexpr uint32_t kPerWarp = 32 * kNvRounds;
   const float g = __ldg(gptr);
   const float d6 = __fmul_rn(6.0f, g);
   const bool fast6 = d6 >= 0x1p-125f && d6 <= 0x1p125f;
   const float r6 = __frcp_rn(d6);
   for (uint32_t base = warp * kPerWarp; base < blocks; base += nwarps * kPerWarp) {
-    uint4 v[kNvRounds];
+    uint4 v[kNvRounds][2];
     uint32_t b[kNvRounds];
 #pragma unroll
     for (int u = 0; u < kNvRounds; ++u) {
-      b[u] = base + 16 * u + sub;
-      v[u] = make_uint4(0, 0, 0, 0);
-      if (b[u] < blocks) {
-        const uint16_t* src;
-        if (DENSE) {
-          src = x + static_cast<uint64_t>(b[u]) * 16;
-        } else {
-          const uint32_t r = b[u] / kb, c = b[u] - r * kb;
-          src = x + static_cast<int64_t>(r) * ldx + c * 16;
-        }
-        v[u] = ld_stream_16(src + 8 * l2);
-      }
+      b[u] = base + 32 * u + lane;
+      v[u][0] = v[u][1] = make_uint4(0, 0, 0, 0);
+      if (b[u] < blocks) nv_load<DENSE>(x, b[u], kb, ldx, v[u][0], v[u][1]);
     }
 #pragma unroll
     for (int u = 0; u < kNvRounds; ++u) {
-      uint32_t packed;
-      const uint32_t sc = nv_block(v[u], g, d6, r6, fast6, &packed);
+      uint32_t packed[2];
+      const uint32_t sc = nv_block(v[u][0], v[u][1], g, d6, r6, fast6, packed);
       if (b[u] < blocks) {
         // row-major [R, K/2]: block b covers bytes 8 b .. 8 b + 7
-        *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(b[u]) * 8 + 4 * l2) = packed;
-        if (l2 == 0) sx[b[u]] = static_cast<uint8_t>(sc);
+        uint32_t* dst = reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(b[u]) * 8);
+        dst[0] = packed[0];
+        dst[1] = packed[1];
+        sx[b[u]] = static_cast<uint8_t>(sc);
       }
     }
   }
@@ -234,17 +251,16 @@ __global__ void __launch_bounds__(kNvThreads)
 
 // The same quantizer with the scales in the tiled FP4 layout (512-byte tiles
 // of 128 rows x 4 factor bytes; 16-byte tile row i holds the cells of rows
-// 32 j + i, j = 0..3).  A warp's unit is 16-byte row i of four neighbouring
-// tiles: four rounds, round j quantizing 16 blocks (512 contiguous bytes of
-// x) of row 32 j + i; lanes 0, 8, 16 and 24 then each hold tile row i of
-// one cell and store it whole.  Rows past R read as zeros and give padding
-// codes.
+// 32 j + i, j = 0..3).  A warp's unit is 16-byte row i of eight neighbouring
+// tiles: four rounds, round j quantizing 32 blocks (1 KB of x) of row
+// 32 j + i, one a lane; lanes 0, 4, .., 28 then each gather tile row i of
+// one cell (the scale codes of their own and the next three lanes' blocks)
+// and store it whole.  Rows past R read as zeros and give padding codes.
 __global__ void __launch_bounds__(kNvThreads)
     quant_nvfp4_1x16_tiled_kernel(const uint16_t* __restrict__ x, uint32_t R, uint32_t kb,
                                   int64_t ldx, const float* __restrict__ gptr,
                                   uint8_t* __restrict__ xq, uint8_t* __restrict__ st) {
   const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t sub = lane >> 1, l2 = lane & 1u;
   const uint32_t warp = (blockIdx.x * kNvThreads + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * kNvThreads) >> 5;
   const float g = __ldg(gptr);
@@ -252,38 +268,44 @@ __global__ void __launch_bounds__(kNvThreads)
   const bool fast6 = d6 >= 0x1p-125f && d6 <= 0x1p125f;
   const float r6 = __frcp_rn(d6);
   const uint32_t cpr = kb >> 2;            // cells (tiles) per 128-row tile
-  const uint32_t quads = (cpr + 3u) >> 2;  // groups of four cells per 128-row tile
-  const uint32_t units = ((R + 127u) >> 7) * quads * 32u;
+  const uint32_t octs = (cpr + 7u) >> 3;   // groups of eight cells per 128-row tile
+  const uint32_t units = ((R + 127u) >> 7) * octs * 32u;
   for (uint32_t unit = warp; unit < units; unit += nwarps) {
     const uint32_t i = unit & 31u, t = unit >> 5;
-    const uint32_t rb = t / quads, cq = t - rb * quads;
-    const uint32_t blk = 16u * cq + sub;  // this lane's block within the row
-    const bool col_ok = blk < kb;         // the last cells of the four may not exist
-    uint4 v[4];
+    const uint32_t rb = t / octs, co = t - rb * octs;
+    const uint32_t blk = 32u * co + lane;  // this lane's block within the row
+    const bool col_ok = blk < kb;          // the last cells of the eight may not exist
+    uint4 v[4][2];
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       const uint32_t row = rb * 128u + 32u * jj + i;
-      v[jj] = make_uint4(0, 0, 0, 0);
-      if (row < R && col_ok)
-        v[jj] = ld_stream_16(x + static_cast<int64_t>(row) * ldx + blk * 16u + 8u * l2);
+      v[jj][0] = v[jj][1] = make_uint4(0, 0, 0, 0);
+      if (row < R && col_ok) {
+        const uint16_t* src = x + static_cast<int64_t>(row) * ldx + blk * 16u;
+        v[jj][0] = ld_stream_16(src);
+        v[jj][1] = ld_stream_16(src + 8);
+      }
     }
     uint32_t cell[4];
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       const uint32_t row = rb * 128u + 32u * jj + i;
-      uint32_t packed;
-      const uint32_t sc = nv_block(v[jj], g, d6, r6, fast6, &packed);
-      if (row < R && col_ok)
-        *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(row) * (8u * kb) + blk * 8u +
-                                     4u * l2) = packed;
-      // lanes 8 q: the cells (blocks in lanes +0, +2, +4, +6)
-      const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, sc, 2);
-      const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, sc, 4);
-      const uint32_t c3 = __shfl_down_sync(0xFFFFFFFFu, sc, 6);
+      uint32_t packed[2];
+      const uint32_t sc = nv_block(v[jj][0], v[jj][1], g, d6, r6, fast6, packed);
+      if (row < R && col_ok) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(row) * (8u * kb) +
+                                                    blk * 8u);
+        dst[0] = packed[0];
+        dst[1] = packed[1];
+      }
+      // lanes 4 q: the cell (blocks in lanes +0 .. +3)
+      const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, sc, 1);
+      const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, sc, 2);
+      const uint32_t c3 = __shfl_down_sync(0xFFFFFFFFu, sc, 3);
       cell[jj] = sc | (c1 << 8) | (c2 << 16) | (c3 << 24);
     }
-    if ((lane & 7u) == 0 && col_ok)
-      *reinterpret_cast<uint4*>(st + (static_cast<uint64_t>(rb) * cpr + 4u * cq + (lane >> 3)) * 512u +
+    if ((lane & 3u) == 0 && col_ok)
+      *reinterpret_cast<uint4*>(st + (static_cast<uint64_t>(rb) * cpr + 8u * co + (lane >> 2)) * 512u +
                                 16u * i) = make_uint4(cell[0], cell[1], cell[2], cell[3]);
   }
 }
@@ -322,8 +344,8 @@ cudaError_t launch_quant_nvfp4_1x16(const void* x, int64_t R, int64_t K, int64_t
   const uint32_t blocks = static_cast<uint32_t>(R * (K / 16));
   if (blocks == 0) return cudaSuccess;
   if (tiled) {
-    // one warp per 16-byte row of four neighbouring tiles (64 blocks)
-    const uint32_t units = static_cast<uint32_t>((R + 127) / 128) * ((kb / 4 + 3) / 4) * 32u;
+    // one warp per 16-byte row of eight neighbouring tiles (128 blocks)
+    const uint32_t units = static_cast<uint32_t>((R + 127) / 128) * ((kb / 4 + 7) / 8) * 32u;
     int per_sm = 0;
     cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         &per_sm, quant_nvfp4_1x16_tiled_kernel, kNvThreads, 0);
@@ -343,7 +365,7 @@ cudaError_t launch_quant_nvfp4_1x16(const void* x, int64_t R, int64_t K, int64_t
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kNvThreads, 0);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
-  const uint32_t per_block = (kNvThreads / 32) * 16 * kNvRounds;
+  const uint32_t per_block = kNvThreads * kNvRounds;
   const uint32_t needed = (blocks + per_block - 1) / per_block;
   uint32_t grid = static_cast<uint32_t>(dev.sm_count) * static_cast<uint32_t>(per_sm);
   if (grid > needed) grid = needed;
