@@ -522,57 +522,88 @@ __global__ void __launch_bounds__(kMxThreads)
   }
 }
 
+// One group of 32 elements held by one thread (v: four 16-byte chunks): the
+// group's UE8M0 code, formed once, and its 32 E2M1 codes as four words.
+__device__ __forceinline__ uint32_t mx_group32(const uint4 (&v)[4], uint32_t (&packed)[4]) {
+  const uint32_t mx = __vmaxu2(__vmaxu2(absmax_pairs(v[0]), absmax_pairs(v[1])),
+                               __vmaxu2(absmax_pairs(v[2]), absmax_pairs(v[3])));
+  const uint32_t code = mx_scale_code(max(mx & 0xFFFFu, mx >> 16));
+  // 2^-e: exponent field 254 - code; code 0 (2^-127) gives 2^127
+  const float inv = __uint_as_float((254u - code) << 23);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+    float y[8];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float2 f = bf16x2_to_f32x2(w[p]);
+      y[2 * p] = f.x * inv;
+      y[2 * p + 1] = f.y * inv;
+    }
+    packed[q] = cvt_e2m1x8(y);
+  }
+  return code;
+}
+
 // The same quantizer with the scales in the tiled FP4 layout: 512-byte tiles
 // of 128 rows x 4 factor bytes; tile (r / 128, f / 4) holds, in its 16-byte
 // row i, the cells (4 factor bytes) of rows 32 j + i, j = 0..3 (the 32-row x
-// 16-byte tile the FP4 GEMM copies into TMEM).  A warp's unit is 16-byte
-// row i of two neighbouring tiles: four rounds, round j quantizing 8 groups
-// (512 contiguous bytes of x, as the row-major kernel reads them) of row
-// 32 j + i; lane 0 then holds tile row i of the first cell and lane 16 of
-// the second, each stored whole.  Consecutive warps take consecutive tile
-// rows, so the scale stores fill whole sectors.  Rows past R read as zeros
-// and give padding codes (127).
+// 16-byte tile the FP4 GEMM copies into TMEM).  One thread per group of 32
+// (64 contiguous bytes of x), so the group's amax takes no shuffle and its
+// scale is formed once for 32 elements.  A warp's unit is 16-byte row i of
+// eight neighbouring tiles: rows 32 j + i, j = 0..3, each 32 groups (2 KB of
+// x), two rows' loads in flight at a time; lanes 0, 4, .., 28 then each hold
+// tile row i of one cell (the codes of their own and the next three lanes'
+// groups) and store it whole.  Rows past R read as zeros and give padding
+// codes (127).  (Four lanes per group, as the row-major kernel: 59.4 us on
+// the quantize-bandwidth activations.)
 __global__ void __launch_bounds__(kMxThreads)
     quant_mxfp4_1x32_tiled_kernel(const uint16_t* __restrict__ x, uint32_t R, uint32_t kg,
                                   int64_t ldx, uint8_t* __restrict__ xq,
                                   uint8_t* __restrict__ st) {
   const uint32_t lane = threadIdx.x & 31u;
-  const uint32_t sub = lane >> 2, l4 = lane & 3u;
   const uint32_t warp = (blockIdx.x * kMxThreads + threadIdx.x) >> 5;
   const uint32_t nwarps = (gridDim.x * kMxThreads) >> 5;
   const uint32_t cpr = kg >> 2;            // cells (tiles) per 128-row tile
-  const uint32_t pairs = (cpr + 1u) >> 1;  // cell pairs per 128-row tile
-  const uint32_t units = ((R + 127u) >> 7) * pairs * 32u;
+  const uint32_t octs = (cpr + 7u) >> 3;   // groups of eight cells per 128-row tile
+  const uint32_t units = ((R + 127u) >> 7) * octs * 32u;
   for (uint32_t unit = warp; unit < units; unit += nwarps) {
     const uint32_t i = unit & 31u, t = unit >> 5;
-    const uint32_t rb = t / pairs, cp = t - rb * pairs;
-    const uint32_t grp = 8u * cp + sub;          // this lane's group within the row
-    const bool col_ok = grp < kg;                // the pair's second cell may not exist
-    uint4 v[4];
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const uint32_t row = rb * 128u + 32u * jj + i;
-      v[jj] = make_uint4(0, 0, 0, 0);
-      if (row < R && col_ok)
-        v[jj] = ld_stream_16(x + static_cast<int64_t>(row) * ldx + grp * 32u + 8u * l4);
-    }
+    const uint32_t rb = t / octs, co = t - rb * octs;
+    const uint32_t grp = 32u * co + lane;  // this lane's group within the row
+    const bool col_ok = grp < kg;          // the last cells of the eight may not exist
     uint32_t cell[4];
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const uint32_t row = rb * 128u + 32u * jj + i;
-      uint32_t packed;
-      const uint32_t code = mx_group(v[jj], &packed);
-      if (row < R && col_ok)
-        *reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(row) * (16u * kg) + grp * 16u +
-                                     4u * l4) = packed;
-      // lanes 0 and 16: the cells (groups in lanes +0, +4, +8, +12)
-      const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, code, 4);
-      const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, code, 8);
-      const uint32_t c3 = __shfl_down_sync(0xFFFFFFFFu, code, 12);
-      cell[jj] = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+    for (int h = 0; h < 2; ++h) {
+      uint4 v[2][4];
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const uint32_t row = rb * 128u + 32u * (2 * h + jj) + i;
+        const uint16_t* src = x + static_cast<int64_t>(row) * ldx + grp * 32u;
+        const bool ok = row < R && col_ok;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[jj][q] = ok ? ld_stream_16(src + 8 * q) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const uint32_t row = rb * 128u + 32u * (2 * h + jj) + i;
+        uint32_t packed[4];
+        const uint32_t code = mx_group32(v[jj], packed);
+        if (row < R && col_ok) {
+          uint32_t* dst = reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(row) * (16u * kg) +
+                                                      grp * 16u);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = packed[q];
+        }
+        // lanes 4 c: the cell (groups in lanes +0 .. +3)
+        const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, code, 1);
+        const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, code, 2);
+        const uint32_t c3 = __shfl_down_sync(0xFFFFFFFFu, code, 3);
+        cell[2 * h + jj] = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+      }
     }
-    if ((lane & 15u) == 0 && col_ok)
-      *reinterpret_cast<uint4*>(st + (static_cast<uint64_t>(rb) * cpr + 2u * cp + (lane >> 4)) * 512u +
+    if ((lane & 3u) == 0 && col_ok)
+      *reinterpret_cast<uint4*>(st + (static_cast<uint64_t>(rb) * cpr + 8u * co + (lane >> 2)) * 512u +
                                 16u * i) = make_uint4(cell[0], cell[1], cell[2], cell[3]);
   }
 }
@@ -586,8 +617,8 @@ cudaError_t launch_quant_mxfp4_1x32(const void* x, int64_t R, int64_t K, int64_t
   const uint32_t groups = static_cast<uint32_t>(R * (K / 32));
   if (groups == 0) return cudaSuccess;
   if (tiled) {
-    // one warp per 16-byte row of two neighbouring tiles (32 groups)
-    const uint32_t units = static_cast<uint32_t>((R + 127) / 128) * ((kg / 4 + 1) / 2) * 32u;
+    // one warp per 16-byte row of eight neighbouring tiles (128 groups)
+    const uint32_t units = static_cast<uint32_t>((R + 127) / 128) * ((kg / 4 + 7) / 8) * 32u;
     int per_sm = 0;
     cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         &per_sm, quant_mxfp4_1x32_tiled_kernel, kMxThreads, 0);
