@@ -287,34 +287,37 @@ __global__ void __launch_bounds__(kNvThreads)
     const uint32_t rb = t / octs, co = t - rb * octs;
     const uint32_t blk = 32u * co + lane;  // this lane's block within the row
     const bool col_ok = blk < kb;          // the last cells of the eight may not exist
-    uint4 v[4][2];
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const uint32_t row = rb * 128u + 32u * jj + i;
-      v[jj][0] = v[jj][1] = make_uint4(0, 0, 0, 0);
-      if (row < R && col_ok) {
-        const uint16_t* src = x + static_cast<int64_t>(row) * ldx + blk * 16u;
-        v[jj][0] = ld_stream_16(src);
-        v[jj][1] = ld_stream_16(src + 8);
-      }
-    }
     uint32_t cell[4];
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const uint32_t row = rb * 128u + 32u * jj + i;
-      uint32_t packed[2];
-      const uint32_t sc = nv_block(v[jj][0], v[jj][1], g, d6, r6, fast6, packed);
-      if (row < R && col_ok) {
-        uint32_t* dst = reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(row) * (8u * kb) +
-                                                    blk * 8u);
-        dst[0] = packed[0];
-        dst[1] = packed[1];
+    for (int h = 0; h < 2; ++h) {  // rows 32 (2 h) + i and 32 (2 h + 1) + i
+      uint4 v[2][2];
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const uint32_t row = rb * 128u + 32u * (2 * h + jj) + i;
+        v[jj][0] = v[jj][1] = make_uint4(0, 0, 0, 0);
+        if (row < R && col_ok) {
+          const uint16_t* src = x + static_cast<int64_t>(row) * ldx + blk * 16u;
+          v[jj][0] = ld_stream_16(src);
+          v[jj][1] = ld_stream_16(src + 8);
+        }
       }
-      // lanes 4 q: the cell (blocks in lanes +0 .. +3)
-      const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, sc, 1);
-      const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, sc, 2);
-      const uint32_t c3 = __shfl_down_sync(0xFFFFFFFFu, sc, 3);
-      cell[jj] = sc | (c1 << 8) | (c2 << 16) | (c3 << 24);
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const uint32_t row = rb * 128u + 32u * (2 * h + jj) + i;
+        uint32_t packed[2];
+        const uint32_t sc = nv_block(v[jj][0], v[jj][1], g, d6, r6, fast6, packed);
+        if (row < R && col_ok) {
+          uint32_t* dst = reinterpret_cast<uint32_t*>(xq + static_cast<uint64_t>(row) * (8u * kb) +
+                                                      blk * 8u);
+          dst[0] = packed[0];
+          dst[1] = packed[1];
+        }
+        // lanes 4 q: the cell (blocks in lanes +0 .. +3)
+        const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, sc, 1);
+        const uint32_t c2 = __shfl_down_sync(0xFFFFFFFFu, sc, 2);
+        const uint32_t c3 = __shfl_down_sync(0xFFFFFFFFu, sc, 3);
+        cell[2 * h + jj] = sc | (c1 << 8) | (c2 << 16) | (c3 << 24);
+      }
     }
     if ((lane & 3u) == 0 && col_ok)
       *reinterpret_cast<uint4*>(st + (static_cast<uint64_t>(rb) * cpr + 8u * co + (lane >> 2)) * 512u +
