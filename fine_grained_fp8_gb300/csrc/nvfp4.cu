@@ -265,9 +265,11 @@ __global__ void __launch_bounds__(kNvThreads)
 // of 128 rows x 4 factor bytes; 16-byte tile row i holds the cells of rows
 // 32 j + i, j = 0..3).  A warp's unit is 16-byte row i of eight neighbouring
 // tiles: four rounds, round j quantizing 32 blocks (1 KB of x) of row
-// 32 j + i, one a lane; lanes 0, 4, .., 28 then each gather tile row i of
-// one cell (the scale codes of their own and the next three lanes' blocks)
-// and store it whole.  Rows past R read as zeros and give padding codes.
+// 32 j + i, one a lane, with two rounds' loads in flight at a time (56
+// registers; all four at once took 74 and measured 1.5% slower); lanes 0,
+// 4, .., 28 then each gather tile row i of one cell (the scale codes of
+// their own and the next three lanes' blocks) and store it whole.  Rows
+// past R read as zeros and give padding codes.
 __global__ void __launch_bounds__(kNvThreads)
     quant_nvfp4_1x16_tiled_kernel(const uint16_t* __restrict__ x, uint32_t R, uint32_t kb,
                                   int64_t ldx, const float* __restrict__ gptr,
