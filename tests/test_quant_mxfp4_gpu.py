@@ -109,3 +109,20 @@ def test_fp4_scales_to_tiles_matches_oracle(fgq, cuda_dev, R, F):
     assert t.numel() == fgq.fp4_scale_tiles_bytes(R, F) == ((R + 127) // 128) * 128 * F
     mask = _defined(R, F)
     assert np.array_equal(t.cpu().numpy()[mask], oracle.fp4_scale_tiles(s)[mask])
+
+
+def test_mxfp4_tiled_codes_at_a_4_byte_offset(fgq, cuda_dev):
+    """Codes written to a buffer only 4-byte aligned (the API's minimum)
+    equal those written to a 16-byte-aligned one, and so do the scale
+    tiles."""
+    R, K = 33, 384
+    x = fgq_inputs.outlier((R, K), 1e-2, 100.0, seed=91).to(cuda_dev)
+    q, t = fgq.quant_mxfp4_1x32_tiled(x)
+    buf = torch.full((R * K // 2 + 16,), 0xAB, dtype=torch.uint8, device=cuda_dev)
+    xq_off = buf[4:4 + R * K // 2].view(R, K // 2)
+    assert xq_off.data_ptr() % 16 == 4
+    q2, t2 = fgq.quant_mxfp4_1x32_tiled(x, xq=xq_off)
+    torch.cuda.synchronize()
+    assert torch.equal(q, q2) and torch.equal(t, t2)
+    # nothing written outside the codes
+    assert bool((buf[:4] == 0xAB).all()) and bool((buf[4 + R * K // 2:] == 0xAB).all())
