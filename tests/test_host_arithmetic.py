@@ -10,10 +10,12 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
 def test_nvfp4_reciprocal_encode_equals_ieee_quotient(tmp_path):
-    """The NVFP4 quantizer encodes RN(x * RN(1/D)) unless that lands within
-    8 ulps of an E2M1 rounding boundary, where it uses RN(x / D); the codes
-    must equal those of RN(x / D) for every bf16 x (and the check must be
-    able to fail: without the fallback it finds mismatches)."""
+    """The NVFP4 quantizer encodes RN(x * r), r any fp32 within 1 ulp of
+    1/D (the hardware reciprocal), unless the bracket RN(y (1 -+ 2^-20))
+    straddles an E2M1 rounding boundary, where it uses RN(x / D); the
+    codes must equal those of RN(x / D) for every bf16 x, and the block
+    scale's E4M3 code the same way (and the check must be able to fail:
+    without the fallback it finds mismatches)."""
     exe = tmp_path / "e2m1_check"
     subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-o", str(exe),
                     os.path.join(HERE, "host", "e2m1_reciprocal_check.c"), "-lm"], check=True)
